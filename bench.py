@@ -1,0 +1,467 @@
+#!/usr/bin/env python
+"""Benchmark of the ragged grouped SwiGLU expert layer on GB300.
+
+One step = the whole hot path over one batch of the large workload (T = 16384 tokens, E = 256
+experts, top-8, d = 2048, h = 512, M = 131072 routed rows): route histogram + offsets +
+placement, permute, grouped up/gate GEMM with fused SwiGLU, grouped down GEMM, weighted
+combine, and the backward (combine backward, down dgrad with fused SwiGLU backward, up dgrad,
+both wgrads, permute backward). Every step is a library kernel called through the C ABI.
+
+Metric: useful expert TFLOP/s, 18*M*d*h per forward+backward step (6*M*d*h forward), M counting
+routed rows only. Prints one JSON line. `--impl reference` times the CPU fp64 oracle instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "useful expert TFLOP/s (6*M*d*h fwd, 18*M*d*h fwd+bwd), fwd+bwd step"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_NOTE = "inputs larger than L2 (129 MB): xp 512 MB, weights 1.6 GB; no flush"
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=100)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default="large")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-variants", action="store_true")
+    return p.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+# ------------------------------------------------------------------------------ CPU oracle timing
+class OracleSampler:
+    """Times the oracle as it stands on a bounded sample of the workload: the route (histogram,
+    offsets, placement) over all slots, then, expert by expert, the permute of that expert's
+    rows, its forward and its backward (combine backward as a scaled permute), until about
+    `seconds` of CPU time. Weight and input generation is not timed."""
+
+    def __init__(self, wl):
+        self.wl = wl
+        self.x = wl.x()
+        self.dout = wl.dout()
+        self.next_expert = 0
+
+    def run(self, seconds: float):
+        import numpy as np
+        from oracle import moe_oracle as O
+        wl = self.wl
+        t0 = time.perf_counter()
+        r = O.route_offsets(wl.ids, wl.E)
+        elapsed = time.perf_counter() - t0
+        segs = O.segments(r["offsets"])
+        picked, rows, flops = 0, 0, 0
+        for _ in range(wl.E):
+            e = self.next_expert
+            self.next_expert = (e + 1) % wl.E
+            s, t = segs[e]
+            if t == s:
+                continue
+            wu, wd = wl.w_ug(e), wl.w_down(e)
+            src = r["sorted_src"][s:t]
+            one = np.array([t - s])
+            t0 = time.perf_counter()
+            xp = O.permute(self.x, src, t - s, wl.k)
+            y, u, a, _ = O.expert_forward(xp, one, lambda i: wu, lambda i: wd)
+            dy = O.permute(self.dout, src, t - s, wl.k, row_scale=wl.weights)
+            O.expert_backward(dy, xp, u, one, lambda i: wu, lambda i: wd)
+            elapsed += time.perf_counter() - t0
+            picked += 1
+            rows += t - s
+            flops += O.flops_fwd_bwd(t - s, wl.d, wl.h)
+            if elapsed >= seconds:
+                break
+        desc = (f"route over all {wl.n} slots, then {picked} of {wl.E} experts ({rows} of {r['M']} rows): "
+                f"permute + fp64 forward + backward per expert")
+        return flops, elapsed, desc
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    from ragged_grouped_gemm_device_gb300 import workloads as W
+    wl = W.make(args.workload)
+    cores = os.cpu_count()
+    sampler = OracleSampler(wl)
+    vals = []
+    desc = ""
+    for i in range(args.warmup + args.steps):
+        flops, el, desc = sampler.run(2.0)
+        if i >= args.warmup:
+            vals.append((flops, el))
+    tot_f = sum(f for f, _ in vals)
+    tot_t = sum(t for _, t in vals)
+    value = tot_f / tot_t / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot_t / len(vals),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(wl),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": "each step: " + desc},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(wl):
+    import numpy as np
+    ids = wl.ids.reshape(-1)
+    counts = np.bincount(ids[(ids >= 0) & (ids < wl.E)], minlength=wl.E)
+    M = int(counts.sum())
+    p = counts[counts > 0] / M
+    ih = 1.0 + float((p * np.log(p)).sum()) / float(np.log(wl.E))
+    scheduled = int(sum(-(-int(c) // 128) * 128 for c in counts))
+    return {"workload": f"{wl.name}: T={wl.T} tokens, E={wl.E} experts, top_k={wl.k}, d={wl.d}, h={wl.h}, SwiGLU",
+            "T": wl.T, "top_k": wl.k, "E": wl.E, "d": wl.d, "h": wl.h, "M": M,
+            "rows_per_expert": {"mean": M / wl.E, "max": int(counts.max()), "min": int(counts.min()),
+                                "empty": int((counts == 0).sum())},
+            "I_H": ih, "scheduled_rows_128": scheduled, "useful_rows": M, "l2": L2_NOTE}
+
+
+# ------------------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.out = tempfile.NamedTemporaryFile(mode="w+", suffix=".csv", delete=False)
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.out, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        self.proc.wait(timeout=10)
+        self.out.flush()
+        self.out.seek(0)
+        rows = [r.split(",") for r in self.out.read().strip().splitlines() if r.strip()]
+        os.unlink(self.out.name)
+        sm, mx, pw, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [c.strip() for c in r]
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1])); mx.append(float(r[2])); pw.append(float(r[3]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, r[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "power_w_max": max(pw),
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------------------ our arm
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for name in ("grouped_gemm.cu", "common.cuh", "permute.cu", "route.cu"):
+        with open(os.path.join(ROOT, "ragged_grouped_gemm_device_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def load_traffic():
+    """DRAM bytes per launch from the committed ncu summary, if the kernels are unchanged."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return {}
+    with open(path) as f:
+        t = json.load(f)
+    return t.get("kernels", {}) if t.get("source_hash") == kernel_source_hash() else {}
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    rank, world, local_rank = dist_env()
+    torch.cuda.set_device(local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    import __graft_entry__
+    if rank == 0 or world == 1:
+        __graft_entry__.build()
+    if world > 1:
+        torch.distributed.barrier()
+    from ragged_grouped_gemm_device_gb300 import _lib
+    from ragged_grouped_gemm_device_gb300 import workloads as W
+    L = _lib
+    L.load()
+
+    wl = W.make(args.workload)
+    T, k, E, d, h, n = wl.T, wl.k, wl.E, wl.d, wl.h, wl.n
+    dev = torch.device("cuda", local_rank)
+    bf = torch.bfloat16
+    x_h = torch.from_numpy(wl.x()).to(bf)
+    dout_h = torch.from_numpy(wl.dout()).to(bf)
+    ids_h = torch.from_numpy(wl.ids)
+    wts_h = torch.from_numpy(wl.weights)
+    w_ug = torch.empty(E, 2 * h, d, dtype=bf, device=dev)
+    w_down = torch.empty(E, h, d, dtype=bf, device=dev)
+    for e in range(E):
+        w_ug[e].copy_(torch.from_numpy(wl.w_ug(e)).to(bf))
+        w_down[e].copy_(torch.from_numpy(wl.w_down(e)).to(bf))
+    x, dout, ids, wts = x_h.to(dev), dout_h.to(dev), ids_h.to(dev), wts_h.to(dev)
+
+    i32 = torch.int32
+    counts = torch.empty(E, dtype=i32, device=dev)
+    offsets = torch.empty(E, dtype=i32, device=dev)
+    sorted_src = torch.empty(n, dtype=i32, device=dev)
+    inv_map = torch.empty(n, dtype=i32, device=dev)
+    route_ws = torch.empty(L.moe_workspace_bytes(L.OP_ROUTE, T, k, E), dtype=torch.uint8, device=dev)
+    xp = torch.empty(n, d, dtype=bf, device=dev)
+    a = torch.empty(n, h, dtype=bf, device=dev)
+    y = torch.empty(n, d, dtype=bf, device=dev)
+    saved = torch.empty(L.moe_workspace_bytes(L.OP_SAVED, T, k, E, d, h), dtype=torch.uint8, device=dev)
+    out = torch.empty(T, d, dtype=bf, device=dev)
+    dy = torch.empty(n, d, dtype=bf, device=dev)
+    du_hi = torch.empty(n, 2 * h, dtype=bf, device=dev)
+    du_lo = torch.empty(n, 2 * h, dtype=bf, device=dev)
+    dxp = torch.empty(n, d, dtype=bf, device=dev)
+    dx = torch.empty(T, d, dtype=bf, device=dev)
+    dw_ug = torch.empty(E, 2 * h, d, dtype=torch.float32, device=dev)
+    dw_down = torch.empty(E, h, d, dtype=torch.float32, device=dev)
+    status = torch.zeros(1, dtype=i32, device=dev)
+    _, p_lo, p_hi = L.saved_views(saved, n, h)
+    stream = torch.cuda.current_stream()
+
+    def inputs():
+        return x, ids, wts, dout
+
+    def step_calls(xin, idin, win, doin):
+        return [
+            ("route", 3, lambda: L.moe_route_offsets(idin, T, k, E, counts, offsets, sorted_src, inv_map, route_ws)),
+            ("permute", 1, lambda: L.moe_permute(xin, sorted_src, offsets, None, T, k, E, d, xp)),
+            ("up_swiglu", 1, lambda: L.moe_grouped_up_swiglu(xp, offsets, sorted_src, win, E, n, d, h, w_ug, a,
+                                                             saved, status)),
+            ("down", 1, lambda: L.moe_grouped_down(a, offsets, sorted_src, win, E, n, d, h, w_down, y, status)),
+            ("combine", 1, lambda: L.moe_unpermute_combine(y, inv_map, None, T, k, d, out)),
+            ("combine_bwd", 1, lambda: L.moe_permute(doin, sorted_src, offsets, None, T, k, E, d, dy)),
+            ("down_dgrad_swiglu", 1, lambda: L.moe_grouped_down_dgrad_swiglu(dy, saved, offsets, sorted_src, win, E,
+                                                                             n, d, h, w_down, du_hi, du_lo, status)),
+            ("up_dgrad", 1, lambda: L.moe_grouped_up_dgrad(du_hi, offsets, E, n, d, h, w_ug, dxp, status)),
+            ("wgrad_down", 1, lambda: L.moe_grouped_wgrad(p_hi, p_lo, h, dy, d, offsets, E, n, dw_down, status)),
+            ("wgrad_up", 1, lambda: L.moe_grouped_wgrad(du_hi, du_lo, 2 * h, xp, d, offsets, E, n, dw_ug, status)),
+            ("permute_bwd", 1, lambda: L.moe_unpermute_combine(dxp, inv_map, None, T, k, d, dx)),
+        ]
+
+    calls = step_calls(*inputs())
+    launches_per_step = sum(c[1] for c in calls)
+    for _ in range(args.warmup):
+        for _, _, fn in calls:
+            fn()
+    torch.cuda.synchronize()
+    assert status.item() == 0, f"device status {status.item()}"
+
+    # ---- timed region: K steps, events between the calls on the launching stream
+    nc = len(calls)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nc + 1)] for _ in range(args.steps)]
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for s in range(args.steps):
+        ev = evs[s]
+        for i, (_, _, fn) in enumerate(calls):
+            ev[i].record(stream)
+            fn()
+        ev[nc].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    elapsed_ms = t_start.elapsed_time(t_end)
+    if world > 1:
+        tt = torch.tensor([elapsed_ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        elapsed_ms = float(tt.item())
+    per_call = {}
+    for i, (name, _, _) in enumerate(calls):
+        per_call[name] = statistics.mean(evs[s][i].elapsed_time(evs[s][i + 1]) for s in range(args.steps))
+    assert status.item() == 0, f"device status {status.item()}"
+
+    M = int(offsets[-1].item())
+    ms_step = elapsed_ms / args.steps
+    fwdbwd_flops = 18.0 * M * d * h
+    value = world * fwdbwd_flops / (ms_step * 1e-3) / 1e12
+    peaks, peak_src = load_peaks()
+    peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    peak_hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    mdh = float(M) * d * h
+    algo_flops = {"up_swiglu": 4 * mdh, "down": 2 * mdh, "down_dgrad_swiglu": 2 * mdh, "up_dgrad": 4 * mdh,
+                  "wgrad_down": 2 * mdh, "wgrad_up": 4 * mdh}
+    gemm_ms = {kname: per_call[kname] for kname in algo_flops}
+    dom = max(gemm_ms, key=gemm_ms.get)
+    achieved = algo_flops[dom] / (gemm_ms[dom] * 1e-3) / 1e12
+    traffic = load_traffic().get(dom)
+    fwd_ms = per_call["up_swiglu"] + per_call["down"]
+    breakdown = {kname: {"ms": round(v, 4)} for kname, v in per_call.items()}
+    for kname, fl in algo_flops.items():
+        breakdown[kname]["tflops"] = round(fl / (per_call[kname] * 1e-3) / 1e12, 1)
+        breakdown[kname]["frac_of_sustained_peak"] = round(fl / (per_call[kname] * 1e-3) / 1e12 / peak_sus, 3)
+    # algorithmic bytes: token rows read once (x and dOut fit in L2), expert rows written/read once
+    hbm_bytes = {"permute": M * d * 2 + T * d * 2 + M * 4, "combine": M * d * 2 + T * d * 2 + T * k * 4,
+                 "combine_bwd": M * d * 2 + T * d * 2 + M * 4, "permute_bwd": M * d * 2 + T * d * 2 + T * k * 4}
+    for kname, b in hbm_bytes.items():
+        breakdown[kname]["gbs"] = round(b / (per_call[kname] * 1e-3) / 1e9, 1)
+        breakdown[kname]["frac_of_hbm_peak"] = round(b / (per_call[kname] * 1e-3) / 1e9 / peak_hbm, 3)
+
+    # ---- end to end through the public calls with host buffers (pinned), copies inside
+    xh, doh = x_h.pin_memory(), dout_h.pin_memory()
+    idh, wh = ids_h.pin_memory(), wts_h.pin_memory()
+    out_h = torch.empty(T, d, dtype=bf).pin_memory()
+    dx_h = torch.empty(T, d, dtype=bf).pin_memory()
+    x2, do2 = torch.empty_like(x), torch.empty_like(dout)
+    id2, w2 = torch.empty_like(ids), torch.empty_like(wts)
+    calls2 = step_calls(x2, id2, w2, do2)
+
+    def e2e_step():
+        x2.copy_(xh, non_blocking=True)
+        id2.copy_(idh, non_blocking=True)
+        w2.copy_(wh, non_blocking=True)
+        do2.copy_(doh, non_blocking=True)
+        for _, _, fn in calls2:
+            fn()
+        out_h.copy_(out, non_blocking=True)
+        dx_h.copy_(dx, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e_steps = max(10, args.steps // 4)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e_steps
+    h2d = x_h.numel() * 2 + dout_h.numel() * 2 + ids_h.numel() * 4 + wts_h.numel() * 4
+    d2h = 2 * T * d * 2
+    if world > 1:
+        tt = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+
+    # ---- forward comparison variants (same kernels): padded BMM at ceil(1.25 M/E), host loop
+    variants = None
+    if not args.no_variants:
+        C = -(-(5 * M) // (4 * E))
+        bmm_ws = torch.empty(L.moe_workspace_bytes(L.OP_PADDED_BMM, T, k, E, d, h, C), dtype=torch.uint8, device=dev)
+        y2 = torch.empty_like(y)
+
+        def time_fn(fn, reps=10):
+            for _ in range(2):
+                fn()
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            b0.record(stream)
+            for _ in range(reps):
+                fn()
+            b1.record(stream)
+            torch.cuda.synchronize()
+            return b0.elapsed_time(b1) / reps, (time.perf_counter() - t0) * 1e3 / reps
+
+        g_ms, _ = time_fn(lambda: L.moe_grouped_swiglu_fwd(xp, offsets, None, None, E, n, d, h, w_ug, w_down, y2,
+                                                           a, None, None, status))
+        b_ms, _ = time_fn(lambda: L.moe_padded_bmm_swiglu_fwd(xp, offsets, E, n, d, h, C, w_ug, w_down, y2, bmm_ws,
+                                                              status))
+        l_dev, l_wall = time_fn(lambda: L.moe_loop_swiglu_fwd(xp, offsets, E, n, d, h, w_ug, w_down, y2, a, None,
+                                                              status), reps=5)
+        fw = 6.0 * mdh
+        variants = {"grouped_fwd": {"ms": g_ms, "tflops": fw / (g_ms * 1e-3) / 1e12},
+                    "padded_bmm_fwd": {"ms": b_ms, "tflops": fw / (b_ms * 1e-3) / 1e12, "C": C,
+                                       "rows_multiplied": E * C, "rho_pad": 1 - M / (E * C)},
+                    "host_loop_fwd": {"ms": l_wall, "tflops": fw / (l_wall * 1e-3) / 1e12,
+                                      "note": "wall time incl. the D2H count copy and host wait"}}
+        del bmm_ws, y2
+        torch.cuda.synchronize()
+        assert status.item() == 0, f"device status {status.item()}"
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded; random-init weights)",
+        "config": workload_config(wl),
+        "fwd": {"ms": fwd_ms, "tflops": 6.0 * mdh / (fwd_ms * 1e-3) / 1e12,
+                "frac_of_sustained_peak": 6.0 * mdh / (fwd_ms * 1e-3) / 1e12 / peak_sus},
+        "roofline": {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peak_sus,
+                     "unit": "TFLOP/s", "frac": achieved / peak_sus, "traffic": traffic,
+                     "peak_source": f"bf16_tflops_sustained ({peak_src})"},
+        "e2e": {"value": world * fwdbwd_flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+        "breakdown": breakdown,
+        "variants": variants,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        flops, el, desc = OracleSampler(wl).run(12.0)
+        line["cpu_baseline"] = {"value": flops / el / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(),
+                                "kind": "oracle", "sample": desc}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

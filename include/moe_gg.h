@@ -1,0 +1,261 @@
+/*
+ * moe_gg.h -- C ABI of the device-scheduled ragged grouped GEMM for one SwiGLU
+ * mixture-of-experts expert layer (GB300, sm_103a).
+ *
+ * The operation is the one of "Section 09: Grouped GEMM" (OLMo-core MoE report): routing turns
+ * an expert layer into a ragged batch of products whose row counts M_e live on the device; the
+ * counts are turned into cumulative int32 offsets on the device (Fig. 37), never copied to the
+ * host, and one grouped kernel computes only the routed rows (§9.3, §9.4). Each expert is the
+ * SwiGLU expert of Eq. 13:
+ *     U_e = X_e W_ug,e^T        X_e [M_e, d],  W_ug,e [2h, d]  (gate rows [0,h), up rows [h,2h))
+ *     Y_e = SwiGLU(U_e) W_down,e                W_down,e [h, d]
+ * with SwiGLU(U) = silu(U[:, :h]) * U[:, h:]. Backward follows Eq. 15 / Table 15.
+ *
+ * Conventions shared by every entry point:
+ *  - Every pointer is a DEVICE pointer owned by the caller, unless stated otherwise. The
+ *    library allocates no device memory; scratch comes from the caller's workspace `ws`
+ *    (size from moe_workspace_bytes()). Work is queued on `stream` (a cudaStream_t; NULL is the
+ *    legacy default stream) and the calls return without synchronising, except
+ *    moe_loop_swiglu_fwd, which by design copies the offsets to the host.
+ *  - bf16 tensors are passed as raw 16-bit patterns (moe_bf16), row-major and contiguous;
+ *    fp32 and int32 tensors likewise.
+ *  - Offsets are int32 inclusive segment ends of length E: expert e owns rows
+ *    [offsets[e-1], offsets[e]) (offsets[-1] = 0), M = offsets[E-1] ("Section 09", Fig. 37:
+ *    counts (1,4,3,2) give [1,5,8,10]). Rows p >= M of the row buffers are neither read for
+ *    results nor written (§9.4: unused capacity stays outside the final offset).
+ *  - Errors found on the host (null pointer, bad size, misalignment, small workspace) return a
+ *    status before anything is launched. Conditions found on the device set bits in the
+ *    optional `dev_status` word (atomic OR; the caller clears it and reads it when it chooses):
+ *    MOE_DEV_TIMEOUT when a bounded wait inside a kernel gave up (the kernel then stops early
+ *    instead of hanging), MOE_DEV_BAD_OFFSETS when offsets decrease or exceed the buffer rows
+ *    (the affected kernel then computes nothing).
+ *  - Limits: 1 <= E <= 1024, 1 <= top_k <= 32, d and h multiples of 8 (16-byte rows for TMA),
+ *    T*top_k < 2^31. Other shapes return MOE_ERR_UNSUPPORTED_SHAPE. GEMM operand pointers must
+ *    be 16-byte aligned.
+ */
+#ifndef MOE_GG_H
+#define MOE_GG_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t moe_bf16;                 /* raw bfloat16 bits */
+typedef struct CUstream_st* moe_stream_t;  /* identical to cudaStream_t */
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,          /* null pointer, negative size, misaligned pointer */
+  MOE_ERR_UNSUPPORTED_SHAPE = 2,    /* shape outside the limits above */
+  MOE_ERR_WORKSPACE_TOO_SMALL = 3,  /* ws_bytes < moe_workspace_bytes(...) */
+  MOE_ERR_CUDA = 4,                 /* a CUDA runtime/driver call failed (see moe_last_cuda_error) */
+  MOE_ERR_DEVICE_TIMEOUT = 5,       /* reserved for callers that map MOE_DEV_TIMEOUT to a status */
+  MOE_ERR_UNSUPPORTED_DEVICE = 6    /* current device is not sm_103 */
+} moe_status_t;
+
+/* bits of the device status word */
+#define MOE_DEV_TIMEOUT 0x1
+#define MOE_DEV_BAD_OFFSETS 0x2
+
+/* operations for moe_workspace_bytes */
+typedef enum {
+  MOE_OP_ROUTE = 0,       /* moe_route_offsets */
+  MOE_OP_FWD = 1,         /* moe_grouped_swiglu_fwd */
+  MOE_OP_BWD = 2,         /* moe_grouped_bwd */
+  MOE_OP_PADDED_BMM = 3,  /* moe_padded_bmm_swiglu_fwd (uses capacity_C) */
+  MOE_OP_LOOP = 4,        /* moe_loop_swiglu_fwd */
+  MOE_OP_SAVED = 5        /* size of the `saved` buffer the forward fills for the backward */
+} moe_op_t;
+
+/* Bytes of caller workspace that `op` needs for these sizes (0 when none). Pure host
+ * arithmetic; no CUDA call. Returns 0 for invalid sizes as well: validate with the call. */
+size_t moe_workspace_bytes(int op, int T, int top_k, int E, int d, int h, int capacity_C);
+
+/*
+ * moe_route_offsets -- route histogram, cumulative offsets, placement and inverse map.
+ * "Section 09: Grouped GEMM", Fig. 37 steps 1-2 and §9.3 (counts and inclusive int32 offsets
+ * computed on the device); "grouped_mm" agent doc (sort rows by expert into contiguous blocks
+ * after dropping ids outside [0, E); precomputed inverse map [N, top_k], sentinel-padded).
+ *
+ *  ids        [T*top_k] int32 expert id of each (token, slot), flat index t*top_k + j.
+ *             Ids outside [0, E) are dropped: not counted, inv_map entry -1.
+ *  counts     [E] out: rows routed to each expert.
+ *  offsets    [E] out: inclusive prefix sum of counts.
+ *  sorted_src [T*top_k] out: flat slot index placed at row p, for p < M; -1 for p >= M.
+ *             Inside a segment rows keep increasing flat-index order (stable).
+ *  inv_map    [T*top_k] out: row of each flat slot, -1 when dropped. inv_map[sorted_src[p]] = p.
+ *  ws         workspace of moe_workspace_bytes(MOE_OP_ROUTE, T, top_k, E, 0, 0, 0) bytes.
+ * Results are deterministic (no order-dependent atomics). T = 0 is allowed (counts = 0).
+ */
+moe_status_t moe_route_offsets(const int32_t* ids, int T, int top_k, int E, int32_t* counts,
+                               int32_t* offsets, int32_t* sorted_src, int32_t* inv_map,
+                               void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * moe_permute -- gather token rows into expert-contiguous order (the forward gather x[idx] of
+ * the "grouped_mm" agent doc); with row_scale it is also the combine's backward
+ * (dY[p] = w[src] * dOut[src / top_k], Eq. 15 applied to the weighted sum).
+ *
+ *  x          [T, d] bf16 token rows.
+ *  sorted_src [T*top_k], offsets [E] as written by moe_route_offsets.
+ *  row_scale  nullable [T*top_k] fp32, indexed by flat slot; the product is rounded once.
+ *  xp         [T*top_k, d] bf16 out: row p < M = x[sorted_src[p] / top_k] (* scale).
+ */
+moe_status_t moe_permute(const moe_bf16* x, const int32_t* sorted_src, const int32_t* offsets,
+                         const float* row_scale, int T, int top_k, int E, int d, moe_bf16* xp,
+                         moe_stream_t stream);
+
+/*
+ * moe_grouped_swiglu_fwd -- the device-scheduled grouped SwiGLU expert forward, Eq. 13.
+ * Two persistent tcgen05 kernels walk the device problem list built from `offsets`
+ * ("Section 09", Fig. 37 steps 3-4): (1) U = xp_e W_ug,e^T with SwiGLU fused into the
+ * epilogue, writing A = SwiGLU(U); (2) y_e = A_e W_down,e. bf16 operands, fp32 accumulation in
+ * tensor memory, bf16 results (one rounding each).
+ *
+ *  xp         [cap, d] bf16 rows in expert order (rows >= M ignored).
+ *  offsets    [E] int32 inclusive; M = offsets[E-1] must be <= cap (else MOE_DEV_BAD_OFFSETS).
+ *  sorted_src, weights  nullable pair: when weights ([T*top_k] fp32, by flat slot) is given,
+ *             row p of y is multiplied by weights[sorted_src[p]] in the down projection's fp32
+ *             epilogue, i.e. the routing weight is applied before the combine (which is then
+ *             called with weights = NULL) instead of inside it. The sum is linear, so the layer
+ *             output is the same; the backward then gathers dOut without a rounding product.
+ *  w_ug       [E, 2h, d] bf16;  w_down [E, h, d] bf16.
+ *  y          [cap, d] bf16 out (rows < M written).
+ *  a_save     [cap, h] bf16 out: bf16(A), the down projection's input.
+ *  saved      nullable, moe_workspace_bytes(MOE_OP_SAVED, T, top_k, ...) bytes for
+ *             cap = T*top_k: what the backward needs beyond a_save, written when non-NULL
+ *             (training): fp32 U [cap, 2h] at byte 0; P - bf16(P) (bf16 [cap, h]) at byte
+ *             S1 = round_up(cap*2h*4, 256); bf16(P) (bf16 [cap, h]) at byte
+ *             S1 + round_up(cap*h*2, 256), written only with weights. P = w*A with weights,
+ *             else A. Keeping U in fp32 and P as a bf16 high+low pair lets the wgrads contract
+ *             over long expert segments without bf16 rounding of saved activations dominating.
+ *  ws         moe_workspace_bytes(MOE_OP_FWD, ...) bytes (currently 0; may be NULL then).
+ */
+moe_status_t moe_grouped_swiglu_fwd(const moe_bf16* xp, const int32_t* offsets,
+                                    const int32_t* sorted_src, const float* weights, int E,
+                                    int cap, int d, int h, const moe_bf16* w_ug,
+                                    const moe_bf16* w_down, moe_bf16* y, moe_bf16* a_save,
+                                    void* saved, void* ws, size_t ws_bytes, int32_t* dev_status,
+                                    moe_stream_t stream);
+
+/*
+ * moe_grouped_bwd -- dgrad and wgrad of the SwiGLU expert, Eq. 15 and Table 15 ("Section 09"
+ * §9.5): M_e is the output-row count of the dgrads and the contraction length of the wgrads.
+ *   dA = w * (dy_e W_down,e^T);  dU = [dA*v*s*(1+g(1-s)), dA*silu(g)] with g,v = U[:, :h],
+ *   U[:, h:], s = sigmoid(g);  dxp_e = dU W_ug,e;  dW_ug,e = dU^T xp_e;  dW_down,e = P_e^T dy_e
+ * with w = weights[sorted_src[p]] and P = w*A when weights are given, else w = 1 and P = A.
+ * dU is computed in fp32 in the dgrad epilogue and kept as a bf16 high+low pair; dxp uses the
+ * high half, the wgrads contract both halves (two MMAs per K step) so that dW carries about
+ * 16 significant bits of the activations instead of 8.
+ *
+ *  dy      [cap, d] bf16 upstream gradient at the grouped-GEMM boundary: the gradient of y, or,
+ *          with weights, the plain gather of dOut (moe_permute with row_scale = NULL).
+ *  xp, a_save, saved, sorted_src, weights as given to the forward (saved required here).
+ *  dxp     [cap, d] bf16 out (rows < M).
+ *  dw_ug   [E, 2h, d] fp32 out;  dw_down [E, h, d] fp32 out. Experts with M_e = 0 get zeros.
+ *  ws      moe_workspace_bytes(MOE_OP_BWD, ...) bytes (holds dU high and low, 2 x [cap, 2h] bf16).
+ */
+moe_status_t moe_grouped_bwd(const moe_bf16* dy, const moe_bf16* xp, const moe_bf16* a_save,
+                             const void* saved, const int32_t* offsets, const int32_t* sorted_src,
+                             const float* weights, int E, int cap, int d, int h,
+                             const moe_bf16* w_ug, const moe_bf16* w_down, moe_bf16* dxp,
+                             float* dw_ug, float* dw_down, void* ws, size_t ws_bytes,
+                             int32_t* dev_status, moe_stream_t stream);
+
+/*
+ * The single kernels the two calls above are made of, one per step of the path, for callers
+ * that schedule (or time) the steps themselves. Same conventions and the same `saved` layout;
+ * sorted_src/weights as in moe_grouped_swiglu_fwd (nullable pair).
+ *
+ * moe_grouped_up_swiglu  -- U = xp_e W_ug,e^T and A = SwiGLU(U) (Eq. 13, first line); writes
+ *                           a_save and, when saved is non-NULL, U and the halves of P.
+ * moe_grouped_down       -- y_e = (w *) A_e W_down,e (Eq. 13, second line); a [cap, h] bf16.
+ * moe_grouped_down_dgrad_swiglu -- dA = (w *) dy_e W_down,e^T (Eq. 15 dgrad of the down
+ *                           projection) with the SwiGLU backward fused: writes dU = [dgate, dup]
+ *                           as bf16 high (du_hi) and low (du_lo) halves, each [cap, 2h].
+ * moe_grouped_up_dgrad   -- dxp_e = dU_e W_ug,e (Eq. 15 dgrad of the up/gate projection).
+ * moe_grouped_wgrad      -- dW_e = P_e^T Q_e over each expert's M_e rows (Eq. 15 wgrad;
+ *                           Table 15: M_e is the contraction length). P = p_hi (+ p_lo when
+ *                           non-NULL: both halves are contracted, ~16-bit activations) is
+ *                           [cap, p_cols] bf16, Q [cap, q_cols] bf16, dW [E, p_cols, q_cols]
+ *                           fp32; experts with M_e = 0 get zeros. For dW_down: P = the saved
+ *                           halves of w*A (or a_save and the low half), Q = dy; for dW_ug:
+ *                           P = dU halves, Q = xp. p_cols and q_cols multiples of 8.
+ */
+moe_status_t moe_grouped_up_swiglu(const moe_bf16* xp, const int32_t* offsets,
+                                   const int32_t* sorted_src, const float* weights, int E, int cap,
+                                   int d, int h, const moe_bf16* w_ug, moe_bf16* a_save,
+                                   void* saved, int32_t* dev_status, moe_stream_t stream);
+moe_status_t moe_grouped_down(const moe_bf16* a, const int32_t* offsets, const int32_t* sorted_src,
+                              const float* weights, int E, int cap, int d, int h,
+                              const moe_bf16* w_down, moe_bf16* y, int32_t* dev_status,
+                              moe_stream_t stream);
+moe_status_t moe_grouped_down_dgrad_swiglu(const moe_bf16* dy, const void* saved,
+                                           const int32_t* offsets, const int32_t* sorted_src,
+                                           const float* weights, int E, int cap, int d, int h,
+                                           const moe_bf16* w_down, moe_bf16* du_hi,
+                                           moe_bf16* du_lo, int32_t* dev_status,
+                                           moe_stream_t stream);
+moe_status_t moe_grouped_up_dgrad(const moe_bf16* du_hi, const int32_t* offsets, int E, int cap,
+                                  int d, int h, const moe_bf16* w_ug, moe_bf16* dxp,
+                                  int32_t* dev_status, moe_stream_t stream);
+moe_status_t moe_grouped_wgrad(const moe_bf16* p_hi, const moe_bf16* p_lo, int p_cols,
+                               const moe_bf16* q, int q_cols, const int32_t* offsets, int E,
+                               int cap, float* dw, int32_t* dev_status, moe_stream_t stream);
+
+/*
+ * moe_unpermute_combine -- atomic-free weighted combine through the inverse map ("grouped_mm"
+ * agent doc: the scatter-back becomes a gather plus a reduction):
+ *     out[t] = sum_{j : inv_map[t*top_k+j] >= 0} w[t,j] * y[inv_map[t*top_k+j]]
+ * accumulated in fp32 in slot order j, rounded once to bf16. weights NULL means all ones (then
+ * it is the permute's backward, dx[t] = sum_j dxp[inv[t,j]]).
+ *
+ *  y [rows, d] bf16 (rows read: those inv_map names);  inv_map [T*top_k];  weights [T*top_k]
+ *  fp32 or NULL;  out [T, d] bf16. Tokens whose slots are all dropped get zeros.
+ */
+moe_status_t moe_unpermute_combine(const moe_bf16* y, const int32_t* inv_map, const float* weights,
+                                   int T, int top_k, int d, moe_bf16* out, moe_stream_t stream);
+
+/*
+ * moe_padded_bmm_swiglu_fwd -- comparison variant: capacity-padded batched GEMM ("Section 09",
+ * Eq. 14 and Fig. 35). Every expert is padded to capacity_C rows ([E, C, d], zero rows added),
+ * the same tcgen05 kernels run the E uniform problems (all E*C rows are multiplied), and the
+ * first min(M_e, C) rows of each expert are copied back; rows beyond C are dropped and get a
+ * zero output row. Arguments as moe_grouped_swiglu_fwd; ws holds the padded buffers
+ * (moe_workspace_bytes(MOE_OP_PADDED_BMM, ..., capacity_C)).
+ */
+moe_status_t moe_padded_bmm_swiglu_fwd(const moe_bf16* xp, const int32_t* offsets, int E, int cap,
+                                       int d, int h, int capacity_C, const moe_bf16* w_ug,
+                                       const moe_bf16* w_down, moe_bf16* y, void* ws,
+                                       size_t ws_bytes, int32_t* dev_status, moe_stream_t stream);
+
+/*
+ * moe_loop_swiglu_fwd -- comparison variant: host-scheduled per-expert loop ("Section 09",
+ * Fig. 36: the counts are copied to the host, the CPU waits, then one GEMM launch per expert
+ * and projection). Copies `offsets` to the host and synchronises `stream` BY DESIGN; then
+ * launches the same tcgen05 kernels once per non-empty expert. Arguments and results as
+ * moe_grouped_swiglu_fwd (saved nullable, a_save required). Offsets that decrease or exceed
+ * cap return MOE_ERR_INVALID_ARG (they are host-visible here).
+ */
+moe_status_t moe_loop_swiglu_fwd(const moe_bf16* xp, const int32_t* offsets, int E, int cap,
+                                 int d, int h, const moe_bf16* w_ug, const moe_bf16* w_down,
+                                 moe_bf16* y, moe_bf16* a_save, void* saved,
+                                 int32_t* dev_status, moe_stream_t stream);
+
+/* Human-readable text of a status (static storage). */
+const char* moe_status_string(moe_status_t status);
+
+/* Text of the last CUDA error seen by this thread inside the library (static per thread). */
+const char* moe_last_cuda_error(void);
+
+/* Version of this ABI (incremented on incompatible change). */
+int moe_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GG_H */

@@ -1,0 +1,204 @@
+"""ctypes binding of libmoe_gg.so (declared in include/moe_gg.h).
+
+Argument marshalling only: each function takes torch tensors (or None for nullable pointers),
+passes their device pointers and the current CUDA stream to the C entry point of the same name,
+and raises MoEError on a non-OK status. Every step runs in the library's CUDA kernels; there is
+no fallback of any kind, and loading fails loudly when the library has not been built.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmoe_gg.so")
+HEADER = os.path.join(os.path.dirname(_HERE), "include", "moe_gg.h")
+
+MOE_OK = 0
+STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED_SHAPE",
+          3: "MOE_ERR_WORKSPACE_TOO_SMALL", 4: "MOE_ERR_CUDA", 5: "MOE_ERR_DEVICE_TIMEOUT",
+          6: "MOE_ERR_UNSUPPORTED_DEVICE"}
+MOE_DEV_TIMEOUT = 0x1
+MOE_DEV_BAD_OFFSETS = 0x2
+OP_ROUTE, OP_FWD, OP_BWD, OP_PADDED_BMM, OP_LOOP, OP_SAVED = range(6)
+
+_P, _I, _S = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+SIGNATURES = {
+    "moe_workspace_bytes": (_S, [_I, _I, _I, _I, _I, _I, _I]),
+    "moe_route_offsets": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P, _S, _P]),
+    "moe_permute": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P]),
+    "moe_grouped_swiglu_fwd": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _S, _P, _P]),
+    "moe_grouped_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _S, _P, _P]),
+    "moe_unpermute_combine": (_I, [_P, _P, _P, _I, _I, _I, _P, _P]),
+    "moe_padded_bmm_swiglu_fwd": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _S, _P, _P]),
+    "moe_loop_swiglu_fwd": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P]),
+    "moe_grouped_up_swiglu": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P]),
+    "moe_grouped_down": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P]),
+    "moe_grouped_down_dgrad_swiglu": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P]),
+    "moe_grouped_up_dgrad": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P]),
+    "moe_grouped_wgrad": (_I, [_P, _P, _I, _P, _I, _P, _I, _I, _P, _P, _P]),
+    "moe_status_string": (ctypes.c_char_p, [_I]),
+    "moe_last_cuda_error": (ctypes.c_char_p, []),
+    "moe_abi_version": (_I, []),
+}
+
+_lib = None
+
+
+class MoEError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        detail = ""
+        if status == 4 and _lib is not None:
+            detail = ": " + _lib.moe_last_cuda_error().decode()
+        super().__init__(f"{fn} returned {STATUS.get(status, status)}{detail}")
+
+
+def header_functions(path: str = HEADER):
+    """Names of the functions include/moe_gg.h declares."""
+    with open(path) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", text)))
+
+
+def load(path: str = LIB_PATH):
+    """Load the library (once) and declare every entry point's C signature."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is not built: run __graft_entry__.build() (nvcc, sm_103a)")
+        lib = ctypes.CDLL(path)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError("tensors passed to the library must be contiguous CUDA tensors")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(fn: str, status: int):
+    if status != MOE_OK:
+        raise MoEError(fn, status)
+
+
+def moe_workspace_bytes(op: int, T: int, top_k: int, E: int, d: int = 0, h: int = 0, capacity_C: int = 0) -> int:
+    return int(load().moe_workspace_bytes(op, T, top_k, E, d, h, capacity_C))
+
+
+def moe_route_offsets(ids, T, top_k, E, counts, offsets, sorted_src, inv_map, ws, stream=None):
+    L = load()
+    ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
+    _check("moe_route_offsets", L.moe_route_offsets(_ptr(ids), T, top_k, E, _ptr(counts), _ptr(offsets),
+                                                    _ptr(sorted_src), _ptr(inv_map), _ptr(ws), ws_bytes,
+                                                    _stream(stream)))
+
+
+def moe_permute(x, sorted_src, offsets, row_scale, T, top_k, E, d, xp, stream=None):
+    _check("moe_permute", load().moe_permute(_ptr(x), _ptr(sorted_src), _ptr(offsets), _ptr(row_scale),
+                                             T, top_k, E, d, _ptr(xp), _stream(stream)))
+
+
+def moe_grouped_swiglu_fwd(xp, offsets, sorted_src, weights, E, cap, d, h, w_ug, w_down, y, a_save,
+                           saved=None, ws=None, dev_status=None, stream=None):
+    ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
+    _check("moe_grouped_swiglu_fwd", load().moe_grouped_swiglu_fwd(
+        _ptr(xp), _ptr(offsets), _ptr(sorted_src), _ptr(weights), E, cap, d, h, _ptr(w_ug), _ptr(w_down),
+        _ptr(y), _ptr(a_save), _ptr(saved), _ptr(ws), ws_bytes, _ptr(dev_status), _stream(stream)))
+
+
+def moe_grouped_bwd(dy, xp, a_save, saved, offsets, sorted_src, weights, E, cap, d, h, w_ug, w_down, dxp,
+                    dw_ug, dw_down, ws, dev_status=None, stream=None):
+    ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
+    _check("moe_grouped_bwd", load().moe_grouped_bwd(
+        _ptr(dy), _ptr(xp), _ptr(a_save), _ptr(saved), _ptr(offsets), _ptr(sorted_src), _ptr(weights), E,
+        cap, d, h, _ptr(w_ug),
+        _ptr(w_down), _ptr(dxp), _ptr(dw_ug), _ptr(dw_down), _ptr(ws), ws_bytes, _ptr(dev_status),
+        _stream(stream)))
+
+
+def moe_grouped_up_swiglu(xp, offsets, sorted_src, weights, E, cap, d, h, w_ug, a_save, saved=None,
+                          dev_status=None, stream=None):
+    _check("moe_grouped_up_swiglu", load().moe_grouped_up_swiglu(
+        _ptr(xp), _ptr(offsets), _ptr(sorted_src), _ptr(weights), E, cap, d, h, _ptr(w_ug), _ptr(a_save),
+        _ptr(saved), _ptr(dev_status), _stream(stream)))
+
+
+def moe_grouped_down(a, offsets, sorted_src, weights, E, cap, d, h, w_down, y, dev_status=None, stream=None):
+    _check("moe_grouped_down", load().moe_grouped_down(
+        _ptr(a), _ptr(offsets), _ptr(sorted_src), _ptr(weights), E, cap, d, h, _ptr(w_down), _ptr(y),
+        _ptr(dev_status), _stream(stream)))
+
+
+def moe_grouped_down_dgrad_swiglu(dy, saved, offsets, sorted_src, weights, E, cap, d, h, w_down, du_hi, du_lo,
+                                  dev_status=None, stream=None):
+    _check("moe_grouped_down_dgrad_swiglu", load().moe_grouped_down_dgrad_swiglu(
+        _ptr(dy), _ptr(saved), _ptr(offsets), _ptr(sorted_src), _ptr(weights), E, cap, d, h, _ptr(w_down),
+        _ptr(du_hi), _ptr(du_lo), _ptr(dev_status), _stream(stream)))
+
+
+def moe_grouped_up_dgrad(du_hi, offsets, E, cap, d, h, w_ug, dxp, dev_status=None, stream=None):
+    _check("moe_grouped_up_dgrad", load().moe_grouped_up_dgrad(
+        _ptr(du_hi), _ptr(offsets), E, cap, d, h, _ptr(w_ug), _ptr(dxp), _ptr(dev_status), _stream(stream)))
+
+
+def moe_grouped_wgrad(p_hi, p_lo, p_cols, q, q_cols, offsets, E, cap, dw, dev_status=None, stream=None):
+    _check("moe_grouped_wgrad", load().moe_grouped_wgrad(
+        _ptr(p_hi), _ptr(p_lo), p_cols, _ptr(q), q_cols, _ptr(offsets), E, cap, _ptr(dw), _ptr(dev_status),
+        _stream(stream)))
+
+
+def saved_views(saved, cap, h):
+    """The parts of the forward's `saved` buffer (uint8 tensor): fp32 U [cap, 2h], then the low
+    and the high halves of P (bf16 [cap, h] each; P = w*A with routing weights, else A, whose
+    high half is then a_save and this slot is unused)."""
+    import torch
+    r = lambda b: (b + 255) // 256 * 256
+    ub, pb = cap * 2 * h * 4, cap * h * 2
+    u = saved[:ub].view(torch.float32).view(cap, 2 * h)
+    p_lo = saved[r(ub):r(ub) + pb].view(torch.bfloat16).view(cap, h)
+    p_hi = saved[r(ub) + r(pb):r(ub) + r(pb) + pb].view(torch.bfloat16).view(cap, h)
+    return u, p_lo, p_hi
+
+
+def moe_unpermute_combine(y, inv_map, weights, T, top_k, d, out, stream=None):
+    _check("moe_unpermute_combine", load().moe_unpermute_combine(
+        _ptr(y), _ptr(inv_map), _ptr(weights), T, top_k, d, _ptr(out), _stream(stream)))
+
+
+def moe_padded_bmm_swiglu_fwd(xp, offsets, E, cap, d, h, capacity_C, w_ug, w_down, y, ws,
+                              dev_status=None, stream=None):
+    ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
+    _check("moe_padded_bmm_swiglu_fwd", load().moe_padded_bmm_swiglu_fwd(
+        _ptr(xp), _ptr(offsets), E, cap, d, h, capacity_C, _ptr(w_ug), _ptr(w_down), _ptr(y), _ptr(ws),
+        ws_bytes, _ptr(dev_status), _stream(stream)))
+
+
+def moe_loop_swiglu_fwd(xp, offsets, E, cap, d, h, w_ug, w_down, y, a_save, saved=None, dev_status=None,
+                        stream=None):
+    _check("moe_loop_swiglu_fwd", load().moe_loop_swiglu_fwd(
+        _ptr(xp), _ptr(offsets), E, cap, d, h, _ptr(w_ug), _ptr(w_down), _ptr(y), _ptr(a_save),
+        _ptr(saved), _ptr(dev_status), _stream(stream)))
+
+
+def moe_status_string(status: int) -> str:
+    return load().moe_status_string(status).decode()
+
+
+def moe_abi_version() -> int:
+    return int(load().moe_abi_version())

@@ -1,0 +1,639 @@
+// Persistent, device-scheduled grouped GEMM on the 5th-generation tensor cores (sm_103a).
+//
+// "Section 09: Grouped GEMM" (Fig. 37): the cumulative expert offsets stay on the GPU, a
+// preparation step derives the problem list, and one grouped kernel schedules tiles across it.
+// Here the preparation is the kernel's own prologue: every CTA reads the E offsets into shared
+// memory, derives each expert's row segment and 128-row tile count, and prefix-sums the tile
+// counts; a tile index then maps to (expert, row block, column block) by binary search. The
+// grid is one CTA per SM; CTA c takes tiles c, c + grid, ... ("thread blocks take tiles in
+// turn"). The host never learns M.
+//
+// Roles (192 threads, warp-specialised):
+//   warp 0      TMA producer: 128B-swizzled operand tiles into a 4-stage shared-memory ring.
+//   warp 1      tensor-memory allocator and MMA issuer: tcgen05.mma 128x256x16 (bf16 in, fp32
+//               accumulate) into one of two 256-column TMEM accumulators, so the epilogue of a
+//               tile overlaps the main loop of the next.
+//   warps 2..5  epilogue: tcgen05.ld of the accumulator, fused SwiGLU (forward or backward),
+//               conversion and row/column-masked stores. A tile that runs past its expert's
+//               segment still multiplies the neighbouring rows (rows of a product are
+//               independent) but never stores them.
+// The wgrad mode contracts over the M_e rows of an expert (Table 15): its operands are
+// MN-major and the rows of the last K block that belong to the next expert are zeroed in
+// shared memory before the MMA reads them. Its A operand comes as a bf16 high/low pair (the
+// activation and its rounding remainder); both halves are multiplied with the same B tile
+// into one fp32 accumulator, which keeps about 16 significant bits of the activations in the
+// weight gradient.
+#include <algorithm>
+#include <cstdio>
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int BM = 128;          // UMMA M: accumulator rows = TMEM lanes
+constexpr int BN = 256;          // UMMA N: accumulator columns
+constexpr int BK = 64;           // one 128-byte swizzle atom of bf16 along K
+constexpr int UK = 16;           // K of one tcgen05.mma kind::f16
+constexpr int STAGES = 4;                     // ring depth of the row-grouped modes
+constexpr int A_BYTES = BM * BK * 2;          // 16 KB
+constexpr int B_BYTES = BN * BK * 2;          // 32 KB
+constexpr int RING_BYTES = STAGES * (A_BYTES + B_BYTES);  // 192 KB, shared by every mode
+constexpr int ATOM_BYTES = 64 * BK * 2;       // one MN-major 64x64 box: 8 KB
+constexpr int THREADS = 192;
+constexpr int TMEM_COLS = 512;                // two 256-column accumulators
+constexpr int MAX_E = 1024;
+constexpr int CTL_BYTES = 256;
+
+struct Ctl {
+  uint64_t full[STAGES];
+  uint64_t empty[STAGES];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t done;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+static_assert(sizeof(Ctl) <= CTL_BYTES, "control block too large");
+
+constexpr size_t smem_bytes_for(int E) {
+  return 1024 + static_cast<size_t>(RING_BYTES) + CTL_BYTES +
+         2 * sizeof(int) * static_cast<size_t>(E + 2);
+}
+
+template <int MODE>
+struct ModeTraits {
+  static constexpr bool wgrad = (MODE == MODE_WGRAD || MODE == MODE_WGRAD_BF16);
+  static constexpr bool a_mn = wgrad;
+  static constexpr bool b_mn = (MODE == MODE_PLAIN_BF16 || wgrad);
+  static constexpr int out_cols_per_tile = (MODE == MODE_UP_SWIGLU) ? 128 : BN;
+  // MODE_WGRAD stages hold A high, A low and B: 64 KB, three of them; the others 48 KB, four
+  static constexpr int a_parts = (MODE == MODE_WGRAD) ? 2 : 1;
+  static constexpr int stage_bytes = a_parts * A_BYTES + B_BYTES;
+  static constexpr int stages = RING_BYTES / stage_bytes;
+};
+
+struct Tile {
+  int e;        // expert index within the problem list
+  int row0;     // first row of the tile (row-grouped) or of the expert segment (wgrad)
+  int rows;     // valid rows of the tile (row-grouped)
+  int m0;       // wgrad: first output row
+  int n0;       // first output column
+  int kblocks;  // K blocks of 64
+  int kvalid;   // wgrad: contraction length M_e
+};
+
+struct Sched {
+  const int* offs;  // offs[e] = first row of expert e, offs[E] = end (E+1 entries)
+  const int* pre;   // row-grouped: prefix of 128-row tiles, E+1 entries
+  int E;
+  int nt;           // column tiles per problem
+  int mt;           // wgrad: row tiles per expert gradient
+  int kblocks;      // row-grouped: K blocks
+  int total;
+};
+
+template <int MODE>
+__device__ __forceinline__ Tile decode_tile(const Sched& s, int t) {
+  Tile ti;
+  if constexpr (ModeTraits<MODE>::wgrad) {
+    const int per = s.mt * s.nt;
+    ti.e = t / per;
+    const int r = t - ti.e * per;
+    const int mi = r / s.nt;
+    ti.m0 = mi * BM;
+    ti.n0 = (r - mi * s.nt) * BN;
+    ti.row0 = s.offs[ti.e];
+    ti.kvalid = s.offs[ti.e + 1] - ti.row0;
+    ti.kblocks = (ti.kvalid + BK - 1) / BK;
+    ti.rows = 0;
+  } else {
+    const int g = t / s.nt;
+    const int n = t - g * s.nt;
+    // largest e with pre[e] <= g (experts without tiles have pre[e] == pre[e+1])
+    int lo = 0, hi = s.E;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (s.pre[mid] <= g) lo = mid; else hi = mid;
+    }
+    ti.e = lo;
+    const int mloc = g - s.pre[lo];
+    ti.row0 = s.offs[lo] + mloc * BM;
+    ti.rows = min(BM, s.offs[lo + 1] - ti.row0);
+    ti.n0 = n * ModeTraits<MODE>::out_cols_per_tile;
+    ti.m0 = 0;
+    ti.kblocks = s.kblocks;
+    ti.kvalid = 0;
+  }
+  return ti;
+}
+
+__device__ __forceinline__ bool warp_all(bool v) { return __all_sync(0xffffffffu, v); }
+
+__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
+
+__device__ __forceinline__ void st_global_v4(void* p, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+  *reinterpret_cast<uint4*>(p) = make_uint4(a, b, c, d);
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(THREADS, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
+                        const __grid_constant__ CUtensorMap map_a_lo,
+                        const __grid_constant__ CUtensorMap map_b, const GemmArgs args) {
+  constexpr int NST = ModeTraits<MODE>::stages;
+  constexpr int SB = ModeTraits<MODE>::stage_bytes;
+  constexpr int APARTS = ModeTraits<MODE>::a_parts;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* stages = smem;
+  Ctl* ctl = reinterpret_cast<Ctl*>(smem + RING_BYTES);
+  int* offs = reinterpret_cast<int*>(smem + RING_BYTES + CTL_BYTES);
+  const int E = args.E;
+  int* pre = offs + (E + 1);
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+
+  // ---- problem list: row segments of the experts (the preparation step, in-kernel)
+  const bool single = args.single_expert >= 0;
+  const int expert_base = single ? args.single_expert : 0;
+  for (int i = tid; i <= E; i += THREADS) {
+    int v;
+    if (single) v = args.single_row0 + (i > 0 ? args.single_rows : 0);
+    else if (args.uniform_rows > 0) v = i * args.uniform_rows;
+    else v = (i == 0) ? 0 : __ldg(args.offsets + i - 1);
+    offs[i] = v;
+  }
+  __syncthreads();
+  bool bad = false;
+  for (int i = tid; i < E; i += THREADS) bad |= (offs[i + 1] < offs[i]) || (offs[i] < 0);
+  if (tid == 0) bad |= offs[E] > args.cap;
+  if (__syncthreads_or(bad)) {
+    if (tid == 0 && blockIdx.x == 0) record_status(args.status, MOE_DEV_BAD_OFFSETS);
+    return;  // uniform across the CTA, before any barrier or tensor memory exists
+  }
+
+  Sched sc;
+  sc.offs = offs;
+  sc.pre = pre;
+  sc.E = E;
+  if constexpr (ModeTraits<MODE>::wgrad) {
+    sc.mt = (args.Mdim + BM - 1) / BM;
+    sc.nt = (args.N + BN - 1) / BN;
+    sc.kblocks = 0;
+    sc.total = E * sc.mt * sc.nt;
+  } else {
+    sc.mt = 0;
+    sc.nt = (args.N + ModeTraits<MODE>::out_cols_per_tile - 1) / ModeTraits<MODE>::out_cols_per_tile;
+    sc.kblocks = (args.K + BK - 1) / BK;
+    if (warp == 0) {
+      int carry = 0;
+      if (lane == 0) pre[0] = 0;
+      for (int base = 0; base < E; base += 32) {
+        const int e = base + lane;
+        int v = (e < E) ? (offs[e + 1] - offs[e] + BM - 1) / BM : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int nb = __shfl_up_sync(0xffffffffu, v, o);
+          if (lane >= o) v += nb;
+        }
+        if (e < E) pre[e + 1] = carry + v;
+        carry += __shfl_sync(0xffffffffu, v, 31);
+      }
+    }
+  }
+
+  // ---- barriers and tensor memory
+  if (tid == 0) {
+    for (int s = 0; s < NST; ++s) {
+      mbar_init(smem_u32(&ctl->full[s]), 1);
+      mbar_init(smem_u32(&ctl->empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&ctl->tfull[b]), 1);
+      mbar_init(smem_u32(&ctl->tempty[b]), 128);
+    }
+    mbar_init(smem_u32(&ctl->done), 1);
+    ctl->abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&map_a);
+    if (APARTS == 2) prefetch_tmap(&map_a_lo);
+    prefetch_tmap(&map_b);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&ctl->tmem_base), TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if constexpr (!ModeTraits<MODE>::wgrad) sc.total = pre[E] * sc.nt;
+  const uint32_t tmem_base = ctl->tmem_base;
+  volatile int* abort_flag = &ctl->abort_flag;
+  const long long tmo = args.timeout_ns;
+  int32_t* status = args.status;
+  const uint32_t stage0 = smem_u32(stages);
+
+  if (warp == 0) {
+    // =========================================================== TMA producer
+    if (lane == 0) {
+      uint32_t it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < sc.total && ok; t += gridDim.x) {
+        const Tile ti = decode_tile<MODE>(sc, t);
+        const int eg = ti.e + expert_base;
+        for (int kb = 0; kb < ti.kblocks; ++kb, ++it) {
+          const int s = it % NST;
+          const uint32_t ph = (it / NST) & 1u;
+          if (!mbar_wait(smem_u32(&ctl->empty[s]), ph ^ 1u, abort_flag, status, tmo)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = smem_u32(&ctl->full[s]);
+          mbar_arrive_expect_tx(fb, SB);
+          const uint32_t sa = stage0 + s * SB;
+          const uint32_t sb = sa + APARTS * A_BYTES;
+          const int k0 = kb * BK;
+          if constexpr (MODE == MODE_UP_SWIGLU) {
+            tma_load_2d(sa, &map_a, k0, ti.row0, fb);
+            tma_load_3d(sb, &map_b, k0, ti.n0, eg, fb);                    // gate rows
+            tma_load_3d(sb + B_BYTES / 2, &map_b, k0, args.h + ti.n0, eg, fb);  // up rows
+          } else if constexpr (MODE == MODE_PLAIN_BF16) {
+            tma_load_2d(sa, &map_a, k0, ti.row0, fb);
+#pragma unroll
+            for (int i = 0; i < BN / 64; ++i) tma_load_3d(sb + i * ATOM_BYTES, &map_b, ti.n0 + 64 * i, k0, eg, fb);
+          } else if constexpr (MODE == MODE_DGRAD_SWIGLU) {
+            tma_load_2d(sa, &map_a, k0, ti.row0, fb);
+            tma_load_3d(sb, &map_b, k0, ti.n0, eg, fb);
+          } else {
+            const int rk = ti.row0 + k0;
+#pragma unroll
+            for (int i = 0; i < BM / 64; ++i) tma_load_2d(sa + i * ATOM_BYTES, &map_a, ti.m0 + 64 * i, rk, fb);
+            if constexpr (APARTS == 2) {
+#pragma unroll
+              for (int i = 0; i < BM / 64; ++i)
+                tma_load_2d(sa + A_BYTES + i * ATOM_BYTES, &map_a_lo, ti.m0 + 64 * i, rk, fb);
+            }
+#pragma unroll
+            for (int i = 0; i < BN / 64; ++i) tma_load_2d(sb + i * ATOM_BYTES, &map_b, ti.n0 + 64 * i, rk, fb);
+          }
+        }
+      }
+      // drain: the copies issued into each stage must land before the CTA can exit
+      const uint32_t first = it > NST ? it - NST : 0u;
+      for (uint32_t j = first; j < it; ++j)
+        mbar_wait(smem_u32(&ctl->full[j % NST]), (j / NST) & 1u, abort_flag, status, tmo, false);
+    }
+  } else if (warp == 1) {
+    // =========================================================== MMA issuer
+    constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, ModeTraits<MODE>::a_mn, ModeTraits<MODE>::b_mn);
+    uint32_t it = 0, acc = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < sc.total && ok; t += gridDim.x) {
+      const Tile ti = decode_tile<MODE>(sc, t);
+      if (ti.kblocks == 0) continue;
+      const uint32_t buf = acc & 1u, use = acc >> 1;
+      ok = warp_all(mbar_wait(smem_u32(&ctl->tempty[buf]), (use & 1u) ^ 1u, abort_flag, status, tmo));
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t dtm = tmem_base + buf * BN;
+      for (int kb = 0; kb < ti.kblocks; ++kb, ++it) {
+        const int s = it % NST;
+        const uint32_t ph = (it / NST) & 1u;
+        ok = warp_all(mbar_wait(smem_u32(&ctl->full[s]), ph, abort_flag, status, tmo));
+        if (!ok) break;
+        tc_fence_after();
+        uint8_t* sp = stages + s * SB;
+        if constexpr (ModeTraits<MODE>::wgrad) {
+          const int valid = ti.kvalid - kb * BK;
+          if (valid < BK) {
+            // rows [valid, 64) of every 64x64 box belong to the next expert: zero them
+            const int nrows = BK - valid;
+            const int per_atom = nrows * 8;
+            const int total = SB / ATOM_BYTES * per_atom;
+            for (int c = lane; c < total; c += 32) {
+              const int atom = c / per_atom;
+              const int rem = c - atom * per_atom;
+              const int r = valid + (rem >> 3);
+              *reinterpret_cast<uint4*>(sp + atom * ATOM_BYTES + r * 128 + (rem & 7) * 16) =
+                  make_uint4(0u, 0u, 0u, 0u);
+            }
+            fence_proxy_async_smem();
+          }
+          __syncwarp();
+        }
+        if (lane == 0) {
+          const uint32_t sa = stage0 + s * SB;
+          const uint32_t sb = sa + APARTS * A_BYTES;
+#pragma unroll
+          for (int part = 0; part < APARTS; ++part) {
+#pragma unroll
+            for (int ks = 0; ks < BK / UK; ++ks) {
+              const uint32_t ap = sa + part * A_BYTES;
+              const uint64_t ad = ModeTraits<MODE>::a_mn
+                                      ? smem_desc_sw128(ap + ks * (UK * 128), ATOM_BYTES, 1024)
+                                      : smem_desc_sw128(ap + ks * (UK * 2), 16, 1024);
+              const uint64_t bd = ModeTraits<MODE>::b_mn
+                                      ? smem_desc_sw128(sb + ks * (UK * 128), ATOM_BYTES, 1024)
+                                      : smem_desc_sw128(sb + ks * (UK * 2), 16, 1024);
+              mma_bf16_ss(dtm, ad, bd, idesc, (kb | ks | part) != 0 ? 1u : 0u);
+            }
+          }
+          mma_commit(smem_u32(&ctl->empty[s]));
+        }
+        __syncwarp();
+      }
+      if (!ok) break;
+      if (lane == 0) mma_commit(smem_u32(&ctl->tfull[buf]));
+      __syncwarp();
+      ++acc;
+    }
+    // every MMA this thread issued must finish before tensor memory is released
+    if (lane == 0) mma_commit(smem_u32(&ctl->done));
+    __syncwarp();
+    mbar_wait(smem_u32(&ctl->done), 0u, abort_flag, status, tmo, false);
+  } else {
+    // =========================================================== epilogue (warps 2..5)
+    const int q = warp & 3;           // TMEM lane quadrant this warp may access
+    const int r_in = q * 32 + lane;   // accumulator row = TMEM lane
+    uint32_t acc = 0;
+    for (int t = blockIdx.x; t < sc.total; t += gridDim.x) {
+      const Tile ti = decode_tile<MODE>(sc, t);
+      if constexpr (ModeTraits<MODE>::wgrad) {
+        if (ti.kblocks == 0) {
+          // empty expert: its gradient is zero
+          const int mrow = ti.m0 + r_in;
+          if (mrow < args.Mdim) {
+            float* dst = reinterpret_cast<float*>(args.out) +
+                         (static_cast<long long>(ti.e + expert_base) * args.Mdim + mrow) * args.ldo;
+            for (int c = ti.n0; c < min(ti.n0 + BN, args.N); c += 4)
+              *reinterpret_cast<float4*>(dst + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+          continue;
+        }
+      }
+      const uint32_t buf = acc & 1u, use = acc >> 1;
+      if (!warp_all(mbar_wait(smem_u32(&ctl->tfull[buf]), use & 1u, abort_flag, status, tmo))) break;
+      tc_fence_after();
+      const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * BN;
+
+      if constexpr (MODE == MODE_UP_SWIGLU) {
+        const bool rv = r_in < ti.rows;
+        const long long row = ti.row0 + r_in;
+        const int h = args.h;
+        bf16* arow = reinterpret_cast<bf16*>(args.out) + row * args.ldo;
+        float* urow = args.out2 ? reinterpret_cast<float*>(args.out2) + row * args.ldo2 : nullptr;
+        bf16* lrow = args.out3 ? reinterpret_cast<bf16*>(args.out3) + row * args.ldo3 : nullptr;
+        // P = w*A (its high half in out4) when row weights are given, else P = A
+        const bool weighted = args.row_weight != nullptr;
+        bf16* prow = weighted && args.out4 ? reinterpret_cast<bf16*>(args.out4) + row * args.ldo3 : nullptr;
+        const float wrow = (weighted && rv) ? __ldg(args.row_weight + __ldg(args.row_src + row)) : 1.0f;
+#pragma unroll 1
+        for (int c = 0; c < 8; ++c) {
+          uint32_t g[16], u[16];
+          tmem_ld16(tb + c * 16, g);
+          tmem_ld16(tb + 128 + c * 16, u);
+          tmem_ld_wait2(g, u);
+          const int col = ti.n0 + c * 16;
+          if (rv && col < h) {
+            uint32_t pa[8], pl[8], ph[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const float a0 = silu_f(__uint_as_float(g[2 * j])) * __uint_as_float(u[2 * j]);
+              const float a1 = silu_f(__uint_as_float(g[2 * j + 1])) * __uint_as_float(u[2 * j + 1]);
+              pa[j] = pack_bf16x2(a0, a1);
+              const float p0 = wrow * a0, p1 = wrow * a1;
+              ph[j] = weighted ? pack_bf16x2(p0, p1) : pa[j];
+              pl[j] = pack_bf16x2(p0 - bf16_lo(ph[j]), p1 - bf16_hi(ph[j]));
+            }
+            const bool two = col + 16 <= h;
+            st_global_v4(arow + col, pa[0], pa[1], pa[2], pa[3]);
+            if (two) st_global_v4(arow + col + 8, pa[4], pa[5], pa[6], pa[7]);
+            if (lrow) {
+              st_global_v4(lrow + col, pl[0], pl[1], pl[2], pl[3]);
+              if (two) st_global_v4(lrow + col + 8, pl[4], pl[5], pl[6], pl[7]);
+            }
+            if (prow) {
+              st_global_v4(prow + col, ph[0], ph[1], ph[2], ph[3]);
+              if (two) st_global_v4(prow + col + 8, ph[4], ph[5], ph[6], ph[7]);
+            }
+            if (urow) {
+#pragma unroll
+              for (int q4 = 0; q4 < 4; ++q4) {
+                if (q4 < 2 || two) {
+                  st_global_v4(urow + col + 4 * q4, g[4 * q4], g[4 * q4 + 1], g[4 * q4 + 2], g[4 * q4 + 3]);
+                  st_global_v4(urow + h + col + 4 * q4, u[4 * q4], u[4 * q4 + 1], u[4 * q4 + 2], u[4 * q4 + 3]);
+                }
+              }
+            }
+          }
+        }
+      } else if constexpr (MODE == MODE_PLAIN_BF16) {
+        const bool rv = r_in < ti.rows;
+        const long long row = ti.row0 + r_in;
+        bf16* orow = reinterpret_cast<bf16*>(args.out) + row * args.ldo;
+        const float wrow =
+            (args.row_weight != nullptr && rv) ? __ldg(args.row_weight + __ldg(args.row_src + row)) : 1.0f;
+#pragma unroll 1
+        for (int c = 0; c < BN / 16; c += 2) {
+          uint32_t v0[16], v1[16];
+          tmem_ld16(tb + c * 16, v0);
+          tmem_ld16(tb + (c + 1) * 16, v1);
+          tmem_ld_wait2(v0, v1);
+          const int col = ti.n0 + c * 16;
+          if (rv) {
+            uint32_t p[16];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              p[j] = pack_bf16x2(wrow * __uint_as_float(v0[2 * j]), wrow * __uint_as_float(v0[2 * j + 1]));
+              p[8 + j] = pack_bf16x2(wrow * __uint_as_float(v1[2 * j]), wrow * __uint_as_float(v1[2 * j + 1]));
+            }
+#pragma unroll
+            for (int hq = 0; hq < 4; ++hq)
+              if (col + hq * 8 < args.N)
+                st_global_v4(orow + col + hq * 8, p[4 * hq], p[4 * hq + 1], p[4 * hq + 2], p[4 * hq + 3]);
+          }
+        }
+      } else if constexpr (MODE == MODE_DGRAD_SWIGLU) {
+        const bool rv = r_in < ti.rows;
+        const long long row = ti.row0 + r_in;
+        const int h = args.h;
+        bf16* hrow = reinterpret_cast<bf16*>(args.out) + row * args.ldo;
+        bf16* lrow = reinterpret_cast<bf16*>(args.out2) + row * args.ldo2;
+        const float* srow = reinterpret_cast<const float*>(args.aux) + row * args.ld_aux;
+        const float wrow =
+            (args.row_weight != nullptr && rv) ? __ldg(args.row_weight + __ldg(args.row_src + row)) : 1.0f;
+#pragma unroll 1
+        for (int c = 0; c < BN / 16; ++c) {
+          uint32_t v[16];
+          tmem_ld16(tb + c * 16, v);
+          tmem_ld_wait(v);
+          const int col = ti.n0 + c * 16;
+          if (rv && col < h) {
+            const bool two = col + 16 <= h;
+            float gv[16], uv[16];
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+              float4 gq = make_float4(0.f, 0.f, 0.f, 0.f), uq = gq;
+              if (q4 < 2 || two) {
+                gq = *reinterpret_cast<const float4*>(srow + col + 4 * q4);
+                uq = *reinterpret_cast<const float4*>(srow + h + col + 4 * q4);
+              }
+              gv[4 * q4] = gq.x; gv[4 * q4 + 1] = gq.y; gv[4 * q4 + 2] = gq.z; gv[4 * q4 + 3] = gq.w;
+              uv[4 * q4] = uq.x; uv[4 * q4 + 1] = uq.y; uv[4 * q4 + 2] = uq.z; uv[4 * q4 + 3] = uq.w;
+            }
+            uint32_t gh[8], gl[8], uh[8], ul[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              float dg[2], du[2];
+#pragma unroll
+              for (int hh = 0; hh < 2; ++hh) {
+                const float g = gv[2 * j + hh], uu = uv[2 * j + hh];
+                const float da = wrow * __uint_as_float(v[2 * j + hh]);
+                const float sg = 1.0f / (1.0f + __expf(-g));
+                dg[hh] = da * uu * sg * (1.0f + g * (1.0f - sg));
+                du[hh] = da * g * sg;
+              }
+              gh[j] = pack_bf16x2(dg[0], dg[1]);
+              uh[j] = pack_bf16x2(du[0], du[1]);
+              gl[j] = pack_bf16x2(dg[0] - bf16_lo(gh[j]), dg[1] - bf16_hi(gh[j]));
+              ul[j] = pack_bf16x2(du[0] - bf16_lo(uh[j]), du[1] - bf16_hi(uh[j]));
+            }
+            st_global_v4(hrow + col, gh[0], gh[1], gh[2], gh[3]);
+            st_global_v4(hrow + h + col, uh[0], uh[1], uh[2], uh[3]);
+            st_global_v4(lrow + col, gl[0], gl[1], gl[2], gl[3]);
+            st_global_v4(lrow + h + col, ul[0], ul[1], ul[2], ul[3]);
+            if (two) {
+              st_global_v4(hrow + col + 8, gh[4], gh[5], gh[6], gh[7]);
+              st_global_v4(hrow + h + col + 8, uh[4], uh[5], uh[6], uh[7]);
+              st_global_v4(lrow + col + 8, gl[4], gl[5], gl[6], gl[7]);
+              st_global_v4(lrow + h + col + 8, ul[4], ul[5], ul[6], ul[7]);
+            }
+          }
+        }
+      } else {  // wgrad modes
+        const int mrow = ti.m0 + r_in;
+        const bool rv = mrow < args.Mdim;
+        float* dst = reinterpret_cast<float*>(args.out) +
+                     (static_cast<long long>(ti.e + expert_base) * args.Mdim + mrow) * args.ldo;
+#pragma unroll 1
+        for (int c = 0; c < BN / 16; ++c) {
+          uint32_t v[16];
+          tmem_ld16(tb + c * 16, v);
+          tmem_ld_wait(v);
+          const int col = ti.n0 + c * 16;
+          if (rv) {
+#pragma unroll
+            for (int hq = 0; hq < 4; ++hq)
+              if (col + hq * 4 < args.N)
+                *reinterpret_cast<uint4*>(dst + col + hq * 4) =
+                    make_uint4(v[4 * hq], v[4 * hq + 1], v[4 * hq + 2], v[4 * hq + 3]);
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(smem_u32(&ctl->tempty[buf]));
+      ++acc;
+    }
+  }
+
+  // ---- teardown: every role has finished (or given up); release tensor memory
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+template <int MODE>
+moe_status_t launch_mode(const CUtensorMap& a, const CUtensorMap& a_lo, const CUtensorMap& b,
+                         const GemmArgs& args, long long max_tiles, cudaStream_t stream) {
+  const size_t smem = smem_bytes_for(args.E);
+  const cudaError_t attr_err = ensure_max_dynamic_smem(
+      reinterpret_cast<const void*>(grouped_gemm_kernel<MODE>), static_cast<int>(smem_bytes_for(MAX_E)));
+  if (attr_err != cudaSuccess) return cuda_fail(attr_err);
+  const long long sms = device_sm_count();
+  const int grid = static_cast<int>(std::max(1LL, std::min(sms, max_tiles)));
+  grouped_gemm_kernel<MODE><<<grid, THREADS, smem, stream>>>(a, a_lo, b, args);
+  const cudaError_t err = cudaGetLastError();
+  return err == cudaSuccess ? MOE_OK : cuda_fail(err);
+}
+
+}  // namespace
+
+int gemm_tiles_n(int mode, int N) {
+  const int w = (mode == MODE_UP_SWIGLU) ? 128 : BN;
+  return (N + w - 1) / w;
+}
+
+bool make_map_rows2d(CUtensorMap* map, const void* ptr, long long rows, long long cols,
+                     int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || rows <= 0 || cols <= 0) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+  const cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t estr[2] = {1u, 1u};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool make_map_weight3d(CUtensorMap* map, const void* ptr, long long E, long long R, long long C,
+                       int box_r) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || E <= 0 || R <= 0 || C <= 0) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(C), static_cast<cuuint64_t>(R),
+                              static_cast<cuuint64_t>(E)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(C) * 2,
+                                 static_cast<cuuint64_t>(R) * static_cast<cuuint64_t>(C) * 2};
+  const cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(box_r), 1u};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+moe_status_t launch_grouped_gemm(int mode, const CUtensorMap& a, const CUtensorMap& a_lo,
+                                 const CUtensorMap& b, const GemmArgs& args, long long max_tiles,
+                                 cudaStream_t stream) {
+  if (args.E < 1 || args.E > MAX_E) return MOE_ERR_UNSUPPORTED_SHAPE;
+  switch (mode) {
+    case MODE_UP_SWIGLU: return launch_mode<MODE_UP_SWIGLU>(a, a_lo, b, args, max_tiles, stream);
+    case MODE_PLAIN_BF16: return launch_mode<MODE_PLAIN_BF16>(a, a_lo, b, args, max_tiles, stream);
+    case MODE_DGRAD_SWIGLU:
+      return launch_mode<MODE_DGRAD_SWIGLU>(a, a_lo, b, args, max_tiles, stream);
+    case MODE_WGRAD: return launch_mode<MODE_WGRAD>(a, a_lo, b, args, max_tiles, stream);
+    case MODE_WGRAD_BF16: return launch_mode<MODE_WGRAD_BF16>(a, a_lo, b, args, max_tiles, stream);
+    default: return MOE_ERR_INVALID_ARG;
+  }
+}
+
+}  // namespace moe

@@ -1,0 +1,100 @@
+// Host-side interface between the library's translation units (not part of the C ABI).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/moe_gg.h"
+
+namespace moe {
+
+// ------------------------------------------------------------------ grouped GEMM (tcgen05)
+enum GemmMode : int {
+  // U = X W_ug^T per row segment, gate and up column blocks in one accumulator; the epilogue
+  // writes bf16(A) for A = silu(gate) * up, and optionally U (fp32) and A - bf16(A) (bf16).
+  // A: rows [cap, d] K-major; B: W_ug [E, 2h, d].
+  MODE_UP_SWIGLU = 0,
+  // Y = P W per row segment with W [E, K, N] (N contiguous, MN-major B); bf16 store.
+  MODE_PLAIN_BF16 = 1,
+  // dA = dY W_down^T per row segment (W_down [E, h, d] K-major B); the epilogue applies the
+  // SwiGLU backward with the saved fp32 U and writes dU = [dgate, dup] as a bf16 high/low pair.
+  MODE_DGRAD_SWIGLU = 2,
+  // dW_e = (P_hi + P_lo)_e^T Q_e, contraction over the M_e rows of expert e (all operands
+  // MN-major, two MMAs per K step into one accumulator); fp32 store, zeros for empty experts.
+  MODE_WGRAD = 3,
+  // as MODE_WGRAD with the high half of P only (plain bf16 activations, one MMA per K step)
+  MODE_WGRAD_BF16 = 4
+};
+
+struct GemmArgs {
+  const int32_t* offsets;  // inclusive offsets [E] on the device, or nullptr (uniform/single)
+  int E;                   // experts in the problem list
+  int uniform_rows;        // > 0: expert e owns rows [e*uniform_rows, (e+1)*uniform_rows)
+  int single_expert;       // >= 0: one problem, expert `single_expert`, rows below
+  int single_row0;
+  int single_rows;
+  int cap;                 // rows of the row-indexed buffers (device check of the offsets)
+  int N;                   // output columns (UP_SWIGLU: h)
+  int K;                   // contraction length of the row-grouped modes
+  int Mdim;                // WGRAD: rows of each expert's gradient
+  int h;                   // SwiGLU half width
+  void* out;               // row-grouped bf16 output, or WGRAD fp32 [E, Mdim, N]
+  long long ldo;           // elements per output row
+  void* out2;              // UP_SWIGLU: optional fp32 U [cap, 2h]; DGRAD_SWIGLU: dU low half
+  long long ldo2;
+  void* out3;              // UP_SWIGLU: optional low half of P [cap, h] (P = w*A, or A)
+  long long ldo3;
+  void* out4;              // UP_SWIGLU with row weights: high half of P = w*A [cap, h]
+  // Optional routing weight of each row: w = row_weight[row_src[row]]. UP_SWIGLU writes P = w*A
+  // for the down wgrad; PLAIN_BF16 scales its output rows (the down projection); DGRAD_SWIGLU
+  // scales dA before the SwiGLU backward.
+  const int32_t* row_src;
+  const float* row_weight;
+  const void* aux;         // DGRAD_SWIGLU: saved fp32 U [cap, 2h]
+  long long ld_aux;
+  int32_t* status;         // optional device status word
+  long long timeout_ns;    // bound of every wait inside the kernel
+};
+
+// Launch one persistent grouped GEMM. `a` and `b` are the operand tensor maps described with
+// each mode; `a_lo` is the low half of the A operand (WGRAD only, else ignored). `max_tiles`
+// bounds the grid (the exact tile count is only known on the device).
+moe_status_t launch_grouped_gemm(int mode, const CUtensorMap& a, const CUtensorMap& a_lo,
+                                 const CUtensorMap& b, const GemmArgs& args, long long max_tiles,
+                                 cudaStream_t stream);
+
+// Tensor maps (bf16, 128-byte swizzle, zero fill outside the tensor).
+//   rows2d: a [rows, cols] row-major matrix; box = 64 columns x box_rows rows.
+//   weight3d: an [E, R, C] tensor; box = 64 x box_r x 1.
+bool make_map_rows2d(CUtensorMap* map, const void* ptr, long long rows, long long cols,
+                     int box_rows);
+bool make_map_weight3d(CUtensorMap* map, const void* ptr, long long E, long long R, long long C,
+                       int box_r);
+
+int gemm_tiles_n(int mode, int N);  // column tiles of one problem
+
+// ------------------------------------------------------------------ helpers
+int device_sm_count();              // SMs of the current device (cached per device)
+long long wait_timeout_ns();        // bound of device waits (default 2 s)
+moe_status_t check_device();        // current device must be sm_103
+moe_status_t cuda_fail(cudaError_t err);  // records the error text, returns MOE_ERR_CUDA
+// Raise a kernel's dynamic shared-memory limit once per (kernel, device).
+cudaError_t ensure_max_dynamic_smem(const void* kernel, int bytes);
+
+// ------------------------------------------------------------------ routing / data movement
+size_t route_workspace_bytes(long long n, int E);
+moe_status_t launch_route(const int32_t* ids, int n, int E, int32_t* counts, int32_t* offsets,
+                          int32_t* sorted_src, int32_t* inv_map, void* ws, cudaStream_t s);
+moe_status_t launch_permute(const void* x, const int32_t* sorted_src, const int32_t* offsets,
+                            const float* row_scale, int n, int k, int E, int d, void* xp,
+                            cudaStream_t s);
+moe_status_t launch_combine(const void* y, const int32_t* inv_map, const float* weights, int T,
+                            int k, int d, void* out, cudaStream_t s);
+moe_status_t launch_pad_rows(const void* src, const int32_t* offsets, int E, int C, int cols,
+                             void* dst, cudaStream_t s);
+moe_status_t launch_unpad_rows(const void* src, const int32_t* offsets, int E, int C, int cap,
+                               int cols, void* dst, cudaStream_t s);
+
+}  // namespace moe

@@ -1,0 +1,543 @@
+// C-ABI entry points (include/moe_gg.h): argument validation, workspace carving, tensor-map
+// construction and stream-ordered launches. No entry point allocates device memory; only
+// moe_loop_swiglu_fwd synchronises (by design, it is the host-scheduled comparison variant).
+#include <algorithm>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "internal.h"
+
+namespace moe {
+
+namespace {
+thread_local char g_last_error[256] = "no error";
+constexpr int MAX_DEVICES = 64;
+constexpr int MAX_E = 1024;
+constexpr int MAX_TOPK = 32;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t round256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
+
+moe_status_t map_fail(const char* what) {
+  std::snprintf(g_last_error, sizeof(g_last_error), "cuTensorMapEncodeTiled failed for %s", what);
+  return MOE_ERR_CUDA;
+}
+
+bool dim_ok(int v) { return v > 0 && v % 8 == 0 && v <= (1 << 20); }
+
+bool shape_ok(int E, int d, int h) { return E >= 1 && E <= MAX_E && dim_ok(d) && dim_ok(h); }
+
+long long row_tiles_bound(long long rows, int E) { return (rows + 127) / 128 + E; }
+
+GemmArgs base_args(int E, int cap, int32_t* status) {
+  GemmArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.E = E;
+  a.single_expert = -1;
+  a.cap = cap;
+  a.status = status;
+  a.timeout_ns = wait_timeout_ns();
+  return a;
+}
+
+// saved = fp32 U [rows, 2h] | low half of P [rows, h] | high half of P [rows, h], P = w*A (or A)
+size_t saved_u_bytes(long long rows, int h) { return round256(static_cast<size_t>(rows) * 2 * h * 4); }
+size_t saved_p_bytes(long long rows, int h) { return round256(static_cast<size_t>(rows) * h * 2); }
+size_t saved_bytes(long long rows, int h) { return saved_u_bytes(rows, h) + 2 * saved_p_bytes(rows, h); }
+const void* saved_p_lo(const void* saved, long long rows, int h) {
+  return static_cast<const uint8_t*>(saved) + saved_u_bytes(rows, h);
+}
+const void* saved_p_hi(const void* saved, long long rows, int h) {
+  return static_cast<const uint8_t*>(saved) + saved_u_bytes(rows, h) + saved_p_bytes(rows, h);
+}
+size_t bwd_ws_half(long long rows, int h) { return round256(static_cast<size_t>(rows) * 2 * h * 2); }
+
+// ---- one launch per step; `src` carries the problem source (device offsets, uniform rows or
+// one expert), `rows` the rows of the row buffers, `tiles_bound` an upper bound of row tiles.
+
+// a6: U = xp W_ug^T, A = SwiGLU(U); saved (nullable) receives fp32 U and the halves of P
+// (P = w*A when src carries row weights, else P = A and its high half is a_save itself).
+moe_status_t run_up_swiglu(const GemmArgs& src, long long rows, long long tiles_bound, int E, int d,
+                           int h, const void* xp, const void* w_ug, void* a_save, void* saved,
+                           cudaStream_t s) {
+  CUtensorMap ma, mb;
+  if (!make_map_rows2d(&ma, xp, rows, d, 128)) return map_fail("xp");
+  if (!make_map_weight3d(&mb, w_ug, E, 2LL * h, d, 128)) return map_fail("w_ug");
+  GemmArgs a = src;
+  a.N = h;
+  a.K = d;
+  a.h = h;
+  a.out = a_save;
+  a.ldo = h;
+  if (saved != nullptr) {
+    a.out2 = saved;
+    a.ldo2 = 2LL * h;
+    a.out3 = const_cast<void*>(saved_p_lo(saved, rows, h));
+    a.out4 = const_cast<void*>(saved_p_hi(saved, rows, h));
+    a.ldo3 = h;
+  }
+  return launch_grouped_gemm(MODE_UP_SWIGLU, ma, ma, mb, a,
+                             tiles_bound * gemm_tiles_n(MODE_UP_SWIGLU, h), s);
+}
+
+// a7: y = A W_down.
+moe_status_t run_down(const GemmArgs& src, long long rows, long long tiles_bound, int E, int d,
+                      int h, const void* a_in, const void* w_down, void* y, cudaStream_t s) {
+  CUtensorMap ma, mb;
+  if (!make_map_rows2d(&ma, a_in, rows, h, 128)) return map_fail("a");
+  if (!make_map_weight3d(&mb, w_down, E, h, d, 64)) return map_fail("w_down");
+  GemmArgs a = src;
+  a.N = d;
+  a.K = h;
+  a.h = h;
+  a.out = y;
+  a.ldo = d;
+  return launch_grouped_gemm(MODE_PLAIN_BF16, ma, ma, mb, a,
+                             tiles_bound * gemm_tiles_n(MODE_PLAIN_BF16, d), s);
+}
+
+// a10: dA = dy W_down^T with the SwiGLU backward -> dU high and low halves.
+moe_status_t run_down_dgrad_swiglu(const GemmArgs& src, long long rows, int E, int d, int h,
+                                   const void* dy, const void* saved, const void* w_down,
+                                   void* du_hi, void* du_lo, cudaStream_t s) {
+  CUtensorMap ma, mb;
+  if (!make_map_rows2d(&ma, dy, rows, d, 128)) return map_fail("dy");
+  if (!make_map_weight3d(&mb, w_down, E, h, d, 256)) return map_fail("w_down");
+  GemmArgs a = src;
+  a.N = h;
+  a.K = d;
+  a.h = h;
+  a.out = du_hi;
+  a.ldo = 2LL * h;
+  a.out2 = du_lo;
+  a.ldo2 = 2LL * h;
+  a.aux = saved;
+  a.ld_aux = 2LL * h;
+  return launch_grouped_gemm(MODE_DGRAD_SWIGLU, ma, ma, mb, a,
+                             row_tiles_bound(rows, src.E) * gemm_tiles_n(MODE_DGRAD_SWIGLU, h), s);
+}
+
+// a12: dxp = dU W_ug.
+moe_status_t run_up_dgrad(const GemmArgs& src, long long rows, int E, int d, int h,
+                          const void* du_hi, const void* w_ug, void* dxp, cudaStream_t s) {
+  CUtensorMap ma, mb;
+  if (!make_map_rows2d(&ma, du_hi, rows, 2LL * h, 128)) return map_fail("dU");
+  if (!make_map_weight3d(&mb, w_ug, E, 2LL * h, d, 64)) return map_fail("w_ug");
+  GemmArgs a = src;
+  a.N = d;
+  a.K = 2 * h;
+  a.h = h;
+  a.out = dxp;
+  a.ldo = d;
+  return launch_grouped_gemm(MODE_PLAIN_BF16, ma, ma, mb, a,
+                             row_tiles_bound(rows, src.E) * gemm_tiles_n(MODE_PLAIN_BF16, d), s);
+}
+
+// a11 / a13: dW_e = (P_hi + P_lo)_e^T Q_e over each expert's rows.
+moe_status_t run_wgrad(const GemmArgs& src, long long rows, int E, const void* p_hi,
+                       const void* p_lo, int p_cols, const void* q, int q_cols, float* dw,
+                       cudaStream_t s) {
+  // with no rows every expert is empty: the maps then describe a one-row placeholder
+  const long long r = std::max(rows, 1LL);
+  CUtensorMap ma, ml, mb;
+  if (!make_map_rows2d(&ma, p_hi, r, p_cols, 64)) return map_fail("p_hi");
+  if (!make_map_rows2d(&ml, p_lo ? p_lo : p_hi, r, p_cols, 64)) return map_fail("p_lo");
+  if (!make_map_rows2d(&mb, q, r, q_cols, 64)) return map_fail("q");
+  GemmArgs a = src;
+  a.N = q_cols;
+  a.Mdim = p_cols;
+  a.out = dw;
+  a.ldo = q_cols;
+  const long long tiles = static_cast<long long>(E) * ((p_cols + 127) / 128) * ((q_cols + 255) / 256);
+  return launch_grouped_gemm(p_lo ? MODE_WGRAD : MODE_WGRAD_BF16, ma, ml, mb, a, tiles, s);
+}
+
+moe_status_t check_grouped_common(int E, int cap, int d, int h) {
+  if (cap < 0 || d <= 0 || h <= 0 || E < 1) return MOE_ERR_INVALID_ARG;
+  if (!shape_ok(E, d, h)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  return MOE_OK;
+}
+
+}  // namespace
+
+moe_status_t cuda_fail(cudaError_t err) {
+  std::snprintf(g_last_error, sizeof(g_last_error), "%s: %s", cudaGetErrorName(err),
+                cudaGetErrorString(err));
+  return MOE_ERR_CUDA;
+}
+
+int device_sm_count() {
+  static int cache[MAX_DEVICES] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) return 1;
+  if (cache[dev] == 0) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cache[dev] = n > 0 ? n : 1;
+  }
+  return cache[dev];
+}
+
+long long wait_timeout_ns() {
+  static const long long v = [] {
+    const char* s = std::getenv("MOE_GG_WAIT_TIMEOUT_NS");
+    const long long t = s ? std::atoll(s) : 0;
+    return t > 0 ? t : 2000000000LL;
+  }();
+  return v;
+}
+
+cudaError_t ensure_max_dynamic_smem(const void* kernel, int bytes) {
+  static std::mutex mu;
+  static std::vector<std::pair<const void*, int>> done;
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  std::lock_guard<std::mutex> lock(mu);
+  for (const auto& p : done)
+    if (p.first == kernel && p.second == dev) return cudaSuccess;
+  err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (err == cudaSuccess) done.emplace_back(kernel, dev);
+  return err;
+}
+
+moe_status_t check_device() {
+  static int ok_cache[MAX_DEVICES] = {0};  // 0 unknown, 1 ok, -1 unsupported
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return cuda_fail(err);
+  if (dev < 0 || dev >= MAX_DEVICES) return MOE_ERR_UNSUPPORTED_DEVICE;
+  if (ok_cache[dev] == 0) {
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    ok_cache[dev] = (major == 10 && minor == 3) ? 1 : -1;
+  }
+  return ok_cache[dev] == 1 ? MOE_OK : MOE_ERR_UNSUPPORTED_DEVICE;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+int moe_abi_version(void) { return 1; }
+
+const char* moe_last_cuda_error(void) { return g_last_error; }
+
+const char* moe_status_string(moe_status_t s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument (null, negative or misaligned)";
+    case MOE_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case MOE_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_DEVICE_TIMEOUT: return "a device-side wait timed out";
+    case MOE_ERR_UNSUPPORTED_DEVICE: return "current device is not sm_103";
+  }
+  return "unknown status";
+}
+
+size_t moe_workspace_bytes(int op, int T, int top_k, int E, int d, int h, int capacity_C) {
+  if (T < 0 || top_k < 1 || top_k > MAX_TOPK || E < 1 || E > MAX_E) return 0;
+  const long long n = static_cast<long long>(T) * top_k;
+  switch (op) {
+    case MOE_OP_ROUTE: return route_workspace_bytes(n, E);
+    case MOE_OP_FWD: return 0;
+    case MOE_OP_BWD: return h > 0 ? 2 * bwd_ws_half(n, h) : 0;
+    case MOE_OP_SAVED: return h > 0 ? saved_bytes(n, h) : 0;
+    case MOE_OP_PADDED_BMM: {
+      if (capacity_C <= 0 || d <= 0 || h <= 0) return 0;
+      const size_t rows = static_cast<size_t>(E) * capacity_C;
+      return round256(rows * d * 2) * 2 + round256(rows * h * 2);
+    }
+    case MOE_OP_LOOP: return 0;
+  }
+  return 0;
+}
+
+moe_status_t moe_route_offsets(const int32_t* ids, int T, int top_k, int E, int32_t* counts,
+                               int32_t* offsets, int32_t* sorted_src, int32_t* inv_map,
+                               void* ws, size_t ws_bytes, moe_stream_t stream) {
+  if (T < 0 || top_k < 1) return MOE_ERR_INVALID_ARG;
+  if (top_k > MAX_TOPK || E < 1 || E > MAX_E) return MOE_ERR_UNSUPPORTED_SHAPE;
+  const long long n = static_cast<long long>(T) * top_k;
+  if (n >= (1LL << 31)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!counts || !offsets) return MOE_ERR_INVALID_ARG;
+  if (n > 0 && (!ids || !sorted_src || !inv_map)) return MOE_ERR_INVALID_ARG;
+  const size_t need = route_workspace_bytes(n, E);
+  if (ws_bytes < need) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  if (need > 0 && !ws) return MOE_ERR_INVALID_ARG;
+  moe_status_t st = check_device();
+  if (st != MOE_OK) return st;
+  return launch_route(ids, static_cast<int>(n), E, counts, offsets, sorted_src, inv_map, ws,
+                      reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_permute(const moe_bf16* x, const int32_t* sorted_src, const int32_t* offsets,
+                         const float* row_scale, int T, int top_k, int E, int d, moe_bf16* xp,
+                         moe_stream_t stream) {
+  if (T < 0 || top_k < 1 || d <= 0) return MOE_ERR_INVALID_ARG;
+  if (top_k > MAX_TOPK || E < 1 || E > MAX_E || d % 8 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+  const long long n = static_cast<long long>(T) * top_k;
+  if (n >= (1LL << 31)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!offsets) return MOE_ERR_INVALID_ARG;
+  if (n > 0 && (!x || !sorted_src || !xp)) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(xp)) return MOE_ERR_INVALID_ARG;
+  moe_status_t st = check_device();
+  if (st != MOE_OK) return st;
+  return launch_permute(x, sorted_src, offsets, row_scale, static_cast<int>(n), top_k, E, d, xp,
+                        reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_unpermute_combine(const moe_bf16* y, const int32_t* inv_map, const float* weights,
+                                   int T, int top_k, int d, moe_bf16* out, moe_stream_t stream) {
+  if (T < 0 || top_k < 1 || d <= 0) return MOE_ERR_INVALID_ARG;
+  if (top_k > MAX_TOPK || d % 8 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (static_cast<long long>(T) * top_k >= (1LL << 31)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (T > 0 && (!y || !inv_map || !out)) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(y) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
+  moe_status_t st = check_device();
+  if (st != MOE_OK) return st;
+  return launch_combine(y, inv_map, weights, T, top_k, d, out,
+                        reinterpret_cast<cudaStream_t>(stream));
+}
+
+// ------------------------------------------------------------------ single grouped kernels
+moe_status_t moe_grouped_up_swiglu(const moe_bf16* xp, const int32_t* offsets,
+                                   const int32_t* sorted_src, const float* weights, int E, int cap,
+                                   int d, int h, const moe_bf16* w_ug, moe_bf16* a_save,
+                                   void* saved, int32_t* dev_status, moe_stream_t stream) {
+  moe_status_t st = check_grouped_common(E, cap, d, h);
+  if (st != MOE_OK) return st;
+  if (!xp || !offsets || !w_ug || !a_save || (weights && !sorted_src)) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(xp) || !aligned16(w_ug) || !aligned16(a_save) || !aligned16(saved))
+    return MOE_ERR_INVALID_ARG;
+  if ((st = check_device()) != MOE_OK || cap == 0) return st;
+  GemmArgs src = base_args(E, cap, dev_status);
+  src.offsets = offsets;
+  src.row_src = sorted_src;
+  src.row_weight = weights;
+  return run_up_swiglu(src, cap, row_tiles_bound(cap, E), E, d, h, xp, w_ug, a_save, saved,
+                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_grouped_down(const moe_bf16* a, const int32_t* offsets, const int32_t* sorted_src,
+                              const float* weights, int E, int cap, int d, int h,
+                              const moe_bf16* w_down, moe_bf16* y, int32_t* dev_status,
+                              moe_stream_t stream) {
+  moe_status_t st = check_grouped_common(E, cap, d, h);
+  if (st != MOE_OK) return st;
+  if (!a || !offsets || !w_down || !y || (weights && !sorted_src)) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(a) || !aligned16(w_down) || !aligned16(y)) return MOE_ERR_INVALID_ARG;
+  if ((st = check_device()) != MOE_OK || cap == 0) return st;
+  GemmArgs src = base_args(E, cap, dev_status);
+  src.offsets = offsets;
+  src.row_src = sorted_src;
+  src.row_weight = weights;
+  return run_down(src, cap, row_tiles_bound(cap, E), E, d, h, a, w_down, y,
+                  reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_grouped_down_dgrad_swiglu(const moe_bf16* dy, const void* saved,
+                                           const int32_t* offsets, const int32_t* sorted_src,
+                                           const float* weights, int E, int cap, int d, int h,
+                                           const moe_bf16* w_down, moe_bf16* du_hi,
+                                           moe_bf16* du_lo, int32_t* dev_status,
+                                           moe_stream_t stream) {
+  moe_status_t st = check_grouped_common(E, cap, d, h);
+  if (st != MOE_OK) return st;
+  if (!dy || !saved || !offsets || !w_down || !du_hi || !du_lo || (weights && !sorted_src))
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(dy) || !aligned16(saved) || !aligned16(w_down) || !aligned16(du_hi) ||
+      !aligned16(du_lo))
+    return MOE_ERR_INVALID_ARG;
+  if ((st = check_device()) != MOE_OK || cap == 0) return st;
+  GemmArgs src = base_args(E, cap, dev_status);
+  src.offsets = offsets;
+  src.row_src = sorted_src;
+  src.row_weight = weights;
+  return run_down_dgrad_swiglu(src, cap, E, d, h, dy, saved, w_down, du_hi, du_lo,
+                               reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_grouped_up_dgrad(const moe_bf16* du_hi, const int32_t* offsets, int E, int cap,
+                                  int d, int h, const moe_bf16* w_ug, moe_bf16* dxp,
+                                  int32_t* dev_status, moe_stream_t stream) {
+  moe_status_t st = check_grouped_common(E, cap, d, h);
+  if (st != MOE_OK) return st;
+  if (!du_hi || !offsets || !w_ug || !dxp) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(du_hi) || !aligned16(w_ug) || !aligned16(dxp)) return MOE_ERR_INVALID_ARG;
+  if ((st = check_device()) != MOE_OK || cap == 0) return st;
+  GemmArgs src = base_args(E, cap, dev_status);
+  src.offsets = offsets;
+  return run_up_dgrad(src, cap, E, d, h, du_hi, w_ug, dxp, reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_grouped_wgrad(const moe_bf16* p_hi, const moe_bf16* p_lo, int p_cols,
+                               const moe_bf16* q, int q_cols, const int32_t* offsets, int E,
+                               int cap, float* dw, int32_t* dev_status, moe_stream_t stream) {
+  if (cap < 0 || E < 1 || p_cols <= 0 || q_cols <= 0) return MOE_ERR_INVALID_ARG;
+  if (E > MAX_E || !dim_ok(p_cols) || !dim_ok(q_cols)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!p_hi || !q || !offsets || !dw) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(p_hi) || !aligned16(p_lo) || !aligned16(q) || !aligned16(dw))
+    return MOE_ERR_INVALID_ARG;
+  moe_status_t st = check_device();
+  if (st != MOE_OK) return st;
+  GemmArgs src = base_args(E, cap, dev_status);
+  src.offsets = offsets;
+  return run_wgrad(src, cap, E, p_hi, p_lo, p_cols, q, q_cols, dw,
+                   reinterpret_cast<cudaStream_t>(stream));
+}
+
+// ------------------------------------------------------------------ composite calls
+moe_status_t moe_grouped_swiglu_fwd(const moe_bf16* xp, const int32_t* offsets,
+                                    const int32_t* sorted_src, const float* weights, int E,
+                                    int cap, int d, int h, const moe_bf16* w_ug,
+                                    const moe_bf16* w_down, moe_bf16* y, moe_bf16* a_save,
+                                    void* saved, void* ws, size_t ws_bytes, int32_t* dev_status,
+                                    moe_stream_t stream) {
+  (void)ws;
+  (void)ws_bytes;
+  moe_status_t st = check_grouped_common(E, cap, d, h);
+  if (st != MOE_OK) return st;
+  if (!xp || !offsets || !w_ug || !w_down || !y || !a_save || (weights && !sorted_src))
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(xp) || !aligned16(w_ug) || !aligned16(w_down) || !aligned16(y) ||
+      !aligned16(a_save) || !aligned16(saved))
+    return MOE_ERR_INVALID_ARG;
+  if ((st = check_device()) != MOE_OK || cap == 0) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  GemmArgs src = base_args(E, cap, dev_status);
+  src.offsets = offsets;
+  src.row_src = sorted_src;
+  src.row_weight = weights;
+  const long long tb = row_tiles_bound(cap, E);
+  st = run_up_swiglu(src, cap, tb, E, d, h, xp, w_ug, a_save, saved, s);
+  if (st != MOE_OK) return st;
+  return run_down(src, cap, tb, E, d, h, a_save, w_down, y, s);
+}
+
+moe_status_t moe_grouped_bwd(const moe_bf16* dy, const moe_bf16* xp, const moe_bf16* a_save,
+                             const void* saved, const int32_t* offsets, const int32_t* sorted_src,
+                             const float* weights, int E, int cap, int d, int h,
+                             const moe_bf16* w_ug, const moe_bf16* w_down, moe_bf16* dxp,
+                             float* dw_ug, float* dw_down, void* ws, size_t ws_bytes,
+                             int32_t* dev_status, moe_stream_t stream) {
+  moe_status_t st = check_grouped_common(E, cap, d, h);
+  if (st != MOE_OK) return st;
+  if (!dy || !xp || !a_save || !saved || !offsets || !w_ug || !w_down || !dxp || !dw_ug ||
+      !dw_down || (weights && !sorted_src))
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(dy) || !aligned16(xp) || !aligned16(a_save) || !aligned16(saved) ||
+      !aligned16(w_ug) || !aligned16(w_down) || !aligned16(dxp) || !aligned16(dw_ug) ||
+      !aligned16(dw_down) || !aligned16(ws))
+    return MOE_ERR_INVALID_ARG;
+  const size_t half = bwd_ws_half(cap, h);
+  if (ws_bytes < 2 * half) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  if (half > 0 && !ws) return MOE_ERR_INVALID_ARG;
+  if ((st = check_device()) != MOE_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  moe_bf16* du_hi = static_cast<moe_bf16*>(ws);
+  moe_bf16* du_lo = reinterpret_cast<moe_bf16*>(static_cast<uint8_t*>(ws) + half);
+  // P = w*A when the forward folded the routing weights in, else P = A (high half = a_save)
+  const void* p_hi = weights ? saved_p_hi(saved, cap, h) : static_cast<const void*>(a_save);
+  const void* p_lo = saved_p_lo(saved, cap, h);
+  GemmArgs src = base_args(E, cap, dev_status);
+  src.offsets = offsets;
+  if (cap > 0) {
+    GemmArgs wsrc = src;
+    wsrc.row_src = sorted_src;
+    wsrc.row_weight = weights;
+    st = run_down_dgrad_swiglu(wsrc, cap, E, d, h, dy, saved, w_down, du_hi, du_lo, s);
+    if (st != MOE_OK) return st;
+    st = run_up_dgrad(src, cap, E, d, h, du_hi, w_ug, dxp, s);
+    if (st != MOE_OK) return st;
+  }
+  // wgrads contract over each expert's rows; empty experts get zeros
+  st = run_wgrad(src, cap, E, p_hi, cap > 0 ? p_lo : p_hi, h, dy, d, dw_down, s);
+  if (st != MOE_OK) return st;
+  return run_wgrad(src, cap, E, cap > 0 ? du_hi : a_save, cap > 0 ? du_lo : a_save, 2 * h, xp, d,
+                   dw_ug, s);
+}
+
+moe_status_t moe_padded_bmm_swiglu_fwd(const moe_bf16* xp, const int32_t* offsets, int E, int cap,
+                                       int d, int h, int capacity_C, const moe_bf16* w_ug,
+                                       const moe_bf16* w_down, moe_bf16* y, void* ws,
+                                       size_t ws_bytes, int32_t* dev_status, moe_stream_t stream) {
+  if (cap < 0 || d <= 0 || h <= 0 || E < 1 || capacity_C < 1) return MOE_ERR_INVALID_ARG;
+  if (!shape_ok(E, d, h)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  const long long rows = static_cast<long long>(E) * capacity_C;
+  if (rows >= (1LL << 31)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!xp || !offsets || !w_ug || !w_down || !y || !ws) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(xp) || !aligned16(w_ug) || !aligned16(w_down) || !aligned16(y) || !aligned16(ws))
+    return MOE_ERR_INVALID_ARG;
+  const size_t bx = round256(static_cast<size_t>(rows) * d * 2);
+  const size_t ba = round256(static_cast<size_t>(rows) * h * 2);
+  if (ws_bytes < 2 * bx + ba) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  moe_status_t st = check_device();
+  if (st != MOE_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  moe_bf16* xpad = reinterpret_cast<moe_bf16*>(base);
+  moe_bf16* ypad = reinterpret_cast<moe_bf16*>(base + bx);
+  moe_bf16* apad = reinterpret_cast<moe_bf16*>(base + 2 * bx);
+  st = launch_pad_rows(xp, offsets, E, capacity_C, d, xpad, s);
+  if (st != MOE_OK) return st;
+  GemmArgs src = base_args(E, static_cast<int>(rows), dev_status);
+  src.uniform_rows = capacity_C;
+  const long long tb = static_cast<long long>(E) * ((capacity_C + 127) / 128);
+  st = run_up_swiglu(src, rows, tb, E, d, h, xpad, w_ug, apad, nullptr, s);
+  if (st != MOE_OK) return st;
+  st = run_down(src, rows, tb, E, d, h, apad, w_down, ypad, s);
+  if (st != MOE_OK) return st;
+  return launch_unpad_rows(ypad, offsets, E, capacity_C, cap, d, y, s);
+}
+
+moe_status_t moe_loop_swiglu_fwd(const moe_bf16* xp, const int32_t* offsets, int E, int cap,
+                                 int d, int h, const moe_bf16* w_ug, const moe_bf16* w_down,
+                                 moe_bf16* y, moe_bf16* a_save, void* saved,
+                                 int32_t* dev_status, moe_stream_t stream) {
+  moe_status_t st = check_grouped_common(E, cap, d, h);
+  if (st != MOE_OK) return st;
+  if (!xp || !offsets || !w_ug || !w_down || !y || !a_save) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(xp) || !aligned16(w_ug) || !aligned16(w_down) || !aligned16(y) ||
+      !aligned16(a_save) || !aligned16(saved))
+    return MOE_ERR_INVALID_ARG;
+  if ((st = check_device()) != MOE_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // Fig. 36: the counts become host-visible first; the CPU waits for them.
+  std::vector<int32_t> off(E);
+  cudaError_t err = cudaMemcpyAsync(off.data(), offsets, sizeof(int32_t) * E, cudaMemcpyDeviceToHost, s);
+  if (err == cudaSuccess) err = cudaStreamSynchronize(s);
+  if (err != cudaSuccess) return cuda_fail(err);
+  int prev = 0;
+  for (int e = 0; e < E; ++e) {
+    if (off[e] < prev || off[e] > cap) return MOE_ERR_INVALID_ARG;
+    prev = off[e];
+  }
+  prev = 0;
+  for (int e = 0; e < E; ++e) {
+    const int rows = off[e] - prev;
+    if (rows > 0) {
+      GemmArgs src = base_args(1, cap, dev_status);
+      src.single_expert = e;
+      src.single_row0 = prev;
+      src.single_rows = rows;
+      const long long tb = (rows + 127) / 128;
+      st = run_up_swiglu(src, cap, tb, E, d, h, xp, w_ug, a_save, saved, s);
+      if (st != MOE_OK) return st;
+      st = run_down(src, cap, tb, E, d, h, a_save, w_down, y, s);
+      if (st != MOE_OK) return st;
+    }
+    prev = off[e];
+  }
+  return MOE_OK;
+}
+
+}  // extern "C"

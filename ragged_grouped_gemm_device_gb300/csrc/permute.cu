@@ -1,0 +1,195 @@
+// Row movement around the grouped GEMM: the permute gather, the atomic-free combine through the
+// inverse map, and the pad/unpad pair of the capacity-padded comparison variant.
+//
+// All of these are HBM-bound copies: one warp per row, 16-byte vector loads and stores,
+// grid sized to a multiple of the SM count and striding over rows.
+#include <algorithm>
+#include <cstdint>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int THREADS = 256;
+constexpr int WARPS = THREADS / 32;
+
+__device__ __forceinline__ uint4 scale_bf16x8(uint4 q, float s) {
+  uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) w[i] = pack_bf16x2(bf16_lo(w[i]) * s, bf16_hi(w[i]) * s);
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// "grouped_mm" agent doc, forward gather x[idx]: xp[p] = x[sorted_src[p] / k] (* scale).
+__global__ void __launch_bounds__(THREADS) permute_kernel(
+    const uint4* __restrict__ x, const int32_t* __restrict__ sorted_src,
+    const int32_t* __restrict__ offsets, const float* __restrict__ row_scale, int n, int k, int E,
+    int vec, uint4* __restrict__ xp) {
+  const int M = min(__ldg(offsets + E - 1), n);
+  const int lane = threadIdx.x & 31;
+  const int gw = blockIdx.x * WARPS + (threadIdx.x >> 5);
+  const int nw = gridDim.x * WARPS;
+  for (int p = gw; p < M; p += nw) {
+    const int src = __ldg(sorted_src + p);
+    if (src < 0 || src >= n) continue;
+    const uint4* xr = x + static_cast<size_t>(src / k) * vec;
+    uint4* orow = xp + static_cast<size_t>(p) * vec;
+    if (row_scale != nullptr) {
+      const float s = __ldg(row_scale + src);
+      for (int v = lane; v < vec; v += 32) orow[v] = scale_bf16x8(__ldg(xr + v), s);
+    } else {
+      for (int v = lane; v < vec; v += 32) orow[v] = __ldg(xr + v);
+    }
+  }
+}
+
+// out[t] = sum_j w[t,j] * y[inv[t,j]] over slots with inv >= 0, fp32 in slot order, one bf16
+// rounding (gather + reduction in place of the scatter-add, "grouped_mm" agent doc).
+__global__ void __launch_bounds__(THREADS) combine_kernel(const uint4* __restrict__ y,
+                                                          const int32_t* __restrict__ inv,
+                                                          const float* __restrict__ weights,
+                                                          int T, int k, int vec,
+                                                          uint4* __restrict__ out) {
+  const int lane = threadIdx.x & 31;
+  const int gw = blockIdx.x * WARPS + (threadIdx.x >> 5);
+  const int nw = gridDim.x * WARPS;
+  for (int t = gw; t < T; t += nw) {
+    // lane j < k holds slot j's row and weight
+    int my_p = -1;
+    float my_w = 0.f;
+    if (lane < k) {
+      my_p = __ldg(inv + static_cast<size_t>(t) * k + lane);
+      my_w = weights ? __ldg(weights + static_cast<size_t>(t) * k + lane) : 1.0f;
+    }
+    // every lane runs the same number of iterations: the shuffles need the whole warp
+    for (int v0 = 0; v0 < vec; v0 += 32) {
+      const int v = v0 + lane;
+      const bool active = v < vec;
+      float acc[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+      for (int j = 0; j < k; ++j) {
+        const int p = __shfl_sync(0xffffffffu, my_p, j);
+        const float wj = __shfl_sync(0xffffffffu, my_w, j);
+        if (p < 0 || !active) continue;
+        const uint4 q = __ldg(y + static_cast<size_t>(p) * vec + v);
+        const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          acc[2 * i] = fmaf(wj, bf16_lo(w4[i]), acc[2 * i]);
+          acc[2 * i + 1] = fmaf(wj, bf16_hi(w4[i]), acc[2 * i + 1]);
+        }
+      }
+      if (active)
+        out[static_cast<size_t>(t) * vec + v] =
+            make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                       pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
+    }
+  }
+}
+
+// Capacity-padded layout (Fig. 35 of "Section 09: Grouped GEMM"): dst[e*C + i] = src row
+// offs[e-1] + i for i < min(M_e, C), zero rows for M_e <= i < C.
+__global__ void __launch_bounds__(THREADS) pad_rows_kernel(const uint4* __restrict__ src,
+                                                           const int32_t* __restrict__ offsets,
+                                                           int E, int C, int vec,
+                                                           uint4* __restrict__ dst) {
+  const int lane = threadIdx.x & 31;
+  const int gw = blockIdx.x * WARPS + (threadIdx.x >> 5);
+  const int nw = gridDim.x * WARPS;
+  const long long rows = static_cast<long long>(E) * C;
+  for (long long q = gw; q < rows; q += nw) {
+    const int e = static_cast<int>(q / C);
+    const int i = static_cast<int>(q - static_cast<long long>(e) * C);
+    const int start = e > 0 ? __ldg(offsets + e - 1) : 0;
+    const int me = __ldg(offsets + e) - start;
+    uint4* d = dst + q * vec;
+    if (i < me) {
+      const uint4* s = src + static_cast<size_t>(start + i) * vec;
+      for (int v = lane; v < vec; v += 32) d[v] = __ldg(s + v);
+    } else {
+      for (int v = lane; v < vec; v += 32) d[v] = make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+}
+
+// Back from the padded layout: row p of expert e (i = p - start_e) takes dst[p] = src[e*C + i]
+// when i < C; rows beyond the capacity were dropped and get zeros.
+__global__ void __launch_bounds__(THREADS) unpad_rows_kernel(const uint4* __restrict__ src,
+                                                             const int32_t* __restrict__ offsets,
+                                                             int E, int C, int cap, int vec,
+                                                             uint4* __restrict__ dst) {
+  const int M = min(__ldg(offsets + E - 1), cap);
+  const int lane = threadIdx.x & 31;
+  const int gw = blockIdx.x * WARPS + (threadIdx.x >> 5);
+  const int nw = gridDim.x * WARPS;
+  for (int p = gw; p < M; p += nw) {
+    int lo = 0, hi = E - 1;  // first e with offsets[e] > p
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (__ldg(offsets + mid) > p) hi = mid; else lo = mid + 1;
+    }
+    const int e = lo;
+    const int i = p - (e > 0 ? __ldg(offsets + e - 1) : 0);
+    uint4* d = dst + static_cast<size_t>(p) * vec;
+    if (i < C) {
+      const uint4* s = src + (static_cast<size_t>(e) * C + i) * vec;
+      for (int v = lane; v < vec; v += 32) d[v] = __ldg(s + v);
+    } else {
+      for (int v = lane; v < vec; v += 32) d[v] = make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+}
+
+int grid_for_rows(long long rows) {
+  const long long want = (rows + WARPS - 1) / WARPS;
+  const long long cap = static_cast<long long>(device_sm_count()) * 8;
+  return static_cast<int>(std::max(1LL, std::min(want, cap)));
+}
+
+moe_status_t last_launch() {
+  const cudaError_t err = cudaGetLastError();
+  return err == cudaSuccess ? MOE_OK : cuda_fail(err);
+}
+
+}  // namespace
+
+moe_status_t launch_permute(const void* x, const int32_t* sorted_src, const int32_t* offsets,
+                            const float* row_scale, int n, int k, int E, int d, void* xp,
+                            cudaStream_t s) {
+  if (n == 0) return MOE_OK;
+  permute_kernel<<<grid_for_rows(n), THREADS, 0, s>>>(
+      static_cast<const uint4*>(x), sorted_src, offsets, row_scale, n, k, E, d / 8,
+      static_cast<uint4*>(xp));
+  return last_launch();
+}
+
+moe_status_t launch_combine(const void* y, const int32_t* inv_map, const float* weights, int T,
+                            int k, int d, void* out, cudaStream_t s) {
+  if (T == 0) return MOE_OK;
+  combine_kernel<<<grid_for_rows(T), THREADS, 0, s>>>(static_cast<const uint4*>(y), inv_map,
+                                                      weights, T, k, d / 8,
+                                                      static_cast<uint4*>(out));
+  return last_launch();
+}
+
+moe_status_t launch_pad_rows(const void* src, const int32_t* offsets, int E, int C, int cols,
+                             void* dst, cudaStream_t s) {
+  const long long rows = static_cast<long long>(E) * C;
+  if (rows == 0) return MOE_OK;
+  pad_rows_kernel<<<grid_for_rows(rows), THREADS, 0, s>>>(static_cast<const uint4*>(src), offsets,
+                                                          E, C, cols / 8, static_cast<uint4*>(dst));
+  return last_launch();
+}
+
+moe_status_t launch_unpad_rows(const void* src, const int32_t* offsets, int E, int C, int cap,
+                               int cols, void* dst, cudaStream_t s) {
+  if (cap == 0) return MOE_OK;
+  unpad_rows_kernel<<<grid_for_rows(cap), THREADS, 0, s>>>(
+      static_cast<const uint4*>(src), offsets, E, C, cap, cols / 8, static_cast<uint4*>(dst));
+  return last_launch();
+}
+
+}  // namespace moe

@@ -1,0 +1,68 @@
+"""CPU-only checks of the C-ABI library: it builds for sm_103a, loads, exports every function the
+header declares, and rejects bad arguments on the host before touching CUDA."""
+import ctypes
+
+import pytest
+
+from ragged_grouped_gemm_device_gb300 import _lib, build
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return _lib.load()
+
+
+def test_header_functions_all_exported(lib):
+    names = _lib.header_functions()
+    assert "moe_grouped_swiglu_fwd" in names and len(names) >= 11
+    for name in names:
+        assert hasattr(lib, name), name
+    assert set(names) == set(_lib.SIGNATURES), "binding and header disagree"
+
+
+def test_abi_version_and_status_strings(lib):
+    assert lib.moe_abi_version() == 1
+    for code in _lib.STATUS:
+        assert lib.moe_status_string(code)
+    assert b"unknown" in lib.moe_status_string(99)
+
+
+def test_workspace_sizes_are_host_arithmetic(lib):
+    # route: one int32 per (warp chunk of 256 slots, expert), rounded to 256 bytes
+    assert _lib.moe_workspace_bytes(_lib.OP_ROUTE, 16384, 8, 256) == (16384 * 8 // 256) * 256 * 4
+    assert _lib.moe_workspace_bytes(_lib.OP_FWD, 16384, 8, 256, 2048, 512) == 0
+    # backward: dU high and low halves, [n, 2h] bf16 each
+    assert _lib.moe_workspace_bytes(_lib.OP_BWD, 16384, 8, 256, 2048, 512) == 2 * 16384 * 8 * 1024 * 2
+    # saved state: fp32 U [n, 2h] and the two bf16 halves of P [n, h]
+    assert _lib.moe_workspace_bytes(_lib.OP_SAVED, 16384, 8, 256, 2048, 512) == 16384 * 8 * (1024 * 4 + 2 * 512 * 2)
+    bmm = _lib.moe_workspace_bytes(_lib.OP_PADDED_BMM, 10, 1, 4, 64, 128, 4)
+    assert bmm == 2 * (16 * 64 * 2) + 16 * 128 * 2  # [16, 64] bf16 x2 and [16, 128] bf16
+    assert _lib.moe_workspace_bytes(_lib.OP_ROUTE, 10, 1, 0) == 0      # invalid E
+    assert _lib.moe_workspace_bytes(_lib.OP_ROUTE, 10, 33, 4) == 0     # top_k above 32
+
+
+def test_invalid_arguments_rejected_before_any_cuda_call(lib):
+    p = ctypes.c_void_p(16)  # never dereferenced: validation fails first
+    INVALID, SHAPE, WS = 1, 2, 3
+    assert lib.moe_route_offsets(p, 10, 1, 0, p, p, p, p, p, 1 << 20, None) == SHAPE      # E = 0
+    assert lib.moe_route_offsets(p, 10, 1, 2000, p, p, p, p, p, 1 << 20, None) == SHAPE   # E > 1024
+    assert lib.moe_route_offsets(p, -1, 1, 4, p, p, p, p, p, 1 << 20, None) == INVALID
+    assert lib.moe_route_offsets(p, 10, 1, 4, None, p, p, p, p, 1 << 20, None) == INVALID
+    assert lib.moe_route_offsets(p, 100000, 8, 256, p, p, p, p, p, 16, None) == WS
+    assert lib.moe_permute(p, p, p, None, 10, 1, 4, 12, p, None) == SHAPE                 # d % 8
+    assert lib.moe_permute(ctypes.c_void_p(18), p, p, None, 10, 1, 4, 16, p, None) == INVALID  # misaligned
+    fwd = lib.moe_grouped_swiglu_fwd
+    assert fwd(p, p, None, None, 4, 10, 64, 100, p, p, p, p, None, None, 0, None, None) == SHAPE    # h % 8
+    assert fwd(p, p, None, None, 4, 10, 64, 128, p, p, p, None, None, None, 0, None, None) == INVALID  # a_save
+    assert fwd(p, p, None, None, 4, -1, 64, 128, p, p, p, p, None, None, 0, None, None) == INVALID
+    assert fwd(p, p, None, p, 4, 10, 64, 128, p, p, p, p, None, None, 0, None, None) == INVALID  # weights w/o src
+    bwd = lib.moe_grouped_bwd
+    assert bwd(p, p, p, p, p, None, None, 4, 10, 64, 128, p, p, p, p, p, p, 0, None, None) == WS
+    assert bwd(p, p, p, None, p, None, None, 4, 10, 64, 128, p, p, p, p, p, p, 1 << 20, None, None) == INVALID
+    assert lib.moe_grouped_wgrad(p, None, 12, p, 64, p, 4, 10, p, None, None) == SHAPE        # p_cols % 8
+    assert lib.moe_grouped_up_dgrad(p, p, 0, 10, 64, 128, p, p, None, None) == INVALID       # E = 0
+    assert lib.moe_unpermute_combine(p, p, None, 10, 40, 64, p, None) == SHAPE            # top_k > 32
+    assert lib.moe_padded_bmm_swiglu_fwd(p, p, 4, 10, 64, 128, 0, p, p, p, p, 1 << 20, None, None) == INVALID
+    assert lib.moe_padded_bmm_swiglu_fwd(p, p, 4, 10, 64, 128, 4, p, p, p, p, 16, None, None) == WS
+    assert lib.moe_loop_swiglu_fwd(p, p, 4, 10, 64, 128, p, p, None, None, p, None, None) == INVALID

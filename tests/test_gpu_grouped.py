@@ -1,0 +1,162 @@
+"""GPU parity of the grouped SwiGLU expert forward and backward (tcgen05 kernels) against the
+fp64 oracle, on the full small and mid-size workloads and on sampled experts of the large one.
+
+Row buffers start NaN-filled, so a tile that read or wrote past its expert's segment (or past
+M) would show up as a non-finite or mismatched value."""
+import numpy as np
+import pytest
+import torch
+
+import gpu_util as G
+from oracle import moe_oracle as O
+from ragged_grouped_gemm_device_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+FWD_CASES = {
+    "toy": lambda: W.make("toy"),
+    "toy_sorted": lambda: W.make("toy_sorted"),
+    # K tail (d = 40 < 64), column tail (h = 24: half of a 16-column chunk), empty experts
+    "edge_small": lambda: W.custom(T=77, k=3, E=9, d=40, h=24, seed=7, invalid_frac=0.05, empty_experts=(0, 4)),
+    # several row tiles per expert with ragged tails, K = 136 (tail of 8), h = 200
+    "edge_wide": lambda: W.custom(T=300, k=2, E=5, d=136, h=200, seed=8),
+    # one expert over many row tiles
+    "edge_one_expert": lambda: W.custom(T=700, k=1, E=1, d=64, h=64, seed=9),
+    # most experts empty, the last one non-empty
+    "edge_sparse": lambda: W.custom(T=100, k=1, E=64, d=64, h=72, seed=10, empty_experts=tuple(range(0, 62))),
+    "balanced": lambda: W.make("balanced"),
+    "finegrained": lambda: W.make("finegrained"),
+    "skew": lambda: W.make("skew"),
+}
+
+BWD_CASES = ["toy", "edge_small", "edge_wide", "edge_one_expert", "edge_sparse", "finegrained", "skew"]
+
+
+def _dy(wl, M):
+    """Upstream gradient at the grouped boundary: N(0,1) rows < M, NaN past M."""
+    dyh = wl.dy(max(wl.n, 1))
+    dy = G.dev_bf16(dyh)
+    dy[M:] = float("nan")
+    dyh = dyh.astype(np.float64)
+    dyh[M:] = 0.0
+    return dy, dyh
+
+
+@pytest.mark.parametrize("name", list(FWD_CASES))
+def test_grouped_forward(lib, name):
+    wl = FWD_CASES[name]()
+    run = G.GpuRun(wl).route().permute().forward()
+    torch.cuda.synchronize()
+    assert run.status.item() == 0
+    r, xp, y, u, a = G.oracle_run(wl)
+    M = r["M"]
+    G.assert_close(G.host(run.a)[:M], a[:M], f"A[{name}]")
+    G.assert_close(G.host(run.u)[:M], u[:M], f"U[{name}]")
+    G.assert_close(G.host(run.y)[:M], y[:M], f"y[{name}]")
+    # unused capacity stays outside the final offset: never written
+    assert np.isnan(G.host(run.y)[M:]).all() and np.isnan(G.host(run.a)[M:]).all()
+
+
+@pytest.mark.parametrize("name", BWD_CASES)
+def test_grouped_backward(lib, name):
+    wl = FWD_CASES[name]()
+    run = G.GpuRun(wl).route().permute().forward()
+    r, xp, y, u, a = G.oracle_run(wl)
+    M = r["M"]
+    dy, dyh = _dy(wl, M)
+    run.backward(dy)
+    torch.cuda.synchronize()
+    assert run.status.item() == 0
+    dxp, dw_ug, dw_down, du = O.expert_backward(dyh, xp, u, r["offsets"], wl.w_ug, wl.w_down)
+    G.assert_close(G.host(run.dxp)[:M], dxp[:M], f"dxp[{name}]")
+    got_ug, got_dn = G.host(run.dw_ug), G.host(run.dw_down)
+    nz = r["counts"] > 0
+    G.assert_close(got_ug[nz], dw_ug[nz], f"dW_ug[{name}]")
+    G.assert_close(got_dn[nz], dw_down[nz], f"dW_down[{name}]")
+    assert not got_ug[~nz].any() and not got_dn[~nz].any(), "empty experts must get zero gradients"
+    assert np.isnan(G.host(run.dxp)[M:]).all()
+
+
+@pytest.mark.slow
+def test_large_forward_backward_sampled_experts(lib):
+    """The large workload at full size; the oracle checks every row and gradient of a sample of
+    experts (first, last, largest, smallest and random ones)."""
+    wl = W.make("large")
+    run = G.GpuRun(wl).route().permute().forward()
+    r = O.route_offsets(wl.ids, wl.E)
+    M = r["M"]
+    experts = G.sample_experts(r["counts"], n_pick=8)
+    xp = O.permute(wl.x(), r["sorted_src"], M, wl.k)
+    y, u, a, _ = O.expert_forward(xp, r["offsets"], wl.w_ug, wl.w_down, experts)
+    dy, dyh = _dy(wl, M)
+    run.backward(dy)
+    torch.cuda.synchronize()
+    assert run.status.item() == 0
+    rows = G.rows_of(r["offsets"], experts)
+    G.assert_close(G.host(run.a)[rows], a[rows], "A[large]")
+    G.assert_close(G.host(run.y)[rows], y[rows], "y[large]")
+    dxp, dw_ug, dw_down, _ = O.expert_backward(dyh, xp, u, r["offsets"], wl.w_ug, wl.w_down, experts)
+    G.assert_close(G.host(run.dxp)[rows], dxp[rows], "dxp[large]")
+    G.assert_close(G.host(run.dw_ug[experts]), dw_ug[experts], "dW_ug[large]")
+    G.assert_close(G.host(run.dw_down[experts]), dw_down[experts], "dW_down[large]")
+    assert np.isfinite(G.host(run.y)[:M]).all() and np.isfinite(G.host(run.dxp)[:M]).all()
+
+
+def test_bad_offsets_flag_and_no_work(lib):
+    """Decreasing offsets, or a final offset beyond the buffer, set MOE_DEV_BAD_OFFSETS and the
+    kernels compute nothing."""
+    from ragged_grouped_gemm_device_gb300 import _lib
+    wl = FWD_CASES["edge_small"]()
+    run = G.GpuRun(wl)
+    for bad in ([5, 3, 9, 9, 9, 9, 9, 9, 9], [1, 2, 3, 4, 5, 6, 7, 8, wl.n + 1]):
+        run.offsets.copy_(torch.tensor(bad, dtype=torch.int32))
+        run.status.zero_()
+        _lib.moe_grouped_swiglu_fwd(run.xp, run.offsets, None, None, wl.E, run.cap, wl.d, wl.h, run.w_ug,
+                                    run.w_down, run.y, run.a, run.saved, None, run.status)
+        torch.cuda.synchronize()
+        assert run.status.item() & _lib.MOE_DEV_BAD_OFFSETS
+        assert np.isnan(G.host(run.y)).all()
+
+
+def test_single_kernel_entry_points_equal_composites(lib):
+    """The per-step entry points (one kernel each) reproduce the composite forward and backward
+    bit for bit, with routing weights folded in; the bf16-only wgrad (no low half) stays within
+    the normalised tolerance."""
+    from ragged_grouped_gemm_device_gb300 import _lib as L
+    wl = W.custom(T=300, k=4, E=7, d=136, h=200, seed=31, invalid_frac=0.05, empty_experts=(3,))
+    run = G.GpuRun(wl).route().permute()
+    n, d, h, E = run.cap, wl.d, wl.h, wl.E
+    y1, a1 = G.nan_filled((n, d)), G.nan_filled((n, h))
+    sv1 = torch.zeros_like(run.saved)
+    L.moe_grouped_swiglu_fwd(run.xp, run.offsets, run.sorted_src, run.weights, E, n, d, h, run.w_ug, run.w_down,
+                             y1, a1, sv1, None, run.status)
+    y2, a2 = G.nan_filled((n, d)), G.nan_filled((n, h))
+    sv2 = torch.zeros_like(run.saved)
+    L.moe_grouped_up_swiglu(run.xp, run.offsets, run.sorted_src, run.weights, E, n, d, h, run.w_ug, a2, sv2,
+                            run.status)
+    L.moe_grouped_down(a2, run.offsets, run.sorted_src, run.weights, E, n, d, h, run.w_down, y2, run.status)
+    dy = G.dev_bf16(wl.dy(n))
+    ws = torch.zeros(L.moe_workspace_bytes(L.OP_BWD, wl.T, wl.k, E, d, h), dtype=torch.uint8, device="cuda")
+    dxp1 = G.nan_filled((n, d))
+    dwu1 = torch.zeros(E, 2 * h, d, device="cuda")
+    dwd1 = torch.zeros(E, h, d, device="cuda")
+    L.moe_grouped_bwd(dy, run.xp, a1, sv1, run.offsets, run.sorted_src, run.weights, E, n, d, h, run.w_ug,
+                      run.w_down, dxp1, dwu1, dwd1, ws, run.status)
+    du_hi, du_lo = G.nan_filled((n, 2 * h)), G.nan_filled((n, 2 * h))
+    dxp2 = G.nan_filled((n, d))
+    dwu2, dwd2, dwu3 = (torch.zeros_like(dwu1), torch.zeros_like(dwd1), torch.zeros_like(dwu1))
+    _, p_lo, p_hi = L.saved_views(sv2, n, h)
+    L.moe_grouped_down_dgrad_swiglu(dy, sv2, run.offsets, run.sorted_src, run.weights, E, n, d, h, run.w_down,
+                                    du_hi, du_lo, run.status)
+    L.moe_grouped_up_dgrad(du_hi, run.offsets, E, n, d, h, run.w_ug, dxp2, run.status)
+    L.moe_grouped_wgrad(p_hi, p_lo, h, dy, d, run.offsets, E, n, dwd2, run.status)
+    L.moe_grouped_wgrad(du_hi, du_lo, 2 * h, run.xp, d, run.offsets, E, n, dwu2, run.status)
+    L.moe_grouped_wgrad(du_hi, None, 2 * h, run.xp, d, run.offsets, E, n, dwu3, run.status)
+    torch.cuda.synchronize()
+    assert run.status.item() == 0
+    M = int(run.offsets[-1].item())
+    for got, want in ((y2, y1), (a2, a1), (dxp2, dxp1)):
+        assert torch.equal(got[:M], want[:M])
+    assert torch.equal(sv2, sv1) and torch.equal(dwu2, dwu1) and torch.equal(dwd2, dwd1)
+    err = (dwu3 - dwu1).double().norm() / dwu1.double().norm()
+    assert err <= G.REL_NORM_TOL, f"bf16-only wgrad normalised error {err:.2e}"

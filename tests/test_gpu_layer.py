@@ -1,0 +1,67 @@
+"""The whole expert layer through the public Python layer (route -> permute -> grouped forward ->
+combine, then the backward), checked end to end against the oracle pipeline."""
+import numpy as np
+import pytest
+import torch
+
+import gpu_util as G
+from oracle import moe_oracle as O
+from ragged_grouped_gemm_device_gb300 import workloads as W
+from ragged_grouped_gemm_device_gb300.layer import ExpertLayer
+
+pytestmark = pytest.mark.gpu
+
+
+def _oracle_layer(wl, dout):
+    r = O.route_offsets(wl.ids, wl.E)
+    xp = O.permute(wl.x(), r["sorted_src"], r["M"], wl.k)
+    y, u, a, _ = O.expert_forward(xp, r["offsets"], wl.w_ug, wl.w_down)
+    out = O.combine(y, r["inv_map"], wl.weights, wl.T, wl.k)
+    dy = O.permute(dout, r["sorted_src"], r["M"], wl.k, row_scale=wl.weights)
+    dxp, dw_ug, dw_down, _ = O.expert_backward(dy, xp, u, r["offsets"], wl.w_ug, wl.w_down)
+    dx = O.combine(dxp, r["inv_map"], None, wl.T, wl.k)
+    return out, dx, dw_ug, dw_down
+
+
+@pytest.mark.parametrize("name", ["toy", "edge", "finegrained"])
+def test_layer_forward_backward(lib, name):
+    if name == "edge":
+        wl = W.custom(T=211, k=4, E=11, d=72, h=40, seed=21, invalid_frac=0.1, empty_experts=(2, 7))
+    else:
+        wl = W.make(name)
+    w_ug, w_down = G.device_weights(wl)
+    layer = ExpertLayer(w_ug, w_down)
+    doutn = wl.dout()
+    out = layer.forward(G.dev_bf16(wl.x()), G.dev_i32(wl.ids), G.dev_f32(wl.weights))
+    dx, dw_ug, dw_down = layer.backward(G.dev_bf16(doutn))
+    torch.cuda.synchronize()
+    assert layer.status.item() == 0
+    o_out, o_dx, o_ug, o_dn = _oracle_layer(wl, doutn)
+    G.assert_close(G.host(out), o_out, f"out[{name}]")
+    G.assert_close(G.host(dx), o_dx, f"dx[{name}]")
+    nz = np.bincount(wl.ids[(wl.ids >= 0) & (wl.ids < wl.E)], minlength=wl.E) > 0
+    G.assert_close(G.host(dw_ug)[nz], o_ug[nz], f"dW_ug[{name}]")
+    G.assert_close(G.host(dw_down)[nz], o_dn[nz], f"dW_down[{name}]")
+
+
+@pytest.mark.slow
+def test_large_layer_sampled_tokens(lib):
+    """Full-size large workload through the layer; the oracle recomputes a sample of tokens (a
+    token's output and input gradient depend only on its own row and its experts)."""
+    wl = W.make("large")
+    w_ug, w_down = G.device_weights(wl)
+    layer = ExpertLayer(w_ug, w_down)
+    doutn = wl.dout()
+    out = layer.forward(G.dev_bf16(wl.x()), G.dev_i32(wl.ids), G.dev_f32(wl.weights))
+    dx, _, _ = layer.backward(G.dev_bf16(doutn))
+    torch.cuda.synchronize()
+    assert layer.status.item() == 0
+    toks = np.sort(np.random.default_rng(3).choice(wl.T, size=48, replace=False))
+    sub = W.Workload("large_sub", T=toks.size, k=wl.k, E=wl.E, d=wl.d, h=wl.h, seed=wl.seed)
+    sub.ids, sub.weights = wl.ids[toks], wl.weights[toks]
+    xs, ds = wl.x()[toks], doutn[toks]
+    sub.x = lambda: xs
+    sub.w_ug, sub.w_down = wl.w_ug, wl.w_down
+    o_out, o_dx, _, _ = _oracle_layer(sub, ds)
+    G.assert_close(G.host(out)[toks], o_out, "out[large]")
+    G.assert_close(G.host(dx)[toks], o_dx, "dx[large]")
