@@ -164,10 +164,11 @@ def moe_grouped_wgrad(p_hi, p_lo, p_cols, q, q_cols, offsets, E, cap, dw, dev_st
 
 
 def saved_views(saved, cap, h):
-    """The parts of the forward's `saved` buffer (uint8 tensor): fp32 U [cap, 2h], then the low
-    and the high halves of P (bf16 [cap, h] each; P = w*A with routing weights, else A, whose
-    high half is then a_save and this slot is unused)."""
+    """The parts of the forward's `saved` buffer (a contiguous tensor of any dtype, read as bytes):
+    fp32 U [cap, 2h], then the low and the high halves of P (bf16 [cap, h] each; P = w*A with
+    routing weights, else A, whose high half is then a_save and this slot is unused)."""
     import torch
+    saved = saved.reshape(-1).view(torch.uint8)
     r = lambda b: (b + 255) // 256 * 256
     ub, pb = cap * 2 * h * 4, cap * h * 2
     u = saved[:ub].view(torch.float32).view(cap, 2 * h)

@@ -188,6 +188,13 @@ def make(name: str, seed: int = 0) -> Workload:
         logits = _rng(seed, _TAG_IDS, 6).standard_normal((wl.T, wl.E))
         wl.ids, wl.weights = _topk_softmax(logits, wl.k)
         return wl
+    if name == "medium":
+        # the large workload's expert shape with a quarter of the tokens and experts: a few GB on
+        # the device, still above the 129 MB L2 (used for detailed profiler captures)
+        wl = Workload("medium", T=4096, k=8, E=64, d=2048, h=512, seed=seed, bwd_from_dout=True)
+        logits = _rng(seed, _TAG_IDS, 7).standard_normal((wl.T, wl.E))
+        wl.ids, wl.weights = _topk_softmax(logits, wl.k)
+        return wl
     raise ValueError(f"unknown workload {name!r}")
 
 
