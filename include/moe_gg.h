@@ -245,6 +245,30 @@ moe_status_t moe_loop_swiglu_fwd(const moe_bf16* xp, const int32_t* offsets, int
                                  moe_bf16* y, moe_bf16* a_save, void* saved,
                                  int32_t* dev_status, moe_stream_t stream);
 
+/*
+ * moe_route_offsets_noalloc -- moe_route_offsets for callers that cannot allocate device memory.
+ * The pages have no counterpart: this is a library convenience. Some callers have no way to
+ * hand over a workspace: code that runs where cudaMalloc is not allowed or not safe (inside a
+ * framework's allocator or stream callbacks, under a fixed memory budget, or from a language
+ * binding with no device allocator of its own). This entry point takes no `ws`: the per-warp
+ * histogram scratch lives in one array inside the library, MOE_NOALLOC_ROUTE_SCRATCH_BYTES
+ * (1 MiB) in size, which every GPU that loads the library keeps until the process exits.
+ *
+ *  Arguments, results and status codes as moe_route_offsets (minus ws / ws_bytes); results are
+ *  bit-identical to it. Returns MOE_ERR_WORKSPACE_TOO_SMALL when the scratch it would need,
+ *  moe_workspace_bytes(MOE_OP_ROUTE, T, top_k, E, 0, 0, 0) = ceil(T*top_k/256) * E * 4 bytes,
+ *  exceeds MOE_NOALLOC_ROUTE_SCRATCH_BYTES.
+ *  Calls no cudaMalloc or cudaFree. The first call on each device looks up the array's device
+ *  address (cudaGetSymbolAddress) with that device current; make that first call before any
+ *  stream capture. Every call shares the one array and every call rewrites each entry before it
+ *  reads it, so nothing has to start at zero; but two calls that overlap on the GPU (different
+ *  streams, or different host threads) race on it and give wrong results.
+ */
+#define MOE_NOALLOC_ROUTE_SCRATCH_BYTES (1u << 20)
+moe_status_t moe_route_offsets_noalloc(const int32_t* ids, int T, int top_k, int E,
+                                       int32_t* counts, int32_t* offsets, int32_t* sorted_src,
+                                       int32_t* inv_map, moe_stream_t stream);
+
 /* Human-readable text of a status (static storage). */
 const char* moe_status_string(moe_status_t status);
 

@@ -38,6 +38,7 @@ SIGNATURES = {
     "moe_grouped_down_dgrad_swiglu": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P]),
     "moe_grouped_up_dgrad": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P]),
     "moe_grouped_wgrad": (_I, [_P, _P, _I, _P, _I, _P, _I, _I, _P, _P, _P]),
+    "moe_route_offsets_noalloc": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P]),
     "moe_status_string": (ctypes.c_char_p, [_I]),
     "moe_last_cuda_error": (ctypes.c_char_p, []),
     "moe_abi_version": (_I, []),
@@ -107,6 +108,13 @@ def moe_route_offsets(ids, T, top_k, E, counts, offsets, sorted_src, inv_map, ws
     _check("moe_route_offsets", L.moe_route_offsets(_ptr(ids), T, top_k, E, _ptr(counts), _ptr(offsets),
                                                     _ptr(sorted_src), _ptr(inv_map), _ptr(ws), ws_bytes,
                                                     _stream(stream)))
+
+
+def moe_route_offsets_noalloc(ids, T, top_k, E, counts, offsets, sorted_src, inv_map, stream=None):
+    """moe_route_offsets without a workspace: for callers that cannot allocate device memory; the
+    scratch is one fixed 1 MiB array inside the library (calls that overlap on the GPU race)."""
+    _check("moe_route_offsets_noalloc", load().moe_route_offsets_noalloc(
+        _ptr(ids), T, top_k, E, _ptr(counts), _ptr(offsets), _ptr(sorted_src), _ptr(inv_map), _stream(stream)))
 
 
 def moe_permute(x, sorted_src, offsets, row_scale, T, top_k, E, d, xp, stream=None):

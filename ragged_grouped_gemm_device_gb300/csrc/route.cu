@@ -17,6 +17,7 @@
 //                           e) + (earlier slots of e in this chunk). Slots keep flat-index
 //                           order inside a segment.
 #include <cstdint>
+#include <mutex>
 
 #include "common.cuh"
 #include "internal.h"
@@ -204,3 +205,59 @@ moe_status_t launch_route(const int32_t* ids, int n, int E, int32_t* counts, int
 }
 
 }  // namespace moe
+
+// ---------------------------------------------------------------------------------------------
+// moe_route_offsets without a caller workspace, for callers that cannot allocate device memory
+// (see include/moe_gg.h). The per-warp histogram scratch is this file-scope device array; its
+// name is only a host-side stand-in in host code, so the host looks up its device address once
+// per device and passes that address to the kernels.
+// ---------------------------------------------------------------------------------------------
+namespace moe {
+namespace {
+
+constexpr int NOALLOC_MAX_DEVICES = 64;
+static __device__ __align__(256) int32_t g_route_scratch[MOE_NOALLOC_ROUTE_SCRATCH_BYTES / sizeof(int32_t)];
+
+std::mutex g_scratch_mu;
+void* g_scratch_addr[NOALLOC_MAX_DEVICES] = {};
+
+// Device address of g_route_scratch on the current device, looked up on first use.
+moe_status_t route_scratch_address(void** addr) {
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return cuda_fail(err);
+  if (dev < 0 || dev >= NOALLOC_MAX_DEVICES) return MOE_ERR_UNSUPPORTED_DEVICE;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (g_scratch_addr[dev] == nullptr) {
+    void* p = nullptr;
+    err = cudaGetSymbolAddress(&p, g_route_scratch);
+    if (err != cudaSuccess) return cuda_fail(err);
+    g_scratch_addr[dev] = p;
+  }
+  *addr = g_scratch_addr[dev];
+  return MOE_OK;
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" moe_status_t moe_route_offsets_noalloc(const int32_t* ids, int T, int top_k, int E,
+                                                  int32_t* counts, int32_t* offsets,
+                                                  int32_t* sorted_src, int32_t* inv_map,
+                                                  moe_stream_t stream) {
+  using namespace moe;
+  if (T < 0 || top_k < 1) return MOE_ERR_INVALID_ARG;
+  if (top_k > 32 || E < 1 || E > MAX_E) return MOE_ERR_UNSUPPORTED_SHAPE;
+  const long long n = static_cast<long long>(T) * top_k;
+  if (n >= (1LL << 31)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!counts || !offsets) return MOE_ERR_INVALID_ARG;
+  if (n > 0 && (!ids || !sorted_src || !inv_map)) return MOE_ERR_INVALID_ARG;
+  // the one array has a fixed size: larger problems must use moe_route_offsets with a workspace
+  if (route_workspace_bytes(n, E) > MOE_NOALLOC_ROUTE_SCRATCH_BYTES) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  moe_status_t st = check_device();
+  if (st != MOE_OK) return st;
+  void* scratch = nullptr;
+  if ((st = route_scratch_address(&scratch)) != MOE_OK) return st;
+  return launch_route(ids, static_cast<int>(n), E, counts, offsets, sorted_src, inv_map, scratch,
+                      reinterpret_cast<cudaStream_t>(stream));
+}
