@@ -265,7 +265,7 @@ def run_ours(args):
     dw_ug = torch.empty(E, 2 * h, d, dtype=torch.float32, device=dev)
     dw_down = torch.empty(E, h, d, dtype=torch.float32, device=dev)
     status = torch.zeros(1, dtype=i32, device=dev)
-    _, p_lo, p_hi = L.saved_views(saved, n, h)
+    _, p_lo = L.saved_views(saved, n, h)
     stream = torch.cuda.current_stream()
 
     def inputs():
@@ -277,13 +277,13 @@ def run_ours(args):
             ("permute", 1, lambda: L.moe_permute(xin, sorted_src, offsets, None, T, k, E, d, xp)),
             ("up_swiglu", 1, lambda: L.moe_grouped_up_swiglu(xp, offsets, sorted_src, win, E, n, d, h, w_ug, a,
                                                              saved, status)),
-            ("down", 1, lambda: L.moe_grouped_down(a, offsets, sorted_src, win, E, n, d, h, w_down, y, status)),
+            ("down", 1, lambda: L.moe_grouped_down(a, offsets, E, n, d, h, w_down, y, status)),
             ("combine", 1, lambda: L.moe_unpermute_combine(y, inv_map, None, T, k, d, out)),
             ("combine_bwd", 1, lambda: L.moe_permute(doin, sorted_src, offsets, None, T, k, E, d, dy)),
             ("down_dgrad_swiglu", 1, lambda: L.moe_grouped_down_dgrad_swiglu(dy, saved, offsets, sorted_src, win, E,
                                                                              n, d, h, w_down, du_hi, du_lo, status)),
             ("up_dgrad", 1, lambda: L.moe_grouped_up_dgrad(du_hi, offsets, E, n, d, h, w_ug, dxp, status)),
-            ("wgrad_down", 1, lambda: L.moe_grouped_wgrad(p_hi, p_lo, h, dy, d, offsets, E, n, dw_down, status)),
+            ("wgrad_down", 1, lambda: L.moe_grouped_wgrad(a, p_lo, h, dy, d, offsets, E, n, dw_down, status)),
             ("wgrad_up", 1, lambda: L.moe_grouped_wgrad(du_hi, du_lo, 2 * h, xp, d, offsets, E, n, dw_ug, status)),
             ("permute_bwd", 1, lambda: L.moe_unpermute_combine(dxp, inv_map, None, T, k, d, dx)),
         ]

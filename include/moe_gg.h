@@ -118,20 +118,21 @@ moe_status_t moe_permute(const moe_bf16* x, const int32_t* sorted_src, const int
  *  xp         [cap, d] bf16 rows in expert order (rows >= M ignored).
  *  offsets    [E] int32 inclusive; M = offsets[E-1] must be <= cap (else MOE_DEV_BAD_OFFSETS).
  *  sorted_src, weights  nullable pair: when weights ([T*top_k] fp32, by flat slot) is given,
- *             row p of y is multiplied by weights[sorted_src[p]] in the down projection's fp32
- *             epilogue, i.e. the routing weight is applied before the combine (which is then
- *             called with weights = NULL) instead of inside it. The sum is linear, so the layer
- *             output is the same; the backward then gathers dOut without a rounding product.
+ *             row p of the SwiGLU output is multiplied by w = weights[sorted_src[p]] in the
+ *             up/gate epilogue (fp32, before the bf16 rounding), so y_p = (w A_p) W_down: the
+ *             routing weight is applied before the combine (which is then called with
+ *             weights = NULL) instead of inside it. The combine is linear, so the layer output
+ *             is the same; the backward then gathers dOut without a rounding product.
  *  w_ug       [E, 2h, d] bf16;  w_down [E, h, d] bf16.
  *  y          [cap, d] bf16 out (rows < M written).
- *  a_save     [cap, h] bf16 out: bf16(A), the down projection's input.
+ *  a_save     [cap, h] bf16 out: bf16(P) with P = w*A (P = A without weights), the down
+ *             projection's input.
  *  saved      nullable, moe_workspace_bytes(MOE_OP_SAVED, T, top_k, ...) bytes for
  *             cap = T*top_k: what the backward needs beyond a_save, written when non-NULL
- *             (training): fp32 U [cap, 2h] at byte 0; P - bf16(P) (bf16 [cap, h]) at byte
- *             S1 = round_up(cap*2h*4, 256); bf16(P) (bf16 [cap, h]) at byte
- *             S1 + round_up(cap*h*2, 256), written only with weights. P = w*A with weights,
- *             else A. Keeping U in fp32 and P as a bf16 high+low pair lets the wgrads contract
- *             over long expert segments without bf16 rounding of saved activations dominating.
+ *             (training): fp32 U [cap, 2h] at byte 0, then P - bf16(P) (bf16 [cap, h]) at byte
+ *             round_up(cap*2h*4, 256). Keeping U in fp32 and P as a bf16 high+low pair
+ *             (a_save + this) lets the wgrads contract over long expert segments without the
+ *             bf16 rounding of saved activations dominating the result.
  *  ws         moe_workspace_bytes(MOE_OP_FWD, ...) bytes (currently 0; may be NULL then).
  */
 moe_status_t moe_grouped_swiglu_fwd(const moe_bf16* xp, const int32_t* offsets,
@@ -146,7 +147,8 @@ moe_status_t moe_grouped_swiglu_fwd(const moe_bf16* xp, const int32_t* offsets,
  * §9.5): M_e is the output-row count of the dgrads and the contraction length of the wgrads.
  *   dA = w * (dy_e W_down,e^T);  dU = [dA*v*s*(1+g(1-s)), dA*silu(g)] with g,v = U[:, :h],
  *   U[:, h:], s = sigmoid(g);  dxp_e = dU W_ug,e;  dW_ug,e = dU^T xp_e;  dW_down,e = P_e^T dy_e
- * with w = weights[sorted_src[p]] and P = w*A when weights are given, else w = 1 and P = A.
+ * with w = weights[sorted_src[p]] and P = w*A (a_save + its saved low half) when weights are
+ * given, else w = 1 and P = A.
  * dU is computed in fp32 in the dgrad epilogue and kept as a bf16 high+low pair; dxp uses the
  * high half, the wgrads contract both halves (two MMAs per K step) so that dW carries about
  * 16 significant bits of the activations instead of 8.
@@ -170,9 +172,10 @@ moe_status_t moe_grouped_bwd(const moe_bf16* dy, const moe_bf16* xp, const moe_b
  * that schedule (or time) the steps themselves. Same conventions and the same `saved` layout;
  * sorted_src/weights as in moe_grouped_swiglu_fwd (nullable pair).
  *
- * moe_grouped_up_swiglu  -- U = xp_e W_ug,e^T and A = SwiGLU(U) (Eq. 13, first line); writes
- *                           a_save and, when saved is non-NULL, U and the halves of P.
- * moe_grouped_down       -- y_e = (w *) A_e W_down,e (Eq. 13, second line); a [cap, h] bf16.
+ * moe_grouped_up_swiglu  -- U = xp_e W_ug,e^T and P = (w *) SwiGLU(U) (Eq. 13, first line);
+ *                           writes a_save = bf16(P) and, when saved is non-NULL, U and P's low
+ *                           half.
+ * moe_grouped_down       -- y_e = a_e W_down,e (Eq. 13, second line); a [cap, h] bf16.
  * moe_grouped_down_dgrad_swiglu -- dA = (w *) dy_e W_down,e^T (Eq. 15 dgrad of the down
  *                           projection) with the SwiGLU backward fused: writes dU = [dgate, dup]
  *                           as bf16 high (du_hi) and low (du_lo) halves, each [cap, 2h].
@@ -181,17 +184,16 @@ moe_status_t moe_grouped_bwd(const moe_bf16* dy, const moe_bf16* xp, const moe_b
  *                           Table 15: M_e is the contraction length). P = p_hi (+ p_lo when
  *                           non-NULL: both halves are contracted, ~16-bit activations) is
  *                           [cap, p_cols] bf16, Q [cap, q_cols] bf16, dW [E, p_cols, q_cols]
- *                           fp32; experts with M_e = 0 get zeros. For dW_down: P = the saved
- *                           halves of w*A (or a_save and the low half), Q = dy; for dW_ug:
- *                           P = dU halves, Q = xp. p_cols and q_cols multiples of 8.
+ *                           fp32; experts with M_e = 0 get zeros. For dW_down: P = a_save and
+ *                           the saved low half, Q = dy; for dW_ug: P = dU halves, Q = xp.
+ *                           p_cols and q_cols multiples of 8.
  */
 moe_status_t moe_grouped_up_swiglu(const moe_bf16* xp, const int32_t* offsets,
                                    const int32_t* sorted_src, const float* weights, int E, int cap,
                                    int d, int h, const moe_bf16* w_ug, moe_bf16* a_save,
                                    void* saved, int32_t* dev_status, moe_stream_t stream);
-moe_status_t moe_grouped_down(const moe_bf16* a, const int32_t* offsets, const int32_t* sorted_src,
-                              const float* weights, int E, int cap, int d, int h,
-                              const moe_bf16* w_down, moe_bf16* y, int32_t* dev_status,
+moe_status_t moe_grouped_down(const moe_bf16* a, const int32_t* offsets, int E, int cap, int d,
+                              int h, const moe_bf16* w_down, moe_bf16* y, int32_t* dev_status,
                               moe_stream_t stream);
 moe_status_t moe_grouped_down_dgrad_swiglu(const moe_bf16* dy, const void* saved,
                                            const int32_t* offsets, const int32_t* sorted_src,

@@ -34,7 +34,7 @@ SIGNATURES = {
     "moe_padded_bmm_swiglu_fwd": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _S, _P, _P]),
     "moe_loop_swiglu_fwd": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P]),
     "moe_grouped_up_swiglu": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P]),
-    "moe_grouped_down": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P]),
+    "moe_grouped_down": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P]),
     "moe_grouped_down_dgrad_swiglu": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P]),
     "moe_grouped_up_dgrad": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P]),
     "moe_grouped_wgrad": (_I, [_P, _P, _I, _P, _I, _P, _I, _I, _P, _P, _P]),
@@ -147,10 +147,9 @@ def moe_grouped_up_swiglu(xp, offsets, sorted_src, weights, E, cap, d, h, w_ug, 
         _ptr(saved), _ptr(dev_status), _stream(stream)))
 
 
-def moe_grouped_down(a, offsets, sorted_src, weights, E, cap, d, h, w_down, y, dev_status=None, stream=None):
+def moe_grouped_down(a, offsets, E, cap, d, h, w_down, y, dev_status=None, stream=None):
     _check("moe_grouped_down", load().moe_grouped_down(
-        _ptr(a), _ptr(offsets), _ptr(sorted_src), _ptr(weights), E, cap, d, h, _ptr(w_down), _ptr(y),
-        _ptr(dev_status), _stream(stream)))
+        _ptr(a), _ptr(offsets), E, cap, d, h, _ptr(w_down), _ptr(y), _ptr(dev_status), _stream(stream)))
 
 
 def moe_grouped_down_dgrad_swiglu(dy, saved, offsets, sorted_src, weights, E, cap, d, h, w_down, du_hi, du_lo,
@@ -173,16 +172,14 @@ def moe_grouped_wgrad(p_hi, p_lo, p_cols, q, q_cols, offsets, E, cap, dw, dev_st
 
 def saved_views(saved, cap, h):
     """The parts of the forward's `saved` buffer (a contiguous tensor of any dtype, read as bytes):
-    fp32 U [cap, 2h], then the low and the high halves of P (bf16 [cap, h] each; P = w*A with
-    routing weights, else A, whose high half is then a_save and this slot is unused)."""
+    fp32 U [cap, 2h], then the low half of P = w*A (bf16 [cap, h]; the high half is a_save)."""
     import torch
     saved = saved.reshape(-1).view(torch.uint8)
-    r = lambda b: (b + 255) // 256 * 256
     ub, pb = cap * 2 * h * 4, cap * h * 2
+    off = (ub + 255) // 256 * 256
     u = saved[:ub].view(torch.float32).view(cap, 2 * h)
-    p_lo = saved[r(ub):r(ub) + pb].view(torch.bfloat16).view(cap, h)
-    p_hi = saved[r(ub) + r(pb):r(ub) + r(pb) + pb].view(torch.bfloat16).view(cap, h)
-    return u, p_lo, p_hi
+    p_lo = saved[off:off + pb].view(torch.bfloat16).view(cap, h)
+    return u, p_lo
 
 
 def moe_unpermute_combine(y, inv_map, weights, T, top_k, d, out, stream=None):

@@ -8,12 +8,13 @@
 // grid is one CTA per SM; CTA c takes tiles c, c + grid, ... ("thread blocks take tiles in
 // turn"). The host never learns M.
 //
-// Roles (192 threads, warp-specialised):
+// Roles (320 threads, warp-specialised):
 //   warp 0      TMA producer: 128B-swizzled operand tiles into a 4-stage shared-memory ring.
 //   warp 1      tensor-memory allocator and MMA issuer: tcgen05.mma 128x256x16 (bf16 in, fp32
 //               accumulate) into one of two 256-column TMEM accumulators, so the epilogue of a
 //               tile overlaps the main loop of the next.
-//   warps 2..5  epilogue: tcgen05.ld of the accumulator, fused SwiGLU (forward or backward),
+//   warps 2..9  epilogue, two warps per TMEM lane quadrant (each takes half of the tile's
+//               columns): tcgen05.ld of the accumulator, fused SwiGLU (forward or backward),
 //               conversion and row/column-masked stores. A tile that runs past its expert's
 //               segment still multiplies the neighbouring rows (rows of a product are
 //               independent) but never stores them.
@@ -42,10 +43,14 @@ constexpr int A_BYTES = BM * BK * 2;          // 16 KB
 constexpr int B_BYTES = BN * BK * 2;          // 32 KB
 constexpr int RING_BYTES = STAGES * (A_BYTES + B_BYTES);  // 192 KB, shared by every mode
 constexpr int ATOM_BYTES = 64 * BK * 2;       // one MN-major 64x64 box: 8 KB
-constexpr int THREADS = 192;
+constexpr int EPI_WARPS = 8;                 // epilogue warps: 2 per TMEM lane quadrant
+constexpr int THREADS = 64 + 32 * EPI_WARPS;
 constexpr int TMEM_COLS = 512;                // two 256-column accumulators
 constexpr int MAX_E = 1024;
 constexpr int CTL_BYTES = 256;
+// per epilogue warp, one 32-row x 16-column fp32 chunk staged for a TMA store (wgrad)
+constexpr int STAGE_OUT_BYTES = 32 * 16 * 4;
+constexpr int STAGING_BYTES = EPI_WARPS * STAGE_OUT_BYTES;
 
 struct Ctl {
   uint64_t full[STAGES];
@@ -59,7 +64,7 @@ struct Ctl {
 static_assert(sizeof(Ctl) <= CTL_BYTES, "control block too large");
 
 constexpr size_t smem_bytes_for(int E) {
-  return 1024 + static_cast<size_t>(RING_BYTES) + CTL_BYTES +
+  return 1024 + static_cast<size_t>(RING_BYTES) + STAGING_BYTES + CTL_BYTES +
          2 * sizeof(int) * static_cast<size_t>(E + 2);
 }
 
@@ -143,7 +148,8 @@ template <int MODE>
 __global__ void __launch_bounds__(THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                         const __grid_constant__ CUtensorMap map_a_lo,
-                        const __grid_constant__ CUtensorMap map_b, const GemmArgs args) {
+                        const __grid_constant__ CUtensorMap map_b,
+                        const __grid_constant__ CUtensorMap map_out, const GemmArgs args) {
   constexpr int NST = ModeTraits<MODE>::stages;
   constexpr int SB = ModeTraits<MODE>::stage_bytes;
   constexpr int APARTS = ModeTraits<MODE>::a_parts;
@@ -151,8 +157,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* stages = smem;
-  Ctl* ctl = reinterpret_cast<Ctl*>(smem + RING_BYTES);
-  int* offs = reinterpret_cast<int*>(smem + RING_BYTES + CTL_BYTES);
+  uint8_t* staging = smem + RING_BYTES;
+  Ctl* ctl = reinterpret_cast<Ctl*>(smem + RING_BYTES + STAGING_BYTES);
+  int* offs = reinterpret_cast<int*>(smem + RING_BYTES + STAGING_BYTES + CTL_BYTES);
   const int E = args.E;
   int* pre = offs + (E + 1);
 
@@ -217,7 +224,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&ctl->tfull[b]), 1);
-      mbar_init(smem_u32(&ctl->tempty[b]), 128);
+      mbar_init(smem_u32(&ctl->tempty[b]), 32 * EPI_WARPS);
     }
     mbar_init(smem_u32(&ctl->done), 1);
     ctl->abort_flag = 0;
@@ -313,16 +320,14 @@ __global__ void __launch_bounds__(THREADS, 1)
         if constexpr (ModeTraits<MODE>::wgrad) {
           const int valid = ti.kvalid - kb * BK;
           if (valid < BK) {
-            // rows [valid, 64) of every 64x64 box belong to the next expert: zero them
-            const int nrows = BK - valid;
-            const int per_atom = nrows * 8;
-            const int total = SB / ATOM_BYTES * per_atom;
-            for (int c = lane; c < total; c += 32) {
-              const int atom = c / per_atom;
-              const int rem = c - atom * per_atom;
-              const int r = valid + (rem >> 3);
-              *reinterpret_cast<uint4*>(sp + atom * ATOM_BYTES + r * 128 + (rem & 7) * 16) =
-                  make_uint4(0u, 0u, 0u, 0u);
+            // rows [valid, 64) of every 64x64 box belong to the next expert: zero them. The
+            // swizzle only permutes 16-byte pieces inside a 128-byte row, so those rows are the
+            // contiguous bytes [valid * 128, 8192) of each box.
+            const int pieces = (BK - valid) * 8;
+#pragma unroll
+            for (int atom = 0; atom < SB / ATOM_BYTES; ++atom) {
+              uint4* base = reinterpret_cast<uint4*>(sp + atom * ATOM_BYTES + valid * 128);
+              for (int c = lane; c < pieces; c += 32) base[c] = make_uint4(0u, 0u, 0u, 0u);
             }
             fence_proxy_async_smem();
           }
@@ -359,8 +364,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     __syncwarp();
     mbar_wait(smem_u32(&ctl->done), 0u, abort_flag, status, tmo, false);
   } else {
-    // =========================================================== epilogue (warps 2..5)
+    // =========================================================== epilogue (warps 2..9)
     const int q = warp & 3;           // TMEM lane quadrant this warp may access
+    const int half = (warp - 2) >> 2; // which half of the tile's columns this warp stores
     const int r_in = q * 32 + lane;   // accumulator row = TMEM lane
     uint32_t acc = 0;
     for (int t = blockIdx.x; t < sc.total; t += gridDim.x) {
@@ -372,7 +378,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (mrow < args.Mdim) {
             float* dst = reinterpret_cast<float*>(args.out) +
                          (static_cast<long long>(ti.e + expert_base) * args.Mdim + mrow) * args.ldo;
-            for (int c = ti.n0; c < min(ti.n0 + BN, args.N); c += 4)
+            for (int c = ti.n0 + half * (BN / 2); c < min(ti.n0 + (half + 1) * (BN / 2), args.N); c += 4)
               *reinterpret_cast<float4*>(dst + c) = make_float4(0.f, 0.f, 0.f, 0.f);
           }
           continue;
@@ -390,27 +396,25 @@ __global__ void __launch_bounds__(THREADS, 1)
         bf16* arow = reinterpret_cast<bf16*>(args.out) + row * args.ldo;
         float* urow = args.out2 ? reinterpret_cast<float*>(args.out2) + row * args.ldo2 : nullptr;
         bf16* lrow = args.out3 ? reinterpret_cast<bf16*>(args.out3) + row * args.ldo3 : nullptr;
-        // P = w*A (its high half in out4) when row weights are given, else P = A
-        const bool weighted = args.row_weight != nullptr;
-        bf16* prow = weighted && args.out4 ? reinterpret_cast<bf16*>(args.out4) + row * args.ldo3 : nullptr;
-        const float wrow = (weighted && rv) ? __ldg(args.row_weight + __ldg(args.row_src + row)) : 1.0f;
+        // P = w*A with the row's routing weight (else P = A): bf16(P) is the down projection's
+        // input, P - bf16(P) its low half for the down wgrad
+        const float wrow =
+            (args.row_weight != nullptr && rv) ? __ldg(args.row_weight + __ldg(args.row_src + row)) : 1.0f;
 #pragma unroll 1
-        for (int c = 0; c < 8; ++c) {
+        for (int c = half * 4; c < half * 4 + 4; ++c) {
           uint32_t g[16], u[16];
           tmem_ld16(tb + c * 16, g);
           tmem_ld16(tb + 128 + c * 16, u);
           tmem_ld_wait2(g, u);
           const int col = ti.n0 + c * 16;
           if (rv && col < h) {
-            uint32_t pa[8], pl[8], ph[8];
+            uint32_t pa[8], pl[8];
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-              const float a0 = silu_f(__uint_as_float(g[2 * j])) * __uint_as_float(u[2 * j]);
-              const float a1 = silu_f(__uint_as_float(g[2 * j + 1])) * __uint_as_float(u[2 * j + 1]);
-              pa[j] = pack_bf16x2(a0, a1);
-              const float p0 = wrow * a0, p1 = wrow * a1;
-              ph[j] = weighted ? pack_bf16x2(p0, p1) : pa[j];
-              pl[j] = pack_bf16x2(p0 - bf16_lo(ph[j]), p1 - bf16_hi(ph[j]));
+              const float p0 = wrow * (silu_f(__uint_as_float(g[2 * j])) * __uint_as_float(u[2 * j]));
+              const float p1 = wrow * (silu_f(__uint_as_float(g[2 * j + 1])) * __uint_as_float(u[2 * j + 1]));
+              pa[j] = pack_bf16x2(p0, p1);
+              pl[j] = pack_bf16x2(p0 - bf16_lo(pa[j]), p1 - bf16_hi(pa[j]));
             }
             const bool two = col + 16 <= h;
             st_global_v4(arow + col, pa[0], pa[1], pa[2], pa[3]);
@@ -418,10 +422,6 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (lrow) {
               st_global_v4(lrow + col, pl[0], pl[1], pl[2], pl[3]);
               if (two) st_global_v4(lrow + col + 8, pl[4], pl[5], pl[6], pl[7]);
-            }
-            if (prow) {
-              st_global_v4(prow + col, ph[0], ph[1], ph[2], ph[3]);
-              if (two) st_global_v4(prow + col + 8, ph[4], ph[5], ph[6], ph[7]);
             }
             if (urow) {
 #pragma unroll
@@ -438,10 +438,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         const bool rv = r_in < ti.rows;
         const long long row = ti.row0 + r_in;
         bf16* orow = reinterpret_cast<bf16*>(args.out) + row * args.ldo;
-        const float wrow =
-            (args.row_weight != nullptr && rv) ? __ldg(args.row_weight + __ldg(args.row_src + row)) : 1.0f;
 #pragma unroll 1
-        for (int c = 0; c < BN / 16; c += 2) {
+        for (int c = half * (BN / 32); c < (half + 1) * (BN / 32); c += 2) {
           uint32_t v0[16], v1[16];
           tmem_ld16(tb + c * 16, v0);
           tmem_ld16(tb + (c + 1) * 16, v1);
@@ -451,8 +449,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             uint32_t p[16];
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-              p[j] = pack_bf16x2(wrow * __uint_as_float(v0[2 * j]), wrow * __uint_as_float(v0[2 * j + 1]));
-              p[8 + j] = pack_bf16x2(wrow * __uint_as_float(v1[2 * j]), wrow * __uint_as_float(v1[2 * j + 1]));
+              p[j] = pack_bf16x2(__uint_as_float(v0[2 * j]), __uint_as_float(v0[2 * j + 1]));
+              p[8 + j] = pack_bf16x2(__uint_as_float(v1[2 * j]), __uint_as_float(v1[2 * j + 1]));
             }
 #pragma unroll
             for (int hq = 0; hq < 4; ++hq)
@@ -469,8 +467,26 @@ __global__ void __launch_bounds__(THREADS, 1)
         const float* srow = reinterpret_cast<const float*>(args.aux) + row * args.ld_aux;
         const float wrow =
             (args.row_weight != nullptr && rv) ? __ldg(args.row_weight + __ldg(args.row_src + row)) : 1.0f;
+        // the saved U of chunk c + 1 is loaded while chunk c is processed
+        auto load_u = [&](int c, float4 (&gq)[4], float4 (&uq)[4]) {
+          const int col = ti.n0 + c * 16;
+          const bool ok = rv && col < h, two = col + 16 <= h;
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            gq[q4] = make_float4(0.f, 0.f, 0.f, 0.f);
+            uq[q4] = gq[q4];
+            if (ok && (q4 < 2 || two)) {
+              gq[q4] = __ldg(reinterpret_cast<const float4*>(srow + col + 4 * q4));
+              uq[q4] = __ldg(reinterpret_cast<const float4*>(srow + h + col + 4 * q4));
+            }
+          }
+        };
+        const int cb = half * (BN / 32), ce = cb + BN / 32;
+        float4 gcur[4], ucur[4], gnxt[4], unxt[4];
+        load_u(cb, gcur, ucur);
 #pragma unroll 1
-        for (int c = 0; c < BN / 16; ++c) {
+        for (int c = cb; c < ce; ++c) {
+          if (c + 1 < ce) load_u(c + 1, gnxt, unxt);
           uint32_t v[16];
           tmem_ld16(tb + c * 16, v);
           tmem_ld_wait(v);
@@ -480,13 +496,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             float gv[16], uv[16];
 #pragma unroll
             for (int q4 = 0; q4 < 4; ++q4) {
-              float4 gq = make_float4(0.f, 0.f, 0.f, 0.f), uq = gq;
-              if (q4 < 2 || two) {
-                gq = *reinterpret_cast<const float4*>(srow + col + 4 * q4);
-                uq = *reinterpret_cast<const float4*>(srow + h + col + 4 * q4);
-              }
-              gv[4 * q4] = gq.x; gv[4 * q4 + 1] = gq.y; gv[4 * q4 + 2] = gq.z; gv[4 * q4 + 3] = gq.w;
-              uv[4 * q4] = uq.x; uv[4 * q4 + 1] = uq.y; uv[4 * q4 + 2] = uq.z; uv[4 * q4 + 3] = uq.w;
+              gv[4 * q4] = gcur[q4].x; gv[4 * q4 + 1] = gcur[q4].y; gv[4 * q4 + 2] = gcur[q4].z; gv[4 * q4 + 3] = gcur[q4].w;
+              uv[4 * q4] = ucur[q4].x; uv[4 * q4 + 1] = ucur[q4].y; uv[4 * q4 + 2] = ucur[q4].z; uv[4 * q4 + 3] = ucur[q4].w;
             }
             uint32_t gh[8], gl[8], uh[8], ul[8];
 #pragma unroll
@@ -516,24 +527,39 @@ __global__ void __launch_bounds__(THREADS, 1)
               st_global_v4(lrow + h + col + 8, ul[4], ul[5], ul[6], ul[7]);
             }
           }
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            gcur[q4] = gnxt[q4];
+            ucur[q4] = unxt[q4];
+          }
         }
       } else {  // wgrad modes
-        const int mrow = ti.m0 + r_in;
-        const bool rv = mrow < args.Mdim;
-        float* dst = reinterpret_cast<float*>(args.out) +
-                     (static_cast<long long>(ti.e + expert_base) * args.Mdim + mrow) * args.ldo;
+        // Each 32-row x 16-column fp32 chunk goes through this warp's staging buffer (64-byte
+        // swizzle: lane r writes its row's 16-byte piece j at piece j ^ ((r >> 1) & 3), which
+        // keeps the shared-memory writes conflict-free) and out by a TMA tensor store, which
+        // writes whole lines and clips at the gradient's row and column bounds.
+        uint8_t* sbuf = staging + (warp - 2) * STAGE_OUT_BYTES;
+        const uint32_t sbuf_addr = smem_u32(sbuf);
+        const int sw = (lane >> 1) & 3;
+        const bool rows_in = ti.m0 + q * 32 < args.Mdim;  // warp-uniform
 #pragma unroll 1
-        for (int c = 0; c < BN / 16; ++c) {
+        for (int c = half * (BN / 32); c < (half + 1) * (BN / 32); ++c) {
           uint32_t v[16];
           tmem_ld16(tb + c * 16, v);
           tmem_ld_wait(v);
-          const int col = ti.n0 + c * 16;
-          if (rv) {
+          // a box that would start past the gradient's last row or column is not stored
+          if (!rows_in || ti.n0 + c * 16 >= args.N) continue;
+          if (lane == 0) bulk_wait_group_read0();  // the previous chunk has left the buffer
+          __syncwarp();
 #pragma unroll
-            for (int hq = 0; hq < 4; ++hq)
-              if (col + hq * 4 < args.N)
-                *reinterpret_cast<uint4*>(dst + col + hq * 4) =
-                    make_uint4(v[4 * hq], v[4 * hq + 1], v[4 * hq + 2], v[4 * hq + 3]);
+          for (int j = 0; j < 4; ++j)
+            *reinterpret_cast<uint4*>(sbuf + lane * 64 + ((j ^ sw) << 4)) =
+                make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_3d(&map_out, sbuf_addr, ti.n0 + c * 16, ti.m0 + q * 32, ti.e + expert_base);
+            bulk_commit_group();
           }
         }
       }
@@ -544,6 +570,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 
   // ---- teardown: every role has finished (or given up); release tensor memory
+  if (ModeTraits<MODE>::wgrad && warp >= 2 && lane == 0) bulk_wait_group0();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -574,14 +601,15 @@ EncodeTiledFn encode_fn() {
 
 template <int MODE>
 moe_status_t launch_mode(const CUtensorMap& a, const CUtensorMap& a_lo, const CUtensorMap& b,
-                         const GemmArgs& args, long long max_tiles, cudaStream_t stream) {
+                         const CUtensorMap& out, const GemmArgs& args, long long max_tiles,
+                         cudaStream_t stream) {
   const size_t smem = smem_bytes_for(args.E);
   const cudaError_t attr_err = ensure_max_dynamic_smem(
       reinterpret_cast<const void*>(grouped_gemm_kernel<MODE>), static_cast<int>(smem_bytes_for(MAX_E)));
   if (attr_err != cudaSuccess) return cuda_fail(attr_err);
   const long long sms = device_sm_count();
   const int grid = static_cast<int>(std::max(1LL, std::min(sms, max_tiles)));
-  grouped_gemm_kernel<MODE><<<grid, THREADS, smem, stream>>>(a, a_lo, b, args);
+  grouped_gemm_kernel<MODE><<<grid, THREADS, smem, stream>>>(a, a_lo, b, out, args);
   const cudaError_t err = cudaGetLastError();
   return err == cudaSuccess ? MOE_OK : cuda_fail(err);
 }
@@ -606,6 +634,20 @@ bool make_map_rows2d(CUtensorMap* map, const void* ptr, long long rows, long lon
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool make_map_grad3d_f32(CUtensorMap* map, const void* ptr, long long E, long long R, long long C) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || E <= 0 || R <= 0 || C <= 0) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(C), static_cast<cuuint64_t>(R),
+                              static_cast<cuuint64_t>(E)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(C) * 4,
+                                 static_cast<cuuint64_t>(R) * static_cast<cuuint64_t>(C) * 4};
+  const cuuint32_t box[3] = {16u, 32u, 1u};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(ptr), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool make_map_weight3d(CUtensorMap* map, const void* ptr, long long E, long long R, long long C,
                        int box_r) {
   EncodeTiledFn fn = encode_fn();
@@ -623,15 +665,20 @@ bool make_map_weight3d(CUtensorMap* map, const void* ptr, long long E, long long
 
 moe_status_t launch_grouped_gemm(int mode, const CUtensorMap& a, const CUtensorMap& a_lo,
                                  const CUtensorMap& b, const GemmArgs& args, long long max_tiles,
-                                 cudaStream_t stream) {
+                                 cudaStream_t stream, const CUtensorMap* out) {
   if (args.E < 1 || args.E > MAX_E) return MOE_ERR_UNSUPPORTED_SHAPE;
+  const CUtensorMap& o = out ? *out : a;
   switch (mode) {
-    case MODE_UP_SWIGLU: return launch_mode<MODE_UP_SWIGLU>(a, a_lo, b, args, max_tiles, stream);
-    case MODE_PLAIN_BF16: return launch_mode<MODE_PLAIN_BF16>(a, a_lo, b, args, max_tiles, stream);
+    case MODE_UP_SWIGLU: return launch_mode<MODE_UP_SWIGLU>(a, a_lo, b, o, args, max_tiles, stream);
+    case MODE_PLAIN_BF16: return launch_mode<MODE_PLAIN_BF16>(a, a_lo, b, o, args, max_tiles, stream);
     case MODE_DGRAD_SWIGLU:
-      return launch_mode<MODE_DGRAD_SWIGLU>(a, a_lo, b, args, max_tiles, stream);
-    case MODE_WGRAD: return launch_mode<MODE_WGRAD>(a, a_lo, b, args, max_tiles, stream);
-    case MODE_WGRAD_BF16: return launch_mode<MODE_WGRAD_BF16>(a, a_lo, b, args, max_tiles, stream);
+      return launch_mode<MODE_DGRAD_SWIGLU>(a, a_lo, b, o, args, max_tiles, stream);
+    case MODE_WGRAD:
+      if (!out) return MOE_ERR_INVALID_ARG;
+      return launch_mode<MODE_WGRAD>(a, a_lo, b, o, args, max_tiles, stream);
+    case MODE_WGRAD_BF16:
+      if (!out) return MOE_ERR_INVALID_ARG;
+      return launch_mode<MODE_WGRAD_BF16>(a, a_lo, b, o, args, max_tiles, stream);
     default: return MOE_ERR_INVALID_ARG;
   }
 }

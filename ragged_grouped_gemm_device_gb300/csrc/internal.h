@@ -13,7 +13,8 @@ namespace moe {
 // ------------------------------------------------------------------ grouped GEMM (tcgen05)
 enum GemmMode : int {
   // U = X W_ug^T per row segment, gate and up column blocks in one accumulator; the epilogue
-  // writes bf16(A) for A = silu(gate) * up, and optionally U (fp32) and A - bf16(A) (bf16).
+  // writes bf16(P) for P = w * silu(gate) * up (w = 1 without routing weights), and optionally
+  // U (fp32) and P - bf16(P) (bf16).
   // A: rows [cap, d] K-major; B: W_ug [E, 2h, d].
   MODE_UP_SWIGLU = 0,
   // Y = P W per row segment with W [E, K, N] (N contiguous, MN-major B); bf16 store.
@@ -46,10 +47,9 @@ struct GemmArgs {
   long long ldo2;
   void* out3;              // UP_SWIGLU: optional low half of P [cap, h] (P = w*A, or A)
   long long ldo3;
-  void* out4;              // UP_SWIGLU with row weights: high half of P = w*A [cap, h]
-  // Optional routing weight of each row: w = row_weight[row_src[row]]. UP_SWIGLU writes P = w*A
-  // for the down wgrad; PLAIN_BF16 scales its output rows (the down projection); DGRAD_SWIGLU
-  // scales dA before the SwiGLU backward.
+  // Optional routing weight of each row: w = row_weight[row_src[row]]. UP_SWIGLU writes
+  // P = w*A (high half to `out`, low half to out3); DGRAD_SWIGLU scales dA by w before the
+  // SwiGLU backward.
   const int32_t* row_src;
   const float* row_weight;
   const void* aux;         // DGRAD_SWIGLU: saved fp32 U [cap, 2h]
@@ -63,7 +63,7 @@ struct GemmArgs {
 // bounds the grid (the exact tile count is only known on the device).
 moe_status_t launch_grouped_gemm(int mode, const CUtensorMap& a, const CUtensorMap& a_lo,
                                  const CUtensorMap& b, const GemmArgs& args, long long max_tiles,
-                                 cudaStream_t stream);
+                                 cudaStream_t stream, const CUtensorMap* out = nullptr);
 
 // Tensor maps (bf16, 128-byte swizzle, zero fill outside the tensor).
 //   rows2d: a [rows, cols] row-major matrix; box = 64 columns x box_rows rows.
@@ -72,6 +72,8 @@ bool make_map_rows2d(CUtensorMap* map, const void* ptr, long long rows, long lon
                      int box_rows);
 bool make_map_weight3d(CUtensorMap* map, const void* ptr, long long E, long long R, long long C,
                        int box_r);
+//   grad3d_f32: an fp32 [E, R, C] gradient, stored through 16-column x 32-row boxes, 64B swizzle.
+bool make_map_grad3d_f32(CUtensorMap* map, const void* ptr, long long E, long long R, long long C);
 
 int gemm_tiles_n(int mode, int N);  // column tiles of one problem
 

@@ -44,23 +44,20 @@ GemmArgs base_args(int E, int cap, int32_t* status) {
   return a;
 }
 
-// saved = fp32 U [rows, 2h] | low half of P [rows, h] | high half of P [rows, h], P = w*A (or A)
+// saved = fp32 U [rows, 2h] | low half of P [rows, h], P = w*A (or A); the high half is a_save
 size_t saved_u_bytes(long long rows, int h) { return round256(static_cast<size_t>(rows) * 2 * h * 4); }
 size_t saved_p_bytes(long long rows, int h) { return round256(static_cast<size_t>(rows) * h * 2); }
-size_t saved_bytes(long long rows, int h) { return saved_u_bytes(rows, h) + 2 * saved_p_bytes(rows, h); }
+size_t saved_bytes(long long rows, int h) { return saved_u_bytes(rows, h) + saved_p_bytes(rows, h); }
 const void* saved_p_lo(const void* saved, long long rows, int h) {
   return static_cast<const uint8_t*>(saved) + saved_u_bytes(rows, h);
-}
-const void* saved_p_hi(const void* saved, long long rows, int h) {
-  return static_cast<const uint8_t*>(saved) + saved_u_bytes(rows, h) + saved_p_bytes(rows, h);
 }
 size_t bwd_ws_half(long long rows, int h) { return round256(static_cast<size_t>(rows) * 2 * h * 2); }
 
 // ---- one launch per step; `src` carries the problem source (device offsets, uniform rows or
 // one expert), `rows` the rows of the row buffers, `tiles_bound` an upper bound of row tiles.
 
-// a6: U = xp W_ug^T, A = SwiGLU(U); saved (nullable) receives fp32 U and the halves of P
-// (P = w*A when src carries row weights, else P = A and its high half is a_save itself).
+// a6: U = xp W_ug^T, P = w*SwiGLU(U) (w = 1 without row weights) into a_save as bf16; saved
+// (nullable) receives fp32 U and the low half of P.
 moe_status_t run_up_swiglu(const GemmArgs& src, long long rows, long long tiles_bound, int E, int d,
                            int h, const void* xp, const void* w_ug, void* a_save, void* saved,
                            cudaStream_t s) {
@@ -77,7 +74,6 @@ moe_status_t run_up_swiglu(const GemmArgs& src, long long rows, long long tiles_
     a.out2 = saved;
     a.ldo2 = 2LL * h;
     a.out3 = const_cast<void*>(saved_p_lo(saved, rows, h));
-    a.out4 = const_cast<void*>(saved_p_hi(saved, rows, h));
     a.ldo3 = h;
   }
   return launch_grouped_gemm(MODE_UP_SWIGLU, ma, ma, mb, a,
@@ -152,8 +148,10 @@ moe_status_t run_wgrad(const GemmArgs& src, long long rows, int E, const void* p
   a.Mdim = p_cols;
   a.out = dw;
   a.ldo = q_cols;
+  CUtensorMap mo;
+  if (!make_map_grad3d_f32(&mo, dw, E, p_cols, q_cols)) return map_fail("dw");
   const long long tiles = static_cast<long long>(E) * ((p_cols + 127) / 128) * ((q_cols + 255) / 256);
-  return launch_grouped_gemm(p_lo ? MODE_WGRAD : MODE_WGRAD_BF16, ma, ml, mb, a, tiles, s);
+  return launch_grouped_gemm(p_lo ? MODE_WGRAD : MODE_WGRAD_BF16, ma, ml, mb, a, tiles, s, &mo);
 }
 
 moe_status_t check_grouped_common(int E, int cap, int d, int h) {
@@ -327,19 +325,16 @@ moe_status_t moe_grouped_up_swiglu(const moe_bf16* xp, const int32_t* offsets,
                        reinterpret_cast<cudaStream_t>(stream));
 }
 
-moe_status_t moe_grouped_down(const moe_bf16* a, const int32_t* offsets, const int32_t* sorted_src,
-                              const float* weights, int E, int cap, int d, int h,
-                              const moe_bf16* w_down, moe_bf16* y, int32_t* dev_status,
+moe_status_t moe_grouped_down(const moe_bf16* a, const int32_t* offsets, int E, int cap, int d,
+                              int h, const moe_bf16* w_down, moe_bf16* y, int32_t* dev_status,
                               moe_stream_t stream) {
   moe_status_t st = check_grouped_common(E, cap, d, h);
   if (st != MOE_OK) return st;
-  if (!a || !offsets || !w_down || !y || (weights && !sorted_src)) return MOE_ERR_INVALID_ARG;
+  if (!a || !offsets || !w_down || !y) return MOE_ERR_INVALID_ARG;
   if (!aligned16(a) || !aligned16(w_down) || !aligned16(y)) return MOE_ERR_INVALID_ARG;
   if ((st = check_device()) != MOE_OK || cap == 0) return st;
   GemmArgs src = base_args(E, cap, dev_status);
   src.offsets = offsets;
-  src.row_src = sorted_src;
-  src.row_weight = weights;
   return run_down(src, cap, row_tiles_bound(cap, E), E, d, h, a, w_down, y,
                   reinterpret_cast<cudaStream_t>(stream));
 }
@@ -420,7 +415,9 @@ moe_status_t moe_grouped_swiglu_fwd(const moe_bf16* xp, const int32_t* offsets,
   const long long tb = row_tiles_bound(cap, E);
   st = run_up_swiglu(src, cap, tb, E, d, h, xp, w_ug, a_save, saved, s);
   if (st != MOE_OK) return st;
-  return run_down(src, cap, tb, E, d, h, a_save, w_down, y, s);
+  GemmArgs dsrc = base_args(E, cap, dev_status);  // the weight is already in a_save
+  dsrc.offsets = offsets;
+  return run_down(dsrc, cap, tb, E, d, h, a_save, w_down, y, s);
 }
 
 moe_status_t moe_grouped_bwd(const moe_bf16* dy, const moe_bf16* xp, const moe_bf16* a_save,
@@ -445,8 +442,8 @@ moe_status_t moe_grouped_bwd(const moe_bf16* dy, const moe_bf16* xp, const moe_b
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   moe_bf16* du_hi = static_cast<moe_bf16*>(ws);
   moe_bf16* du_lo = reinterpret_cast<moe_bf16*>(static_cast<uint8_t*>(ws) + half);
-  // P = w*A when the forward folded the routing weights in, else P = A (high half = a_save)
-  const void* p_hi = weights ? saved_p_hi(saved, cap, h) : static_cast<const void*>(a_save);
+  // P = w*A (or A): its high half is a_save, its low half is in saved
+  const void* p_hi = a_save;
   const void* p_lo = saved_p_lo(saved, cap, h);
   GemmArgs src = base_args(E, cap, dev_status);
   src.offsets = offsets;

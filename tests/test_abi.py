@@ -34,8 +34,8 @@ def test_workspace_sizes_are_host_arithmetic(lib):
     assert _lib.moe_workspace_bytes(_lib.OP_FWD, 16384, 8, 256, 2048, 512) == 0
     # backward: dU high and low halves, [n, 2h] bf16 each
     assert _lib.moe_workspace_bytes(_lib.OP_BWD, 16384, 8, 256, 2048, 512) == 2 * 16384 * 8 * 1024 * 2
-    # saved state: fp32 U [n, 2h] and the two bf16 halves of P [n, h]
-    assert _lib.moe_workspace_bytes(_lib.OP_SAVED, 16384, 8, 256, 2048, 512) == 16384 * 8 * (1024 * 4 + 2 * 512 * 2)
+    # saved state: fp32 U [n, 2h] and the low bf16 half of P [n, h]
+    assert _lib.moe_workspace_bytes(_lib.OP_SAVED, 16384, 8, 256, 2048, 512) == 16384 * 8 * (1024 * 4 + 512 * 2)
     bmm = _lib.moe_workspace_bytes(_lib.OP_PADDED_BMM, 10, 1, 4, 64, 128, 4)
     assert bmm == 2 * (16 * 64 * 2) + 16 * 128 * 2  # [16, 64] bf16 x2 and [16, 128] bf16
     assert _lib.moe_workspace_bytes(_lib.OP_ROUTE, 10, 1, 0) == 0      # invalid E

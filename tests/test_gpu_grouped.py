@@ -134,7 +134,7 @@ def test_single_kernel_entry_points_equal_composites(lib):
     sv2 = torch.zeros_like(run.saved)
     L.moe_grouped_up_swiglu(run.xp, run.offsets, run.sorted_src, run.weights, E, n, d, h, run.w_ug, a2, sv2,
                             run.status)
-    L.moe_grouped_down(a2, run.offsets, run.sorted_src, run.weights, E, n, d, h, run.w_down, y2, run.status)
+    L.moe_grouped_down(a2, run.offsets, E, n, d, h, run.w_down, y2, run.status)
     dy = G.dev_bf16(wl.dy(n))
     ws = torch.zeros(L.moe_workspace_bytes(L.OP_BWD, wl.T, wl.k, E, d, h), dtype=torch.uint8, device="cuda")
     dxp1 = G.nan_filled((n, d))
@@ -145,11 +145,11 @@ def test_single_kernel_entry_points_equal_composites(lib):
     du_hi, du_lo = G.nan_filled((n, 2 * h)), G.nan_filled((n, 2 * h))
     dxp2 = G.nan_filled((n, d))
     dwu2, dwd2, dwu3 = (torch.zeros_like(dwu1), torch.zeros_like(dwd1), torch.zeros_like(dwu1))
-    _, p_lo, p_hi = L.saved_views(sv2, n, h)
+    _, p_lo = L.saved_views(sv2, n, h)
     L.moe_grouped_down_dgrad_swiglu(dy, sv2, run.offsets, run.sorted_src, run.weights, E, n, d, h, run.w_down,
                                     du_hi, du_lo, run.status)
     L.moe_grouped_up_dgrad(du_hi, run.offsets, E, n, d, h, run.w_ug, dxp2, run.status)
-    L.moe_grouped_wgrad(p_hi, p_lo, h, dy, d, run.offsets, E, n, dwd2, run.status)
+    L.moe_grouped_wgrad(a2, p_lo, h, dy, d, run.offsets, E, n, dwd2, run.status)
     L.moe_grouped_wgrad(du_hi, du_lo, 2 * h, run.xp, d, run.offsets, E, n, dwu2, run.status)
     L.moe_grouped_wgrad(du_hi, None, 2 * h, run.xp, d, run.offsets, E, n, dwu3, run.status)
     torch.cuda.synchronize()
