@@ -6,7 +6,9 @@
 // memory, derives each expert's row segment and 128-row tile count, and prefix-sums the tile
 // counts; a tile index then maps to (expert, row block, column block) by binary search. The
 // grid is one CTA per SM; CTA c takes tiles c, c + grid, ... ("thread blocks take tiles in
-// turn"). The host never learns M.
+// turn"). The wgrad modes launch as clusters of two: cluster c takes pair tiles c, c +
+// clusters, ..., a pair tile being two 128-row tiles that share their B operand, which the two
+// CTAs load half each and multicast to both. The host never learns M.
 //
 // Roles (320 threads, warp-specialised):
 //   warp 0      TMA producer: 128B-swizzled operand tiles into a 4-stage shared-memory ring.
@@ -78,6 +80,14 @@ struct ModeTraits {
   static constexpr int a_parts = (MODE == MODE_WGRAD) ? 2 : 1;
   static constexpr int stage_bytes = a_parts * A_BYTES + B_BYTES;
   static constexpr int stages = RING_BYTES / stage_bytes;
+  // Cluster pairs: two CTAs take two row tiles that share the B tile (row tiles 2j and 2j+1 of
+  // one expert, or of one expert's gradient); each loads half of B and multicasts it to both,
+  // so each SM pulls a third fewer operand bytes. An expert with an odd number of row tiles
+  // leaves one CTA of its last pair idle, which cost more than the saved bytes in the
+  // row-grouped modes (measured on the large workload), so only the wgrad modes pair up: a
+  // gradient's row tiles come in even numbers whenever the width is a multiple of 256.
+  static constexpr bool pair = wgrad;
+  static_assert(pair == wgrad, "the producer pairs exactly the wgrad modes");
 };
 
 struct Tile {
@@ -88,6 +98,7 @@ struct Tile {
   int n0;       // first output column
   int kblocks;  // K blocks of 64
   int kvalid;   // wgrad: contraction length M_e
+  bool active;  // cluster pairs: false when this CTA's half of the pair has no rows
 };
 
 struct Sched {
@@ -96,19 +107,26 @@ struct Sched {
   int E;
   int nt;           // column tiles per problem
   int mt;           // wgrad: row tiles per expert gradient
+  int mdim;         // wgrad: rows of each expert's gradient
   int kblocks;      // row-grouped: K blocks
-  int total;
+  int total;        // tiles (pair tiles for cluster pairs)
 };
 
 template <int MODE>
-__device__ __forceinline__ Tile decode_tile(const Sched& s, int t) {
+__device__ __forceinline__ Tile decode_tile(const Sched& s, int t, int rank) {
   Tile ti;
+  ti.active = true;
   if constexpr (ModeTraits<MODE>::wgrad) {
-    const int per = s.mt * s.nt;
+    // (expert, row tile, column tile); with cluster pairs the row index counts pairs of row
+    // tiles and this CTA takes row tile 2 * pair + rank
+    constexpr bool P = ModeTraits<MODE>::pair;
+    const int mp = P ? (s.mt + 1) / 2 : s.mt;
+    const int per = mp * s.nt;
     ti.e = t / per;
     const int r = t - ti.e * per;
     const int mi = r / s.nt;
-    ti.m0 = mi * BM;
+    ti.m0 = (P ? 2 * mi + rank : mi) * BM;
+    ti.active = ti.m0 < s.mdim;
     ti.n0 = (r - mi * s.nt) * BN;
     ti.row0 = s.offs[ti.e];
     ti.kvalid = s.offs[ti.e + 1] - ti.row0;
@@ -117,16 +135,24 @@ __device__ __forceinline__ Tile decode_tile(const Sched& s, int t) {
   } else {
     const int g = t / s.nt;
     const int n = t - g * s.nt;
-    // largest e with pre[e] <= g (experts without tiles have pre[e] == pre[e+1])
+    // largest e with pre[e] <= g (experts without tiles have pre[e] == pre[e+1]); pre counts
+    // pairs of 128-row tiles per expert
     int lo = 0, hi = s.E;
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
       if (s.pre[mid] <= g) lo = mid; else hi = mid;
     }
     ti.e = lo;
-    const int mloc = g - s.pre[lo];
-    ti.row0 = s.offs[lo] + mloc * BM;
-    ti.rows = min(BM, s.offs[lo + 1] - ti.row0);
+    if constexpr (ModeTraits<MODE>::pair) {
+      const int mloc = 2 * (g - s.pre[lo]) + rank;
+      const int me = s.offs[lo + 1] - s.offs[lo];
+      ti.row0 = s.offs[lo] + mloc * BM;
+      ti.rows = min(BM, me - mloc * BM);
+      ti.active = mloc * BM < me;
+    } else {
+      ti.row0 = s.offs[lo] + (g - s.pre[lo]) * BM;
+      ti.rows = min(BM, s.offs[lo + 1] - ti.row0);
+    }
     ti.n0 = n * ModeTraits<MODE>::out_cols_per_tile;
     ti.m0 = 0;
     ti.kblocks = s.kblocks;
@@ -192,11 +218,13 @@ __global__ void __launch_bounds__(THREADS, 1)
   sc.E = E;
   if constexpr (ModeTraits<MODE>::wgrad) {
     sc.mt = (args.Mdim + BM - 1) / BM;
+    sc.mdim = args.Mdim;
     sc.nt = (args.N + BN - 1) / BN;
     sc.kblocks = 0;
-    sc.total = E * sc.mt * sc.nt;
+    sc.total = E * (ModeTraits<MODE>::pair ? (sc.mt + 1) / 2 : sc.mt) * sc.nt;
   } else {
     sc.mt = 0;
+    sc.mdim = 0;
     sc.nt = (args.N + ModeTraits<MODE>::out_cols_per_tile - 1) / ModeTraits<MODE>::out_cols_per_tile;
     sc.kblocks = (args.K + BK - 1) / BK;
     if (warp == 0) {
@@ -204,7 +232,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (lane == 0) pre[0] = 0;
       for (int base = 0; base < E; base += 32) {
         const int e = base + lane;
-        int v = (e < E) ? (offs[e + 1] - offs[e] + BM - 1) / BM : 0;
+        const int mt_e = (e < E) ? (offs[e + 1] - offs[e] + BM - 1) / BM : 0;
+        int v = ModeTraits<MODE>::pair ? (mt_e + 1) / 2 : mt_e;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
           const int nb = __shfl_up_sync(0xffffffffu, v, o);
@@ -220,7 +249,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (tid == 0) {
     for (int s = 0; s < NST; ++s) {
       mbar_init(smem_u32(&ctl->full[s]), 1);
-      mbar_init(smem_u32(&ctl->empty[s]), 1);
+      mbar_init(smem_u32(&ctl->empty[s]), ModeTraits<MODE>::pair ? 2 : 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&ctl->tfull[b]), 1);
@@ -240,7 +269,13 @@ __global__ void __launch_bounds__(THREADS, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // the peer's barriers must exist before any multicast or remote arrive can reach them
+  if constexpr (ModeTraits<MODE>::pair) cluster_sync_all();
   if constexpr (!ModeTraits<MODE>::wgrad) sc.total = pre[E] * sc.nt;
+  constexpr bool PAIR = ModeTraits<MODE>::pair;
+  const int rank = PAIR ? static_cast<int>(cluster_ctarank()) : 0;
+  const int t_first = PAIR ? static_cast<int>(cluster_id_x()) : static_cast<int>(blockIdx.x);
+  const int t_step = PAIR ? static_cast<int>(nclusters_x()) : static_cast<int>(gridDim.x);
   const uint32_t tmem_base = ctl->tmem_base;
   volatile int* abort_flag = &ctl->abort_flag;
   const long long tmo = args.timeout_ns;
@@ -252,8 +287,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (lane == 0) {
       uint32_t it = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < sc.total && ok; t += gridDim.x) {
-        const Tile ti = decode_tile<MODE>(sc, t);
+      for (int t = t_first; t < sc.total && ok; t += t_step) {
+        const Tile ti = decode_tile<MODE>(sc, t, rank);
         const int eg = ti.e + expert_base;
         for (int kb = 0; kb < ti.kblocks; ++kb, ++it) {
           const int s = it % NST;
@@ -263,32 +298,43 @@ __global__ void __launch_bounds__(THREADS, 1)
             break;
           }
           const uint32_t fb = smem_u32(&ctl->full[s]);
-          mbar_arrive_expect_tx(fb, SB);
+          mbar_arrive_expect_tx(fb, (!PAIR || ti.active) ? SB : B_BYTES);
           const uint32_t sa = stage0 + s * SB;
           const uint32_t sb = sa + APARTS * A_BYTES;
           const int k0 = kb * BK;
+          // A: this CTA's own rows. The B tile is loaded whole into this CTA's shared memory,
+          // except with cluster pairs (wgrad), where this CTA loads half `rank` and multicasts it
+          // to both CTAs of the pair (multicast exists only in cluster launches). The issue path
+          // is kept straight-line: it is on the critical path of the MN-major modes.
           if constexpr (MODE == MODE_UP_SWIGLU) {
             tma_load_2d(sa, &map_a, k0, ti.row0, fb);
-            tma_load_3d(sb, &map_b, k0, ti.n0, eg, fb);                    // gate rows
-            tma_load_3d(sb + B_BYTES / 2, &map_b, k0, args.h + ti.n0, eg, fb);  // up rows
+            tma_load_3d(sb, &map_b, k0, ti.n0, eg, fb);                            // gate rows
+            tma_load_3d(sb + B_BYTES / 2, &map_b, k0, args.h + ti.n0, eg, fb);     // up rows
           } else if constexpr (MODE == MODE_PLAIN_BF16) {
             tma_load_2d(sa, &map_a, k0, ti.row0, fb);
 #pragma unroll
-            for (int i = 0; i < BN / 64; ++i) tma_load_3d(sb + i * ATOM_BYTES, &map_b, ti.n0 + 64 * i, k0, eg, fb);
+            for (int i = 0; i < BN / 64; ++i)
+              tma_load_3d(sb + i * ATOM_BYTES, &map_b, ti.n0 + 64 * i, k0, eg, fb);
           } else if constexpr (MODE == MODE_DGRAD_SWIGLU) {
             tma_load_2d(sa, &map_a, k0, ti.row0, fb);
-            tma_load_3d(sb, &map_b, k0, ti.n0, eg, fb);
+            tma_load_3d(sb, &map_b, k0, ti.n0, eg, fb);  // 256 rows of W_down in one box
           } else {
-            const int rk = ti.row0 + k0;
+            static_assert(ModeTraits<MODE>::pair, "the wgrad modes load B as cluster pairs");
+            const int rk = ti.row0 + k0;  // first contraction row of this K block
+            if (ti.active) {
 #pragma unroll
-            for (int i = 0; i < BM / 64; ++i) tma_load_2d(sa + i * ATOM_BYTES, &map_a, ti.m0 + 64 * i, rk, fb);
-            if constexpr (APARTS == 2) {
+              for (int i = 0; i < BM / 64; ++i) tma_load_2d(sa + i * ATOM_BYTES, &map_a, ti.m0 + 64 * i, rk, fb);
+              if constexpr (APARTS == 2) {
 #pragma unroll
-              for (int i = 0; i < BM / 64; ++i)
-                tma_load_2d(sa + A_BYTES + i * ATOM_BYTES, &map_a_lo, ti.m0 + 64 * i, rk, fb);
+                for (int i = 0; i < BM / 64; ++i)
+                  tma_load_2d(sa + A_BYTES + i * ATOM_BYTES, &map_a_lo, ti.m0 + 64 * i, rk, fb);
+              }
             }
 #pragma unroll
-            for (int i = 0; i < BN / 64; ++i) tma_load_2d(sb + i * ATOM_BYTES, &map_b, ti.n0 + 64 * i, rk, fb);
+            for (int i = 0; i < 2; ++i) {
+              const int box = 2 * rank + i;
+              tma_load_2d_mc(sb + box * ATOM_BYTES, &map_b, ti.n0 + 64 * box, rk, fb, 0x3);
+            }
           }
         }
       }
@@ -302,13 +348,16 @@ __global__ void __launch_bounds__(THREADS, 1)
     constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, ModeTraits<MODE>::a_mn, ModeTraits<MODE>::b_mn);
     uint32_t it = 0, acc = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < sc.total && ok; t += gridDim.x) {
-      const Tile ti = decode_tile<MODE>(sc, t);
+    for (int t = t_first; t < sc.total && ok; t += t_step) {
+      const Tile ti = decode_tile<MODE>(sc, t, rank);
       if (ti.kblocks == 0) continue;
       const uint32_t buf = acc & 1u, use = acc >> 1;
-      ok = warp_all(mbar_wait(smem_u32(&ctl->tempty[buf]), (use & 1u) ^ 1u, abort_flag, status, tmo));
-      if (!ok) break;
-      tc_fence_after();
+      const bool act = !PAIR || ti.active;  // compile-time true without cluster pairs
+      if (act) {
+        ok = warp_all(mbar_wait(smem_u32(&ctl->tempty[buf]), (use & 1u) ^ 1u, abort_flag, status, tmo));
+        if (!ok) break;
+        tc_fence_after();
+      }
       const uint32_t dtm = tmem_base + buf * BN;
       for (int kb = 0; kb < ti.kblocks; ++kb, ++it) {
         const int s = it % NST;
@@ -319,7 +368,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         uint8_t* sp = stages + s * SB;
         if constexpr (ModeTraits<MODE>::wgrad) {
           const int valid = ti.kvalid - kb * BK;
-          if (valid < BK) {
+          if (valid < BK && act) {
             // rows [valid, 64) of every 64x64 box belong to the next expert: zero them. The
             // swizzle only permutes 16-byte pieces inside a 128-byte row, so those rows are the
             // contiguous bytes [valid * 128, 8192) of each box.
@@ -347,17 +396,21 @@ __global__ void __launch_bounds__(THREADS, 1)
               const uint64_t bd = ModeTraits<MODE>::b_mn
                                       ? smem_desc_sw128(sb + ks * (UK * 128), ATOM_BYTES, 1024)
                                       : smem_desc_sw128(sb + ks * (UK * 2), 16, 1024);
-              mma_bf16_ss(dtm, ad, bd, idesc, (kb | ks | part) != 0 ? 1u : 0u);
+              if (act) mma_bf16_ss(dtm, ad, bd, idesc, (kb | ks | part) != 0 ? 1u : 0u);
             }
           }
-          mma_commit(smem_u32(&ctl->empty[s]));
+          // release the stage (for cluster pairs: in both CTAs, whose producers refill it)
+          if constexpr (PAIR) mma_commit_mc(smem_u32(&ctl->empty[s]), 0x3);
+          else mma_commit(smem_u32(&ctl->empty[s]));
         }
         __syncwarp();
       }
       if (!ok) break;
-      if (lane == 0) mma_commit(smem_u32(&ctl->tfull[buf]));
-      __syncwarp();
-      ++acc;
+      if (act) {
+        if (lane == 0) mma_commit(smem_u32(&ctl->tfull[buf]));
+        __syncwarp();
+        ++acc;
+      }
     }
     // every MMA this thread issued must finish before tensor memory is released
     if (lane == 0) mma_commit(smem_u32(&ctl->done));
@@ -369,8 +422,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int half = (warp - 2) >> 2; // which half of the tile's columns this warp stores
     const int r_in = q * 32 + lane;   // accumulator row = TMEM lane
     uint32_t acc = 0;
-    for (int t = blockIdx.x; t < sc.total; t += gridDim.x) {
-      const Tile ti = decode_tile<MODE>(sc, t);
+    for (int t = t_first; t < sc.total; t += t_step) {
+      const Tile ti = decode_tile<MODE>(sc, t, rank);
+      if (PAIR && !ti.active) continue;
       if constexpr (ModeTraits<MODE>::wgrad) {
         if (ti.kblocks == 0) {
           // empty expert: its gradient is zero
@@ -573,6 +627,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (ModeTraits<MODE>::wgrad && warp >= 2 && lane == 0) bulk_wait_group0();
   tc_fence_before();
   __syncthreads();
+  // neither CTA of a pair leaves while the other may still write to its shared memory
+  if constexpr (ModeTraits<MODE>::pair) cluster_sync_all();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, TMEM_COLS);
@@ -608,8 +664,34 @@ moe_status_t launch_mode(const CUtensorMap& a, const CUtensorMap& a_lo, const CU
       reinterpret_cast<const void*>(grouped_gemm_kernel<MODE>), static_cast<int>(smem_bytes_for(MAX_E)));
   if (attr_err != cudaSuccess) return cuda_fail(attr_err);
   const long long sms = device_sm_count();
-  const int grid = static_cast<int>(std::max(1LL, std::min(sms, max_tiles)));
-  grouped_gemm_kernel<MODE><<<grid, THREADS, smem, stream>>>(a, a_lo, b, out, args);
+  if constexpr (ModeTraits<MODE>::pair) {
+    // clusters of two CTAs, as many as can be resident at once (persistent)
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(sms & ~1LL));
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, grouped_gemm_kernel<MODE>, &cfg) != cudaSuccess ||
+        clusters < 1) {
+      cudaGetLastError();
+      clusters = static_cast<int>(sms / 2);
+    }
+    const long long pairs = std::max(1LL, std::min<long long>(clusters, (max_tiles + 1) / 2));
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
+    const cudaError_t lerr = cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<MODE>, a, a_lo, b, out, args);
+    if (lerr != cudaSuccess) return cuda_fail(lerr);
+  } else {
+    const int grid = static_cast<int>(std::max(1LL, std::min(sms, max_tiles)));
+    grouped_gemm_kernel<MODE><<<grid, THREADS, smem, stream>>>(a, a_lo, b, out, args);
+  }
   const cudaError_t err = cudaGetLastError();
   return err == cudaSuccess ? MOE_OK : cuda_fail(err);
 }
