@@ -195,21 +195,28 @@ class ClockSampler:
 
 # ------------------------------------------------------------------------------ our arm
 def kernel_source_hash():
+    """Hash of the kernel sources: DRAM traffic taken by the profiler is valid only for them."""
     h = hashlib.sha256()
-    for name in ("grouped_gemm.cu", "common.cuh", "permute.cu", "route.cu"):
-        with open(os.path.join(ROOT, "ragged_grouped_gemm_device_gb300", "csrc", name), "rb") as f:
+    csrc = os.path.join(ROOT, "ragged_grouped_gemm_device_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
 def load_traffic():
-    """DRAM bytes per launch from the committed ncu summary, if the kernels are unchanged."""
-    path = os.path.join(ROOT, "profiles", "traffic.json")
+    """DRAM bytes per launch (large workload) from the committed ncu summary, if the kernels are
+    unchanged since the capture: the summary's `traffic_per_launch_large:` line holds a JSON
+    object with the source hash and the bytes per kernel."""
+    path = os.path.join(ROOT, "profiles", "ncu_full_grouped_gemm_medium.md")
     if not os.path.exists(path):
         return {}
     with open(path) as f:
-        t = json.load(f)
-    return t.get("kernels", {}) if t.get("source_hash") == kernel_source_hash() else {}
+        for line in f:
+            if line.startswith("traffic_per_launch_large:"):
+                t = json.loads(line.split(":", 1)[1])
+                return t.get("kernels", {}) if t.get("source_hash") == kernel_source_hash() else {}
+    return {}
 
 
 def run_ours(args):
