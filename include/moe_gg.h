@@ -127,12 +127,20 @@ moe_status_t moe_permute(const moe_bf16* x, const int32_t* sorted_src, const int
  *  y          [cap, d] bf16 out (rows < M written).
  *  a_save     [cap, h] bf16 out: bf16(P) with P = w*A (P = A without weights), the down
  *             projection's input.
- *  saved      nullable, moe_workspace_bytes(MOE_OP_SAVED, T, top_k, ...) bytes for
+ *  saved      nullable, moe_workspace_bytes(MOE_OP_SAVED, T, top_k, E, d, h) bytes for
  *             cap = T*top_k: what the backward needs beyond a_save, written when non-NULL
- *             (training): fp32 U [cap, 2h] at byte 0, then P - bf16(P) (bf16 [cap, h]) at byte
- *             round_up(cap*2h*4, 256). Keeping U in fp32 and P as a bf16 high+low pair
- *             (a_save + this) lets the wgrads contract over long expert segments without the
- *             bf16 rounding of saved activations dominating the result.
+ *             (training). Byte 0: P - bf16(P), bf16 [cap, h] row-major. Byte
+ *             round_up(cap*h*2, 256): U in fp32, blocked as the kernels' epilogues hold it --
+ *             for the G-th 128-row tile of the problem list (experts in order, ceil(M_e/128)
+ *             tiles each, at most (cap + 127 E)/128), lane quadrant q (tile rows 32q..32q+31)
+ *             and 16-column chunk ci (ci < H = ceil(h/16): gate columns 16ci..; else up columns
+ *             16(ci-H)..), a 2 KB block at float offset ((G*4 + q)*2H + ci)*512 holding float4
+ *             j (columns 4j..4j+3 of the chunk) of tile row 32q+l at float4 j*32 + l. The
+ *             slots of tile rows past the expert's segment are left unwritten. Keeping U in
+ *             fp32 and P as a bf16 high+low pair (a_save + the low half) lets the wgrads
+ *             contract over long expert segments without the bf16 rounding of saved
+ *             activations dominating the result; the blocked U makes each warp's store (and
+ *             the dgrad's load) of it one contiguous 512-byte access.
  *  ws         moe_workspace_bytes(MOE_OP_FWD, ...) bytes (currently 0; may be NULL then).
  */
 moe_status_t moe_grouped_swiglu_fwd(const moe_bf16* xp, const int32_t* offsets,

@@ -172,13 +172,15 @@ def moe_grouped_wgrad(p_hi, p_lo, p_cols, q, q_cols, offsets, E, cap, dw, dev_st
 
 def saved_views(saved, cap, h):
     """The parts of the forward's `saved` buffer (a contiguous tensor of any dtype, read as bytes):
-    fp32 U [cap, 2h], then the low half of P = w*A (bf16 [cap, h]; the high half is a_save)."""
+    the low half of P = w*A (bf16 [cap, h]; the high half is a_save) at byte 0, then fp32 U in
+    the kernels' blocked layout (a flat fp32 view; see the header for the block order)."""
     import torch
     saved = saved.reshape(-1).view(torch.uint8)
-    ub, pb = cap * 2 * h * 4, cap * h * 2
-    off = (ub + 255) // 256 * 256
-    u = saved[:ub].view(torch.float32).view(cap, 2 * h)
-    p_lo = saved[off:off + pb].view(torch.bfloat16).view(cap, h)
+    pb = cap * h * 2
+    off = (pb + 255) // 256 * 256
+    p_lo = saved[:pb].view(torch.bfloat16).view(cap, h)
+    ub = (saved.numel() - off) // 4 * 4
+    u = saved[off:off + ub].view(torch.float32)
     return u, p_lo
 
 

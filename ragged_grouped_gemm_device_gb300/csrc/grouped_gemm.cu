@@ -92,6 +92,7 @@ struct ModeTraits {
 
 struct Tile {
   int e;        // expert index within the problem list
+  int g;        // row-grouped: row tile index over the whole problem list
   int row0;     // first row of the tile (row-grouped) or of the expert segment (wgrad)
   int rows;     // valid rows of the tile (row-grouped)
   int m0;       // wgrad: first output row
@@ -132,6 +133,7 @@ __device__ __forceinline__ Tile decode_tile(const Sched& s, int t, int rank) {
     ti.kvalid = s.offs[ti.e + 1] - ti.row0;
     ti.kblocks = (ti.kvalid + BK - 1) / BK;
     ti.rows = 0;
+    ti.g = 0;
   } else {
     const int g = t / s.nt;
     const int n = t - g * s.nt;
@@ -143,6 +145,7 @@ __device__ __forceinline__ Tile decode_tile(const Sched& s, int t, int rank) {
       if (s.pre[mid] <= g) lo = mid; else hi = mid;
     }
     ti.e = lo;
+    ti.g = g;
     if constexpr (ModeTraits<MODE>::pair) {
       const int mloc = 2 * (g - s.pre[lo]) + rank;
       const int me = s.offs[lo + 1] - s.offs[lo];
@@ -163,7 +166,27 @@ __device__ __forceinline__ Tile decode_tile(const Sched& s, int t, int rank) {
 
 __device__ __forceinline__ bool warp_all(bool v) { return __all_sync(0xffffffffu, v); }
 
-__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
+// x / (1 + e^-x) and 1 / (1 + e^-x) with the approximate division (an infinite denominator
+// gives 0, the limit)
+__device__ __forceinline__ float silu_f(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
+__device__ __forceinline__ float sigmoid_f(float g) { return __fdividef(1.0f, 1.0f + __expf(-g)); }
+
+// The saved fp32 U, blocked the way the epilogue holds it: for row tile G (of the problem
+// list), TMEM lane quadrant q and 16-column chunk ci (ci < H16 = ceil(h/16): gate columns
+// 16ci.., else up columns 16(ci - H16)..), one 2 KB block of 4 x 32 float4 with float4 j of
+// lane l at j * 32 + l. A warp's load or store of one float4 per lane is then one contiguous
+// 512 bytes, and the chunks of one (G, q) are contiguous. Each row tile owns its blocks; the
+// slots of its rows past the expert's segment are neither written nor read.
+__device__ __forceinline__ float4* u_block(const void* base, long long G, int q, int ci, int c2) {
+  return const_cast<float4*>(reinterpret_cast<const float4*>(base)) + ((G * 4 + q) * c2 + ci) * 128;
+}
+
+// 32-byte store (sm_100+ global vector width); the address must be 32-byte aligned
+__device__ __forceinline__ void st_global_v8(void* p, const uint32_t* v) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(v[0]), "r"(v[1]),
+               "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
+}
 
 __device__ __forceinline__ void st_global_v4(void* p, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {
@@ -438,6 +461,28 @@ __global__ void __launch_bounds__(THREADS, 1)
           continue;
         }
       }
+      // dgrad: the saved U does not depend on the accumulator, so this warp requests its first
+      // chunk before waiting for the tile. (An L2 prefetch of the next tile's U measured slower.)
+      float4 gcur[4], ucur[4];
+      if constexpr (MODE == MODE_DGRAD_SWIGLU) {
+        const int h16 = (args.h + 15) >> 4;
+        const int cw = BN / 32;  // 16-column chunks per warp
+        const int c0 = (ti.n0 >> 4) + half * cw;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          gcur[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+          ucur[j] = gcur[j];
+        }
+        if (r_in < ti.rows && c0 < h16) {
+          const float4* bg = u_block(args.aux, args.tile_base + ti.g, q, c0, 2 * h16);
+          const float4* bu = u_block(args.aux, args.tile_base + ti.g, q, h16 + c0, 2 * h16);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            gcur[j] = __ldg(bg + j * 32 + lane);
+            ucur[j] = __ldg(bu + j * 32 + lane);
+          }
+        }
+      }
       const uint32_t buf = acc & 1u, use = acc >> 1;
       if (!warp_all(mbar_wait(smem_u32(&ctl->tfull[buf]), use & 1u, abort_flag, status, tmo))) break;
       tc_fence_after();
@@ -448,8 +493,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         const long long row = ti.row0 + r_in;
         const int h = args.h;
         bf16* arow = reinterpret_cast<bf16*>(args.out) + row * args.ldo;
-        float* urow = args.out2 ? reinterpret_cast<float*>(args.out2) + row * args.ldo2 : nullptr;
         bf16* lrow = args.out3 ? reinterpret_cast<bf16*>(args.out3) + row * args.ldo3 : nullptr;
+        const long long G = args.tile_base + ti.g;
+        const int h16 = (h + 15) >> 4;
         // P = w*A with the row's routing weight (else P = A): bf16(P) is the down projection's
         // input, P - bf16(P) its low half for the down wgrad
         const float wrow =
@@ -461,6 +507,16 @@ __global__ void __launch_bounds__(THREADS, 1)
           tmem_ld16(tb + 128 + c * 16, u);
           tmem_ld_wait2(g, u);
           const int col = ti.n0 + c * 16;
+          if (args.out2 != nullptr && rv && col < h) {
+            // U in its blocked layout: 512 contiguous bytes per warp-wide store
+            uint32_t* bg = reinterpret_cast<uint32_t*>(u_block(args.out2, G, q, col >> 4, 2 * h16));
+            uint32_t* bu = reinterpret_cast<uint32_t*>(u_block(args.out2, G, q, h16 + (col >> 4), 2 * h16));
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              st_global_v4(bg + (j * 32 + lane) * 4, g[4 * j], g[4 * j + 1], g[4 * j + 2], g[4 * j + 3]);
+              st_global_v4(bu + (j * 32 + lane) * 4, u[4 * j], u[4 * j + 1], u[4 * j + 2], u[4 * j + 3]);
+            }
+          }
           if (rv && col < h) {
             uint32_t pa[8], pl[8];
 #pragma unroll
@@ -471,19 +527,15 @@ __global__ void __launch_bounds__(THREADS, 1)
               pl[j] = pack_bf16x2(p0 - bf16_lo(pa[j]), p1 - bf16_hi(pa[j]));
             }
             const bool two = col + 16 <= h;
-            st_global_v4(arow + col, pa[0], pa[1], pa[2], pa[3]);
-            if (two) st_global_v4(arow + col + 8, pa[4], pa[5], pa[6], pa[7]);
-            if (lrow) {
-              st_global_v4(lrow + col, pl[0], pl[1], pl[2], pl[3]);
-              if (two) st_global_v4(lrow + col + 8, pl[4], pl[5], pl[6], pl[7]);
-            }
-            if (urow) {
-#pragma unroll
-              for (int q4 = 0; q4 < 4; ++q4) {
-                if (q4 < 2 || two) {
-                  st_global_v4(urow + col + 4 * q4, g[4 * q4], g[4 * q4 + 1], g[4 * q4 + 2], g[4 * q4 + 3]);
-                  st_global_v4(urow + h + col + 4 * q4, u[4 * q4], u[4 * q4 + 1], u[4 * q4 + 2], u[4 * q4 + 3]);
-                }
+            if (args.vec32) {
+              st_global_v8(arow + col, pa);
+              if (lrow) st_global_v8(lrow + col, pl);
+            } else {
+              st_global_v4(arow + col, pa[0], pa[1], pa[2], pa[3]);
+              if (two) st_global_v4(arow + col + 8, pa[4], pa[5], pa[6], pa[7]);
+              if (lrow) {
+                st_global_v4(lrow + col, pl[0], pl[1], pl[2], pl[3]);
+                if (two) st_global_v4(lrow + col + 8, pl[4], pl[5], pl[6], pl[7]);
               }
             }
           }
@@ -516,75 +568,109 @@ __global__ void __launch_bounds__(THREADS, 1)
         const bool rv = r_in < ti.rows;
         const long long row = ti.row0 + r_in;
         const int h = args.h;
+        const int h16 = (h + 15) >> 4;
+        const long long G = args.tile_base + ti.g;
         bf16* hrow = reinterpret_cast<bf16*>(args.out) + row * args.ldo;
         bf16* lrow = reinterpret_cast<bf16*>(args.out2) + row * args.ldo2;
-        const float* srow = reinterpret_cast<const float*>(args.aux) + row * args.ld_aux;
         const float wrow =
             (args.row_weight != nullptr && rv) ? __ldg(args.row_weight + __ldg(args.row_src + row)) : 1.0f;
-        // the saved U of chunk c + 1 is loaded while chunk c is processed
+        // saved U of chunk c (zeros past the last column chunk), one coalesced float4 per lane
         auto load_u = [&](int c, float4 (&gq)[4], float4 (&uq)[4]) {
-          const int col = ti.n0 + c * 16;
-          const bool ok = rv && col < h, two = col + 16 <= h;
+          const int ci = (ti.n0 >> 4) + c;
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            gq[q4] = make_float4(0.f, 0.f, 0.f, 0.f);
-            uq[q4] = gq[q4];
-            if (ok && (q4 < 2 || two)) {
-              gq[q4] = __ldg(reinterpret_cast<const float4*>(srow + col + 4 * q4));
-              uq[q4] = __ldg(reinterpret_cast<const float4*>(srow + h + col + 4 * q4));
+          for (int j = 0; j < 4; ++j) {
+            gq[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+            uq[j] = gq[j];
+          }
+          if (rv && ci < h16) {
+            const float4* bg = u_block(args.aux, G, q, ci, 2 * h16);
+            const float4* bu = u_block(args.aux, G, q, h16 + ci, 2 * h16);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              gq[j] = __ldg(bg + j * 32 + lane);
+              uq[j] = __ldg(bu + j * 32 + lane);
             }
           }
         };
-        const int cb = half * (BN / 32), ce = cb + BN / 32;
-        float4 gcur[4], ucur[4], gnxt[4], unxt[4];
-        load_u(cb, gcur, ucur);
-#pragma unroll 1
-        for (int c = cb; c < ce; ++c) {
-          if (c + 1 < ce) load_u(c + 1, gnxt, unxt);
-          uint32_t v[16];
-          tmem_ld16(tb + c * 16, v);
-          tmem_ld_wait(v);
+        // dA = w * acc; dgate = dA * up * s * (1 + gate * (1 - s)), dup = dA * silu(gate), as
+        // bf16 high and low halves
+        auto process = [&](int c, const uint32_t (&v)[16]) {
           const int col = ti.n0 + c * 16;
-          if (rv && col < h) {
-            const bool two = col + 16 <= h;
-            float gv[16], uv[16];
+          if (!rv || col >= h) return;
+          const bool two = col + 16 <= h;
+          const float gv[16] = {gcur[0].x, gcur[0].y, gcur[0].z, gcur[0].w, gcur[1].x, gcur[1].y,
+                                gcur[1].z, gcur[1].w, gcur[2].x, gcur[2].y, gcur[2].z, gcur[2].w,
+                                gcur[3].x, gcur[3].y, gcur[3].z, gcur[3].w};
+          const float uv[16] = {ucur[0].x, ucur[0].y, ucur[0].z, ucur[0].w, ucur[1].x, ucur[1].y,
+                                ucur[1].z, ucur[1].w, ucur[2].x, ucur[2].y, ucur[2].z, ucur[2].w,
+                                ucur[3].x, ucur[3].y, ucur[3].z, ucur[3].w};
+          uint32_t gh[8], gl[8], uh[8], ul[8];
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-              gv[4 * q4] = gcur[q4].x; gv[4 * q4 + 1] = gcur[q4].y; gv[4 * q4 + 2] = gcur[q4].z; gv[4 * q4 + 3] = gcur[q4].w;
-              uv[4 * q4] = ucur[q4].x; uv[4 * q4 + 1] = ucur[q4].y; uv[4 * q4 + 2] = ucur[q4].z; uv[4 * q4 + 3] = ucur[q4].w;
-            }
-            uint32_t gh[8], gl[8], uh[8], ul[8];
+          for (int j = 0; j < 8; ++j) {
+            float dg[2], du[2];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              float dg[2], du[2];
-#pragma unroll
-              for (int hh = 0; hh < 2; ++hh) {
-                const float g = gv[2 * j + hh], uu = uv[2 * j + hh];
-                const float da = wrow * __uint_as_float(v[2 * j + hh]);
-                const float sg = 1.0f / (1.0f + __expf(-g));
-                dg[hh] = da * uu * sg * (1.0f + g * (1.0f - sg));
-                du[hh] = da * g * sg;
-              }
-              gh[j] = pack_bf16x2(dg[0], dg[1]);
-              uh[j] = pack_bf16x2(du[0], du[1]);
-              gl[j] = pack_bf16x2(dg[0] - bf16_lo(gh[j]), dg[1] - bf16_hi(gh[j]));
-              ul[j] = pack_bf16x2(du[0] - bf16_lo(uh[j]), du[1] - bf16_hi(uh[j]));
+            for (int hh = 0; hh < 2; ++hh) {
+              const float g = gv[2 * j + hh], uu = uv[2 * j + hh];
+              const float da = wrow * __uint_as_float(v[2 * j + hh]);
+              const float sg = sigmoid_f(g);
+              dg[hh] = da * uu * sg * (1.0f + g * (1.0f - sg));
+              du[hh] = da * g * sg;
             }
-            st_global_v4(hrow + col, gh[0], gh[1], gh[2], gh[3]);
-            st_global_v4(hrow + h + col, uh[0], uh[1], uh[2], uh[3]);
-            st_global_v4(lrow + col, gl[0], gl[1], gl[2], gl[3]);
-            st_global_v4(lrow + h + col, ul[0], ul[1], ul[2], ul[3]);
-            if (two) {
-              st_global_v4(hrow + col + 8, gh[4], gh[5], gh[6], gh[7]);
-              st_global_v4(hrow + h + col + 8, uh[4], uh[5], uh[6], uh[7]);
-              st_global_v4(lrow + col + 8, gl[4], gl[5], gl[6], gl[7]);
-              st_global_v4(lrow + h + col + 8, ul[4], ul[5], ul[6], ul[7]);
-            }
+            gh[j] = pack_bf16x2(dg[0], dg[1]);
+            uh[j] = pack_bf16x2(du[0], du[1]);
+            gl[j] = pack_bf16x2(dg[0] - bf16_lo(gh[j]), dg[1] - bf16_hi(gh[j]));
+            ul[j] = pack_bf16x2(du[0] - bf16_lo(uh[j]), du[1] - bf16_hi(uh[j]));
           }
+          if (args.vec32) {
+            // whole 16-column chunks (h % 16 == 0), 32-byte aligned rows: one full sector a row
+            st_global_v8(hrow + col, gh);
+            st_global_v8(hrow + h + col, uh);
+            st_global_v8(lrow + col, gl);
+            st_global_v8(lrow + h + col, ul);
+            return;
+          }
+          st_global_v4(hrow + col, gh[0], gh[1], gh[2], gh[3]);
+          st_global_v4(hrow + h + col, uh[0], uh[1], uh[2], uh[3]);
+          st_global_v4(lrow + col, gl[0], gl[1], gl[2], gl[3]);
+          st_global_v4(lrow + h + col, ul[0], ul[1], ul[2], ul[3]);
+          if (two) {
+            st_global_v4(hrow + col + 8, gh[4], gh[5], gh[6], gh[7]);
+            st_global_v4(hrow + h + col + 8, uh[4], uh[5], uh[6], uh[7]);
+            st_global_v4(lrow + col + 8, gl[4], gl[5], gl[6], gl[7]);
+            st_global_v4(lrow + h + col + 8, ul[4], ul[5], ul[6], ul[7]);
+          }
+        };
+        const int cb = half * (BN / 32), ce = cb + BN / 32;  // an even number of chunks
+        float4 gnxt[4], unxt[4];
+        uint32_t v0[16], v1[16];
+        tmem_ld16(tb + cb * 16, v0);
+        tmem_ld_wait(v0);
+        // two chunks per iteration: the accumulator columns and saved U of the next chunk are
+        // in flight while the current one is processed
+#pragma unroll 1
+        for (int c = cb; c < ce; c += 2) {
+          tmem_ld16(tb + (c + 1) * 16, v1);
+          load_u(c + 1, gnxt, unxt);
+          process(c, v0);
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            gcur[q4] = gnxt[q4];
-            ucur[q4] = unxt[q4];
+          for (int j = 0; j < 4; ++j) {
+            gcur[j] = gnxt[j];
+            ucur[j] = unxt[j];
+          }
+          tmem_ld_wait(v1);
+          const bool more = c + 2 < ce;
+          if (more) {
+            tmem_ld16(tb + (c + 2) * 16, v0);
+            load_u(c + 2, gnxt, unxt);
+          }
+          process(c + 1, v1);
+          if (more) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              gcur[j] = gnxt[j];
+              ucur[j] = unxt[j];
+            }
+            tmem_ld_wait(v0);
           }
         }
       } else {  // wgrad modes

@@ -43,7 +43,8 @@ struct GemmArgs {
   int h;                   // SwiGLU half width
   void* out;               // row-grouped bf16 output, or WGRAD fp32 [E, Mdim, N]
   long long ldo;           // elements per output row
-  void* out2;              // UP_SWIGLU: optional fp32 U [cap, 2h]; DGRAD_SWIGLU: dU low half
+  void* out2;              // UP_SWIGLU: optional fp32 U, blocked by row tile (see u_block);
+                           // DGRAD_SWIGLU: dU low half
   long long ldo2;
   void* out3;              // UP_SWIGLU: optional low half of P [cap, h] (P = w*A, or A)
   long long ldo3;
@@ -52,8 +53,14 @@ struct GemmArgs {
   // SwiGLU backward.
   const int32_t* row_src;
   const float* row_weight;
-  const void* aux;         // DGRAD_SWIGLU: saved fp32 U [cap, 2h]
+  const void* aux;         // DGRAD_SWIGLU: the saved fp32 U in the blocked layout of out2
   long long ld_aux;
+  // First row tile of this problem list in the blocked U: 0 for a whole problem list, the row
+  // tiles of the experts before it for one expert (single_expert)
+  long long tile_base;
+  // UP_SWIGLU, DGRAD_SWIGLU: 1 when every bf16 row output is 32-byte aligned at each 16-column
+  // chunk (bases 32-byte aligned, h % 16 == 0), so a chunk row is one 32-byte store
+  int vec32;
   int32_t* status;         // optional device status word
   long long timeout_ns;    // bound of every wait inside the kernel
 };

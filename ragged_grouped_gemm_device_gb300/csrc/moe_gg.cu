@@ -19,6 +19,7 @@ constexpr int MAX_E = 1024;
 constexpr int MAX_TOPK = 32;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned32(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }
 
 size_t round256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
 
@@ -44,12 +45,20 @@ GemmArgs base_args(int E, int cap, int32_t* status) {
   return a;
 }
 
-// saved = fp32 U [rows, 2h] | low half of P [rows, h], P = w*A (or A); the high half is a_save
-size_t saved_u_bytes(long long rows, int h) { return round256(static_cast<size_t>(rows) * 2 * h * 4); }
+// saved = low half of P [rows, h] bf16 (P = w*A, or A; the high half is a_save) | fp32 U in
+// blocks of 32 rows x 16 columns per (row tile, lane quadrant, column chunk). The row tiles of
+// any problem list with at most `rows` rows number at most sum_e ceil(M_e / 128) <=
+// (rows + 127 E) / 128; each holds 4 quadrants x 2 ceil(h/16) chunks of 2 KB.
 size_t saved_p_bytes(long long rows, int h) { return round256(static_cast<size_t>(rows) * h * 2); }
-size_t saved_bytes(long long rows, int h) { return saved_u_bytes(rows, h) + saved_p_bytes(rows, h); }
-const void* saved_p_lo(const void* saved, long long rows, int h) {
-  return static_cast<const uint8_t*>(saved) + saved_u_bytes(rows, h);
+long long saved_u_tiles(long long rows, int E) { return (rows + 127LL * E) / 128; }
+size_t saved_u_bytes(long long rows, int h, int E) {
+  return round256(static_cast<size_t>(saved_u_tiles(rows, E)) * 4 * (2 * ((h + 15) / 16)) * 2048);
+}
+size_t saved_bytes(long long rows, int h, int E) {
+  return saved_p_bytes(rows, h) + saved_u_bytes(rows, h, E);
+}
+const void* saved_u(const void* saved, long long rows, int h) {
+  return static_cast<const uint8_t*>(saved) + saved_p_bytes(rows, h);
 }
 size_t bwd_ws_half(long long rows, int h) { return round256(static_cast<size_t>(rows) * 2 * h * 2); }
 
@@ -71,11 +80,11 @@ moe_status_t run_up_swiglu(const GemmArgs& src, long long rows, long long tiles_
   a.out = a_save;
   a.ldo = h;
   if (saved != nullptr) {
-    a.out2 = saved;
-    a.ldo2 = 2LL * h;
-    a.out3 = const_cast<void*>(saved_p_lo(saved, rows, h));
+    a.out2 = const_cast<void*>(saved_u(saved, rows, h));
+    a.out3 = saved;
     a.ldo3 = h;
   }
+  a.vec32 = (h % 16 == 0 && aligned32(a_save) && (saved == nullptr || aligned32(saved))) ? 1 : 0;
   return launch_grouped_gemm(MODE_UP_SWIGLU, ma, ma, mb, a,
                              tiles_bound * gemm_tiles_n(MODE_UP_SWIGLU, h), s);
 }
@@ -111,8 +120,8 @@ moe_status_t run_down_dgrad_swiglu(const GemmArgs& src, long long rows, int E, i
   a.ldo = 2LL * h;
   a.out2 = du_lo;
   a.ldo2 = 2LL * h;
-  a.aux = saved;
-  a.ld_aux = 2LL * h;
+  a.aux = saved_u(saved, rows, h);
+  a.vec32 = (h % 16 == 0 && aligned32(du_hi) && aligned32(du_lo)) ? 1 : 0;
   return launch_grouped_gemm(MODE_DGRAD_SWIGLU, ma, ma, mb, a,
                              row_tiles_bound(rows, src.E) * gemm_tiles_n(MODE_DGRAD_SWIGLU, h), s);
 }
@@ -248,7 +257,7 @@ size_t moe_workspace_bytes(int op, int T, int top_k, int E, int d, int h, int ca
     case MOE_OP_ROUTE: return route_workspace_bytes(n, E);
     case MOE_OP_FWD: return 0;
     case MOE_OP_BWD: return h > 0 ? 2 * bwd_ws_half(n, h) : 0;
-    case MOE_OP_SAVED: return h > 0 ? saved_bytes(n, h) : 0;
+    case MOE_OP_SAVED: return h > 0 ? saved_bytes(n, h, E) : 0;
     case MOE_OP_PADDED_BMM: {
       if (capacity_C <= 0 || d <= 0 || h <= 0) return 0;
       const size_t rows = static_cast<size_t>(E) * capacity_C;
@@ -444,7 +453,7 @@ moe_status_t moe_grouped_bwd(const moe_bf16* dy, const moe_bf16* xp, const moe_b
   moe_bf16* du_lo = reinterpret_cast<moe_bf16*>(static_cast<uint8_t*>(ws) + half);
   // P = w*A (or A): its high half is a_save, its low half is in saved
   const void* p_hi = a_save;
-  const void* p_lo = saved_p_lo(saved, cap, h);
+  const void* p_lo = saved;
   GemmArgs src = base_args(E, cap, dev_status);
   src.offsets = offsets;
   if (cap > 0) {
@@ -519,6 +528,7 @@ moe_status_t moe_loop_swiglu_fwd(const moe_bf16* xp, const int32_t* offsets, int
     prev = off[e];
   }
   prev = 0;
+  long long tile_base = 0;  // row tiles of the experts before e, as the grouped kernels count
   for (int e = 0; e < E; ++e) {
     const int rows = off[e] - prev;
     if (rows > 0) {
@@ -526,6 +536,8 @@ moe_status_t moe_loop_swiglu_fwd(const moe_bf16* xp, const int32_t* offsets, int
       src.single_expert = e;
       src.single_row0 = prev;
       src.single_rows = rows;
+      src.tile_base = tile_base;
+      tile_base += (rows + 127) / 128;
       const long long tb = (rows + 127) / 128;
       st = run_up_swiglu(src, cap, tb, E, d, h, xp, w_ug, a_save, saved, s);
       if (st != MOE_OK) return st;

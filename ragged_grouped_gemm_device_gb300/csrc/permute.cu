@@ -36,12 +36,17 @@ __global__ void __launch_bounds__(THREADS) permute_kernel(
     if (src < 0 || src >= n) continue;
     const uint4* xr = x + static_cast<size_t>(src / k) * vec;
     uint4* orow = xp + static_cast<size_t>(p) * vec;
-    if (row_scale != nullptr) {
-      const float s = __ldg(row_scale + src);
-      for (int v = lane; v < vec; v += 32) orow[v] = scale_bf16x8(__ldg(xr + v), s);
-    } else {
-      for (int v = lane; v < vec; v += 32) orow[v] = __ldg(xr + v);
+    const float s = (row_scale != nullptr) ? __ldg(row_scale + src) : 1.0f;
+    int v = lane;
+    // four 16-byte loads in flight per lane before their stores
+    for (; v + 96 < vec; v += 128) {
+      uint4 q[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) q[i] = __ldg(xr + v + 32 * i);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) orow[v + 32 * i] = row_scale ? scale_bf16x8(q[i], s) : q[i];
     }
+    for (; v < vec; v += 32) orow[v] = row_scale ? scale_bf16x8(__ldg(xr + v), s) : __ldg(xr + v);
   }
 }
 
@@ -70,16 +75,28 @@ __global__ void __launch_bounds__(THREADS) combine_kernel(const uint4* __restric
       float acc[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-      for (int j = 0; j < k; ++j) {
-        const int p = __shfl_sync(0xffffffffu, my_p, j);
-        const float wj = __shfl_sync(0xffffffffu, my_w, j);
-        if (p < 0 || !active) continue;
-        const uint4 q = __ldg(y + static_cast<size_t>(p) * vec + v);
-        const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
+      // up to eight slot rows loaded before they are summed, still in slot order (k <= 32)
+      for (int j0 = 0; j0 < k; j0 += 8) {
+        uint4 q[8];
+        float wj[8];
+        bool ok[8];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          acc[2 * i] = fmaf(wj, bf16_lo(w4[i]), acc[2 * i]);
-          acc[2 * i + 1] = fmaf(wj, bf16_hi(w4[i]), acc[2 * i + 1]);
+        for (int jj = 0; jj < 8; ++jj) {
+          const int j = j0 + jj;
+          const int p = __shfl_sync(0xffffffffu, my_p, j & 31);
+          wj[jj] = __shfl_sync(0xffffffffu, my_w, j & 31);
+          ok[jj] = active && j < k && p >= 0;
+          q[jj] = ok[jj] ? __ldg(y + static_cast<size_t>(p) * vec + v) : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {
+          if (!ok[jj]) continue;
+          const uint32_t w4[4] = {q[jj].x, q[jj].y, q[jj].z, q[jj].w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            acc[2 * i] = fmaf(wj[jj], bf16_lo(w4[i]), acc[2 * i]);
+            acc[2 * i + 1] = fmaf(wj[jj], bf16_hi(w4[i]), acc[2 * i + 1]);
+          }
         }
       }
       if (active)
@@ -143,9 +160,18 @@ __global__ void __launch_bounds__(THREADS) unpad_rows_kernel(const uint4* __rest
   }
 }
 
-int grid_for_rows(long long rows) {
+// One warp per row, at most one wave: the SM count times the blocks of this kernel that fit on
+// an SM at once (the grid strides over the remaining rows).
+template <typename Kernel>
+int grid_for_rows(Kernel kernel, long long rows) {
   const long long want = (rows + WARPS - 1) / WARPS;
-  const long long cap = static_cast<long long>(device_sm_count()) * 8;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, THREADS, 0) != cudaSuccess ||
+      per_sm < 1) {
+    (void)cudaGetLastError();
+    per_sm = 1;
+  }
+  const long long cap = static_cast<long long>(device_sm_count()) * per_sm;
   return static_cast<int>(std::max(1LL, std::min(want, cap)));
 }
 
@@ -160,7 +186,7 @@ moe_status_t launch_permute(const void* x, const int32_t* sorted_src, const int3
                             const float* row_scale, int n, int k, int E, int d, void* xp,
                             cudaStream_t s) {
   if (n == 0) return MOE_OK;
-  permute_kernel<<<grid_for_rows(n), THREADS, 0, s>>>(
+  permute_kernel<<<grid_for_rows(permute_kernel, n), THREADS, 0, s>>>(
       static_cast<const uint4*>(x), sorted_src, offsets, row_scale, n, k, E, d / 8,
       static_cast<uint4*>(xp));
   return last_launch();
@@ -169,9 +195,8 @@ moe_status_t launch_permute(const void* x, const int32_t* sorted_src, const int3
 moe_status_t launch_combine(const void* y, const int32_t* inv_map, const float* weights, int T,
                             int k, int d, void* out, cudaStream_t s) {
   if (T == 0) return MOE_OK;
-  combine_kernel<<<grid_for_rows(T), THREADS, 0, s>>>(static_cast<const uint4*>(y), inv_map,
-                                                      weights, T, k, d / 8,
-                                                      static_cast<uint4*>(out));
+  combine_kernel<<<grid_for_rows(combine_kernel, T), THREADS, 0, s>>>(
+      static_cast<const uint4*>(y), inv_map, weights, T, k, d / 8, static_cast<uint4*>(out));
   return last_launch();
 }
 
@@ -179,15 +204,15 @@ moe_status_t launch_pad_rows(const void* src, const int32_t* offsets, int E, int
                              void* dst, cudaStream_t s) {
   const long long rows = static_cast<long long>(E) * C;
   if (rows == 0) return MOE_OK;
-  pad_rows_kernel<<<grid_for_rows(rows), THREADS, 0, s>>>(static_cast<const uint4*>(src), offsets,
-                                                          E, C, cols / 8, static_cast<uint4*>(dst));
+  pad_rows_kernel<<<grid_for_rows(pad_rows_kernel, rows), THREADS, 0, s>>>(
+      static_cast<const uint4*>(src), offsets, E, C, cols / 8, static_cast<uint4*>(dst));
   return last_launch();
 }
 
 moe_status_t launch_unpad_rows(const void* src, const int32_t* offsets, int E, int C, int cap,
                                int cols, void* dst, cudaStream_t s) {
   if (cap == 0) return MOE_OK;
-  unpad_rows_kernel<<<grid_for_rows(cap), THREADS, 0, s>>>(
+  unpad_rows_kernel<<<grid_for_rows(unpad_rows_kernel, cap), THREADS, 0, s>>>(
       static_cast<const uint4*>(src), offsets, E, C, cap, cols / 8, static_cast<uint4*>(dst));
   return last_launch();
 }

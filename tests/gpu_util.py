@@ -67,6 +67,34 @@ def assert_close(got, ref, what: str):
         f"{what}: |err| {np.abs(err).flat[worst]:.3e} > bound {bound.flat[worst]:.3e} at {np.unravel_index(worst, err.shape)}")
 
 
+def unblock_u(u_flat: torch.Tensor, offsets: np.ndarray, h: int) -> torch.Tensor:
+    """Rows [M, 2h] of the saved U from its blocked layout, as the header states it: row p of
+    expert e (the segment starting at s_e) is row r = p - s_e of row tile G = (row tiles of the
+    experts before e) + r // 128, lane l = r % 32 of quadrant q = (r % 128) // 32; column c is
+    in 16-column chunk ci = c // 16 for gate columns and ceil(h/16) + (c - h) // 16 for up
+    columns, in float4 j = (c % 16) // 4 at float ((((G*4 + q)*C2 + ci)*4 + j)*32 + l)*4 + c % 4,
+    C2 = 2 ceil(h/16)."""
+    h16 = (h + 15) // 16
+    c2 = 2 * h16
+    starts = np.concatenate([[0], offsets[:-1]])
+    tiles = (offsets - starts + 127) // 128
+    tile0 = np.concatenate([[0], np.cumsum(tiles)[:-1]])
+    M = int(offsets[-1])
+    p = np.arange(M)
+    e = np.searchsorted(offsets, p, side="right")
+    r = p - starts[e]
+    g = tile0[e] + r // 128
+    q = (r % 128) // 32
+    lane = r % 32
+    c = np.arange(2 * h)
+    cc = np.where(c < h, c, c - h)
+    ci = cc // 16 + np.where(c < h, 0, h16)
+    j = (cc % 16) // 4
+    idx = ((((g[:, None] * 4 + q[:, None]) * c2 + ci[None, :]) * 4 + j[None, :]) * 32 + lane[:, None]) * 4 \
+        + (cc % 4)[None, :]
+    return u_flat[torch.from_numpy(idx).to(u_flat.device)]
+
+
 class GpuRun:
     """The library pipeline (route, permute, grouped forward, optional backward, combine) on
     a workload, with NaN-filled row buffers so that rows past M cannot leak into results."""
@@ -124,9 +152,9 @@ class GpuRun:
 
     @property
     def u(self):
-        """The fp32 U the forward saved, [n, 2h]."""
-        n, h = max(self.cap, 1), self.wl.h
-        return self.saved[: n * 2 * h].view(n, 2 * h)
+        """The fp32 U the forward saved, as [M, 2h] rows (unblocked)."""
+        u_flat, _ = _lib.saved_views(self.saved, max(self.cap, 1), self.wl.h)
+        return unblock_u(u_flat, self.offsets.cpu().numpy().astype(np.int64), self.wl.h)
 
     def combine(self):
         wl = self.wl

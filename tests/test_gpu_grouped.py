@@ -157,6 +157,41 @@ def test_single_kernel_entry_points_equal_composites(lib):
     M = int(run.offsets[-1].item())
     for got, want in ((y2, y1), (a2, a1), (dxp2, dxp1)):
         assert torch.equal(got[:M], want[:M])
-    assert torch.equal(sv2, sv1) and torch.equal(dwu2, dwu1) and torch.equal(dwd2, dwd1)
+    # saved compared as bytes: bit for bit, whatever values it holds
+    assert torch.equal(sv2.view(torch.uint8), sv1.view(torch.uint8))
+    assert torch.equal(dwu2, dwu1) and torch.equal(dwd2, dwd1)
     err = (dwu3 - dwu1).double().norm() / dwu1.double().norm()
     assert err <= G.REL_NORM_TOL, f"bf16-only wgrad normalised error {err:.2e}"
+
+
+def test_outputs_at_16_byte_alignment_match_32_byte_aligned(lib):
+    """Row outputs whose base is 16- but not 32-byte aligned take the 16-byte store path of the
+    up/gate and dgrad epilogues; the results are bit-identical to the 32-byte path."""
+    from ragged_grouped_gemm_device_gb300 import _lib as L
+    wl = W.custom(T=200, k=2, E=5, d=128, h=256, seed=41, empty_experts=(2,))
+    run = G.GpuRun(wl).route().permute()
+    n, d, h, E = run.cap, wl.d, wl.h, wl.E
+    M = int(run.offsets[-1].item())
+
+    def shifted(rows, cols, shift):
+        """A [rows, cols] bf16 view whose first element sits `shift` elements into a NaN buffer."""
+        buf = G.nan_filled((rows * cols + 16,))
+        return buf[shift:shift + rows * cols].view(rows, cols)
+
+    sv = torch.zeros(L.moe_workspace_bytes(L.OP_SAVED, wl.T, wl.k, E, d, h) + 32, dtype=torch.uint8, device="cuda")
+    results = []
+    for shift in (0, 8):  # 8 bf16 = 16 bytes
+        a = shifted(n, h, shift)
+        saved = sv[2 * shift:2 * shift + L.moe_workspace_bytes(L.OP_SAVED, wl.T, wl.k, E, d, h)]
+        saved.zero_()
+        L.moe_grouped_up_swiglu(run.xp, run.offsets, run.sorted_src, run.weights, E, n, d, h, run.w_ug, a, saved,
+                                run.status)
+        dy = G.dev_bf16(wl.dy(n))
+        du_hi, du_lo = shifted(n, 2 * h, shift), shifted(n, 2 * h, shift)
+        L.moe_grouped_down_dgrad_swiglu(dy, saved, run.offsets, run.sorted_src, run.weights, E, n, d, h,
+                                        run.w_down, du_hi, du_lo, run.status)
+        torch.cuda.synchronize()
+        assert run.status.item() == 0
+        results.append((a[:M].clone(), saved.clone(), du_hi[:M].clone(), du_lo[:M].clone()))
+    for x0, x1 in zip(*results):
+        assert torch.equal(x0.view(torch.uint8), x1.view(torch.uint8))

@@ -54,4 +54,6 @@ def test_host_loop_matches_oracle(lib, name):
     M = r["M"]
     G.assert_close(G.host(run.y)[:M], y[:M], f"loop y[{name}]")
     G.assert_close(G.host(run.a)[:M], a[:M], f"loop A[{name}]")
+    # the saved U of expert e lands in the row tiles the grouped kernels give it
+    G.assert_close(G.host(run.u)[:M], u[:M], f"loop U[{name}]")
     assert np.isnan(G.host(run.y)[M:]).all()
