@@ -50,7 +50,8 @@ constexpr int THREADS = 64 + 32 * EPI_WARPS;
 constexpr int TMEM_COLS = 512;                // two 256-column accumulators
 constexpr int MAX_E = 1024;
 constexpr int CTL_BYTES = 256;
-// per epilogue warp, one 32-row x 16-column fp32 chunk staged for a TMA store (wgrad)
+// per epilogue warp, one 32-row x 16-column fp32 chunk staged for a TMA store (wgrad), or two
+// 32-row x 16-column bf16 boxes (dgrad)
 constexpr int STAGE_OUT_BYTES = 32 * 16 * 4;
 constexpr int STAGING_BYTES = EPI_WARPS * STAGE_OUT_BYTES;
 
@@ -198,7 +199,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                         const __grid_constant__ CUtensorMap map_a_lo,
                         const __grid_constant__ CUtensorMap map_b,
-                        const __grid_constant__ CUtensorMap map_out, const GemmArgs args) {
+                        const __grid_constant__ CUtensorMap map_out,
+                        const __grid_constant__ CUtensorMap map_out2, const GemmArgs args) {
   constexpr int NST = ModeTraits<MODE>::stages;
   constexpr int SB = ModeTraits<MODE>::stage_bytes;
   constexpr int APARTS = ModeTraits<MODE>::a_parts;
@@ -445,6 +447,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int half = (warp - 2) >> 2; // which half of the tile's columns this warp stores
     const int r_in = q * 32 + lane;   // accumulator row = TMEM lane
     uint32_t acc = 0;
+    uint32_t box_ctr = 0;             // dgrad: staging boxes this warp has stored
     for (int t = t_first; t < sc.total; t += t_step) {
       const Tile ti = decode_tile<MODE>(sc, t, rank);
       if (PAIR && !ti.active) continue;
@@ -574,6 +577,28 @@ __global__ void __launch_bounds__(THREADS, 1)
         bf16* lrow = reinterpret_cast<bf16*>(args.out2) + row * args.ldo2;
         const float wrow =
             (args.row_weight != nullptr && rv) ? __ldg(args.row_weight + __ldg(args.row_src + row)) : 1.0f;
+        // A warp whose 32 rows all belong to the tile's expert sends whole 16-column chunks out
+        // through two 1 KB staging boxes (32-byte swizzle: lane r's 16-byte piece j at piece
+        // j ^ ((r >> 2) & 1), conflict-free) and TMA tensor stores: full sectors from the copy
+        // engine instead of 32 rows of 16-byte stores per instruction. A box never crosses into
+        // the up half or past the slab, so rows of the next expert are never written.
+        const bool slab_full = q * 32 + 32 <= ti.rows;  // warp-uniform
+        const int y0 = static_cast<int>(ti.row0) + q * 32;
+        auto stage_store = [&](const uint32_t (&w)[8], const CUtensorMap* map, int x) {
+          uint8_t* sbuf = staging + (warp - 2) * STAGE_OUT_BYTES + (box_ctr & 1u) * 1024;
+          if (lane == 0) bulk_wait_group_read1();  // this buffer's previous box has been read
+          __syncwarp();
+          const int sw = (lane >> 2) & 1;
+          *reinterpret_cast<uint4*>(sbuf + lane * 32 + (sw << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+          *reinterpret_cast<uint4*>(sbuf + lane * 32 + ((sw ^ 1) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(map, smem_u32(sbuf), x, y0);
+            bulk_commit_group();
+          }
+          ++box_ctr;
+        };
         // saved U of chunk c (zeros past the last column chunk), one coalesced float4 per lane
         auto load_u = [&](int c, float4 (&gq)[4], float4 (&uq)[4]) {
           const int ci = (ti.n0 >> 4) + c;
@@ -620,6 +645,13 @@ __global__ void __launch_bounds__(THREADS, 1)
             uh[j] = pack_bf16x2(du[0], du[1]);
             gl[j] = pack_bf16x2(dg[0] - bf16_lo(gh[j]), dg[1] - bf16_hi(gh[j]));
             ul[j] = pack_bf16x2(du[0] - bf16_lo(uh[j]), du[1] - bf16_hi(uh[j]));
+          }
+          if (slab_full && two) {
+            stage_store(gh, &map_out, col);
+            stage_store(uh, &map_out, h + col);
+            stage_store(gl, &map_out2, col);
+            stage_store(ul, &map_out2, h + col);
+            return;
           }
           if (args.vec32) {
             // whole 16-column chunks (h % 16 == 0), 32-byte aligned rows: one full sector a row
@@ -710,7 +742,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 
   // ---- teardown: every role has finished (or given up); release tensor memory
-  if (ModeTraits<MODE>::wgrad && warp >= 2 && lane == 0) bulk_wait_group0();
+  if ((ModeTraits<MODE>::wgrad || MODE == MODE_DGRAD_SWIGLU) && warp >= 2 && lane == 0) bulk_wait_group0();
   tc_fence_before();
   __syncthreads();
   // neither CTA of a pair leaves while the other may still write to its shared memory
@@ -743,8 +775,8 @@ EncodeTiledFn encode_fn() {
 
 template <int MODE>
 moe_status_t launch_mode(const CUtensorMap& a, const CUtensorMap& a_lo, const CUtensorMap& b,
-                         const CUtensorMap& out, const GemmArgs& args, long long max_tiles,
-                         cudaStream_t stream) {
+                         const CUtensorMap& out, const CUtensorMap& out2, const GemmArgs& args,
+                         long long max_tiles, cudaStream_t stream) {
   const size_t smem = smem_bytes_for(args.E);
   const cudaError_t attr_err = ensure_max_dynamic_smem(
       reinterpret_cast<const void*>(grouped_gemm_kernel<MODE>), static_cast<int>(smem_bytes_for(MAX_E)));
@@ -772,11 +804,11 @@ moe_status_t launch_mode(const CUtensorMap& a, const CUtensorMap& a_lo, const CU
     }
     const long long pairs = std::max(1LL, std::min<long long>(clusters, (max_tiles + 1) / 2));
     cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
-    const cudaError_t lerr = cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<MODE>, a, a_lo, b, out, args);
+    const cudaError_t lerr = cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<MODE>, a, a_lo, b, out, out2, args);
     if (lerr != cudaSuccess) return cuda_fail(lerr);
   } else {
     const int grid = static_cast<int>(std::max(1LL, std::min(sms, max_tiles)));
-    grouped_gemm_kernel<MODE><<<grid, THREADS, smem, stream>>>(a, a_lo, b, out, args);
+    grouped_gemm_kernel<MODE><<<grid, THREADS, smem, stream>>>(a, a_lo, b, out, out2, args);
   }
   const cudaError_t err = cudaGetLastError();
   return err == cudaSuccess ? MOE_OK : cuda_fail(err);
@@ -816,6 +848,18 @@ bool make_map_grad3d_f32(CUtensorMap* map, const void* ptr, long long E, long lo
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool make_map_rows2d_store(CUtensorMap* map, const void* ptr, long long rows, long long cols) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || rows <= 0 || cols <= 0) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+  const cuuint32_t box[2] = {16u, 32u};
+  const cuuint32_t estr[2] = {1u, 1u};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool make_map_weight3d(CUtensorMap* map, const void* ptr, long long E, long long R, long long C,
                        int box_r) {
   EncodeTiledFn fn = encode_fn();
@@ -833,20 +877,23 @@ bool make_map_weight3d(CUtensorMap* map, const void* ptr, long long E, long long
 
 moe_status_t launch_grouped_gemm(int mode, const CUtensorMap& a, const CUtensorMap& a_lo,
                                  const CUtensorMap& b, const GemmArgs& args, long long max_tiles,
-                                 cudaStream_t stream, const CUtensorMap* out) {
+                                 cudaStream_t stream, const CUtensorMap* out,
+                                 const CUtensorMap* out2) {
   if (args.E < 1 || args.E > MAX_E) return MOE_ERR_UNSUPPORTED_SHAPE;
   const CUtensorMap& o = out ? *out : a;
+  const CUtensorMap& o2 = out2 ? *out2 : a;
   switch (mode) {
-    case MODE_UP_SWIGLU: return launch_mode<MODE_UP_SWIGLU>(a, a_lo, b, o, args, max_tiles, stream);
-    case MODE_PLAIN_BF16: return launch_mode<MODE_PLAIN_BF16>(a, a_lo, b, o, args, max_tiles, stream);
+    case MODE_UP_SWIGLU: return launch_mode<MODE_UP_SWIGLU>(a, a_lo, b, o, o2, args, max_tiles, stream);
+    case MODE_PLAIN_BF16: return launch_mode<MODE_PLAIN_BF16>(a, a_lo, b, o, o2, args, max_tiles, stream);
     case MODE_DGRAD_SWIGLU:
-      return launch_mode<MODE_DGRAD_SWIGLU>(a, a_lo, b, o, args, max_tiles, stream);
+      if (!out || !out2) return MOE_ERR_INVALID_ARG;
+      return launch_mode<MODE_DGRAD_SWIGLU>(a, a_lo, b, o, o2, args, max_tiles, stream);
     case MODE_WGRAD:
       if (!out) return MOE_ERR_INVALID_ARG;
-      return launch_mode<MODE_WGRAD>(a, a_lo, b, o, args, max_tiles, stream);
+      return launch_mode<MODE_WGRAD>(a, a_lo, b, o, o2, args, max_tiles, stream);
     case MODE_WGRAD_BF16:
       if (!out) return MOE_ERR_INVALID_ARG;
-      return launch_mode<MODE_WGRAD_BF16>(a, a_lo, b, o, args, max_tiles, stream);
+      return launch_mode<MODE_WGRAD_BF16>(a, a_lo, b, o, o2, args, max_tiles, stream);
     default: return MOE_ERR_INVALID_ARG;
   }
 }

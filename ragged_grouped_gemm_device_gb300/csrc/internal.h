@@ -20,7 +20,8 @@ enum GemmMode : int {
   // Y = P W per row segment with W [E, K, N] (N contiguous, MN-major B); bf16 store.
   MODE_PLAIN_BF16 = 1,
   // dA = dY W_down^T per row segment (W_down [E, h, d] K-major B); the epilogue applies the
-  // SwiGLU backward with the saved fp32 U and writes dU = [dgate, dup] as a bf16 high/low pair.
+  // SwiGLU backward with the saved fp32 U and writes dU = [dgate, dup] as a bf16 high/low pair
+  // (out/out2, with their rows2d_store maps as the kernel's two output maps).
   MODE_DGRAD_SWIGLU = 2,
   // dW_e = (P_hi + P_lo)_e^T Q_e, contraction over the M_e rows of expert e (all operands
   // MN-major, two MMAs per K step into one accumulator); fp32 store, zeros for empty experts.
@@ -70,7 +71,8 @@ struct GemmArgs {
 // bounds the grid (the exact tile count is only known on the device).
 moe_status_t launch_grouped_gemm(int mode, const CUtensorMap& a, const CUtensorMap& a_lo,
                                  const CUtensorMap& b, const GemmArgs& args, long long max_tiles,
-                                 cudaStream_t stream, const CUtensorMap* out = nullptr);
+                                 cudaStream_t stream, const CUtensorMap* out = nullptr,
+                                 const CUtensorMap* out2 = nullptr);
 
 // Tensor maps (bf16, 128-byte swizzle, zero fill outside the tensor).
 //   rows2d: a [rows, cols] row-major matrix; box = 64 columns x box_rows rows.
@@ -80,6 +82,9 @@ bool make_map_rows2d(CUtensorMap* map, const void* ptr, long long rows, long lon
 bool make_map_weight3d(CUtensorMap* map, const void* ptr, long long E, long long R, long long C,
                        int box_r);
 //   grad3d_f32: an fp32 [E, R, C] gradient, stored through 16-column x 32-row boxes, 64B swizzle.
+//   rows2d_store: a bf16 [rows, cols] row-major output, stored through 16-column x 32-row boxes,
+//   32B swizzle (cols * 2 bytes a multiple of 16).
+bool make_map_rows2d_store(CUtensorMap* map, const void* ptr, long long rows, long long cols);
 bool make_map_grad3d_f32(CUtensorMap* map, const void* ptr, long long E, long long R, long long C);
 
 int gemm_tiles_n(int mode, int N);  // column tiles of one problem

@@ -122,8 +122,12 @@ moe_status_t run_down_dgrad_swiglu(const GemmArgs& src, long long rows, int E, i
   a.ldo2 = 2LL * h;
   a.aux = saved_u(saved, rows, h);
   a.vec32 = (h % 16 == 0 && aligned32(du_hi) && aligned32(du_lo)) ? 1 : 0;
+  CUtensorMap mhi, mlo;
+  if (!make_map_rows2d_store(&mhi, du_hi, rows, 2LL * h)) return map_fail("du_hi");
+  if (!make_map_rows2d_store(&mlo, du_lo, rows, 2LL * h)) return map_fail("du_lo");
   return launch_grouped_gemm(MODE_DGRAD_SWIGLU, ma, ma, mb, a,
-                             row_tiles_bound(rows, src.E) * gemm_tiles_n(MODE_DGRAD_SWIGLU, h), s);
+                             row_tiles_bound(rows, src.E) * gemm_tiles_n(MODE_DGRAD_SWIGLU, h), s,
+                             &mhi, &mlo);
 }
 
 // a12: dxp = dU W_ug.
