@@ -10,8 +10,10 @@
 // clusters, ..., a pair tile being two 128-row tiles that share their B operand, which the two
 // CTAs load half each and multicast to both. The host never learns M.
 //
-// Roles (320 threads, warp-specialised):
-//   warp 0      TMA producer: 128B-swizzled operand tiles into a 4-stage shared-memory ring.
+// Roles (352 threads, warp-specialised):
+//   warp 0      TMA producer of the A operand: 128B-swizzled tiles into a 4-stage
+//               shared-memory ring (3 stages of A high, A low and B in the hi/lo wgrad).
+//   warp 10     TMA producer of the B operand into the same stages.
 //   warp 1      tensor-memory allocator and MMA issuer: tcgen05.mma 128x256x16 (bf16 in, fp32
 //               accumulate) into one of two 256-column TMEM accumulators, so the epilogue of a
 //               tile overlaps the main loop of the next.
@@ -46,7 +48,8 @@ constexpr int B_BYTES = BN * BK * 2;          // 32 KB
 constexpr int RING_BYTES = STAGES * (A_BYTES + B_BYTES);  // 192 KB, shared by every mode
 constexpr int ATOM_BYTES = 64 * BK * 2;       // one MN-major 64x64 box: 8 KB
 constexpr int EPI_WARPS = 8;                 // epilogue warps: 2 per TMEM lane quadrant
-constexpr int THREADS = 64 + 32 * EPI_WARPS;
+constexpr int PRODUCER_B_WARP = 2 + EPI_WARPS;  // second TMA producer (B operand)
+constexpr int THREADS = 32 * (PRODUCER_B_WARP + 1);
 constexpr int TMEM_COLS = 512;                // two 256-column accumulators
 constexpr int MAX_E = 1024;
 constexpr int CTL_BYTES = 256;
@@ -89,6 +92,8 @@ struct ModeTraits {
   // gradient's row tiles come in even numbers whenever the width is a multiple of 256.
   static constexpr bool pair = wgrad;
   static_assert(pair == wgrad, "the producer pairs exactly the wgrad modes");
+  // A and B parts of each stage loaded by two producer threads (see the producer role)
+  static constexpr bool split_producer = true;
 };
 
 struct Tile {
@@ -273,7 +278,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   // ---- barriers and tensor memory
   if (tid == 0) {
     for (int s = 0; s < NST; ++s) {
-      mbar_init(smem_u32(&ctl->full[s]), 1);
+      mbar_init(smem_u32(&ctl->full[s]), ModeTraits<MODE>::split_producer ? 2 : 1);
       mbar_init(smem_u32(&ctl->empty[s]), ModeTraits<MODE>::pair ? 2 : 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -307,14 +312,24 @@ __global__ void __launch_bounds__(THREADS, 1)
   int32_t* status = args.status;
   const uint32_t stage0 = smem_u32(stages);
 
-  if (warp == 0) {
-    // =========================================================== TMA producer
+  // Two producer threads fill each stage: lane 0 of warp 0 loads the A part, lane 0 of the last
+  // warp the B part. Each arrives on the stage's full barrier (count 2) with the bytes it will
+  // deliver, so the phase completes when both have arrived and every byte has landed, in
+  // whatever order. One instruction stream per part halves the serial issue latency per stage
+  // (the MN-major B part alone is four boxes).
+  constexpr bool SPLIT = ModeTraits<MODE>::split_producer;
+  const int prole = (warp == 0) ? 0 : (SPLIT && warp == PRODUCER_B_WARP) ? 1 : -1;
+  if (prole >= 0) {
+    // =========================================================== TMA producers
     if (lane == 0) {
+      const bool do_a = prole == 0, do_b = !SPLIT || prole == 1;
       uint32_t it = 0;
       bool ok = true;
       for (int t = t_first; t < sc.total && ok; t += t_step) {
         const Tile ti = decode_tile<MODE>(sc, t, rank);
         const int eg = ti.e + expert_base;
+        const uint32_t a_bytes = (!PAIR || ti.active) ? static_cast<uint32_t>(APARTS * A_BYTES) : 0u;
+        const uint32_t bytes = (do_a ? a_bytes : 0u) + (do_b ? static_cast<uint32_t>(B_BYTES) : 0u);
         for (int kb = 0; kb < ti.kblocks; ++kb, ++it) {
           const int s = it % NST;
           const uint32_t ph = (it / NST) & 1u;
@@ -323,7 +338,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             break;
           }
           const uint32_t fb = smem_u32(&ctl->full[s]);
-          mbar_arrive_expect_tx(fb, (!PAIR || ti.active) ? SB : B_BYTES);
+          mbar_arrive_expect_tx(fb, bytes);
           const uint32_t sa = stage0 + s * SB;
           const uint32_t sb = sa + APARTS * A_BYTES;
           const int k0 = kb * BK;
@@ -331,22 +346,26 @@ __global__ void __launch_bounds__(THREADS, 1)
           // except with cluster pairs (wgrad), where this CTA loads half `rank` and multicasts it
           // to both CTAs of the pair (multicast exists only in cluster launches). The issue path
           // is kept straight-line: it is on the critical path of the MN-major modes.
+          if constexpr (!ModeTraits<MODE>::wgrad) {
+            if (do_a) tma_load_2d(sa, &map_a, k0, ti.row0, fb);
+          }
           if constexpr (MODE == MODE_UP_SWIGLU) {
-            tma_load_2d(sa, &map_a, k0, ti.row0, fb);
-            tma_load_3d(sb, &map_b, k0, ti.n0, eg, fb);                            // gate rows
-            tma_load_3d(sb + B_BYTES / 2, &map_b, k0, args.h + ti.n0, eg, fb);     // up rows
+            if (do_b) {
+              tma_load_3d(sb, &map_b, k0, ti.n0, eg, fb);                            // gate rows
+              tma_load_3d(sb + B_BYTES / 2, &map_b, k0, args.h + ti.n0, eg, fb);     // up rows
+            }
           } else if constexpr (MODE == MODE_PLAIN_BF16) {
-            tma_load_2d(sa, &map_a, k0, ti.row0, fb);
+            if (do_b) {
 #pragma unroll
-            for (int i = 0; i < BN / 64; ++i)
-              tma_load_3d(sb + i * ATOM_BYTES, &map_b, ti.n0 + 64 * i, k0, eg, fb);
+              for (int i = 0; i < BN / 64; ++i)
+                tma_load_3d(sb + i * ATOM_BYTES, &map_b, ti.n0 + 64 * i, k0, eg, fb);
+            }
           } else if constexpr (MODE == MODE_DGRAD_SWIGLU) {
-            tma_load_2d(sa, &map_a, k0, ti.row0, fb);
-            tma_load_3d(sb, &map_b, k0, ti.n0, eg, fb);  // 256 rows of W_down in one box
+            if (do_b) tma_load_3d(sb, &map_b, k0, ti.n0, eg, fb);  // 256 rows of W_down in one box
           } else {
             static_assert(ModeTraits<MODE>::pair, "the wgrad modes load B as cluster pairs");
             const int rk = ti.row0 + k0;  // first contraction row of this K block
-            if (ti.active) {
+            if (do_a && ti.active) {
 #pragma unroll
               for (int i = 0; i < BM / 64; ++i) tma_load_2d(sa + i * ATOM_BYTES, &map_a, ti.m0 + 64 * i, rk, fb);
               if constexpr (APARTS == 2) {
@@ -355,15 +374,17 @@ __global__ void __launch_bounds__(THREADS, 1)
                   tma_load_2d(sa + A_BYTES + i * ATOM_BYTES, &map_a_lo, ti.m0 + 64 * i, rk, fb);
               }
             }
+            if (do_b) {
 #pragma unroll
-            for (int i = 0; i < 2; ++i) {
-              const int box = 2 * rank + i;
-              tma_load_2d_mc(sb + box * ATOM_BYTES, &map_b, ti.n0 + 64 * box, rk, fb, 0x3);
+              for (int i = 0; i < 2; ++i) {
+                const int box = 2 * rank + i;
+                tma_load_2d_mc(sb + box * ATOM_BYTES, &map_b, ti.n0 + 64 * box, rk, fb, 0x3);
+              }
             }
           }
         }
       }
-      // drain: the copies issued into each stage must land before the CTA can exit
+      // drain: the copies this thread issued into each stage must land before the CTA can exit
       const uint32_t first = it > NST ? it - NST : 0u;
       for (uint32_t j = first; j < it; ++j)
         mbar_wait(smem_u32(&ctl->full[j % NST]), (j / NST) & 1u, abort_flag, status, tmo, false);
@@ -441,7 +462,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (lane == 0) mma_commit(smem_u32(&ctl->done));
     __syncwarp();
     mbar_wait(smem_u32(&ctl->done), 0u, abort_flag, status, tmo, false);
-  } else {
+  } else if (warp >= 2 && warp < 2 + EPI_WARPS) {
     // =========================================================== epilogue (warps 2..9)
     const int q = warp & 3;           // TMEM lane quadrant this warp may access
     const int half = (warp - 2) >> 2; // which half of the tile's columns this warp stores
