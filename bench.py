@@ -194,11 +194,16 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------------------ our arm
+GEMM_SOURCES = ("common.cuh", "grouped_gemm.cu", "internal.h", "moe_gg.cu")
+
+
 def kernel_source_hash():
-    """Hash of the kernel sources: DRAM traffic taken by the profiler is valid only for them."""
+    """Hash of the grouped GEMM's sources (device code, launch arguments and tensor maps): DRAM
+    traffic taken by the profiler is valid only for them. The routing and row-movement kernels
+    (route.cu, permute.cu) do not enter it."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "ragged_grouped_gemm_device_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in GEMM_SOURCES:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]

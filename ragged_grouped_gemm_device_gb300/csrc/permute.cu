@@ -22,7 +22,10 @@ __device__ __forceinline__ uint4 scale_bf16x8(uint4 q, float s) {
   return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-// "grouped_mm" agent doc, forward gather x[idx]: xp[p] = x[sorted_src[p] / k] (* scale).
+// "grouped_mm" agent doc, forward gather x[idx]: xp[p] = x[sorted_src[p] / k] (* scale). The
+// rows of xp are written with streaming stores (evict-first), so the T·k written rows do not
+// push the T source rows, each read k times, out of L2 (measured 152 -> 139 us on the large
+// workload).
 __global__ void __launch_bounds__(THREADS) permute_kernel(
     const uint4* __restrict__ x, const int32_t* __restrict__ sorted_src,
     const int32_t* __restrict__ offsets, const float* __restrict__ row_scale, int n, int k, int E,
@@ -44,9 +47,9 @@ __global__ void __launch_bounds__(THREADS) permute_kernel(
 #pragma unroll
       for (int i = 0; i < 4; ++i) q[i] = __ldg(xr + v + 32 * i);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) orow[v + 32 * i] = row_scale ? scale_bf16x8(q[i], s) : q[i];
+      for (int i = 0; i < 4; ++i) __stcs(orow + v + 32 * i, row_scale ? scale_bf16x8(q[i], s) : q[i]);
     }
-    for (; v < vec; v += 32) orow[v] = row_scale ? scale_bf16x8(__ldg(xr + v), s) : __ldg(xr + v);
+    for (; v < vec; v += 32) __stcs(orow + v, row_scale ? scale_bf16x8(__ldg(xr + v), s) : __ldg(xr + v));
   }
 }
 
