@@ -367,35 +367,71 @@ def run_ours(args):
         breakdown[kname]["gbs"] = round(b / (per_call[kname] * 1e-3) / 1e9, 1)
         breakdown[kname]["frac_of_hbm_peak"] = round(b / (per_call[kname] * 1e-3) / 1e9 / peak_hbm, 3)
 
-    # ---- end to end through the public calls with host buffers (pinned), copies inside
+    # ---- end to end through the public calls with host buffers (pinned), copies inside. As a
+    # training loop would: the inputs of a step go host -> device on one copy stream into one of
+    # two device buffers while the GPU computes the step before, and out / dx come back on a
+    # second copy stream while the backward (or the next step) runs. Every step's copies lie
+    # between the start and end events: the copy streams wait on the start event, and the end
+    # event waits on the last read-back.
     xh, doh = x_h.pin_memory(), dout_h.pin_memory()
     idh, wh = ids_h.pin_memory(), wts_h.pin_memory()
     out_h = torch.empty(T, d, dtype=bf).pin_memory()
     dx_h = torch.empty(T, d, dtype=bf).pin_memory()
-    x2, do2 = torch.empty_like(x), torch.empty_like(dout)
-    id2, w2 = torch.empty_like(ids), torch.empty_like(wts)
-    calls2 = step_calls(x2, id2, w2, do2)
+    bufs = [(torch.empty_like(x), torch.empty_like(ids), torch.empty_like(wts), torch.empty_like(dout))
+            for _ in range(2)]
+    calls_b = [step_calls(*b) for b in bufs]
+    n_fwd = [c[0] for c in calls].index("combine") + 1  # calls up to the combine produce out
+    cs_in, cs_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev = lambda: torch.cuda.Event()
+    ev_in, ev_free = [ev(), ev()], [ev(), ev()]
+    ev_out, ev_dx, ev_outcp, ev_dxcp = ev(), ev(), ev(), ev()
 
-    def e2e_step():
-        x2.copy_(xh, non_blocking=True)
-        id2.copy_(idh, non_blocking=True)
-        w2.copy_(wh, non_blocking=True)
-        do2.copy_(doh, non_blocking=True)
-        for _, _, fn in calls2:
-            fn()
-        out_h.copy_(out, non_blocking=True)
-        dx_h.copy_(dx, non_blocking=True)
+    def h2d(j, after):
+        with torch.cuda.stream(cs_in):
+            cs_in.wait_event(after)
+            for dst, src in zip(bufs[j], (xh, idh, wh, doh)):
+                dst.copy_(src, non_blocking=True)
+            ev_in[j].record(cs_in)
 
-    for _ in range(3):
-        e2e_step()
+    def e2e_run(n_steps, start_ev):
+        start_ev.record(stream)
+        for j in range(min(2, n_steps)):
+            h2d(j, start_ev)
+        for i in range(n_steps):
+            j = i % 2
+            stream.wait_event(ev_in[j])
+            if i > 0:
+                stream.wait_event(ev_outcp)  # the previous step's out has been read back
+            for _, _, fn in calls_b[j][:n_fwd]:
+                fn()
+            ev_out.record(stream)
+            with torch.cuda.stream(cs_out):
+                cs_out.wait_event(ev_out)
+                out_h.copy_(out, non_blocking=True)
+                ev_outcp.record(cs_out)
+            if i > 0:
+                stream.wait_event(ev_dxcp)
+            for _, _, fn in calls_b[j][n_fwd:]:
+                fn()
+            ev_dx.record(stream)
+            ev_free[j].record(stream)
+            with torch.cuda.stream(cs_out):
+                cs_out.wait_event(ev_dx)
+                dx_h.copy_(dx, non_blocking=True)
+                ev_dxcp.record(cs_out)
+            if i + 2 < n_steps:
+                h2d(j, ev_free[j])
+        stream.wait_event(ev_outcp)
+        stream.wait_event(ev_dxcp)
+
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_run(3, e0)
     torch.cuda.synchronize()
     e_steps = max(10, args.steps // 4)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e_steps):
-        e2e_step()
+    e2e_run(e_steps, e0)
     e1.record(stream)
     torch.cuda.synchronize()
+    assert status.item() == 0, f"device status {status.item()}"
     e2e_ms = e0.elapsed_time(e1) / e_steps
     h2d = x_h.numel() * 2 + dout_h.numel() * 2 + ids_h.numel() * 4 + wts_h.numel() * 4
     d2h = 2 * T * d * 2
