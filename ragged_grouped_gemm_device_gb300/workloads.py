@@ -216,3 +216,88 @@ def custom(T: int, k: int, E: int, d: int, h: int, seed: int = 0, invalid_frac: 
 
 
 NAMES = ("toy", "balanced", "finegrained", "skew", "large")
+
+
+# ---------------------------------------------------------------------------------------------
+# One square expert projection (Figs. 38 and 40 of "Section 09: Grouped GEMM"): 16 local
+# experts, Y_e = X_e W_e with W_e [K, N], K = N = 4096.
+_TAG_PROJ_W, _TAG_PROJ_X, _TAG_HIST, _TAG_PERM = 8, 9, 10, 11
+
+
+def projection_weight(e: int, K: int, N: int, seed: int = 0) -> np.ndarray:
+    """Expert e's projection weight [K, N], N(0, 1/sqrt(K)), bf16 values in float32."""
+    return _normal_bf16(_rng(seed, _TAG_PROJ_W, e, K, N), (K, N), 1.0 / np.sqrt(K))
+
+
+def projection_x(rows: int, K: int, seed: int = 0) -> np.ndarray:
+    """Projection input rows [rows, K], N(0, 1), bf16 values in float32."""
+    return _normal_bf16(_rng(seed, _TAG_PROJ_X, rows, K), (rows, K))
+
+
+def balanced_counts(M: int, E: int) -> np.ndarray:
+    """M rows over E experts as evenly as possible (the first M mod E experts get one more)."""
+    c = np.full(E, M // E, np.int64)
+    c[: M % E] += 1
+    return c
+
+
+def _entropy_imbalance(counts: np.ndarray) -> float:
+    """Eq. 18 of "Section 09" for a drawn histogram, used only to stratify the draws:
+    1 + sum_e p_e log p_e / log E over the experts with rows."""
+    p = np.asarray(counts, np.float64) / float(np.sum(counts))
+    p = p[p > 0]
+    return 1.0 + float(np.sum(p * np.log(p))) / float(np.log(len(counts)))
+
+
+def dirichlet_histograms(M: int = 65536, E: int = 16, n_bins: int = 10, per_bin: int = 10,
+                         tile: int = 128, align: int = 8, seed: int = 0,
+                         max_draws: int = 400000) -> list:
+    """Fig. 40's fixed-work histograms: symmetric-Dirichlet proposals (concentration drawn
+    log-uniformly from 10^-2.5 to 10^2) turned into exact counts that are multiples of `align`,
+    hold at least one `tile` of rows per expert and sum to M (each expert gets one tile, the
+    remaining (M - E*tile)/align units of `align` rows go by largest remainder of the
+    proposal, ties to the lower expert). Kept: `per_bin` histograms with distinct sorted counts
+    in each of `n_bins` equal-width ranges of I_H between 0 and the largest admissible I_H
+    (one expert holding everything but the other experts' single tiles).
+
+    Returns a list of (counts int64 [E], I_H), bin by bin."""
+    units = M - E * tile
+    if units < 0 or units % align:
+        raise ValueError("M - E*tile must be a non-negative multiple of align")
+    units //= align
+    top = np.full(E, tile, np.int64)
+    top[0] += units * align
+    i_max = _entropy_imbalance(top)
+    rng = _rng(seed, _TAG_HIST, M, E, n_bins, per_bin)
+    bins = [[] for _ in range(n_bins)]
+    seen = set()
+    for _ in range(max_draws):
+        if all(len(b) >= per_bin for b in bins):
+            break
+        alpha = 10.0 ** rng.uniform(-2.5, 2.0)
+        p = rng.dirichlet(np.full(E, alpha))
+        if not np.all(np.isfinite(p)) or p.sum() <= 0:
+            continue
+        quota = p / p.sum() * units
+        alloc = np.floor(quota).astype(np.int64)
+        rest = int(units - alloc.sum())
+        order = np.argsort(-(quota - alloc), kind="stable")
+        alloc[order[:rest]] += 1
+        counts = tile + align * alloc
+        key = tuple(sorted(counts.tolist()))
+        if key in seen:
+            continue
+        ih = _entropy_imbalance(counts)
+        b = min(int(ih / i_max * n_bins), n_bins - 1)
+        if len(bins[b]) < per_bin:
+            bins[b].append((counts, ih))
+            seen.add(key)
+    if not all(len(b) >= per_bin for b in bins):
+        raise RuntimeError("could not fill every I_H range; raise max_draws")
+    return [item for b in bins for item in b]
+
+
+def expert_permutations(E: int, n: int, seed: int = 0) -> list:
+    """n seeded permutations of the expert indices (the first is the identity)."""
+    rng = _rng(seed, _TAG_PERM, E, n)
+    return [np.arange(E)] + [rng.permutation(E) for _ in range(n - 1)]

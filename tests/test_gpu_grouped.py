@@ -24,12 +24,17 @@ FWD_CASES = {
     "edge_one_expert": lambda: W.custom(T=700, k=1, E=1, d=64, h=64, seed=9),
     # most experts empty, the last one non-empty
     "edge_sparse": lambda: W.custom(T=100, k=1, E=64, d=64, h=72, seed=10, empty_experts=tuple(range(0, 62))),
+    # the largest problem list (E = 1024 experts of ~12 rows, every 41st empty): the in-kernel
+    # offsets and tile prefix at their maximum size, one ragged tile per expert
+    "edge_max_experts": lambda: W.custom(T=3000, k=4, E=1024, d=64, h=64, seed=11,
+                                         empty_experts=tuple(range(0, 1024, 41))),
     "balanced": lambda: W.make("balanced"),
     "finegrained": lambda: W.make("finegrained"),
     "skew": lambda: W.make("skew"),
 }
 
-BWD_CASES = ["toy", "edge_small", "edge_wide", "edge_one_expert", "edge_sparse", "finegrained", "skew"]
+BWD_CASES = ["toy", "edge_small", "edge_wide", "edge_one_expert", "edge_sparse", "edge_max_experts",
+             "finegrained", "skew"]
 
 
 def _dy(wl, M):
