@@ -159,6 +159,22 @@ def combine(y: np.ndarray, inv_map: np.ndarray, weights, T: int, k: int) -> np.n
     return out
 
 
+def routing_weight_grad(dout: np.ndarray, y: np.ndarray, inv_map: np.ndarray, T: int,
+                        k: int) -> np.ndarray:
+    """Gradient of the combine (agent doc: scatter back with routing weights) with respect to
+    the routing weights. out[t] = sum_j w[t,j] * y[inv[t,j]] is linear in w, so
+    dL/dw[t,j] = <dOut[t], y[inv[t,j]]> with y the unweighted expert output; 0 for a dropped
+    slot. Returns float64 [T, k]."""
+    dout = np.asarray(dout, np.float64)
+    y = np.asarray(y, np.float64)
+    inv = np.asarray(inv_map).reshape(T, k).astype(np.int64)
+    dw = np.zeros((T, k), np.float64)
+    for j in range(k):
+        ok = inv[:, j] >= 0
+        dw[ok, j] = np.einsum("td,td->t", dout[ok], y[inv[ok, j]])
+    return dw
+
+
 # ---------------------------------------------------------------------------------------------
 # a10-a13: backward (Eq. 15, Table 15) of the SwiGLU expert
 # ---------------------------------------------------------------------------------------------

@@ -175,6 +175,7 @@ def _torch_layer_grads(wl, dout):
     x = torch.tensor(wl.x(), dtype=torch.float64, requires_grad=True)
     wu = torch.tensor(wl.w_ug_all(), dtype=torch.float64, requires_grad=True)
     wd = torch.tensor(wl.w_down_all(), dtype=torch.float64, requires_grad=True)
+    wr = torch.tensor(wl.weights.astype(np.float64), requires_grad=True)
     rows = []
     for t in range(wl.T):
         acc = torch.zeros(wl.d, dtype=torch.float64)
@@ -182,11 +183,12 @@ def _torch_layer_grads(wl, dout):
             e = int(wl.ids[t, j])
             if 0 <= e < wl.E:
                 g, v = (wu[e] @ x[t]).split(wl.h)
-                acc = acc + float(wl.weights[t, j]) * ((torch.nn.functional.silu(g) * v) @ wd[e])
+                acc = acc + wr[t, j] * ((torch.nn.functional.silu(g) * v) @ wd[e])
         rows.append(acc)
     out = torch.stack(rows)
     (out * torch.from_numpy(dout.astype(np.float64))).sum().backward()
-    return out.detach().numpy(), x.grad.numpy(), wu.grad.numpy(), wd.grad.numpy()
+    dwr = wr.grad.numpy() if wr.grad is not None else np.zeros_like(wl.weights, np.float64)
+    return out.detach().numpy(), x.grad.numpy(), wu.grad.numpy(), wd.grad.numpy(), dwr
 
 
 def _oracle_layer_grads(wl, dout):
@@ -194,7 +196,8 @@ def _oracle_layer_grads(wl, dout):
     dy = O.permute(dout, r["sorted_src"], r["M"], wl.k, row_scale=wl.weights)
     dxp, dw_ug, dw_down, _ = O.expert_backward(dy, xp, u, r["offsets"], wl.w_ug, wl.w_down)
     dx = O.combine(dxp, r["inv_map"], None, wl.T, wl.k)
-    return out, dx, dw_ug, dw_down
+    dwr = O.routing_weight_grad(dout, y, r["inv_map"], wl.T, wl.k)
+    return out, dx, dw_ug, dw_down, dwr
 
 
 def test_backward_matches_torch_autograd_fp64():
@@ -204,12 +207,34 @@ def test_backward_matches_torch_autograd_fp64():
     got = _oracle_layer_grads(wl, dout)
     for g_, w_ in zip(got, want):
         np.testing.assert_allclose(g_, w_, rtol=1e-11, atol=1e-11)
+    # dropped slots (ids outside [0, E)) carry no gradient
+    assert not got[4][(wl.ids < 0) | (wl.ids >= wl.E)].any()
+
+
+def test_routing_weight_grad_central_differences_on_toy():
+    """The layer loss <dOut, out> is linear in each routing weight: a central difference is
+    exact up to rounding."""
+    wl = W.custom(T=7, k=2, E=3, d=8, h=12, seed=12, invalid_frac=0.15)
+    dout = W._normal_bf16(np.random.default_rng(9), (wl.T, wl.d)).astype(np.float64)
+    r, x, xp, y, u, a, out, _ = _layer(wl)
+    dwr = O.routing_weight_grad(dout, y, r["inv_map"], wl.T, wl.k)
+
+    def loss(w):
+        return float((O.combine(y, r["inv_map"], w, wl.T, wl.k) * dout).sum())
+
+    w0 = wl.weights.astype(np.float64)
+    for t in range(wl.T):
+        for j in range(wl.k):
+            plus, minus = w0.copy(), w0.copy()
+            plus[t, j] += 0.5
+            minus[t, j] -= 0.5
+            assert loss(plus) - loss(minus) == pytest.approx(dwr[t, j], rel=1e-12, abs=1e-12)
 
 
 def test_backward_central_differences_on_toy():
     wl = W.make("toy")
     dout = W._normal_bf16(np.random.default_rng(3), (wl.T, wl.d)).astype(np.float64)
-    _, dx, dw_ug, dw_down = _oracle_layer_grads(wl, dout)
+    _, dx, dw_ug, dw_down, _ = _oracle_layer_grads(wl, dout)
     x0, wu0, wd0 = wl.x().astype(np.float64), wl.w_ug_all().astype(np.float64), wl.w_down_all().astype(np.float64)
     r = O.route_offsets(wl.ids, wl.E)
 
@@ -257,7 +282,7 @@ def test_combine_equals_scatter_add_reference():
 def test_results_invariant_to_expert_relabelling():
     wl = W.custom(T=21, k=2, E=5, d=8, h=12, seed=6, invalid_frac=0.1, empty_experts=(2,))
     dout = W._normal_bf16(np.random.default_rng(8), (wl.T, wl.d))
-    out, dx, dw_ug, dw_down = _oracle_layer_grads(wl, dout)
+    out, dx, dw_ug, dw_down, dwr = _oracle_layer_grads(wl, dout)
     pi = np.array([3, 0, 4, 1, 2])
     wu, wd = wl.w_ug_all(), wl.w_down_all()
     wl2 = W.custom(T=21, k=2, E=5, d=8, h=12, seed=6, invalid_frac=0.1, empty_experts=(2,))
@@ -268,8 +293,8 @@ def test_results_invariant_to_expert_relabelling():
     wl2.w_down = lambda e: wd[inv_pi[e]]
     wl2.w_ug_all = lambda: wu[inv_pi]
     wl2.w_down_all = lambda: wd[inv_pi]
-    out2, dx2, dw_ug2, dw_down2 = _oracle_layer_grads(wl2, dout)
-    assert np.array_equal(out, out2) and np.array_equal(dx, dx2)
+    out2, dx2, dw_ug2, dw_down2, dwr2 = _oracle_layer_grads(wl2, dout)
+    assert np.array_equal(out, out2) and np.array_equal(dx, dx2) and np.array_equal(dwr, dwr2)
     assert np.array_equal(dw_ug2, dw_ug[inv_pi]) and np.array_equal(dw_down2, dw_down[inv_pi])
 
 
@@ -302,3 +327,13 @@ def test_planted_mistakes_are_caught(monkeypatch):
     monkeypatch.setattr(O, "combine", lambda y, inv, w, T, k: real_combine(y, inv, None, T, k))  # weights dropped
     *_, out, _ = _layer(wl)
     assert not np.allclose(out, want, rtol=1e-6)
+    monkeypatch.setattr(O, "combine", real_combine)
+    # routing-weight gradient taken against the weighted output, or against the wrong slot
+    dout = W._normal_bf16(np.random.default_rng(4), (wl.T, wl.d))
+    want_dwr = _torch_layer_grads(wl, dout)[4]
+    real_rwg = O.routing_weight_grad
+    w2 = wl.weights.astype(np.float64)
+    for bad in (lambda do, y, inv, T, k: real_rwg(do, y, inv, T, k) * w2,
+                lambda do, y, inv, T, k: real_rwg(do, y, np.roll(np.asarray(inv).reshape(T, k), 1, axis=1), T, k)):
+        monkeypatch.setattr(O, "routing_weight_grad", bad)
+        assert not np.allclose(_oracle_layer_grads(wl, dout)[4], want_dwr, rtol=1e-6)
