@@ -4,8 +4,9 @@
 One step = the whole hot path over one batch of the large workload (T = 16384 tokens, E = 256
 experts, top-8, d = 2048, h = 512, M = 131072 routed rows): route histogram + offsets +
 placement, permute, grouped up/gate GEMM with fused SwiGLU, grouped down GEMM, weighted
-combine, and the backward (combine backward, down dgrad with fused SwiGLU backward, up dgrad,
-both wgrads, permute backward). Every step is a library kernel called through the C ABI.
+combine, and the backward (combine backward, down dgrad with fused SwiGLU backward and the
+routing-weight gradient, up dgrad, both wgrads, permute backward). Every step is a library
+kernel called through the C ABI.
 
 Metric: useful expert TFLOP/s, 18*M*d*h per forward+backward step (6*M*d*h forward), M counting
 routed rows only. Prints one JSON line. `--impl reference` times the CPU fp64 oracle instead.
@@ -93,6 +94,8 @@ class OracleSampler:
             y, u, a, _ = O.expert_forward(xp, one, lambda i: wu, lambda i: wd)
             dy = O.permute(self.dout, src, t - s, wl.k, row_scale=wl.weights)
             O.expert_backward(dy, xp, u, one, lambda i: wu, lambda i: wd)
+            # routing-weight gradient of this expert's slots: <dOut[token], unweighted y row>
+            O.routing_weight_grad(O.permute(self.dout, src, t - s, wl.k), y, np.arange(t - s), t - s, 1)
             elapsed += time.perf_counter() - t0
             picked += 1
             rows += t - s
@@ -100,7 +103,7 @@ class OracleSampler:
             if elapsed >= seconds:
                 break
         desc = (f"route over all {wl.n} slots, then {picked} of {wl.E} experts ({rows} of {r['M']} rows): "
-                f"permute + fp64 forward + backward per expert")
+                f"permute + fp64 forward + backward (incl. routing-weight gradient) per expert")
         return flops, elapsed, desc
 
 
@@ -279,6 +282,8 @@ def run_ours(args):
     dx = torch.empty(T, d, dtype=bf, device=dev)
     dw_ug = torch.empty(E, 2 * h, d, dtype=torch.float32, device=dev)
     dw_down = torch.empty(E, h, d, dtype=torch.float32, device=dev)
+    dw_part = torch.empty(n, L.routing_grad_parts(h), dtype=torch.float32, device=dev)
+    dw_route = torch.empty(T, k, dtype=torch.float32, device=dev)
     status = torch.zeros(1, dtype=i32, device=dev)
     _, p_lo = L.saved_views(saved, n, h)
     stream = torch.cuda.current_stream()
@@ -296,7 +301,9 @@ def run_ours(args):
             ("combine", 1, lambda: L.moe_unpermute_combine(y, inv_map, None, T, k, d, out)),
             ("combine_bwd", 1, lambda: L.moe_permute(doin, sorted_src, offsets, None, T, k, E, d, dy)),
             ("down_dgrad_swiglu", 1, lambda: L.moe_grouped_down_dgrad_swiglu(dy, saved, offsets, sorted_src, win, E,
-                                                                             n, d, h, w_down, du_hi, du_lo, status)),
+                                                                             n, d, h, w_down, du_hi, du_lo, status,
+                                                                             dw_part=dw_part)),
+            ("routing_weight_grad", 1, lambda: L.moe_routing_weight_grad(dw_part, inv_map, T, k, h, dw_route)),
             ("up_dgrad", 1, lambda: L.moe_grouped_up_dgrad(du_hi, offsets, E, n, d, h, w_ug, dxp, status)),
             ("wgrad_down", 1, lambda: L.moe_grouped_wgrad(a, p_lo, h, dy, d, offsets, E, n, dw_down, status)),
             ("wgrad_up", 1, lambda: L.moe_grouped_wgrad(du_hi, du_lo, 2 * h, xp, d, offsets, E, n, dw_ug, status)),

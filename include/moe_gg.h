@@ -64,7 +64,7 @@ typedef enum {
 typedef enum {
   MOE_OP_ROUTE = 0,       /* moe_route_offsets */
   MOE_OP_FWD = 1,         /* moe_grouped_swiglu_fwd */
-  MOE_OP_BWD = 2,         /* moe_grouped_bwd */
+  MOE_OP_BWD = 2,         /* moe_grouped_bwd (dU halves, routing-gradient partials) */
   MOE_OP_PADDED_BMM = 3,  /* moe_padded_bmm_swiglu_fwd (uses capacity_C) */
   MOE_OP_LOOP = 4,        /* moe_loop_swiglu_fwd */
   MOE_OP_SAVED = 5        /* size of the `saved` buffer the forward fills for the backward */
@@ -166,14 +166,23 @@ moe_status_t moe_grouped_swiglu_fwd(const moe_bf16* xp, const int32_t* offsets,
  *  xp, a_save, saved, sorted_src, weights as given to the forward (saved required here).
  *  dxp     [cap, d] bf16 out (rows < M).
  *  dw_ug   [E, 2h, d] fp32 out;  dw_down [E, h, d] fp32 out. Experts with M_e = 0 get zeros.
- *  ws      moe_workspace_bytes(MOE_OP_BWD, ...) bytes (holds dU high and low, 2 x [cap, 2h] bf16).
+ *  inv_map, dw_route  nullable pair: when dw_route ([cap] fp32, by flat slot t*top_k + j,
+ *          cap = T*top_k) is given, it receives the routing-weight gradient of the combine,
+ *          dw_route[t*top_k+j] = <dOut[t], y~_p> with p = inv_map[t*top_k+j] and y~_p = A_p
+ *          W_down,e the unweighted expert output (0 for a dropped slot). It is computed as
+ *          <A_p, dy_p W_down,e^T> in the dgrad epilogue (dy = the gather of dOut), from fp32
+ *          U and the fp32 accumulator, and summed over fixed partial slots in index order:
+ *          deterministic.
+ *  ws      moe_workspace_bytes(MOE_OP_BWD, ...) bytes: dU high and low (2 x [cap, 2h] bf16),
+ *          then the routing-gradient partials ([cap, 2 ceil(h/256)] fp32, used with dw_route).
  */
 moe_status_t moe_grouped_bwd(const moe_bf16* dy, const moe_bf16* xp, const moe_bf16* a_save,
                              const void* saved, const int32_t* offsets, const int32_t* sorted_src,
                              const float* weights, int E, int cap, int d, int h,
                              const moe_bf16* w_ug, const moe_bf16* w_down, moe_bf16* dxp,
-                             float* dw_ug, float* dw_down, void* ws, size_t ws_bytes,
-                             int32_t* dev_status, moe_stream_t stream);
+                             float* dw_ug, float* dw_down, const int32_t* inv_map,
+                             float* dw_route, void* ws, size_t ws_bytes, int32_t* dev_status,
+                             moe_stream_t stream);
 
 /*
  * The single kernels the two calls above are made of, one per step of the path, for callers
@@ -186,7 +195,13 @@ moe_status_t moe_grouped_bwd(const moe_bf16* dy, const moe_bf16* xp, const moe_b
  * moe_grouped_down       -- y_e = a_e W_down,e (Eq. 13, second line); a [cap, h] bf16.
  * moe_grouped_down_dgrad_swiglu -- dA = (w *) dy_e W_down,e^T (Eq. 15 dgrad of the down
  *                           projection) with the SwiGLU backward fused: writes dU = [dgate, dup]
- *                           as bf16 high (du_hi) and low (du_lo) halves, each [cap, 2h].
+ *                           as bf16 high (du_hi) and low (du_lo) halves, each [cap, 2h]. With
+ *                           dw_part (nullable, [cap, 2 ceil(h/256)] fp32) it also writes, for
+ *                           every row p < M, the partial sums of <A_p, dy_p W_down,e^T> over
+ *                           the row's 128-column pieces (see moe_routing_weight_grad).
+ * moe_routing_weight_grad -- dw_route[s] = sum of the partials of row inv_map[s] in index order
+ *                           (0 for a dropped slot), s < T*top_k: the routing-weight gradient of
+ *                           the combine, as in moe_grouped_bwd.
  * moe_grouped_up_dgrad   -- dxp_e = dU_e W_ug,e (Eq. 15 dgrad of the up/gate projection).
  * moe_grouped_wgrad      -- dW_e = P_e^T Q_e over each expert's M_e rows (Eq. 15 wgrad;
  *                           Table 15: M_e is the contraction length). P = p_hi (+ p_lo when
@@ -207,8 +222,10 @@ moe_status_t moe_grouped_down_dgrad_swiglu(const moe_bf16* dy, const void* saved
                                            const int32_t* offsets, const int32_t* sorted_src,
                                            const float* weights, int E, int cap, int d, int h,
                                            const moe_bf16* w_down, moe_bf16* du_hi,
-                                           moe_bf16* du_lo, int32_t* dev_status,
+                                           moe_bf16* du_lo, float* dw_part, int32_t* dev_status,
                                            moe_stream_t stream);
+moe_status_t moe_routing_weight_grad(const float* dw_part, const int32_t* inv_map, int T,
+                                     int top_k, int h, float* dw_route, moe_stream_t stream);
 moe_status_t moe_grouped_up_dgrad(const moe_bf16* du_hi, const int32_t* offsets, int E, int cap,
                                   int d, int h, const moe_bf16* w_ug, moe_bf16* dxp,
                                   int32_t* dev_status, moe_stream_t stream);

@@ -29,13 +29,15 @@ SIGNATURES = {
     "moe_route_offsets": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P, _S, _P]),
     "moe_permute": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P]),
     "moe_grouped_swiglu_fwd": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _S, _P, _P]),
-    "moe_grouped_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _S, _P, _P]),
+    "moe_grouped_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _S, _P,
+                             _P]),
     "moe_unpermute_combine": (_I, [_P, _P, _P, _I, _I, _I, _P, _P]),
     "moe_padded_bmm_swiglu_fwd": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _S, _P, _P]),
     "moe_loop_swiglu_fwd": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P]),
     "moe_grouped_up_swiglu": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P]),
     "moe_grouped_down": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P]),
-    "moe_grouped_down_dgrad_swiglu": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P]),
+    "moe_grouped_down_dgrad_swiglu": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
+    "moe_routing_weight_grad": (_I, [_P, _P, _I, _I, _I, _P, _P]),
     "moe_grouped_up_dgrad": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P]),
     "moe_grouped_wgrad": (_I, [_P, _P, _I, _P, _I, _P, _I, _I, _P, _P, _P]),
     "moe_route_offsets_noalloc": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P]),
@@ -131,13 +133,13 @@ def moe_grouped_swiglu_fwd(xp, offsets, sorted_src, weights, E, cap, d, h, w_ug,
 
 
 def moe_grouped_bwd(dy, xp, a_save, saved, offsets, sorted_src, weights, E, cap, d, h, w_ug, w_down, dxp,
-                    dw_ug, dw_down, ws, dev_status=None, stream=None):
+                    dw_ug, dw_down, ws, dev_status=None, stream=None, inv_map=None, dw_route=None):
     ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
     _check("moe_grouped_bwd", load().moe_grouped_bwd(
         _ptr(dy), _ptr(xp), _ptr(a_save), _ptr(saved), _ptr(offsets), _ptr(sorted_src), _ptr(weights), E,
         cap, d, h, _ptr(w_ug),
-        _ptr(w_down), _ptr(dxp), _ptr(dw_ug), _ptr(dw_down), _ptr(ws), ws_bytes, _ptr(dev_status),
-        _stream(stream)))
+        _ptr(w_down), _ptr(dxp), _ptr(dw_ug), _ptr(dw_down), _ptr(inv_map), _ptr(dw_route), _ptr(ws), ws_bytes,
+        _ptr(dev_status), _stream(stream)))
 
 
 def moe_grouped_up_swiglu(xp, offsets, sorted_src, weights, E, cap, d, h, w_ug, a_save, saved=None,
@@ -153,10 +155,20 @@ def moe_grouped_down(a, offsets, E, cap, d, h, w_down, y, dev_status=None, strea
 
 
 def moe_grouped_down_dgrad_swiglu(dy, saved, offsets, sorted_src, weights, E, cap, d, h, w_down, du_hi, du_lo,
-                                  dev_status=None, stream=None):
+                                  dev_status=None, stream=None, dw_part=None):
     _check("moe_grouped_down_dgrad_swiglu", load().moe_grouped_down_dgrad_swiglu(
         _ptr(dy), _ptr(saved), _ptr(offsets), _ptr(sorted_src), _ptr(weights), E, cap, d, h, _ptr(w_down),
-        _ptr(du_hi), _ptr(du_lo), _ptr(dev_status), _stream(stream)))
+        _ptr(du_hi), _ptr(du_lo), _ptr(dw_part), _ptr(dev_status), _stream(stream)))
+
+
+def routing_grad_parts(h):
+    """Partial sums per row the dgrad leaves for the routing-weight gradient: 2 ceil(h/256)."""
+    return 2 * ((h + 255) // 256)
+
+
+def moe_routing_weight_grad(dw_part, inv_map, T, top_k, h, dw_route, stream=None):
+    _check("moe_routing_weight_grad", load().moe_routing_weight_grad(
+        _ptr(dw_part), _ptr(inv_map), T, top_k, h, _ptr(dw_route), _stream(stream)))
 
 
 def moe_grouped_up_dgrad(du_hi, offsets, E, cap, d, h, w_ug, dxp, dev_status=None, stream=None):

@@ -639,7 +639,10 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
         };
         // dA = w * acc; dgate = dA * up * s * (1 + gate * (1 - s)), dup = dA * silu(gate), as
-        // bf16 high and low halves
+        // bf16 high and low halves. With dw_part: this lane's share of <A, acc> for the
+        // routing-weight gradient, A = silu(gate) * up unweighted and acc = dy W_down^T before w
+        // (<A, dy W_down^T> = <A W_down, dy>: the unweighted expert output against dOut).
+        float dw_acc = 0.f;
         auto process = [&](int c, const uint32_t (&v)[16]) {
           const int col = ti.n0 + c * 16;
           if (!rv || col >= h) return;
@@ -657,10 +660,12 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
               const float g = gv[2 * j + hh], uu = uv[2 * j + hh];
-              const float da = wrow * __uint_as_float(v[2 * j + hh]);
+              const float acc_raw = __uint_as_float(v[2 * j + hh]);
+              const float da = wrow * acc_raw;
               const float sg = sigmoid_f(g);
               dg[hh] = da * uu * sg * (1.0f + g * (1.0f - sg));
               du[hh] = da * g * sg;
+              if (two || j < 4) dw_acc = fmaf(g * sg * uu, acc_raw, dw_acc);  // columns < h
             }
             gh[j] = pack_bf16x2(dg[0], dg[1]);
             uh[j] = pack_bf16x2(du[0], du[1]);
@@ -726,6 +731,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             tmem_ld_wait(v0);
           }
         }
+        // every (row, column tile, half) slot is written once, zero when it has no column < h
+        if (args.dw_part != nullptr && rv)
+          args.dw_part[row * args.dw_np + (ti.n0 / BN) * 2 + half] = dw_acc;
       } else {  // wgrad modes
         // Each 32-row x 16-column fp32 chunk goes through this warp's staging buffer (64-byte
         // swizzle: lane r writes its row's 16-byte piece j at piece j ^ ((r >> 1) & 3), which

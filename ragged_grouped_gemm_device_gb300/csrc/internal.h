@@ -62,6 +62,10 @@ struct GemmArgs {
   // UP_SWIGLU, DGRAD_SWIGLU: 1 when every bf16 row output is 32-byte aligned at each 16-column
   // chunk (bases 32-byte aligned, h % 16 == 0), so a chunk row is one 32-byte store
   int vec32;
+  // DGRAD_SWIGLU, optional: per row p, dw_np fp32 partial sums of <A_p, G_p> (A = SwiGLU(U)
+  // unweighted, G = dy W_down^T before the routing weight), one per (column tile, warp half)
+  float* dw_part;
+  int dw_np;
   int32_t* status;         // optional device status word
   long long timeout_ns;    // bound of every wait inside the kernel
 };
@@ -108,6 +112,9 @@ moe_status_t launch_combine(const void* y, const int32_t* inv_map, const float* 
                             int k, int d, void* out, cudaStream_t s);
 moe_status_t launch_pad_rows(const void* src, const int32_t* offsets, int E, int C, int cols,
                              void* dst, cudaStream_t s);
+// dw[s] = sum of the dw_np partials of row inv_map[s] in index order, 0 for a dropped slot.
+moe_status_t launch_routing_weight_grad(const float* part, int np, const int32_t* inv_map,
+                                        int n_slots, float* dw, cudaStream_t s);
 moe_status_t launch_unpad_rows(const void* src, const int32_t* offsets, int E, int C, int cap,
                                int cols, void* dst, cudaStream_t s);
 

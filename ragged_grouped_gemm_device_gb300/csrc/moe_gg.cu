@@ -61,6 +61,11 @@ const void* saved_u(const void* saved, long long rows, int h) {
   return static_cast<const uint8_t*>(saved) + saved_p_bytes(rows, h);
 }
 size_t bwd_ws_half(long long rows, int h) { return round256(static_cast<size_t>(rows) * 2 * h * 2); }
+// routing-weight gradient partials: one per (256-column tile, warp half) of the dgrad, per row
+int route_grad_parts(int h) { return 2 * ((h + 255) / 256); }
+size_t route_grad_part_bytes(long long rows, int h) {
+  return round256(static_cast<size_t>(rows) * route_grad_parts(h) * 4);
+}
 
 // ---- one launch per step; `src` carries the problem source (device offsets, uniform rows or
 // one expert), `rows` the rows of the row buffers, `tiles_bound` an upper bound of row tiles.
@@ -108,7 +113,7 @@ moe_status_t run_down(const GemmArgs& src, long long rows, long long tiles_bound
 // a10: dA = dy W_down^T with the SwiGLU backward -> dU high and low halves.
 moe_status_t run_down_dgrad_swiglu(const GemmArgs& src, long long rows, int E, int d, int h,
                                    const void* dy, const void* saved, const void* w_down,
-                                   void* du_hi, void* du_lo, cudaStream_t s) {
+                                   void* du_hi, void* du_lo, float* dw_part, cudaStream_t s) {
   CUtensorMap ma, mb;
   if (!make_map_rows2d(&ma, dy, rows, d, 128)) return map_fail("dy");
   if (!make_map_weight3d(&mb, w_down, E, h, d, 256)) return map_fail("w_down");
@@ -122,6 +127,8 @@ moe_status_t run_down_dgrad_swiglu(const GemmArgs& src, long long rows, int E, i
   a.ldo2 = 2LL * h;
   a.aux = saved_u(saved, rows, h);
   a.vec32 = (h % 16 == 0 && aligned32(du_hi) && aligned32(du_lo)) ? 1 : 0;
+  a.dw_part = dw_part;
+  a.dw_np = route_grad_parts(h);
   CUtensorMap mhi, mlo;
   if (!make_map_rows2d_store(&mhi, du_hi, rows, 2LL * h)) return map_fail("du_hi");
   if (!make_map_rows2d_store(&mlo, du_lo, rows, 2LL * h)) return map_fail("du_lo");
@@ -237,7 +244,7 @@ using namespace moe;
 
 extern "C" {
 
-int moe_abi_version(void) { return 1; }
+int moe_abi_version(void) { return 2; }
 
 const char* moe_last_cuda_error(void) { return g_last_error; }
 
@@ -260,7 +267,7 @@ size_t moe_workspace_bytes(int op, int T, int top_k, int E, int d, int h, int ca
   switch (op) {
     case MOE_OP_ROUTE: return route_workspace_bytes(n, E);
     case MOE_OP_FWD: return 0;
-    case MOE_OP_BWD: return h > 0 ? 2 * bwd_ws_half(n, h) : 0;
+    case MOE_OP_BWD: return h > 0 ? 2 * bwd_ws_half(n, h) + route_grad_part_bytes(n, h) : 0;
     case MOE_OP_SAVED: return h > 0 ? saved_bytes(n, h, E) : 0;
     case MOE_OP_PADDED_BMM: {
       if (capacity_C <= 0 || d <= 0 || h <= 0) return 0;
@@ -356,22 +363,36 @@ moe_status_t moe_grouped_down_dgrad_swiglu(const moe_bf16* dy, const void* saved
                                            const int32_t* offsets, const int32_t* sorted_src,
                                            const float* weights, int E, int cap, int d, int h,
                                            const moe_bf16* w_down, moe_bf16* du_hi,
-                                           moe_bf16* du_lo, int32_t* dev_status,
+                                           moe_bf16* du_lo, float* dw_part, int32_t* dev_status,
                                            moe_stream_t stream) {
   moe_status_t st = check_grouped_common(E, cap, d, h);
   if (st != MOE_OK) return st;
   if (!dy || !saved || !offsets || !w_down || !du_hi || !du_lo || (weights && !sorted_src))
     return MOE_ERR_INVALID_ARG;
   if (!aligned16(dy) || !aligned16(saved) || !aligned16(w_down) || !aligned16(du_hi) ||
-      !aligned16(du_lo))
+      !aligned16(du_lo) || (reinterpret_cast<uintptr_t>(dw_part) & 3u))
     return MOE_ERR_INVALID_ARG;
   if ((st = check_device()) != MOE_OK || cap == 0) return st;
   GemmArgs src = base_args(E, cap, dev_status);
   src.offsets = offsets;
   src.row_src = sorted_src;
   src.row_weight = weights;
-  return run_down_dgrad_swiglu(src, cap, E, d, h, dy, saved, w_down, du_hi, du_lo,
+  return run_down_dgrad_swiglu(src, cap, E, d, h, dy, saved, w_down, du_hi, du_lo, dw_part,
                                reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_routing_weight_grad(const float* dw_part, const int32_t* inv_map, int T,
+                                     int top_k, int h, float* dw_route, moe_stream_t stream) {
+  if (T < 0 || top_k < 1 || h <= 0) return MOE_ERR_INVALID_ARG;
+  if (top_k > MAX_TOPK) return MOE_ERR_UNSUPPORTED_SHAPE;
+  const long long n = static_cast<long long>(T) * top_k;
+  if (n > INT32_MAX) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (n == 0) return MOE_OK;
+  if (!dw_part || !inv_map || !dw_route) return MOE_ERR_INVALID_ARG;
+  moe_status_t st = check_device();
+  if (st != MOE_OK) return st;
+  return launch_routing_weight_grad(dw_part, route_grad_parts(h), inv_map, static_cast<int>(n),
+                                    dw_route, reinterpret_cast<cudaStream_t>(stream));
 }
 
 moe_status_t moe_grouped_up_dgrad(const moe_bf16* du_hi, const int32_t* offsets, int E, int cap,
@@ -437,24 +458,27 @@ moe_status_t moe_grouped_bwd(const moe_bf16* dy, const moe_bf16* xp, const moe_b
                              const void* saved, const int32_t* offsets, const int32_t* sorted_src,
                              const float* weights, int E, int cap, int d, int h,
                              const moe_bf16* w_ug, const moe_bf16* w_down, moe_bf16* dxp,
-                             float* dw_ug, float* dw_down, void* ws, size_t ws_bytes,
-                             int32_t* dev_status, moe_stream_t stream) {
+                             float* dw_ug, float* dw_down, const int32_t* inv_map,
+                             float* dw_route, void* ws, size_t ws_bytes, int32_t* dev_status,
+                             moe_stream_t stream) {
   moe_status_t st = check_grouped_common(E, cap, d, h);
   if (st != MOE_OK) return st;
   if (!dy || !xp || !a_save || !saved || !offsets || !w_ug || !w_down || !dxp || !dw_ug ||
-      !dw_down || (weights && !sorted_src))
+      !dw_down || (weights && !sorted_src) || (dw_route && !inv_map))
     return MOE_ERR_INVALID_ARG;
   if (!aligned16(dy) || !aligned16(xp) || !aligned16(a_save) || !aligned16(saved) ||
       !aligned16(w_ug) || !aligned16(w_down) || !aligned16(dxp) || !aligned16(dw_ug) ||
       !aligned16(dw_down) || !aligned16(ws))
     return MOE_ERR_INVALID_ARG;
   const size_t half = bwd_ws_half(cap, h);
-  if (ws_bytes < 2 * half) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  if (ws_bytes < 2 * half + (dw_route ? route_grad_part_bytes(cap, h) : 0))
+    return MOE_ERR_WORKSPACE_TOO_SMALL;
   if (half > 0 && !ws) return MOE_ERR_INVALID_ARG;
   if ((st = check_device()) != MOE_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   moe_bf16* du_hi = static_cast<moe_bf16*>(ws);
   moe_bf16* du_lo = reinterpret_cast<moe_bf16*>(static_cast<uint8_t*>(ws) + half);
+  float* dw_part = dw_route ? reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + 2 * half) : nullptr;
   // P = w*A (or A): its high half is a_save, its low half is in saved
   const void* p_hi = a_save;
   const void* p_lo = saved;
@@ -464,8 +488,12 @@ moe_status_t moe_grouped_bwd(const moe_bf16* dy, const moe_bf16* xp, const moe_b
     GemmArgs wsrc = src;
     wsrc.row_src = sorted_src;
     wsrc.row_weight = weights;
-    st = run_down_dgrad_swiglu(wsrc, cap, E, d, h, dy, saved, w_down, du_hi, du_lo, s);
+    st = run_down_dgrad_swiglu(wsrc, cap, E, d, h, dy, saved, w_down, du_hi, du_lo, dw_part, s);
     if (st != MOE_OK) return st;
+    if (dw_route) {
+      st = launch_routing_weight_grad(dw_part, route_grad_parts(h), inv_map, cap, dw_route, s);
+      if (st != MOE_OK) return st;
+    }
     st = run_up_dgrad(src, cap, E, d, h, du_hi, w_ug, dxp, s);
     if (st != MOE_OK) return st;
   }

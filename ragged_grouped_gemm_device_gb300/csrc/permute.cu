@@ -110,6 +110,21 @@ __global__ void __launch_bounds__(THREADS) combine_kernel(const uint4* __restric
   }
 }
 
+// Routing-weight gradient of the combine: dw[s] = <dOut[t], y_unweighted[inv[s]]>, assembled
+// from the per-row partial sums the dgrad epilogue left (summed in index order, so the result
+// does not depend on scheduling); 0 for a dropped slot.
+__global__ void __launch_bounds__(THREADS) routing_weight_grad_kernel(
+    const float* __restrict__ part, int np, const int32_t* __restrict__ inv, int n_slots,
+    float* __restrict__ dw) {
+  for (int sl = blockIdx.x * THREADS + threadIdx.x; sl < n_slots; sl += gridDim.x * THREADS) {
+    const int p = __ldg(inv + sl);
+    float acc = 0.f;
+    if (p >= 0)
+      for (int i = 0; i < np; ++i) acc += __ldg(part + static_cast<size_t>(p) * np + i);
+    dw[sl] = acc;
+  }
+}
+
 // Capacity-padded layout (Fig. 35 of "Section 09: Grouped GEMM"): dst[e*C + i] = src row
 // offs[e-1] + i for i < min(M_e, C), zero rows for M_e <= i < C.
 __global__ void __launch_bounds__(THREADS) pad_rows_kernel(const uint4* __restrict__ src,
@@ -200,6 +215,15 @@ moe_status_t launch_combine(const void* y, const int32_t* inv_map, const float* 
   if (T == 0) return MOE_OK;
   combine_kernel<<<grid_for_rows(combine_kernel, T), THREADS, 0, s>>>(
       static_cast<const uint4*>(y), inv_map, weights, T, k, d / 8, static_cast<uint4*>(out));
+  return last_launch();
+}
+
+moe_status_t launch_routing_weight_grad(const float* part, int np, const int32_t* inv_map,
+                                        int n_slots, float* dw, cudaStream_t s) {
+  if (n_slots == 0) return MOE_OK;
+  const int grid = static_cast<int>(std::min<long long>((n_slots + THREADS - 1) / THREADS,
+                                                        4LL * device_sm_count()));
+  routing_weight_grad_kernel<<<grid, THREADS, 0, s>>>(part, np, inv_map, n_slots, dw);
   return last_launch();
 }
 

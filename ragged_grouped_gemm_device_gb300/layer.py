@@ -45,6 +45,7 @@ class ExpertLayer:
         self.dx = torch.empty(T, d, dtype=bf, device=dev)
         self.dw_ug = torch.empty(E, 2 * h, d, dtype=torch.float32, device=dev)
         self.dw_down = torch.empty(E, h, d, dtype=torch.float32, device=dev)
+        self.dw_route = torch.empty(T, k, dtype=torch.float32, device=dev)
         bw = _lib.moe_workspace_bytes(_lib.OP_BWD, T, k, E, d, h)
         self.bwd_ws = torch.empty(max(bw, 1), dtype=torch.uint8, device=dev)
         self._key = (T, k)
@@ -65,12 +66,13 @@ class ExpertLayer:
         return self.out
 
     def backward(self, dout: torch.Tensor, stream=None):
-        """dout [T, d] bf16 -> (dx [T, d] bf16, dW_ug [E, 2h, d] fp32, dW_down [E, h, d] fp32)."""
+        """dout [T, d] bf16 -> (dx [T, d] bf16, dW_ug [E, 2h, d] fp32, dW_down [E, h, d] fp32,
+        d_weights [T, k] fp32: the gradient of the routing weights, 0 for dropped slots)."""
         T, k, E, d, h, n = self.T, self.k, self.E, self.d, self.h, self.T * self.k
         _lib.moe_permute(dout, self.sorted_src, self.offsets, None, T, k, E, d, self.dy, stream)
         _lib.moe_grouped_bwd(self.dy, self.xp, self.a, self.saved, self.offsets, self.sorted_src, self.weights,
                              E, n, d, h, self.w_ug,
                              self.w_down, self.dxp, self.dw_ug, self.dw_down, self.bwd_ws, self.status,
-                             stream)
+                             stream, inv_map=self.inv_map, dw_route=self.dw_route)
         _lib.moe_unpermute_combine(self.dxp, self.inv_map, None, T, k, d, self.dx, stream)
-        return self.dx, self.dw_ug, self.dw_down
+        return self.dx, self.dw_ug, self.dw_down, self.dw_route

@@ -22,7 +22,7 @@ def test_header_functions_all_exported(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert lib.moe_abi_version() == 1
+    assert lib.moe_abi_version() == 2
     for code in _lib.STATUS:
         assert lib.moe_status_string(code)
     assert b"unknown" in lib.moe_status_string(99)
@@ -32,8 +32,11 @@ def test_workspace_sizes_are_host_arithmetic(lib):
     # route: one int32 per (warp chunk of 256 slots, expert), rounded to 256 bytes
     assert _lib.moe_workspace_bytes(_lib.OP_ROUTE, 16384, 8, 256) == (16384 * 8 // 256) * 256 * 4
     assert _lib.moe_workspace_bytes(_lib.OP_FWD, 16384, 8, 256, 2048, 512) == 0
-    # backward: dU high and low halves, [n, 2h] bf16 each
-    assert _lib.moe_workspace_bytes(_lib.OP_BWD, 16384, 8, 256, 2048, 512) == 2 * 16384 * 8 * 1024 * 2
+    # backward: dU high and low halves, [n, 2h] bf16 each, then the routing-gradient partials,
+    # [n, 2 ceil(h/256)] fp32
+    assert _lib.moe_workspace_bytes(_lib.OP_BWD, 16384, 8, 256, 2048, 512) == \
+        2 * 16384 * 8 * 1024 * 2 + 16384 * 8 * 4 * 4
+    assert _lib.routing_grad_parts(512) == 4 and _lib.routing_grad_parts(1000) == 8
     # saved state: the low bf16 half of P [n, h], then fp32 U in 2 KB blocks (32 rows x 16
     # columns) for each of at most (n + 127 E) / 128 row tiles, 4 lane quadrants and 2 ceil(h/16)
     # column chunks
@@ -65,8 +68,20 @@ def test_invalid_arguments_rejected_before_any_cuda_call(lib):
     assert fwd(p, p, None, None, 4, -1, 64, 128, p, p, p, p, None, None, 0, None, None) == INVALID
     assert fwd(p, p, None, p, 4, 10, 64, 128, p, p, p, p, None, None, 0, None, None) == INVALID  # weights w/o src
     bwd = lib.moe_grouped_bwd
-    assert bwd(p, p, p, p, p, None, None, 4, 10, 64, 128, p, p, p, p, p, p, 0, None, None) == WS
-    assert bwd(p, p, p, None, p, None, None, 4, 10, 64, 128, p, p, p, p, p, p, 1 << 20, None, None) == INVALID
+    assert bwd(p, p, p, p, p, None, None, 4, 10, 64, 128, p, p, p, p, p, None, None, p, 0, None, None) == WS
+    assert bwd(p, p, p, None, p, None, None, 4, 10, 64, 128, p, p, p, p, p, None, None, p, 1 << 20, None,
+               None) == INVALID
+    # dw_route without inv_map; a workspace large enough for dU but not for the partials
+    assert bwd(p, p, p, p, p, None, None, 4, 10, 64, 128, p, p, p, p, p, None, p, p, 1 << 20, None,
+               None) == INVALID
+    need = _lib.moe_workspace_bytes(_lib.OP_BWD, 10, 1, 4, 64, 128)
+    assert bwd(p, p, p, p, p, None, None, 4, 10, 64, 128, p, p, p, p, p, p, p, p, need - 256, None,
+               None) == WS
+    rwg = lib.moe_routing_weight_grad
+    assert rwg(p, p, 10, 0, 128, p, None) == INVALID                                       # top_k = 0
+    assert rwg(p, p, 10, 40, 128, p, None) == SHAPE                                        # top_k > 32
+    assert rwg(None, p, 10, 2, 128, p, None) == INVALID
+    assert rwg(None, None, 0, 2, 128, None, None) == 0                                     # no slots: no-op
     assert lib.moe_grouped_wgrad(p, None, 12, p, 64, p, 4, 10, p, None, None) == SHAPE        # p_cols % 8
     assert lib.moe_grouped_up_dgrad(p, p, 0, 10, 64, 128, p, p, None, None) == INVALID       # E = 0
     assert lib.moe_unpermute_combine(p, p, None, 10, 40, 64, p, None) == SHAPE            # top_k > 32

@@ -145,14 +145,18 @@ def test_single_kernel_entry_points_equal_composites(lib):
     dxp1 = G.nan_filled((n, d))
     dwu1 = torch.zeros(E, 2 * h, d, device="cuda")
     dwd1 = torch.zeros(E, h, d, device="cuda")
+    dwr1 = torch.full((n,), float("nan"), device="cuda")
     L.moe_grouped_bwd(dy, run.xp, a1, sv1, run.offsets, run.sorted_src, run.weights, E, n, d, h, run.w_ug,
-                      run.w_down, dxp1, dwu1, dwd1, ws, run.status)
+                      run.w_down, dxp1, dwu1, dwd1, ws, run.status, inv_map=run.inv_map, dw_route=dwr1)
     du_hi, du_lo = G.nan_filled((n, 2 * h)), G.nan_filled((n, 2 * h))
     dxp2 = G.nan_filled((n, d))
     dwu2, dwd2, dwu3 = (torch.zeros_like(dwu1), torch.zeros_like(dwd1), torch.zeros_like(dwu1))
     _, p_lo = L.saved_views(sv2, n, h)
+    part = torch.full((n, L.routing_grad_parts(h)), float("nan"), device="cuda")
     L.moe_grouped_down_dgrad_swiglu(dy, sv2, run.offsets, run.sorted_src, run.weights, E, n, d, h, run.w_down,
-                                    du_hi, du_lo, run.status)
+                                    du_hi, du_lo, run.status, dw_part=part)
+    dwr2 = torch.full((n,), float("nan"), device="cuda")
+    L.moe_routing_weight_grad(part, run.inv_map, wl.T, wl.k, h, dwr2)
     L.moe_grouped_up_dgrad(du_hi, run.offsets, E, n, d, h, run.w_ug, dxp2, run.status)
     L.moe_grouped_wgrad(a2, p_lo, h, dy, d, run.offsets, E, n, dwd2, run.status)
     L.moe_grouped_wgrad(du_hi, du_lo, 2 * h, run.xp, d, run.offsets, E, n, dwu2, run.status)
@@ -165,6 +169,7 @@ def test_single_kernel_entry_points_equal_composites(lib):
     # saved compared as bytes: bit for bit, whatever values it holds
     assert torch.equal(sv2.view(torch.uint8), sv1.view(torch.uint8))
     assert torch.equal(dwu2, dwu1) and torch.equal(dwd2, dwd1)
+    assert torch.equal(dwr2, dwr1) and torch.isfinite(dwr1).all()
     err = (dwu3 - dwu1).double().norm() / dwu1.double().norm()
     assert err <= G.REL_NORM_TOL, f"bf16-only wgrad normalised error {err:.2e}"
 

@@ -20,7 +20,8 @@ def _oracle_layer(wl, dout):
     dy = O.permute(dout, r["sorted_src"], r["M"], wl.k, row_scale=wl.weights)
     dxp, dw_ug, dw_down, _ = O.expert_backward(dy, xp, u, r["offsets"], wl.w_ug, wl.w_down)
     dx = O.combine(dxp, r["inv_map"], None, wl.T, wl.k)
-    return out, dx, dw_ug, dw_down
+    dwr = O.routing_weight_grad(dout, y, r["inv_map"], wl.T, wl.k)
+    return out, dx, dw_ug, dw_down, dwr
 
 
 @pytest.mark.parametrize("name", ["toy", "edge", "finegrained"])
@@ -33,10 +34,13 @@ def test_layer_forward_backward(lib, name):
     layer = ExpertLayer(w_ug, w_down)
     doutn = wl.dout()
     out = layer.forward(G.dev_bf16(wl.x()), G.dev_i32(wl.ids), G.dev_f32(wl.weights))
-    dx, dw_ug, dw_down = layer.backward(G.dev_bf16(doutn))
+    dx, dw_ug, dw_down, dwr = layer.backward(G.dev_bf16(doutn))
     torch.cuda.synchronize()
     assert layer.status.item() == 0
-    o_out, o_dx, o_ug, o_dn = _oracle_layer(wl, doutn)
+    o_out, o_dx, o_ug, o_dn, o_dwr = _oracle_layer(wl, doutn)
+    G.assert_close(G.host(dwr), o_dwr, f"d_weights[{name}]")
+    dropped = (wl.ids < 0) | (wl.ids >= wl.E)
+    assert not G.host(dwr)[dropped].any()
     G.assert_close(G.host(out), o_out, f"out[{name}]")
     G.assert_close(G.host(dx), o_dx, f"dx[{name}]")
     nz = np.bincount(wl.ids[(wl.ids >= 0) & (wl.ids < wl.E)], minlength=wl.E) > 0
@@ -53,7 +57,7 @@ def test_large_layer_sampled_tokens(lib):
     layer = ExpertLayer(w_ug, w_down)
     doutn = wl.dout()
     out = layer.forward(G.dev_bf16(wl.x()), G.dev_i32(wl.ids), G.dev_f32(wl.weights))
-    dx, _, _ = layer.backward(G.dev_bf16(doutn))
+    dx, _, _, dwr = layer.backward(G.dev_bf16(doutn))
     torch.cuda.synchronize()
     assert layer.status.item() == 0
     toks = np.sort(np.random.default_rng(3).choice(wl.T, size=48, replace=False))
@@ -62,6 +66,7 @@ def test_large_layer_sampled_tokens(lib):
     xs, ds = wl.x()[toks], doutn[toks]
     sub.x = lambda: xs
     sub.w_ug, sub.w_down = wl.w_ug, wl.w_down
-    o_out, o_dx, _, _ = _oracle_layer(sub, ds)
+    o_out, o_dx, _, _, o_dwr = _oracle_layer(sub, ds)
     G.assert_close(G.host(out)[toks], o_out, "out[large]")
     G.assert_close(G.host(dx)[toks], o_dx, "dx[large]")
+    G.assert_close(G.host(dwr)[toks], o_dwr, "d_weights[large]")
