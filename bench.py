@@ -58,6 +58,22 @@ def dist_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
 
 
+def max_over_ranks(value: float, world: int, device) -> float:
+    """The largest of every rank's `value` (the slowest replica sets the job's time)."""
+    if world <= 1:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(world: int, flops_per_rank: float, ms: float) -> float:
+    """Whole-job throughput of `world` replicas that each did `flops_per_rank` in `ms` (max over
+    ranks): weak scaling, the work grows with the replicas."""
+    return world * flops_per_rank / (ms * 1e-3) / 1e12
+
+
 # ------------------------------------------------------------------------------ CPU oracle timing
 class OracleSampler:
     """Times the oracle as it stands on a bounded sample of the workload: the route (histogram,
@@ -341,11 +357,7 @@ def run_ours(args):
     if world > 1:
         torch.distributed.barrier()
     clk = clocks.stop()
-    elapsed_ms = t_start.elapsed_time(t_end)
-    if world > 1:
-        tt = torch.tensor([elapsed_ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        elapsed_ms = float(tt.item())
+    elapsed_ms = max_over_ranks(t_start.elapsed_time(t_end), world, dev)
     per_call = {}
     for i, (name, _, _) in enumerate(calls):
         per_call[name] = statistics.mean(evs[s][i].elapsed_time(evs[s][i + 1]) for s in range(args.steps))
@@ -354,7 +366,7 @@ def run_ours(args):
     M = int(offsets[-1].item())
     ms_step = elapsed_ms / args.steps
     fwdbwd_flops = 18.0 * M * d * h
-    value = world * fwdbwd_flops / (ms_step * 1e-3) / 1e12
+    value = job_tflops(world, fwdbwd_flops, ms_step)
     peaks, peak_src = load_peaks()
     peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
     peak_hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
@@ -445,10 +457,7 @@ def run_ours(args):
     e2e_ms = e0.elapsed_time(e1) / e_steps
     h2d = x_h.numel() * 2 + dout_h.numel() * 2 + ids_h.numel() * 4 + wts_h.numel() * 4
     d2h = 2 * T * d * 2
-    if world > 1:
-        tt = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
+    e2e_ms = max_over_ranks(e2e_ms, world, dev)
 
     # ---- forward comparison variants (same kernels): padded BMM at ceil(1.25 M/E), host loop
     variants = None
@@ -496,7 +505,7 @@ def run_ours(args):
         "roofline": {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peak_sus,
                      "unit": "TFLOP/s", "frac": achieved / peak_sus, "traffic": traffic,
                      "peak_source": f"bf16_tflops_sustained ({peak_src})"},
-        "e2e": {"value": world * fwdbwd_flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_ms,
+        "e2e": {"value": job_tflops(world, fwdbwd_flops, e2e_ms), "unit": "TFLOP/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
