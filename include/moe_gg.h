@@ -29,9 +29,14 @@
  *    MOE_DEV_TIMEOUT when a bounded wait inside a kernel gave up (the kernel then stops early
  *    instead of hanging), MOE_DEV_BAD_OFFSETS when offsets decrease or exceed the buffer rows
  *    (the affected kernel then computes nothing).
- *  - Limits: 1 <= E <= 1024, 1 <= top_k <= 32, d and h multiples of 8 (16-byte rows for TMA),
- *    T*top_k < 2^31. Other shapes return MOE_ERR_UNSUPPORTED_SHAPE. GEMM operand pointers must
- *    be 16-byte aligned.
+ *  - Limits: 1 <= E <= 1024, 1 <= top_k <= 32, 1 <= d, h <= 2^20, T*top_k < 2^31. The
+ *    grouped kernels read operands by TMA, which needs 16-byte row pitches (d and h multiples
+ *    of 8). moe_permute, moe_unpermute_combine, moe_grouped_swiglu_fwd and moe_grouped_bwd also
+ *    take other widths: the row kernels then move one element per lane step, and the two
+ *    composite calls run the same kernels on zero-padded copies of width round_up(w, 8) held
+ *    in their workspace (exact: the padding is zeros) and copy the results back. The single
+ *    grouped-kernel entry points and the comparison variants need multiples of 8. Other
+ *    shapes return MOE_ERR_UNSUPPORTED_SHAPE. Base pointers must be 16-byte aligned.
  */
 #ifndef MOE_GG_H
 #define MOE_GG_H
@@ -141,7 +146,9 @@ moe_status_t moe_permute(const moe_bf16* x, const int32_t* sorted_src, const int
  *             contract over long expert segments without the bf16 rounding of saved
  *             activations dominating the result; the blocked U makes each warp's store (and
  *             the dgrad's load) of it one contiguous 512-byte access.
- *  ws         moe_workspace_bytes(MOE_OP_FWD, ...) bytes (currently 0; may be NULL then).
+ *  ws         moe_workspace_bytes(MOE_OP_FWD, ...) bytes: 0 (ws may be NULL) when d and h are
+ *             multiples of 8, else the zero-padded copies of xp, y, a, W_ug, W_down. With h not
+ *             a multiple of 8, `saved` holds the padded width round_up(h, 8) in place of h.
  */
 moe_status_t moe_grouped_swiglu_fwd(const moe_bf16* xp, const int32_t* offsets,
                                     const int32_t* sorted_src, const float* weights, int E,
@@ -174,7 +181,9 @@ moe_status_t moe_grouped_swiglu_fwd(const moe_bf16* xp, const int32_t* offsets,
  *          U and the fp32 accumulator, and summed over fixed partial slots in index order:
  *          deterministic.
  *  ws      moe_workspace_bytes(MOE_OP_BWD, ...) bytes: dU high and low (2 x [cap, 2h] bf16),
- *          then the routing-gradient partials ([cap, 2 ceil(h/256)] fp32, used with dw_route).
+ *          then the routing-gradient partials ([cap, 2 ceil(h/256)] fp32, used with dw_route);
+ *          for d or h not multiples of 8, first the zero-padded copies of dy, xp, dxp, a, the
+ *          weights and the two gradients, then the above at the padded widths.
  */
 moe_status_t moe_grouped_bwd(const moe_bf16* dy, const moe_bf16* xp, const moe_bf16* a_save,
                              const void* saved, const int32_t* offsets, const int32_t* sorted_src,

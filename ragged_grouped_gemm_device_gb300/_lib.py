@@ -184,10 +184,12 @@ def moe_grouped_wgrad(p_hi, p_lo, p_cols, q, q_cols, offsets, E, cap, dw, dev_st
 
 def saved_views(saved, cap, h):
     """The parts of the forward's `saved` buffer (a contiguous tensor of any dtype, read as bytes):
-    the low half of P = w*A (bf16 [cap, h]; the high half is a_save) at byte 0, then fp32 U in
-    the kernels' blocked layout (a flat fp32 view; see the header for the block order)."""
+    the low half of P = w*A (bf16 [cap, h8]; the high half is a_save) at byte 0, then fp32 U in
+    the kernels' blocked layout (a flat fp32 view; see the header for the block order). h8 = h
+    rounded up to a multiple of 8: widths that are not are stored zero-padded."""
     import torch
     saved = saved.reshape(-1).view(torch.uint8)
+    h = (h + 7) // 8 * 8
     pb = cap * h * 2
     off = (pb + 255) // 256 * 256
     p_lo = saved[:pb].view(torch.bfloat16).view(cap, h)

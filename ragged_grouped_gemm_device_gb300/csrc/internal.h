@@ -112,6 +112,13 @@ moe_status_t launch_combine(const void* y, const int32_t* inv_map, const float* 
                             int k, int d, void* out, cudaStream_t s);
 moe_status_t launch_pad_rows(const void* src, const int32_t* offsets, int E, int C, int cols,
                              void* dst, cudaStream_t s);
+// Pitch change between a narrow row layout (rows in blocks of blk, sub-blocks of sub, `cols`
+// columns) and a wide one (blocks of blk8, sub-blocks of sub8, cols8 columns, zero filled):
+// to_wide packs (writes rows_out wide rows), else unpacks (writes rows_out narrow rows). With
+// offsets, rows at or past M = offsets[E-1] are skipped. bf16 or fp32 elements.
+moe_status_t launch_pitch_repack(const void* src, void* dst, bool fp32, long long rows_out,
+                                int cols, int cols8, int blk, int sub, int blk8, int sub8,
+                                bool to_wide, const int32_t* offsets, int E, cudaStream_t s);
 // dw[s] = sum of the dw_np partials of row inv_map[s] in index order, 0 for a dropped slot.
 moe_status_t launch_routing_weight_grad(const float* part, int np, const int32_t* inv_map,
                                         int n_slots, float* dw, cudaStream_t s);

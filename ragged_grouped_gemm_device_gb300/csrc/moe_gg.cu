@@ -32,6 +32,13 @@ bool dim_ok(int v) { return v > 0 && v % 8 == 0 && v <= (1 << 20); }
 
 bool shape_ok(int E, int d, int h) { return E >= 1 && E <= MAX_E && dim_ok(d) && dim_ok(h); }
 
+// Widths whose bf16 rows are not 16-byte multiples (TMA needs 16-byte row pitches) are run by
+// the composite calls on zero-padded copies of width round8(w); the result is exact (the extra
+// columns and rows are zeros, which add nothing to any sum).
+int round8(int v) { return (v + 7) & ~7; }
+bool any_width_ok(int v) { return v > 0 && v <= (1 << 20); }
+bool odd_pitch(int d, int h) { return d % 8 != 0 || h % 8 != 0; }
+
 long long row_tiles_bound(long long rows, int E) { return (rows + 127) / 128 + E; }
 
 GemmArgs base_args(int E, int cap, int32_t* status) {
@@ -65,6 +72,52 @@ size_t bwd_ws_half(long long rows, int h) { return round256(static_cast<size_t>(
 int route_grad_parts(int h) { return 2 * ((h + 255) / 256); }
 size_t route_grad_part_bytes(long long rows, int h) {
   return round256(static_cast<size_t>(rows) * route_grad_parts(h) * 4);
+}
+size_t bwd_core_bytes(long long rows, int h) { return 2 * bwd_ws_half(rows, h) + route_grad_part_bytes(rows, h); }
+
+// Workspace of the repacked (odd-pitch) composites: each piece rounded to 256 bytes, in order.
+size_t bf16_bytes(long long rows, int cols) { return round256(static_cast<size_t>(rows) * cols * 2); }
+size_t f32_bytes(long long rows, int cols) { return round256(static_cast<size_t>(rows) * cols * 4); }
+size_t fwd_repack_bytes(long long cap, int E, int d, int h) {
+  const int d8 = round8(d), h8 = round8(h);
+  return 2 * bf16_bytes(cap, d8) + bf16_bytes(cap, h8) + bf16_bytes(static_cast<long long>(E) * 2 * h8, d8) +
+         bf16_bytes(static_cast<long long>(E) * h8, d8);
+}
+size_t bwd_repack_bytes(long long cap, int E, int d, int h) {
+  const int d8 = round8(d), h8 = round8(h);
+  return 3 * bf16_bytes(cap, d8) + bf16_bytes(cap, h8) + bf16_bytes(static_cast<long long>(E) * 2 * h8, d8) +
+         bf16_bytes(static_cast<long long>(E) * h8, d8) + f32_bytes(static_cast<long long>(E) * 2 * h8, d8) +
+         f32_bytes(static_cast<long long>(E) * h8, d8) + bwd_core_bytes(cap, h8);
+}
+
+// Takes consecutive 256-byte aligned pieces from a workspace.
+struct Carver {
+  uint8_t* p;
+  void* take(size_t bytes) {
+    void* r = p;
+    p += bytes;
+    return r;
+  }
+};
+
+// Activation rows [cap, w] <-> [cap, w8] (rows below M only); weights [E*blk rows] with their
+// sub-blocks of `sub` rows widened to round8(sub) rows.
+moe_status_t pack_rows(const void* src, void* dst, long long cap, int w, const int32_t* offsets, int E,
+                       cudaStream_t s) {
+  const int c = static_cast<int>(cap);
+  return launch_pitch_repack(src, dst, false, cap, w, round8(w), c, c, c, c, true, offsets, E, s);
+}
+moe_status_t unpack_rows(const void* src, void* dst, long long cap, int w, const int32_t* offsets, int E,
+                         cudaStream_t s) {
+  const int c = static_cast<int>(cap);
+  return launch_pitch_repack(src, dst, false, cap, w, round8(w), c, c, c, c, false, offsets, E, s);
+}
+moe_status_t repack_weight(const void* src, void* dst, bool fp32, int E, int nsub, int sub, int cols,
+                           bool to_wide, cudaStream_t s) {
+  const int sub8 = round8(sub);
+  const long long rows = static_cast<long long>(E) * nsub * (to_wide ? sub8 : sub);
+  return launch_pitch_repack(src, dst, fp32, rows, cols, round8(cols), nsub * sub, sub, nsub * sub8, sub8,
+                             to_wide, nullptr, E, s);
 }
 
 // ---- one launch per step; `src` carries the problem source (device offsets, uniform rows or
@@ -180,6 +233,13 @@ moe_status_t check_grouped_common(int E, int cap, int d, int h) {
   return MOE_OK;
 }
 
+// The composite calls: any width (odd pitches go through zero-padded copies)
+moe_status_t check_grouped_any_width(int E, int cap, int d, int h) {
+  if (cap < 0 || d <= 0 || h <= 0 || E < 1) return MOE_ERR_INVALID_ARG;
+  if (E > MAX_E || !any_width_ok(d) || !any_width_ok(h)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  return MOE_OK;
+}
+
 }  // namespace
 
 moe_status_t cuda_fail(cudaError_t err) {
@@ -266,9 +326,13 @@ size_t moe_workspace_bytes(int op, int T, int top_k, int E, int d, int h, int ca
   const long long n = static_cast<long long>(T) * top_k;
   switch (op) {
     case MOE_OP_ROUTE: return route_workspace_bytes(n, E);
-    case MOE_OP_FWD: return 0;
-    case MOE_OP_BWD: return h > 0 ? 2 * bwd_ws_half(n, h) + route_grad_part_bytes(n, h) : 0;
-    case MOE_OP_SAVED: return h > 0 ? saved_bytes(n, h, E) : 0;
+    case MOE_OP_FWD:
+      if (!any_width_ok(d) || !any_width_ok(h)) return 0;
+      return odd_pitch(d, h) ? fwd_repack_bytes(n, E, d, h) : 0;
+    case MOE_OP_BWD:
+      if (!any_width_ok(d) || !any_width_ok(h)) return 0;
+      return odd_pitch(d, h) ? bwd_repack_bytes(n, E, d, h) : bwd_core_bytes(n, h);
+    case MOE_OP_SAVED: return any_width_ok(h) ? saved_bytes(n, round8(h), E) : 0;
     case MOE_OP_PADDED_BMM: {
       if (capacity_C <= 0 || d <= 0 || h <= 0) return 0;
       const size_t rows = static_cast<size_t>(E) * capacity_C;
@@ -301,7 +365,7 @@ moe_status_t moe_permute(const moe_bf16* x, const int32_t* sorted_src, const int
                          const float* row_scale, int T, int top_k, int E, int d, moe_bf16* xp,
                          moe_stream_t stream) {
   if (T < 0 || top_k < 1 || d <= 0) return MOE_ERR_INVALID_ARG;
-  if (top_k > MAX_TOPK || E < 1 || E > MAX_E || d % 8 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (top_k > MAX_TOPK || E < 1 || E > MAX_E || !any_width_ok(d)) return MOE_ERR_UNSUPPORTED_SHAPE;
   const long long n = static_cast<long long>(T) * top_k;
   if (n >= (1LL << 31)) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (!offsets) return MOE_ERR_INVALID_ARG;
@@ -316,7 +380,7 @@ moe_status_t moe_permute(const moe_bf16* x, const int32_t* sorted_src, const int
 moe_status_t moe_unpermute_combine(const moe_bf16* y, const int32_t* inv_map, const float* weights,
                                    int T, int top_k, int d, moe_bf16* out, moe_stream_t stream) {
   if (T < 0 || top_k < 1 || d <= 0) return MOE_ERR_INVALID_ARG;
-  if (top_k > MAX_TOPK || d % 8 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (top_k > MAX_TOPK || !any_width_ok(d)) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (static_cast<long long>(T) * top_k >= (1LL << 31)) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (T > 0 && (!y || !inv_map || !out)) return MOE_ERR_INVALID_ARG;
   if (!aligned16(y) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
@@ -431,15 +495,15 @@ moe_status_t moe_grouped_swiglu_fwd(const moe_bf16* xp, const int32_t* offsets,
                                     const moe_bf16* w_down, moe_bf16* y, moe_bf16* a_save,
                                     void* saved, void* ws, size_t ws_bytes, int32_t* dev_status,
                                     moe_stream_t stream) {
-  (void)ws;
-  (void)ws_bytes;
-  moe_status_t st = check_grouped_common(E, cap, d, h);
+  moe_status_t st = check_grouped_any_width(E, cap, d, h);
   if (st != MOE_OK) return st;
   if (!xp || !offsets || !w_ug || !w_down || !y || !a_save || (weights && !sorted_src))
     return MOE_ERR_INVALID_ARG;
   if (!aligned16(xp) || !aligned16(w_ug) || !aligned16(w_down) || !aligned16(y) ||
-      !aligned16(a_save) || !aligned16(saved))
+      !aligned16(a_save) || !aligned16(saved) || !aligned16(ws))
     return MOE_ERR_INVALID_ARG;
+  const bool odd = odd_pitch(d, h);
+  if (odd && ws_bytes < fwd_repack_bytes(cap, E, d, h)) return MOE_ERR_WORKSPACE_TOO_SMALL;
   if ((st = check_device()) != MOE_OK || cap == 0) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   GemmArgs src = base_args(E, cap, dev_status);
@@ -447,35 +511,43 @@ moe_status_t moe_grouped_swiglu_fwd(const moe_bf16* xp, const int32_t* offsets,
   src.row_src = sorted_src;
   src.row_weight = weights;
   const long long tb = row_tiles_bound(cap, E);
-  st = run_up_swiglu(src, cap, tb, E, d, h, xp, w_ug, a_save, saved, s);
-  if (st != MOE_OK) return st;
   GemmArgs dsrc = base_args(E, cap, dev_status);  // the weight is already in a_save
   dsrc.offsets = offsets;
-  return run_down(dsrc, cap, tb, E, d, h, a_save, w_down, y, s);
+  if (!odd) {
+    st = run_up_swiglu(src, cap, tb, E, d, h, xp, w_ug, a_save, saved, s);
+    if (st != MOE_OK) return st;
+    return run_down(dsrc, cap, tb, E, d, h, a_save, w_down, y, s);
+  }
+  // zero-padded copies of width d8 / h8 (gate and up halves of W_ug widened separately)
+  const int d8 = round8(d), h8 = round8(h);
+  Carver cv{static_cast<uint8_t*>(ws)};
+  void* xp8 = cv.take(bf16_bytes(cap, d8));
+  void* y8 = cv.take(bf16_bytes(cap, d8));
+  void* a8 = cv.take(bf16_bytes(cap, h8));
+  void* wug8 = cv.take(bf16_bytes(static_cast<long long>(E) * 2 * h8, d8));
+  void* wdn8 = cv.take(bf16_bytes(static_cast<long long>(E) * h8, d8));
+  if ((st = pack_rows(xp, xp8, cap, d, offsets, E, s)) != MOE_OK) return st;
+  if ((st = repack_weight(w_ug, wug8, false, E, 2, h, d, true, s)) != MOE_OK) return st;
+  if ((st = repack_weight(w_down, wdn8, false, E, 1, h, d, true, s)) != MOE_OK) return st;
+  if ((st = run_up_swiglu(src, cap, tb, E, d8, h8, xp8, wug8, a8, saved, s)) != MOE_OK) return st;
+  if ((st = run_down(dsrc, cap, tb, E, d8, h8, a8, wdn8, y8, s)) != MOE_OK) return st;
+  if ((st = unpack_rows(y8, y, cap, d, offsets, E, s)) != MOE_OK) return st;
+  return unpack_rows(a8, a_save, cap, h, offsets, E, s);
 }
 
-moe_status_t moe_grouped_bwd(const moe_bf16* dy, const moe_bf16* xp, const moe_bf16* a_save,
-                             const void* saved, const int32_t* offsets, const int32_t* sorted_src,
-                             const float* weights, int E, int cap, int d, int h,
-                             const moe_bf16* w_ug, const moe_bf16* w_down, moe_bf16* dxp,
-                             float* dw_ug, float* dw_down, const int32_t* inv_map,
-                             float* dw_route, void* ws, size_t ws_bytes, int32_t* dev_status,
-                             moe_stream_t stream) {
-  moe_status_t st = check_grouped_common(E, cap, d, h);
-  if (st != MOE_OK) return st;
-  if (!dy || !xp || !a_save || !saved || !offsets || !w_ug || !w_down || !dxp || !dw_ug ||
-      !dw_down || (weights && !sorted_src) || (dw_route && !inv_map))
-    return MOE_ERR_INVALID_ARG;
-  if (!aligned16(dy) || !aligned16(xp) || !aligned16(a_save) || !aligned16(saved) ||
-      !aligned16(w_ug) || !aligned16(w_down) || !aligned16(dxp) || !aligned16(dw_ug) ||
-      !aligned16(dw_down) || !aligned16(ws))
-    return MOE_ERR_INVALID_ARG;
+}  // extern "C"
+
+namespace moe {
+namespace {
+
+// The backward on 16-byte row pitches (d, h multiples of 8). ws: dU high and low halves, then
+// the routing-gradient partials (used with dw_route).
+moe_status_t grouped_bwd_core(const void* dy, const void* xp, const void* a_save, const void* saved,
+                              const int32_t* offsets, const int32_t* sorted_src, const float* weights,
+                              int E, int cap, int d, int h, const void* w_ug, const void* w_down,
+                              void* dxp, float* dw_ug, float* dw_down, const int32_t* inv_map,
+                              float* dw_route, void* ws, int32_t* dev_status, cudaStream_t s) {
   const size_t half = bwd_ws_half(cap, h);
-  if (ws_bytes < 2 * half + (dw_route ? route_grad_part_bytes(cap, h) : 0))
-    return MOE_ERR_WORKSPACE_TOO_SMALL;
-  if (half > 0 && !ws) return MOE_ERR_INVALID_ARG;
-  if ((st = check_device()) != MOE_OK) return st;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   moe_bf16* du_hi = static_cast<moe_bf16*>(ws);
   moe_bf16* du_lo = reinterpret_cast<moe_bf16*>(static_cast<uint8_t*>(ws) + half);
   float* dw_part = dw_route ? reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + 2 * half) : nullptr;
@@ -484,6 +556,7 @@ moe_status_t moe_grouped_bwd(const moe_bf16* dy, const moe_bf16* xp, const moe_b
   const void* p_lo = saved;
   GemmArgs src = base_args(E, cap, dev_status);
   src.offsets = offsets;
+  moe_status_t st = MOE_OK;
   if (cap > 0) {
     GemmArgs wsrc = src;
     wsrc.row_src = sorted_src;
@@ -502,6 +575,63 @@ moe_status_t moe_grouped_bwd(const moe_bf16* dy, const moe_bf16* xp, const moe_b
   if (st != MOE_OK) return st;
   return run_wgrad(src, cap, E, cap > 0 ? du_hi : a_save, cap > 0 ? du_lo : a_save, 2 * h, xp, d,
                    dw_ug, s);
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" {
+
+moe_status_t moe_grouped_bwd(const moe_bf16* dy, const moe_bf16* xp, const moe_bf16* a_save,
+                             const void* saved, const int32_t* offsets, const int32_t* sorted_src,
+                             const float* weights, int E, int cap, int d, int h,
+                             const moe_bf16* w_ug, const moe_bf16* w_down, moe_bf16* dxp,
+                             float* dw_ug, float* dw_down, const int32_t* inv_map,
+                             float* dw_route, void* ws, size_t ws_bytes, int32_t* dev_status,
+                             moe_stream_t stream) {
+  moe_status_t st = check_grouped_any_width(E, cap, d, h);
+  if (st != MOE_OK) return st;
+  if (!dy || !xp || !a_save || !saved || !offsets || !w_ug || !w_down || !dxp || !dw_ug ||
+      !dw_down || (weights && !sorted_src) || (dw_route && !inv_map))
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(dy) || !aligned16(xp) || !aligned16(a_save) || !aligned16(saved) ||
+      !aligned16(w_ug) || !aligned16(w_down) || !aligned16(dxp) || !aligned16(dw_ug) ||
+      !aligned16(dw_down) || !aligned16(ws))
+    return MOE_ERR_INVALID_ARG;
+  const bool odd = odd_pitch(d, h);
+  const size_t need = odd ? bwd_repack_bytes(cap, E, d, h)
+                          : 2 * bwd_ws_half(cap, h) + (dw_route ? route_grad_part_bytes(cap, h) : 0);
+  if (ws_bytes < need) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  if (need > 0 && !ws) return MOE_ERR_INVALID_ARG;
+  if ((st = check_device()) != MOE_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (!odd)
+    return grouped_bwd_core(dy, xp, a_save, saved, offsets, sorted_src, weights, E, cap, d, h, w_ug,
+                            w_down, dxp, dw_ug, dw_down, inv_map, dw_route, ws, dev_status, s);
+  // zero-padded copies of width d8 / h8; the gradients come back to the caller's widths
+  const int d8 = round8(d), h8 = round8(h);
+  Carver cv{static_cast<uint8_t*>(ws)};
+  void* dy8 = cv.take(bf16_bytes(cap, d8));
+  void* xp8 = cv.take(bf16_bytes(cap, d8));
+  void* dxp8 = cv.take(bf16_bytes(cap, d8));
+  void* a8 = cv.take(bf16_bytes(cap, h8));
+  void* wug8 = cv.take(bf16_bytes(static_cast<long long>(E) * 2 * h8, d8));
+  void* wdn8 = cv.take(bf16_bytes(static_cast<long long>(E) * h8, d8));
+  float* dwug8 = static_cast<float*>(cv.take(f32_bytes(static_cast<long long>(E) * 2 * h8, d8)));
+  float* dwdn8 = static_cast<float*>(cv.take(f32_bytes(static_cast<long long>(E) * h8, d8)));
+  void* core_ws = cv.take(bwd_core_bytes(cap, h8));
+  (void)core_ws;
+  if ((st = pack_rows(dy, dy8, cap, d, offsets, E, s)) != MOE_OK) return st;
+  if ((st = pack_rows(xp, xp8, cap, d, offsets, E, s)) != MOE_OK) return st;
+  if ((st = pack_rows(a_save, a8, cap, h, offsets, E, s)) != MOE_OK) return st;
+  if ((st = repack_weight(w_ug, wug8, false, E, 2, h, d, true, s)) != MOE_OK) return st;
+  if ((st = repack_weight(w_down, wdn8, false, E, 1, h, d, true, s)) != MOE_OK) return st;
+  st = grouped_bwd_core(dy8, xp8, a8, saved, offsets, sorted_src, weights, E, cap, d8, h8, wug8, wdn8,
+                        dxp8, dwug8, dwdn8, inv_map, dw_route, core_ws, dev_status, s);
+  if (st != MOE_OK) return st;
+  if ((st = unpack_rows(dxp8, dxp, cap, d, offsets, E, s)) != MOE_OK) return st;
+  if ((st = repack_weight(dwug8, dw_ug, true, E, 2, h, d, false, s)) != MOE_OK) return st;
+  return repack_weight(dwdn8, dw_down, true, E, 1, h, d, false, s);
 }
 
 moe_status_t moe_padded_bmm_swiglu_fwd(const moe_bf16* xp, const int32_t* offsets, int E, int cap,

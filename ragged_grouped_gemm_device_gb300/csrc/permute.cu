@@ -125,6 +125,82 @@ __global__ void __launch_bounds__(THREADS) routing_weight_grad_kernel(
   }
 }
 
+// ---- rows whose pitch is not a multiple of 16 bytes (d % 8 != 0): one bf16 per lane step,
+// the same arithmetic as the vector kernels above (scale and rounding, fp32 sums in slot order)
+__global__ void __launch_bounds__(THREADS) permute_scalar_kernel(
+    const bf16* __restrict__ x, const int32_t* __restrict__ sorted_src,
+    const int32_t* __restrict__ offsets, const float* __restrict__ row_scale, int n, int k, int E,
+    int d, bf16* __restrict__ xp) {
+  const int M = min(__ldg(offsets + E - 1), n);
+  const int lane = threadIdx.x & 31;
+  const int gw = blockIdx.x * WARPS + (threadIdx.x >> 5);
+  const int nw = gridDim.x * WARPS;
+  for (int p = gw; p < M; p += nw) {
+    const int src = __ldg(sorted_src + p);
+    if (src < 0 || src >= n) continue;
+    const bf16* xr = x + static_cast<size_t>(src / k) * d;
+    bf16* orow = xp + static_cast<size_t>(p) * d;
+    const float s = (row_scale != nullptr) ? __ldg(row_scale + src) : 1.0f;
+    for (int c = lane; c < d; c += 32)
+      orow[c] = row_scale ? __float2bfloat16_rn(__bfloat162float(xr[c]) * s) : xr[c];
+  }
+}
+
+__global__ void __launch_bounds__(THREADS) combine_scalar_kernel(const bf16* __restrict__ y,
+                                                                 const int32_t* __restrict__ inv,
+                                                                 const float* __restrict__ weights,
+                                                                 int T, int k, int d,
+                                                                 bf16* __restrict__ out) {
+  const int lane = threadIdx.x & 31;
+  const int gw = blockIdx.x * WARPS + (threadIdx.x >> 5);
+  const int nw = gridDim.x * WARPS;
+  for (int t = gw; t < T; t += nw) {
+    for (int c = lane; c < d; c += 32) {
+      float acc = 0.f;
+      for (int j = 0; j < k; ++j) {
+        const int p = __ldg(inv + static_cast<size_t>(t) * k + j);
+        if (p < 0) continue;
+        const float wj = weights ? __ldg(weights + static_cast<size_t>(t) * k + j) : 1.0f;
+        acc = fmaf(wj, __bfloat162float(y[static_cast<size_t>(p) * d + c]), acc);
+      }
+      out[static_cast<size_t>(t) * d + c] = __float2bfloat16_rn(acc);
+    }
+  }
+}
+
+// Pitch change with a row remap, for shapes whose rows are not 16-byte multiples: the narrow
+// layout has rows in blocks of `blk`, split into sub-blocks of `sub` rows; the wide layout has
+// blocks of `blk8` rows and sub-blocks of `sub8` >= sub rows (the extra rows and the columns
+// past `cols` are zero). Wide row r8 = b*blk8 + s*sub8 + j holds narrow row b*blk + s*sub + j
+// when j < sub. to_wide: write every wide row (zero fill); else write every narrow row. With
+// `offsets`, only rows below M = offsets[E-1] are written (one block: the activation rows).
+template <typename Elem>
+__global__ void __launch_bounds__(THREADS) pitch_repack_kernel(
+    const Elem* __restrict__ src, Elem* __restrict__ dst, long long rows_out, int cols, int cols8,
+    int blk, int sub, int blk8, int sub8, bool to_wide, const int32_t* __restrict__ offsets,
+    int E) {
+  const long long lim = offsets ? min(rows_out, static_cast<long long>(__ldg(offsets + E - 1))) : rows_out;
+  const int lane = threadIdx.x & 31;
+  const long long gw = static_cast<long long>(blockIdx.x) * WARPS + (threadIdx.x >> 5);
+  const long long nw = static_cast<long long>(gridDim.x) * WARPS;
+  for (long long r = gw; r < lim; r += nw) {
+    if (to_wide) {
+      const long long b = r / blk8;
+      const int i = static_cast<int>(r - b * blk8), sb = i / sub8, j = i - sb * sub8;
+      const bool has = j < sub;
+      const Elem* srow = src + (b * blk + static_cast<long long>(sb) * sub + j) * cols;
+      Elem* drow = dst + r * cols8;
+      for (int c = lane; c < cols8; c += 32) drow[c] = (has && c < cols) ? srow[c] : Elem(0.0f);
+    } else {
+      const long long b = r / blk;
+      const int i = static_cast<int>(r - b * blk), sb = i / sub, j = i - sb * sub;
+      const Elem* srow = src + (b * blk8 + static_cast<long long>(sb) * sub8 + j) * cols8;
+      Elem* drow = dst + r * cols;
+      for (int c = lane; c < cols; c += 32) drow[c] = srow[c];
+    }
+  }
+}
+
 // Capacity-padded layout (Fig. 35 of "Section 09: Grouped GEMM"): dst[e*C + i] = src row
 // offs[e-1] + i for i < min(M_e, C), zero rows for M_e <= i < C.
 __global__ void __launch_bounds__(THREADS) pad_rows_kernel(const uint4* __restrict__ src,
@@ -204,6 +280,11 @@ moe_status_t launch_permute(const void* x, const int32_t* sorted_src, const int3
                             const float* row_scale, int n, int k, int E, int d, void* xp,
                             cudaStream_t s) {
   if (n == 0) return MOE_OK;
+  if (d % 8 != 0) {
+    permute_scalar_kernel<<<grid_for_rows(permute_scalar_kernel, n), THREADS, 0, s>>>(
+        static_cast<const bf16*>(x), sorted_src, offsets, row_scale, n, k, E, d, static_cast<bf16*>(xp));
+    return last_launch();
+  }
   permute_kernel<<<grid_for_rows(permute_kernel, n), THREADS, 0, s>>>(
       static_cast<const uint4*>(x), sorted_src, offsets, row_scale, n, k, E, d / 8,
       static_cast<uint4*>(xp));
@@ -213,8 +294,29 @@ moe_status_t launch_permute(const void* x, const int32_t* sorted_src, const int3
 moe_status_t launch_combine(const void* y, const int32_t* inv_map, const float* weights, int T,
                             int k, int d, void* out, cudaStream_t s) {
   if (T == 0) return MOE_OK;
+  if (d % 8 != 0) {
+    combine_scalar_kernel<<<grid_for_rows(combine_scalar_kernel, T), THREADS, 0, s>>>(
+        static_cast<const bf16*>(y), inv_map, weights, T, k, d, static_cast<bf16*>(out));
+    return last_launch();
+  }
   combine_kernel<<<grid_for_rows(combine_kernel, T), THREADS, 0, s>>>(
       static_cast<const uint4*>(y), inv_map, weights, T, k, d / 8, static_cast<uint4*>(out));
+  return last_launch();
+}
+
+moe_status_t launch_pitch_repack(const void* src, void* dst, bool fp32, long long rows_out,
+                                int cols, int cols8, int blk, int sub, int blk8, int sub8,
+                                bool to_wide, const int32_t* offsets, int E, cudaStream_t s) {
+  if (rows_out == 0) return MOE_OK;
+  if (fp32) {
+    pitch_repack_kernel<float><<<grid_for_rows(pitch_repack_kernel<float>, rows_out), THREADS, 0, s>>>(
+        static_cast<const float*>(src), static_cast<float*>(dst), rows_out, cols, cols8, blk, sub, blk8,
+        sub8, to_wide, offsets, E);
+  } else {
+    pitch_repack_kernel<bf16><<<grid_for_rows(pitch_repack_kernel<bf16>, rows_out), THREADS, 0, s>>>(
+        static_cast<const bf16*>(src), static_cast<bf16*>(dst), rows_out, cols, cols8, blk, sub, blk8,
+        sub8, to_wide, offsets, E);
+  }
   return last_launch();
 }
 

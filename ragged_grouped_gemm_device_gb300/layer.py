@@ -46,6 +46,8 @@ class ExpertLayer:
         self.dw_ug = torch.empty(E, 2 * h, d, dtype=torch.float32, device=dev)
         self.dw_down = torch.empty(E, h, d, dtype=torch.float32, device=dev)
         self.dw_route = torch.empty(T, k, dtype=torch.float32, device=dev)
+        fw = _lib.moe_workspace_bytes(_lib.OP_FWD, T, k, E, d, h)
+        self.fwd_ws = torch.empty(fw, dtype=torch.uint8, device=dev) if fw > 0 else None
         bw = _lib.moe_workspace_bytes(_lib.OP_BWD, T, k, E, d, h)
         self.bwd_ws = torch.empty(max(bw, 1), dtype=torch.uint8, device=dev)
         self._key = (T, k)
@@ -61,7 +63,7 @@ class ExpertLayer:
         _lib.moe_permute(x, self.sorted_src, self.offsets, None, T, k, E, d, self.xp, stream)
         # the routing weight is applied in the down projection's epilogue; the combine sums
         _lib.moe_grouped_swiglu_fwd(self.xp, self.offsets, self.sorted_src, weights, E, n, d, h, self.w_ug,
-                                    self.w_down, self.y, self.a, self.saved, None, self.status, stream)
+                                    self.w_down, self.y, self.a, self.saved, self.fwd_ws, self.status, stream)
         _lib.moe_unpermute_combine(self.y, self.inv_map, None, T, k, d, self.out, stream)
         return self.out
 

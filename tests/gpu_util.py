@@ -146,15 +146,20 @@ class GpuRun:
 
     def forward(self):
         wl = self.wl
+        fw = _lib.moe_workspace_bytes(_lib.OP_FWD, wl.T, wl.k, wl.E, wl.d, wl.h)
+        ws = torch.empty(fw, dtype=torch.uint8, device="cuda") if fw > 0 else None
         _lib.moe_grouped_swiglu_fwd(self.xp, self.offsets, None, None, wl.E, self.cap, wl.d, wl.h, self.w_ug,
-                                    self.w_down, self.y, self.a, self.saved, None, self.status)
+                                    self.w_down, self.y, self.a, self.saved, ws, self.status)
         return self
 
     @property
     def u(self):
         """The fp32 U the forward saved, as [M, 2h] rows (unblocked)."""
-        u_flat, _ = _lib.saved_views(self.saved, max(self.cap, 1), self.wl.h)
-        return unblock_u(u_flat, self.offsets.cpu().numpy().astype(np.int64), self.wl.h)
+        h = self.wl.h
+        h8 = (h + 7) // 8 * 8  # widths that are not multiples of 8 are stored zero-padded
+        u_flat, _ = _lib.saved_views(self.saved, max(self.cap, 1), h)
+        u8 = unblock_u(u_flat, self.offsets.cpu().numpy().astype(np.int64), h8)
+        return torch.cat([u8[:, :h], u8[:, h8:h8 + h]], dim=1)
 
     def combine(self):
         wl = self.wl

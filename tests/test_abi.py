@@ -32,6 +32,14 @@ def test_workspace_sizes_are_host_arithmetic(lib):
     # route: one int32 per (warp chunk of 256 slots, expert), rounded to 256 bytes
     assert _lib.moe_workspace_bytes(_lib.OP_ROUTE, 16384, 8, 256) == (16384 * 8 // 256) * 256 * 4
     assert _lib.moe_workspace_bytes(_lib.OP_FWD, 16384, 8, 256, 2048, 512) == 0
+    # odd pitches: zero-padded copies (xp, y [n, d8], a [n, h8], W_ug [E, 2 h8, d8], W_down
+    # [E, h8, d8]), each rounded to 256 bytes
+    r256 = lambda b: (b + 255) // 256 * 256
+    n, E, d8, h8 = 10 * 3, 6, 64, 48
+    assert _lib.moe_workspace_bytes(_lib.OP_FWD, 10, 3, E, 60, 44) == \
+        2 * r256(n * d8 * 2) + r256(n * h8 * 2) + r256(E * 2 * h8 * d8 * 2) + r256(E * h8 * d8 * 2)
+    assert _lib.moe_workspace_bytes(_lib.OP_SAVED, 10, 3, E, 60, 44) == \
+        _lib.moe_workspace_bytes(_lib.OP_SAVED, 10, 3, E, 64, 48)
     # backward: dU high and low halves, [n, 2h] bf16 each, then the routing-gradient partials,
     # [n, 2 ceil(h/256)] fp32
     assert _lib.moe_workspace_bytes(_lib.OP_BWD, 16384, 8, 256, 2048, 512) == \
@@ -60,10 +68,13 @@ def test_invalid_arguments_rejected_before_any_cuda_call(lib):
     assert lib.moe_route_offsets(p, -1, 1, 4, p, p, p, p, p, 1 << 20, None) == INVALID
     assert lib.moe_route_offsets(p, 10, 1, 4, None, p, p, p, p, 1 << 20, None) == INVALID
     assert lib.moe_route_offsets(p, 100000, 8, 256, p, p, p, p, p, 16, None) == WS
-    assert lib.moe_permute(p, p, p, None, 10, 1, 4, 12, p, None) == SHAPE                 # d % 8
+    assert lib.moe_permute(p, p, p, None, 10, 1, 4, (1 << 20) + 8, p, None) == SHAPE      # d too wide
+    assert lib.moe_permute(p, p, p, None, 10, 1, 4, 0, p, None) == INVALID                 # d = 0
     assert lib.moe_permute(ctypes.c_void_p(18), p, p, None, 10, 1, 4, 16, p, None) == INVALID  # misaligned
     fwd = lib.moe_grouped_swiglu_fwd
-    assert fwd(p, p, None, None, 4, 10, 64, 100, p, p, p, p, None, None, 0, None, None) == SHAPE    # h % 8
+    # h % 8 != 0: run on zero-padded copies, which need the forward workspace
+    assert fwd(p, p, None, None, 4, 10, 64, 100, p, p, p, p, None, None, 0, None, None) == WS
+    assert lib.moe_grouped_up_swiglu(p, p, None, None, 4, 10, 64, 100, p, p, None, None, None) == SHAPE
     assert fwd(p, p, None, None, 4, 10, 64, 128, p, p, p, None, None, None, 0, None, None) == INVALID  # a_save
     assert fwd(p, p, None, None, 4, -1, 64, 128, p, p, p, p, None, None, 0, None, None) == INVALID
     assert fwd(p, p, None, p, 4, 10, 64, 128, p, p, p, p, None, None, 0, None, None) == INVALID  # weights w/o src

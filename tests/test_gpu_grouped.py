@@ -28,13 +28,17 @@ FWD_CASES = {
     # offsets and tile prefix at their maximum size, one ragged tile per expert
     "edge_max_experts": lambda: W.custom(T=3000, k=4, E=1024, d=64, h=64, seed=11,
                                          empty_experts=tuple(range(0, 1024, 41))),
+    # widths whose bf16 rows are not 16-byte multiples: zero-padded copies inside the composites
+    "edge_odd_width": lambda: W.custom(T=150, k=3, E=6, d=60, h=44, seed=13, invalid_frac=0.05,
+                                       empty_experts=(1,)),
+    "edge_odd_width2": lambda: W.custom(T=90, k=2, E=5, d=77, h=33, seed=14),
     "balanced": lambda: W.make("balanced"),
     "finegrained": lambda: W.make("finegrained"),
     "skew": lambda: W.make("skew"),
 }
 
 BWD_CASES = ["toy", "edge_small", "edge_wide", "edge_one_expert", "edge_sparse", "edge_max_experts",
-             "finegrained", "skew"]
+             "edge_odd_width", "edge_odd_width2", "finegrained", "skew"]
 
 
 def _dy(wl, M):

@@ -25,6 +25,8 @@ CASES = {
     "all_dropped": lambda: W.custom(T=50, k=2, E=4, d=16, h=8, seed=4, invalid_frac=1.0),
     "one_token": lambda: W.custom(T=1, k=8, E=16, d=16, h=8, seed=5),
     "top32": lambda: W.custom(T=129, k=32, E=40, d=16, h=8, seed=6, invalid_frac=0.05),
+    # rows of 154 bytes: the element-wise gather and combine
+    "odd_width": lambda: W.custom(T=333, k=3, E=7, d=77, h=8, seed=15, invalid_frac=0.05),
 }
 
 
