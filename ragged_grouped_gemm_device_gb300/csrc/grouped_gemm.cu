@@ -568,25 +568,45 @@ __global__ void __launch_bounds__(THREADS, 1)
         const bool rv = r_in < ti.rows;
         const long long row = ti.row0 + r_in;
         bf16* orow = reinterpret_cast<bf16*>(args.out) + row * args.ldo;
-#pragma unroll 1
-        for (int c = half * (BN / 32); c < (half + 1) * (BN / 32); c += 2) {
-          uint32_t v0[16], v1[16];
-          tmem_ld16(tb + c * 16, v0);
-          tmem_ld16(tb + (c + 1) * 16, v1);
-          tmem_ld_wait2(v0, v1);
+        // 32 columns (two 16-column chunks) at a time; the next pair's accumulator columns are
+        // in flight while this pair is converted and stored
+        auto store_pair = [&](int c, const uint32_t (&v0)[16], const uint32_t (&v1)[16]) {
           const int col = ti.n0 + c * 16;
-          if (rv) {
-            uint32_t p[16];
+          if (!rv) return;
+          uint32_t p[16];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              p[j] = pack_bf16x2(__uint_as_float(v0[2 * j]), __uint_as_float(v0[2 * j + 1]));
-              p[8 + j] = pack_bf16x2(__uint_as_float(v1[2 * j]), __uint_as_float(v1[2 * j + 1]));
-            }
-#pragma unroll
-            for (int hq = 0; hq < 4; ++hq)
-              if (col + hq * 8 < args.N)
-                st_global_v4(orow + col + hq * 8, p[4 * hq], p[4 * hq + 1], p[4 * hq + 2], p[4 * hq + 3]);
+          for (int j = 0; j < 8; ++j) {
+            p[j] = pack_bf16x2(__uint_as_float(v0[2 * j]), __uint_as_float(v0[2 * j + 1]));
+            p[8 + j] = pack_bf16x2(__uint_as_float(v1[2 * j]), __uint_as_float(v1[2 * j + 1]));
           }
+          if (args.vec32 && col + 32 <= args.N) {
+            st_global_v8(orow + col, p);
+            st_global_v8(orow + col + 16, p + 8);
+            return;
+          }
+#pragma unroll
+          for (int hq = 0; hq < 4; ++hq)
+            if (col + hq * 8 < args.N)
+              st_global_v4(orow + col + hq * 8, p[4 * hq], p[4 * hq + 1], p[4 * hq + 2], p[4 * hq + 3]);
+        };
+        const int cb = half * (BN / 32), ce = cb + BN / 32;  // four pairs of chunks
+        uint32_t va[16], vb[16], vc[16], vd[16];
+        tmem_ld16(tb + cb * 16, va);
+        tmem_ld16(tb + (cb + 1) * 16, vb);
+        tmem_ld_wait2(va, vb);
+#pragma unroll 1
+        for (int c = cb; c < ce; c += 4) {
+          tmem_ld16(tb + (c + 2) * 16, vc);
+          tmem_ld16(tb + (c + 3) * 16, vd);
+          store_pair(c, va, vb);
+          tmem_ld_wait2(vc, vd);
+          const bool more = c + 4 < ce;
+          if (more) {
+            tmem_ld16(tb + (c + 4) * 16, va);
+            tmem_ld16(tb + (c + 5) * 16, vb);
+          }
+          store_pair(c + 2, vc, vd);
+          if (more) tmem_ld_wait2(va, vb);
         }
       } else if constexpr (MODE == MODE_DGRAD_SWIGLU) {
         const bool rv = r_in < ti.rows;

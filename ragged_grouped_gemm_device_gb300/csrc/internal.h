@@ -59,8 +59,9 @@ struct GemmArgs {
   // First row tile of this problem list in the blocked U: 0 for a whole problem list, the row
   // tiles of the experts before it for one expert (single_expert)
   long long tile_base;
-  // UP_SWIGLU, DGRAD_SWIGLU: 1 when every bf16 row output is 32-byte aligned at each 16-column
-  // chunk (bases 32-byte aligned, h % 16 == 0), so a chunk row is one 32-byte store
+  // 1 when every bf16 row output is 32-byte aligned at each 16-column chunk (bases 32-byte
+  // aligned; h % 16 == 0 for UP_SWIGLU and DGRAD_SWIGLU, N % 16 == 0 for PLAIN_BF16), so a chunk
+  // row is one 32-byte store
   int vec32;
   // DGRAD_SWIGLU, optional: per row p, dw_np fp32 partial sums of <A_p, G_p> (A = SwiGLU(U)
   // unweighted, G = dy W_down^T before the routing weight), one per (column tile, warp half)

@@ -159,6 +159,7 @@ moe_status_t run_down(const GemmArgs& src, long long rows, long long tiles_bound
   a.h = h;
   a.out = y;
   a.ldo = d;
+  a.vec32 = (d % 16 == 0 && aligned32(y)) ? 1 : 0;
   return launch_grouped_gemm(MODE_PLAIN_BF16, ma, ma, mb, a,
                              tiles_bound * gemm_tiles_n(MODE_PLAIN_BF16, d), s);
 }
@@ -202,6 +203,7 @@ moe_status_t run_up_dgrad(const GemmArgs& src, long long rows, int E, int d, int
   a.h = h;
   a.out = dxp;
   a.ldo = d;
+  a.vec32 = (d % 16 == 0 && aligned32(dxp)) ? 1 : 0;
   return launch_grouped_gemm(MODE_PLAIN_BF16, ma, ma, mb, a,
                              row_tiles_bound(rows, src.E) * gemm_tiles_n(MODE_PLAIN_BF16, d), s);
 }
