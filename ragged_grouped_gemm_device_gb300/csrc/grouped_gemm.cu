@@ -524,14 +524,11 @@ __global__ void __launch_bounds__(THREADS, 1)
         // input, P - bf16(P) its low half for the down wgrad
         const float wrow =
             (args.row_weight != nullptr && rv) ? __ldg(args.row_weight + __ldg(args.row_src + row)) : 1.0f;
-#pragma unroll 1
-        for (int c = half * 4; c < half * 4 + 4; ++c) {
-          uint32_t g[16], u[16];
-          tmem_ld16(tb + c * 16, g);
-          tmem_ld16(tb + 128 + c * 16, u);
-          tmem_ld_wait2(g, u);
+        // chunk c's gate and up columns: U (blocked), then bf16(P) and its low half
+        auto process = [&](int c, const uint32_t (&g)[16], const uint32_t (&u)[16]) {
           const int col = ti.n0 + c * 16;
-          if (args.out2 != nullptr && rv && col < h) {
+          if (!rv || col >= h) return;
+          if (args.out2 != nullptr) {
             // U in its blocked layout: 512 contiguous bytes per warp-wide store
             uint32_t* bg = reinterpret_cast<uint32_t*>(u_block(args.out2, G, q, col >> 4, 2 * h16));
             uint32_t* bu = reinterpret_cast<uint32_t*>(u_block(args.out2, G, q, h16 + (col >> 4), 2 * h16));
@@ -541,28 +538,47 @@ __global__ void __launch_bounds__(THREADS, 1)
               st_global_v4(bu + (j * 32 + lane) * 4, u[4 * j], u[4 * j + 1], u[4 * j + 2], u[4 * j + 3]);
             }
           }
-          if (rv && col < h) {
-            uint32_t pa[8], pl[8];
+          uint32_t pa[8], pl[8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const float p0 = wrow * (silu_f(__uint_as_float(g[2 * j])) * __uint_as_float(u[2 * j]));
-              const float p1 = wrow * (silu_f(__uint_as_float(g[2 * j + 1])) * __uint_as_float(u[2 * j + 1]));
-              pa[j] = pack_bf16x2(p0, p1);
-              pl[j] = pack_bf16x2(p0 - bf16_lo(pa[j]), p1 - bf16_hi(pa[j]));
-            }
-            const bool two = col + 16 <= h;
-            if (args.vec32) {
-              st_global_v8(arow + col, pa);
-              if (lrow) st_global_v8(lrow + col, pl);
-            } else {
-              st_global_v4(arow + col, pa[0], pa[1], pa[2], pa[3]);
-              if (two) st_global_v4(arow + col + 8, pa[4], pa[5], pa[6], pa[7]);
-              if (lrow) {
-                st_global_v4(lrow + col, pl[0], pl[1], pl[2], pl[3]);
-                if (two) st_global_v4(lrow + col + 8, pl[4], pl[5], pl[6], pl[7]);
-              }
+          for (int j = 0; j < 8; ++j) {
+            const float p0 = wrow * (silu_f(__uint_as_float(g[2 * j])) * __uint_as_float(u[2 * j]));
+            const float p1 = wrow * (silu_f(__uint_as_float(g[2 * j + 1])) * __uint_as_float(u[2 * j + 1]));
+            pa[j] = pack_bf16x2(p0, p1);
+            pl[j] = pack_bf16x2(p0 - bf16_lo(pa[j]), p1 - bf16_hi(pa[j]));
+          }
+          const bool two = col + 16 <= h;
+          if (args.vec32) {
+            st_global_v8(arow + col, pa);
+            if (lrow) st_global_v8(lrow + col, pl);
+          } else {
+            st_global_v4(arow + col, pa[0], pa[1], pa[2], pa[3]);
+            if (two) st_global_v4(arow + col + 8, pa[4], pa[5], pa[6], pa[7]);
+            if (lrow) {
+              st_global_v4(lrow + col, pl[0], pl[1], pl[2], pl[3]);
+              if (two) st_global_v4(lrow + col + 8, pl[4], pl[5], pl[6], pl[7]);
             }
           }
+        };
+        // four chunks per warp; chunk c+1's accumulator columns are in flight while chunk c is
+        // processed
+        const int cb = half * 4;
+        uint32_t ga[16], ua[16], gb[16], ub[16];
+        tmem_ld16(tb + cb * 16, ga);
+        tmem_ld16(tb + 128 + cb * 16, ua);
+        tmem_ld_wait2(ga, ua);
+#pragma unroll 1
+        for (int c = cb; c < cb + 4; c += 2) {
+          tmem_ld16(tb + (c + 1) * 16, gb);
+          tmem_ld16(tb + 128 + (c + 1) * 16, ub);
+          process(c, ga, ua);
+          tmem_ld_wait2(gb, ub);
+          const bool more = c + 2 < cb + 4;
+          if (more) {
+            tmem_ld16(tb + (c + 2) * 16, ga);
+            tmem_ld16(tb + 128 + (c + 2) * 16, ua);
+          }
+          process(c + 1, gb, ub);
+          if (more) tmem_ld_wait2(ga, ua);
         }
       } else if constexpr (MODE == MODE_PLAIN_BF16) {
         const bool rv = r_in < ti.rows;
