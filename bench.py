@@ -40,7 +40,7 @@ def parse_args():
     p.add_argument("--workload", default="large")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-variants", action="store_true")
-    p.add_argument("--sweep", choices=["capacity", "histogram"], default=None,
+    p.add_argument("--sweep", choices=["capacity", "histogram", "configs"], default=None,
                    help="single-projection studies instead of the step: grouped vs capacity-padded "
                         "BMM over routed-row counts, or throughput vs load imbalance")
     return p.parse_args()
@@ -671,6 +671,69 @@ def run_sweep_histogram(args):
     return 0
 
 
+def run_sweep_configs(args):
+    """Forward of the SwiGLU expert on each named workload: the grouped composite call against
+    the in-library capacity-padded BMM (C = ceil(1.25 M/E), same kernels) and the host-scheduled
+    per-expert loop (wall time, including its count copy and host wait). Grouped and BMM: mean
+    of 20 launches queued in a CUDA graph after 10 warm-ups; loop: mean of 5 calls."""
+    import torch
+    from ragged_grouped_gemm_device_gb300 import _lib as L
+    from ragged_grouped_gemm_device_gb300 import workloads as W
+    dev, bf, i32 = "cuda", torch.bfloat16, torch.int32
+    rows = []
+    for name in ("toy", "balanced", "finegrained", "skew", "large"):
+        wl = W.make(name)
+        T, k, E, d, h, n = wl.T, wl.k, wl.E, wl.d, wl.h, wl.n
+        gen = torch.Generator(device=dev).manual_seed(1)
+        x = torch.randn(T, d, device=dev, generator=gen).to(bf)
+        w_ug = (torch.randn(E, 2 * h, d, device=dev, generator=gen) * d ** -0.5).to(bf)
+        w_down = (torch.randn(E, h, d, device=dev, generator=gen) * h ** -0.5).to(bf)
+        ids = torch.from_numpy(wl.ids).to(dev)
+        counts, offsets = torch.empty(E, dtype=i32, device=dev), torch.empty(E, dtype=i32, device=dev)
+        ss, inv = torch.empty(n, dtype=i32, device=dev), torch.empty(n, dtype=i32, device=dev)
+        rws = torch.empty(max(L.moe_workspace_bytes(L.OP_ROUTE, T, k, E), 1), dtype=torch.uint8, device=dev)
+        xp = torch.empty(n, d, dtype=bf, device=dev)
+        L.moe_route_offsets(ids, T, k, E, counts, offsets, ss, inv, rws)
+        L.moe_permute(x, ss, offsets, None, T, k, E, d, xp)
+        torch.cuda.synchronize()
+        M = int(offsets[-1].item())
+        C = -(-(5 * M) // (4 * E))
+        dropped = int(torch.clamp(counts.long() - C, min=0).sum().item())  # rows the padded BMM drops
+        y = torch.empty(n, d, dtype=bf, device=dev)
+        a = torch.empty(n, h, dtype=bf, device=dev)
+        status = torch.zeros(1, dtype=i32, device=dev)
+        bws = torch.empty(L.moe_workspace_bytes(L.OP_PADDED_BMM, T, k, E, d, h, C), dtype=torch.uint8, device=dev)
+        t_g = queued_mean_ms(lambda: L.moe_grouped_swiglu_fwd(xp, offsets, None, None, E, n, d, h, w_ug, w_down,
+                                                              y, a, None, None, status))
+        t_b = queued_mean_ms(lambda: L.moe_padded_bmm_swiglu_fwd(xp, offsets, E, n, d, h, C, w_ug, w_down, y,
+                                                                 bws, status))
+        loop = lambda: L.moe_loop_swiglu_fwd(xp, offsets, E, n, d, h, w_ug, w_down, y, a, None, status)
+        for _ in range(2):
+            loop()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(5):
+            loop()
+        torch.cuda.synchronize()
+        t_l = (time.perf_counter() - t0) * 1e3 / 5
+        assert status.item() == 0, f"device status {status.item()}"
+        fl = 6.0 * M * d * h
+        row = {"sweep": "configs", "workload": name, "T": T, "top_k": k, "E": E, "d": d, "h": h, "M": M,
+               "C": C, "padded_bmm_dropped_rows": dropped, "grouped_ms": t_g, "padded_bmm_ms": t_b,
+               "host_loop_ms": t_l,
+               "grouped_tflops": fl / t_g / 1e9, "padded_bmm_tflops": fl / t_b / 1e9,
+               "host_loop_tflops": fl / t_l / 1e9, "speedup_vs_bmm": t_b / t_g, "speedup_vs_loop": t_l / t_g}
+        rows.append(row)
+        print(json.dumps(row), flush=True)
+        del x, w_ug, w_down, xp, y, a, bws
+        torch.cuda.empty_cache()
+    print(json.dumps({"sweep": "configs", "summary": True,
+                      "grouped_beats_padded_bmm_everywhere": all(r["speedup_vs_bmm"] > 1 for r in rows),
+                      "grouped_beats_host_loop_everywhere": all(r["speedup_vs_loop"] > 1 for r in rows)}),
+          flush=True)
+    return 0
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
@@ -679,6 +742,8 @@ def main():
         return run_sweep_capacity(args)
     if args.sweep == "histogram":
         return run_sweep_histogram(args)
+    if args.sweep == "configs":
+        return run_sweep_configs(args)
     return run_ours(args)
 
 

@@ -72,3 +72,22 @@ def test_large_layer_sampled_tokens(lib):
     G.assert_close(G.host(out)[toks], o_out, "out[large]")
     G.assert_close(G.host(dx)[toks], o_dx, "dx[large]")
     G.assert_close(G.host(dwr)[toks], o_dwr, "d_weights[large]")
+
+
+def test_layer_is_deterministic(lib):
+    """Stable placement, the atomic-free combine and fixed-slot partial sums make every output of
+    the layer bit-identical from one run to the next."""
+    wl = W.custom(T=700, k=4, E=24, d=256, h=192, seed=23, invalid_frac=0.05, empty_experts=(5,))
+    w_ug, w_down = G.device_weights(wl)
+    x, ids, wts, dout = G.dev_bf16(wl.x()), G.dev_i32(wl.ids), G.dev_f32(wl.weights), G.dev_bf16(wl.dout())
+    runs = []
+    for _ in range(2):
+        layer = ExpertLayer(w_ug, w_down)
+        out = layer.forward(x, ids, wts).clone()
+        grads = [g.clone() for g in layer.backward(dout)]
+        torch.cuda.synchronize()
+        assert layer.status.item() == 0
+        runs.append([out] + grads)
+    for a, b in zip(*runs):
+        assert torch.equal(a.view(torch.uint8) if a.dtype == torch.bfloat16 else a.view(torch.int32),
+                           b.view(torch.uint8) if b.dtype == torch.bfloat16 else b.view(torch.int32))
