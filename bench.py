@@ -40,7 +40,7 @@ def parse_args():
     p.add_argument("--workload", default="large")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-variants", action="store_true")
-    p.add_argument("--sweep", choices=["capacity", "histogram", "configs"], default=None,
+    p.add_argument("--sweep", choices=["capacity", "histogram", "configs", "partition"], default=None,
                    help="single-projection studies instead of the step: grouped vs capacity-padded "
                         "BMM over routed-row counts, or throughput vs load imbalance")
     return p.parse_args()
@@ -734,6 +734,46 @@ def run_sweep_configs(args):
     return 0
 
 
+def run_sweep_partition(args):
+    """Fig. 39 of "Section 09: Grouped GEMM" on one GB300: one dense projection [T, 8192] @
+    [8192, 81920] against its exact split into E = 4 or 8 expert GEMMs (Eq. 17: expert e owns
+    columns [e N/E, (e+1) N/E) of the weight; the grouped input repeats the dense input E
+    times). Same useful FLOPs, weights and outputs; dense = cuBLAS (torch.matmul), grouped = the
+    grouped kernel over the uniform problem list. Mean of 20 launches queued in a CUDA graph."""
+    import torch
+    from ragged_grouped_gemm_device_gb300 import _lib as L
+    dev, bf = "cuda", torch.bfloat16
+    K, N = 8192, 81920
+    gen = torch.Generator(device=dev).manual_seed(3)
+    w = (torch.randn(K, N, device=dev, generator=gen) * K ** -0.5).to(bf)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    rows = []
+    for T in (256, 1024, 4096, 8192, 16384, 32768, 65536):
+        x = torch.randn(T, K, device=dev, generator=gen).to(bf)
+        y = torch.empty(T, N, dtype=bf, device=dev)
+        t_dense = queued_mean_ms(lambda: torch.matmul(x, w, out=y))
+        del y
+        row = {"sweep": "partition", "T": T, "K": K, "N": N, "dense_cublas_ms": t_dense,
+               "dense_cublas_tflops": 2.0 * T * K * N / t_dense / 1e9}
+        for E in (4, 8):
+            wg = w.view(K, E, N // E).permute(1, 0, 2).contiguous()   # [E, K, N/E]
+            xr = x.repeat(E, 1)                                          # expert e owns rows [eT, (e+1)T)
+            yg = torch.empty(E * T, N // E, dtype=bf, device=dev)
+            offs = torch.arange(1, E + 1, dtype=torch.int32, device=dev) * T
+            t_g = queued_mean_ms(lambda: L.moe_grouped_down(xr, offs, E, E * T, N // E, K, wg, yg, status))
+            row[f"grouped_{E}_ms"] = t_g
+            row[f"grouped_{E}_tflops"] = 2.0 * T * K * N / t_g / 1e9
+            row[f"grouped_{E}_vs_dense"] = t_dense / t_g
+            del wg, xr, yg
+        torch.cuda.synchronize()
+        assert status.item() == 0, f"device status {status.item()}"
+        rows.append(row)
+        print(json.dumps(row), flush=True)
+        del x
+        torch.cuda.empty_cache()
+    return 0
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
@@ -744,6 +784,8 @@ def main():
         return run_sweep_histogram(args)
     if args.sweep == "configs":
         return run_sweep_configs(args)
+    if args.sweep == "partition":
+        return run_sweep_partition(args)
     return run_ours(args)
 
 

@@ -52,6 +52,7 @@ constexpr int PRODUCER_B_WARP = 2 + EPI_WARPS;  // second TMA producer (B operan
 constexpr int THREADS = 32 * (PRODUCER_B_WARP + 1);
 constexpr int TMEM_COLS = 512;                // two 256-column accumulators
 constexpr int MAX_E = 1024;
+constexpr int RASTER_M = 16;                  // row tiles per raster group (see decode_tile)
 constexpr int CTL_BYTES = 256;
 // per epilogue warp, one 32-row x 16-column fp32 chunk staged for a TMA store (wgrad), or two
 // 32-row x 16-column bf16 boxes (dgrad)
@@ -141,25 +142,36 @@ __device__ __forceinline__ Tile decode_tile(const Sched& s, int t, int rank) {
     ti.rows = 0;
     ti.g = 0;
   } else {
-    const int g = t / s.nt;
-    const int n = t - g * s.nt;
-    // largest e with pre[e] <= g (experts without tiles have pre[e] == pre[e+1]); pre counts
-    // pairs of 128-row tiles per expert
+    // expert e owns tiles [pre[e]*nt, pre[e+1]*nt): largest e with pre[e] <= t/nt (experts
+    // without tiles have pre[e] == pre[e+1]); pre counts 128-row tiles (pairs with clusters)
+    const int nt = s.nt;
+    const int gq = t / nt;
     int lo = 0, hi = s.E;
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
-      if (s.pre[mid] <= g) lo = mid; else hi = mid;
+      if (s.pre[mid] <= gq) lo = mid; else hi = mid;
     }
     ti.e = lo;
-    ti.g = g;
+    // Inside the expert, groups of up to RASTER_M row tiles are walked column tile by column
+    // tile (row tile fastest): the CTAs in flight then share a few column slices of the weight
+    // and a few row tiles of the input, which stay in L2 even when the expert's weight does not
+    // (a weight of 8192 x 20480 columns would otherwise be re-read for every row tile).
+    const int mt_e = s.pre[lo + 1] - s.pre[lo];
+    const int l = t - s.pre[lo] * nt;
+    const int grp = l / (RASTER_M * nt);
+    const int gm = min(RASTER_M, mt_e - grp * RASTER_M);
+    const int within = l - grp * RASTER_M * nt;
+    const int m_local = grp * RASTER_M + within % gm;
+    const int n = within / gm;
+    ti.g = s.pre[lo] + m_local;
     if constexpr (ModeTraits<MODE>::pair) {
-      const int mloc = 2 * (g - s.pre[lo]) + rank;
+      const int mloc = 2 * m_local + rank;
       const int me = s.offs[lo + 1] - s.offs[lo];
       ti.row0 = s.offs[lo] + mloc * BM;
       ti.rows = min(BM, me - mloc * BM);
       ti.active = mloc * BM < me;
     } else {
-      ti.row0 = s.offs[lo] + (g - s.pre[lo]) * BM;
+      ti.row0 = s.offs[lo] + m_local * BM;
       ti.rows = min(BM, s.offs[lo + 1] - ti.row0);
     }
     ti.n0 = n * ModeTraits<MODE>::out_cols_per_tile;
