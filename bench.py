@@ -133,8 +133,11 @@ def run_reference(args):
     sampler = OracleSampler(wl)
     vals = []
     desc = ""
+    # each step is a bounded sample: 2 s of oracle work, less when many steps are asked for,
+    # so that the whole reference run stays near two minutes
+    per_step = min(2.0, 120.0 / max(1, args.warmup + args.steps))
     for i in range(args.warmup + args.steps):
-        flops, el, desc = sampler.run(2.0)
+        flops, el, desc = sampler.run(per_step)
         if i >= args.warmup:
             vals.append((flops, el))
     tot_f = sum(f for f, _ in vals)
