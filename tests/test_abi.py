@@ -99,3 +99,15 @@ def test_invalid_arguments_rejected_before_any_cuda_call(lib):
     assert lib.moe_padded_bmm_swiglu_fwd(p, p, 4, 10, 64, 128, 0, p, p, p, p, 1 << 20, None, None) == INVALID
     assert lib.moe_padded_bmm_swiglu_fwd(p, p, 4, 10, 64, 128, 4, p, p, p, p, 16, None, None) == WS
     assert lib.moe_loop_swiglu_fwd(p, p, 4, 10, 64, 128, p, p, None, None, p, None, None) == INVALID
+
+
+def test_binding_argument_counts_match_header():
+    """Every ctypes signature of the binding has as many arguments as the header declares."""
+    import re
+    text = re.sub(r"/\*.*?\*/", "", open(_lib.HEADER).read(), flags=re.S)
+    for name, (_, args) in _lib.SIGNATURES.items():
+        m = re.search(r"\b" + name + r"\s*\(([^;]*?)\)\s*;", text)
+        assert m, name
+        params = m.group(1).strip()
+        n = 0 if params in ("", "void") else params.count(",") + 1
+        assert len(args) == n, (name, len(args), n)
