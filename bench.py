@@ -40,9 +40,10 @@ def parse_args():
     p.add_argument("--workload", default="large")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-variants", action="store_true")
-    p.add_argument("--sweep", choices=["capacity", "histogram", "configs", "partition"], default=None,
+    p.add_argument("--sweep", choices=["capacity", "histogram", "configs", "partition", "hbm"], default=None,
                    help="single-projection studies instead of the step: grouped vs capacity-padded "
-                        "BMM over routed-row counts, or throughput vs load imbalance")
+                        "BMM over routed-row counts, or throughput vs load imbalance; hbm: the "
+                        "device's write-only, read-only and copy rates on the step's row volume")
     return p.parse_args()
 
 
@@ -780,6 +781,44 @@ def run_sweep_partition(args):
     return 0
 
 
+def run_sweep_hbm(args):
+    """HBM rates of plain PyTorch kernels on the volume the row kernels move (one 512 MiB bf16
+    buffer, the size of xp / y / dxp on the large workload): write only (fill), read only (sum),
+    a 1:1 copy, and the gathers' mix of ~8 bytes written per byte read. The gathers and combines
+    are compared with these (they are write- or read-dominated, the measured peak is a 1:1 copy).
+    Mean of 20 calls after 3 warm-ups, CUDA events."""
+    import torch
+    torch.cuda.set_device(0)
+    n = 131072 * 2048
+    a = torch.empty(n, dtype=torch.bfloat16, device="cuda").normal_()
+    b = torch.empty(n, dtype=torch.bfloat16, device="cuda")
+    small = torch.randn(n // 8, dtype=torch.bfloat16, device="cuda")
+    res = {}
+
+    def rate(fn, nbytes, name, reps=20):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / reps
+        res[name] = {"ms": round(ms, 4), "gbs": round(nbytes / ms / 1e6, 1)}
+
+    rate(lambda: b.fill_(1.0), 2 * n, "write_only_fill")
+    rate(lambda: a.sum(), 2 * n, "read_only_sum")
+    rate(lambda: b.copy_(a), 4 * n, "copy_1to1")
+    bv = b.view(8, n // 8)
+    rate(lambda: bv.copy_(small.expand(8, n // 8)), 2 * n + 2 * n // 8, "write8_read1_broadcast")
+    peaks, src = load_peaks()
+    print(json.dumps({"sweep": "hbm", "bytes_per_buffer": 2 * n, "rates": res,
+                      "measured_copy_peak_gbs": peaks.get("hbm_gbs"), "peak_source": src}), flush=True)
+    return 0
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
@@ -792,6 +831,8 @@ def main():
         return run_sweep_configs(args)
     if args.sweep == "partition":
         return run_sweep_partition(args)
+    if args.sweep == "hbm":
+        return run_sweep_hbm(args)
     return run_ours(args)
 
 

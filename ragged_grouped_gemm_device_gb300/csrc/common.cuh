@@ -69,16 +69,16 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
                                           int32_t* status, long long timeout_ns,
                                           bool honour_abort = true) {
   if (mbar_try_wait(bar, parity)) return true;
+  // try_wait itself suspends the thread for a while when the phase is not complete, so the
+  // clock and the abort flag are checked after every unsuccessful try
   const uint64_t t0 = globaltimer_ns();
-  for (uint32_t i = 1;; ++i) {
+  for (;;) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 31u) == 0) {
-      if (honour_abort && *abort_flag) return false;
-      if (static_cast<long long>(globaltimer_ns() - t0) > timeout_ns) {
-        *abort_flag = 1;
-        record_status(status, MOE_DEV_TIMEOUT);
-        return false;
-      }
+    if (honour_abort && *abort_flag) return false;
+    if (static_cast<long long>(globaltimer_ns() - t0) > timeout_ns) {
+      *abort_flag = 1;
+      record_status(status, MOE_DEV_TIMEOUT);
+      return false;
     }
   }
 }

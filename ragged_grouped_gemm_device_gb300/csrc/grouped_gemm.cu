@@ -396,10 +396,13 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
         }
       }
-      // drain: the copies this thread issued into each stage must land before the CTA can exit
+      // drain: the copies this thread issued into each stage must land before the CTA can exit.
+      // After an abort a stage may lack the other producer's part and never complete; the first
+      // wait that runs out (drain_ns, seconds) has outlasted every copy issued here, so stop.
       const uint32_t first = it > NST ? it - NST : 0u;
       for (uint32_t j = first; j < it; ++j)
-        mbar_wait(smem_u32(&ctl->full[j % NST]), (j / NST) & 1u, abort_flag, status, tmo, false);
+        if (!mbar_wait(smem_u32(&ctl->full[j % NST]), (j / NST) & 1u, abort_flag, status, args.drain_ns, false))
+          break;
     }
   } else if (warp == 1) {
     // =========================================================== MMA issuer
@@ -473,7 +476,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     // every MMA this thread issued must finish before tensor memory is released
     if (lane == 0) mma_commit(smem_u32(&ctl->done));
     __syncwarp();
-    mbar_wait(smem_u32(&ctl->done), 0u, abort_flag, status, tmo, false);
+    mbar_wait(smem_u32(&ctl->done), 0u, abort_flag, status, args.drain_ns, false);
   } else if (warp >= 2 && warp < 2 + EPI_WARPS) {
     // =========================================================== epilogue (warps 2..9)
     const int q = warp & 3;           // TMEM lane quadrant this warp may access

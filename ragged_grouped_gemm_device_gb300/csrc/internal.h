@@ -68,7 +68,10 @@ struct GemmArgs {
   float* dw_part;
   int dw_np;
   int32_t* status;         // optional device status word
-  long long timeout_ns;    // bound of every wait inside the kernel
+  long long timeout_ns;    // bound of every wait of the main loops
+  // bound of the teardown waits that let this CTA's in-flight copies and MMAs finish before it
+  // frees tensor memory and exits (never below 2 s, whatever timeout_ns is)
+  long long drain_ns;
 };
 
 // Launch one persistent grouped GEMM. `a` and `b` are the operand tensor maps described with

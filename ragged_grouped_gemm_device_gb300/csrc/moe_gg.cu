@@ -49,6 +49,7 @@ GemmArgs base_args(int E, int cap, int32_t* status) {
   a.cap = cap;
   a.status = status;
   a.timeout_ns = wait_timeout_ns();
+  a.drain_ns = std::max(a.timeout_ns, 2000000000LL);
   return a;
 }
 
