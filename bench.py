@@ -124,6 +124,44 @@ class OracleSampler:
         return flops, elapsed, desc
 
 
+def blas_threads():
+    """Threads of numpy's BLAS pool: threadpoolctl's report when it is installed, else the
+    OPENBLAS/OMP thread variables, else the host's cores (OpenBLAS's default)."""
+    try:
+        from threadpoolctl import threadpool_info
+        n = [p["num_threads"] for p in threadpool_info() if p.get("user_api") == "blas"]
+        if n:
+            return max(n)
+    except Exception:
+        pass
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        if os.environ.get(var, "").isdigit():
+            return int(os.environ[var])
+    return os.cpu_count()
+
+
+SINGLE_THREAD_CHILD = """
+import json, sys
+sys.path.insert(0, sys.argv[1])
+import bench
+from ragged_grouped_gemm_device_gb300 import workloads as W
+flops, el, desc = bench.OracleSampler(W.make(sys.argv[2])).run(float(sys.argv[3]))
+print(json.dumps({"value": flops / el / 1e12, "sample": desc, "blas_threads": bench.blas_threads()}))
+"""
+
+
+def oracle_single_thread(workload: str, seconds: float):
+    """The same oracle sample on one core: a child process whose BLAS pools are pinned to one
+    thread before numpy loads (fork + exec: the child touches no CUDA state)."""
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    try:
+        res = subprocess.run([sys.executable, "-c", SINGLE_THREAD_CHILD, ROOT, workload, str(seconds)],
+                             env=env, capture_output=True, text=True, timeout=300)
+        return json.loads(res.stdout.strip().splitlines()[-1])
+    except Exception as exc:  # reported, never fatal: the GPU numbers stand without it
+        return {"error": f"{type(exc).__name__}: {exc}"[:200]}
+
+
 def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
@@ -149,8 +187,8 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot_t / len(vals),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": workload_config(wl),
-        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-                         "sample": "each step: " + desc},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "blas_threads": blas_threads(),
+                         "kind": "oracle", "sample": "each step: " + desc},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -522,7 +560,8 @@ def run_ours(args):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         flops, el, desc = OracleSampler(wl).run(12.0)
         line["cpu_baseline"] = {"value": flops / el / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(),
-                                "kind": "oracle", "sample": desc}
+                                "blas_threads": blas_threads(), "kind": "oracle", "sample": desc,
+                                "single_thread": oracle_single_thread(args.workload, 6.0)}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
