@@ -95,7 +95,7 @@ def unblock_u(u_flat: torch.Tensor, offsets: np.ndarray, h: int) -> torch.Tensor
     return u_flat[torch.from_numpy(idx).to(u_flat.device)]
 
 
-class GpuRun:
+class DevicePipeline:
     """The library pipeline (route, permute, grouped forward, optional backward, combine) on
     a workload, with NaN-filled row buffers so that rows past M cannot leak into results."""
 

@@ -54,7 +54,7 @@ def _dy(wl, M):
 @pytest.mark.parametrize("name", list(FWD_CASES))
 def test_grouped_forward(lib, name):
     wl = FWD_CASES[name]()
-    run = G.GpuRun(wl).route().permute().forward()
+    run = G.DevicePipeline(wl).route().permute().forward()
     torch.cuda.synchronize()
     assert run.status.item() == 0
     r, xp, y, u, a = G.oracle_run(wl)
@@ -69,7 +69,7 @@ def test_grouped_forward(lib, name):
 @pytest.mark.parametrize("name", BWD_CASES)
 def test_grouped_backward(lib, name):
     wl = FWD_CASES[name]()
-    run = G.GpuRun(wl).route().permute().forward()
+    run = G.DevicePipeline(wl).route().permute().forward()
     r, xp, y, u, a = G.oracle_run(wl)
     M = r["M"]
     dy, dyh = _dy(wl, M)
@@ -91,7 +91,7 @@ def test_large_forward_backward_sampled_experts(lib):
     """The large workload at full size; the oracle checks every row and gradient of a sample of
     experts (first, last, largest, smallest and random ones)."""
     wl = W.make("large")
-    run = G.GpuRun(wl).route().permute().forward()
+    run = G.DevicePipeline(wl).route().permute().forward()
     r = O.route_offsets(wl.ids, wl.E)
     M = r["M"]
     experts = G.sample_experts(r["counts"], n_pick=8)
@@ -116,7 +116,7 @@ def test_bad_offsets_flag_and_no_work(lib):
     kernels compute nothing."""
     from ragged_grouped_gemm_device_gb300 import _lib
     wl = FWD_CASES["edge_small"]()
-    run = G.GpuRun(wl)
+    run = G.DevicePipeline(wl)
     for bad in ([5, 3, 9, 9, 9, 9, 9, 9, 9], [1, 2, 3, 4, 5, 6, 7, 8, wl.n + 1]):
         run.offsets.copy_(torch.tensor(bad, dtype=torch.int32))
         run.status.zero_()
@@ -133,7 +133,7 @@ def test_single_kernel_entry_points_equal_composites(lib):
     the normalised tolerance."""
     from ragged_grouped_gemm_device_gb300 import _lib as L
     wl = W.custom(T=300, k=4, E=7, d=136, h=200, seed=31, invalid_frac=0.05, empty_experts=(3,))
-    run = G.GpuRun(wl).route().permute()
+    run = G.DevicePipeline(wl).route().permute()
     n, d, h, E = run.cap, wl.d, wl.h, wl.E
     y1, a1 = G.nan_filled((n, d)), G.nan_filled((n, h))
     sv1 = torch.zeros_like(run.saved)
@@ -183,7 +183,7 @@ def test_outputs_at_16_byte_alignment_match_32_byte_aligned(lib):
     up/gate and dgrad epilogues; the results are bit-identical to the 32-byte path."""
     from ragged_grouped_gemm_device_gb300 import _lib as L
     wl = W.custom(T=200, k=2, E=5, d=128, h=256, seed=41, empty_experts=(2,))
-    run = G.GpuRun(wl).route().permute()
+    run = G.DevicePipeline(wl).route().permute()
     n, d, h, E = run.cap, wl.d, wl.h, wl.E
     M = int(run.offsets[-1].item())
 

@@ -33,7 +33,7 @@ CASES = {
 @pytest.mark.parametrize("name", list(CASES))
 def test_route_offsets_bit_exact(lib, name):
     wl = CASES[name]()
-    run = G.GpuRun(wl, with_u=False).route()
+    run = G.DevicePipeline(wl, with_u=False).route()
     torch.cuda.synchronize()
     r = O.route_offsets(wl.ids, wl.E)
     assert np.array_equal(run.counts.cpu().numpy(), r["counts"])
@@ -56,7 +56,7 @@ def test_route_zero_tokens(lib):
 @pytest.mark.parametrize("name", ["toy", "balanced", "finegrained", "skew", "invalid_ids", "single_expert", "top32"])
 def test_permute_bit_exact_and_tail_untouched(lib, name):
     wl = CASES[name]()
-    run = G.GpuRun(wl, with_u=False).route().permute()
+    run = G.DevicePipeline(wl, with_u=False).route().permute()
     torch.cuda.synchronize()
     r = O.route_offsets(wl.ids, wl.E)
     M = r["M"]
@@ -68,7 +68,7 @@ def test_permute_bit_exact_and_tail_untouched(lib, name):
 
 def test_permute_row_scale_rounds_once(lib):
     wl = CASES["invalid_ids"]()
-    run = G.GpuRun(wl, with_u=False).route()
+    run = G.DevicePipeline(wl, with_u=False).route()
     _lib.moe_permute(run.x, run.sorted_src, run.offsets, run.weights, wl.T, wl.k, wl.E, wl.d, run.xp)
     torch.cuda.synchronize()
     r = O.route_offsets(wl.ids, wl.E)
@@ -82,7 +82,7 @@ def test_permute_row_scale_rounds_once(lib):
 @pytest.mark.parametrize("name", ["toy", "balanced", "finegrained", "invalid_ids", "all_dropped", "top32"])
 def test_combine_matches_oracle(lib, name):
     wl = CASES[name]()
-    run = G.GpuRun(wl, with_u=False).route()
+    run = G.DevicePipeline(wl, with_u=False).route()
     yh = W._normal_bf16(np.random.default_rng(7), (max(wl.n, 1), wl.d))
     y = G.dev_bf16(yh)
     out = torch.full((wl.T, wl.d), float("nan"), dtype=torch.bfloat16, device="cuda")
@@ -100,7 +100,7 @@ def test_combine_matches_oracle(lib, name):
 @pytest.mark.parametrize("k", [1, 2, 8])
 def test_permute_then_combine_is_k_times_identity(lib, k):
     wl = W.custom(T=1000, k=k, E=13, d=264, h=8, seed=k)
-    run = G.GpuRun(wl, with_u=False).route().permute()
+    run = G.DevicePipeline(wl, with_u=False).route().permute()
     out = torch.empty(wl.T, wl.d, dtype=torch.bfloat16, device="cuda")
     _lib.moe_unpermute_combine(run.xp, run.inv_map, None, wl.T, k, wl.d, out)
     torch.cuda.synchronize()

@@ -16,7 +16,7 @@ pytestmark = pytest.mark.gpu
 @pytest.mark.parametrize("name,C", [("toy", 4), ("toy", 2), ("edge", None), ("balanced", None), ("skew", None)])
 def test_padded_bmm_matches_oracle(lib, name, C):
     wl = W.custom(T=300, k=2, E=5, d=136, h=200, seed=8) if name == "edge" else W.make(name)
-    run = G.GpuRun(wl).route().permute()
+    run = G.DevicePipeline(wl).route().permute()
     r = O.route_offsets(wl.ids, wl.E)
     M = r["M"]
     if C is None:
@@ -45,7 +45,7 @@ def test_host_loop_matches_oracle(lib, name):
         wl = W.custom(T=100, k=1, E=64, d=64, h=72, seed=10, empty_experts=tuple(range(0, 62)))
     else:
         wl = W.make(name)
-    run = G.GpuRun(wl).route().permute()
+    run = G.DevicePipeline(wl).route().permute()
     _lib.moe_loop_swiglu_fwd(run.xp, run.offsets, wl.E, run.cap, wl.d, wl.h, run.w_ug, run.w_down, run.y,
                              run.a, run.saved, run.status)
     torch.cuda.synchronize()

@@ -20,7 +20,7 @@ pytestmark = pytest.mark.gpu
 
 
 def _route(wl, noalloc):
-    run = G.GpuRun(wl, with_u=False)
+    run = G.DevicePipeline(wl, with_u=False)
     if noalloc:
         _lib.moe_route_offsets_noalloc(run.ids, wl.T, wl.k, wl.E, run.counts, run.offsets, run.sorted_src,
                                        run.inv_map)
