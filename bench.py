@@ -594,6 +594,24 @@ def queued_mean_ms(fn, warmup=10, samples=20):
     return e0.elapsed_time(e1) / samples
 
 
+def median_ms(fn, warmup=3, samples=50):
+    """Median device time of `fn` over `samples` launches, each timed alone between two events
+    on the current stream and synchronised (the pages' median of 50)."""
+    import torch
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(samples):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn()
+        e1.record()
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    return statistics.median(ts)
+
+
 def projection_setup(max_rows, seed=0):
     """Device inputs of the square projection: X [max_rows, K] ~ N(0, 1) and W [E, K, N] ~
     N(0, 1/sqrt(K)), bf16, drawn on the device from a seeded generator (the values do not
@@ -721,7 +739,8 @@ def run_sweep_configs(args):
     """Forward of the SwiGLU expert on each named workload: the grouped composite call against
     the in-library capacity-padded BMM (C = ceil(1.25 M/E), same kernels) and the host-scheduled
     per-expert loop (wall time, including its count copy and host wait). Grouped and BMM: mean
-    of 20 launches queued in a CUDA graph after 10 warm-ups; loop: mean of 5 calls."""
+    of 20 launches queued in a CUDA graph after 10 warm-ups, and the median of 50 launches each
+    timed alone; loop: mean of 5 calls."""
     import torch
     from ragged_grouped_gemm_device_gb300 import _lib as L
     from ragged_grouped_gemm_device_gb300 import workloads as W
@@ -749,10 +768,11 @@ def run_sweep_configs(args):
         a = torch.empty(n, h, dtype=bf, device=dev)
         status = torch.zeros(1, dtype=i32, device=dev)
         bws = torch.empty(L.moe_workspace_bytes(L.OP_PADDED_BMM, T, k, E, d, h, C), dtype=torch.uint8, device=dev)
-        t_g = queued_mean_ms(lambda: L.moe_grouped_swiglu_fwd(xp, offsets, None, None, E, n, d, h, w_ug, w_down,
-                                                              y, a, None, None, status))
-        t_b = queued_mean_ms(lambda: L.moe_padded_bmm_swiglu_fwd(xp, offsets, E, n, d, h, C, w_ug, w_down, y,
-                                                                 bws, status))
+        fwd_g = lambda: L.moe_grouped_swiglu_fwd(xp, offsets, None, None, E, n, d, h, w_ug, w_down, y, a, None,
+                                                 None, status)
+        fwd_b = lambda: L.moe_padded_bmm_swiglu_fwd(xp, offsets, E, n, d, h, C, w_ug, w_down, y, bws, status)
+        t_g, t_b = queued_mean_ms(fwd_g), queued_mean_ms(fwd_b)
+        m_g, m_b = median_ms(fwd_g), median_ms(fwd_b)
         loop = lambda: L.moe_loop_swiglu_fwd(xp, offsets, E, n, d, h, w_ug, w_down, y, a, None, status)
         for _ in range(2):
             loop()
@@ -768,7 +788,9 @@ def run_sweep_configs(args):
                "C": C, "padded_bmm_dropped_rows": dropped, "grouped_ms": t_g, "padded_bmm_ms": t_b,
                "host_loop_ms": t_l,
                "grouped_tflops": fl / t_g / 1e9, "padded_bmm_tflops": fl / t_b / 1e9,
-               "host_loop_tflops": fl / t_l / 1e9, "speedup_vs_bmm": t_b / t_g, "speedup_vs_loop": t_l / t_g}
+               "host_loop_tflops": fl / t_l / 1e9, "speedup_vs_bmm": t_b / t_g, "speedup_vs_loop": t_l / t_g,
+               "grouped_median50_ms": m_g, "padded_bmm_median50_ms": m_b,
+               "grouped_median50_tflops": fl / m_g / 1e9, "padded_bmm_median50_tflops": fl / m_b / 1e9}
         rows.append(row)
         print(json.dumps(row), flush=True)
         del x, w_ug, w_down, xp, y, a, bws
