@@ -40,10 +40,12 @@ def parse_args():
     p.add_argument("--workload", default="large")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-variants", action="store_true")
-    p.add_argument("--sweep", choices=["capacity", "histogram", "configs", "partition", "hbm"], default=None,
+    p.add_argument("--sweep", choices=["capacity", "histogram", "configs", "partition", "hbm", "oracle"],
+                   default=None,
                    help="single-projection studies instead of the step: grouped vs capacity-padded "
                         "BMM over routed-row counts, or throughput vs load imbalance; hbm: the "
-                        "device's write-only, read-only and copy rates on the step's row volume")
+                        "device's write-only, read-only and copy rates on the step's row volume; "
+                        "oracle: the CPU baseline on every workload, all cores and one")
     return p.parse_args()
 
 
@@ -160,6 +162,70 @@ def oracle_single_thread(workload: str, seconds: float):
         return json.loads(res.stdout.strip().splitlines()[-1])
     except Exception as exc:  # reported, never fatal: the GPU numbers stand without it
         return {"error": f"{type(exc).__name__}: {exc}"[:200]}
+
+
+def oracle_rates(wl, seconds: float) -> dict:
+    """The oracle as it stands on a bounded sample of one workload, forward and forward +
+    backward separately: expert by expert (in index order, empty experts skipped), the permute
+    of its rows and its fp64 forward (6*M_e*d*h), or forward + backward (18*M_e*d*h), until about
+    `seconds` of CPU time each. Weight generation is not timed."""
+    import numpy as np
+    from oracle import moe_oracle as O
+    x, dout = wl.x(), wl.dout()
+    r = O.route_offsets(wl.ids, wl.E)
+    segs = O.segments(r["offsets"])
+    order = [e for e in range(wl.E) if segs[e][1] > segs[e][0]]
+    out = {}
+    for mode in ("fwd", "fwd_bwd"):
+        el, fl, rows, nexp = 0.0, 0, 0, 0
+        for e in order:
+            s, t = segs[e]
+            wu, wd = wl.w_ug(e), wl.w_down(e)
+            src = r["sorted_src"][s:t]
+            one = np.array([t - s])
+            t0 = time.perf_counter()
+            xp = O.permute(x, src, t - s, wl.k)
+            _, u, _, _ = O.expert_forward(xp, one, lambda i: wu, lambda i: wd)
+            if mode == "fwd_bwd":
+                dy = O.permute(dout, src, t - s, wl.k, row_scale=wl.weights)
+                O.expert_backward(dy, xp, u, one, lambda i: wu, lambda i: wd)
+            el += time.perf_counter() - t0
+            fl += (O.flops_fwd_bwd if mode == "fwd_bwd" else O.flops_fwd)(t - s, wl.d, wl.h)
+            rows += t - s
+            nexp += 1
+            if el >= seconds:
+                break
+        out[mode] = {"tflops": fl / el / 1e12, "experts": nexp, "rows": rows, "seconds": round(el, 2)}
+    return out
+
+
+ORACLE_SWEEP = ("balanced", "finegrained", "skew", "large")
+ORACLE_SWEEP_CHILD = """
+import json, sys
+sys.path.insert(0, sys.argv[1])
+import bench
+from ragged_grouped_gemm_device_gb300 import workloads as W
+print(json.dumps({n: bench.oracle_rates(W.make(n), float(sys.argv[2])) for n in bench.ORACLE_SWEEP}))
+"""
+
+
+def run_sweep_oracle(args):
+    """The CPU baseline on every mid-size and large workload: the oracle's forward and forward +
+    backward rates on all host cores (numpy's BLAS pool) and, in a child process whose BLAS pools
+    are pinned to one thread, on one core. No GPU is used."""
+    from ragged_grouped_gemm_device_gb300 import workloads as W
+    seconds = 3.0
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    child = subprocess.run([sys.executable, "-c", ORACLE_SWEEP_CHILD, ROOT, str(seconds)], env=env,
+                           capture_output=True, text=True, timeout=900)
+    single = json.loads(child.stdout.strip().splitlines()[-1]) if child.returncode == 0 else {}
+    for name in ORACLE_SWEEP:
+        wl = W.make(name)
+        row = {"sweep": "oracle", "workload": name, "T": wl.T, "top_k": wl.k, "E": wl.E, "d": wl.d, "h": wl.h,
+               "cores": os.cpu_count(), "blas_threads": blas_threads(), "all_cores": oracle_rates(wl, seconds),
+               "single_thread": single.get(name, {"error": child.stderr[-300:]})}
+        print(json.dumps(row), flush=True)
+    return 0
 
 
 def run_reference(args):
@@ -894,6 +960,8 @@ def main():
         return run_sweep_partition(args)
     if args.sweep == "hbm":
         return run_sweep_hbm(args)
+    if args.sweep == "oracle":
+        return run_sweep_oracle(args)
     return run_ours(args)
 
 

@@ -23,3 +23,10 @@ def test_single_thread_sample_runs_with_one_blas_thread():
     assert "error" not in r, r
     assert r["blas_threads"] == 1 and r["value"] > 0
     assert bench.blas_threads() >= 1
+
+
+def test_oracle_rates_time_forward_and_backward_separately():
+    r = bench.oracle_rates(W.make("toy"), 10.0)
+    assert set(r) == {"fwd", "fwd_bwd"}
+    for mode in r.values():
+        assert mode["experts"] == 4 and mode["rows"] == 10 and mode["tflops"] > 0
