@@ -806,7 +806,9 @@ def run_sweep_configs(args):
     the in-library capacity-padded BMM (C = ceil(1.25 M/E), same kernels) and the host-scheduled
     per-expert loop (wall time, including its count copy and host wait). Grouped and BMM: mean
     of 20 launches queued in a CUDA graph after 10 warm-ups, and the median of 50 launches each
-    timed alone; loop: mean of 5 calls."""
+    timed alone; loop: mean of 5 calls. Workloads with a backward also time the grouped GEMMs of
+    a training step (a6-a7 with the saved state, then a10-a13 from dY at the grouped boundary,
+    the two composite calls; 18*M*d*h useful FLOPs), graph-queued."""
     import torch
     from ragged_grouped_gemm_device_gb300 import _lib as L
     from ragged_grouped_gemm_device_gb300 import workloads as W
@@ -839,6 +841,24 @@ def run_sweep_configs(args):
         fwd_b = lambda: L.moe_padded_bmm_swiglu_fwd(xp, offsets, E, n, d, h, C, w_ug, w_down, y, bws, status)
         t_g, t_b = queued_mean_ms(fwd_g), queued_mean_ms(fwd_b)
         m_g, m_b = median_ms(fwd_g), median_ms(fwd_b)
+        train = None
+        if wl.has_bwd:
+            sv = torch.empty(L.moe_workspace_bytes(L.OP_SAVED, T, k, E, d, h), dtype=torch.uint8, device=dev)
+            bw = torch.empty(max(L.moe_workspace_bytes(L.OP_BWD, T, k, E, d, h), 1), dtype=torch.uint8,
+                             device=dev)
+            dyb = torch.randn(n, d, device=dev, generator=gen).to(bf)
+            dxp = torch.empty(n, d, dtype=bf, device=dev)
+            dwu = torch.empty(E, 2 * h, d, device=dev)
+            dwd = torch.empty(E, h, d, device=dev)
+            fwd_t = lambda: L.moe_grouped_swiglu_fwd(xp, offsets, None, None, E, n, d, h, w_ug, w_down, y, a,
+                                                     sv, None, status)
+            bwd_t = lambda: L.moe_grouped_bwd(dyb, xp, a, sv, offsets, None, None, E, n, d, h, w_ug, w_down,
+                                              dxp, dwu, dwd, bw, status)
+            t_ft, t_bt = queued_mean_ms(fwd_t), queued_mean_ms(bwd_t)
+            train = {"fwd_ms": t_ft, "bwd_ms": t_bt,
+                     "fwd_bwd_tflops": 18.0 * M * d * h / (t_ft + t_bt) / 1e9,
+                     "bwd_tflops": 12.0 * M * d * h / t_bt / 1e9}
+            del sv, bw, dyb, dxp, dwu, dwd
         loop = lambda: L.moe_loop_swiglu_fwd(xp, offsets, E, n, d, h, w_ug, w_down, y, a, None, status)
         for _ in range(2):
             loop()
@@ -856,7 +876,8 @@ def run_sweep_configs(args):
                "grouped_tflops": fl / t_g / 1e9, "padded_bmm_tflops": fl / t_b / 1e9,
                "host_loop_tflops": fl / t_l / 1e9, "speedup_vs_bmm": t_b / t_g, "speedup_vs_loop": t_l / t_g,
                "grouped_median50_ms": m_g, "padded_bmm_median50_ms": m_b,
-               "grouped_median50_tflops": fl / m_g / 1e9, "padded_bmm_median50_tflops": fl / m_b / 1e9}
+               "grouped_median50_tflops": fl / m_g / 1e9, "padded_bmm_median50_tflops": fl / m_b / 1e9,
+               "training_gemms": train}
         rows.append(row)
         print(json.dumps(row), flush=True)
         del x, w_ug, w_down, xp, y, a, bws
