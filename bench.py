@@ -40,12 +40,13 @@ def parse_args():
     p.add_argument("--workload", default="large")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-variants", action="store_true")
-    p.add_argument("--sweep", choices=["capacity", "histogram", "configs", "partition", "hbm", "oracle"],
+    p.add_argument("--sweep", choices=["capacity", "histogram", "configs", "precision", "oracle"],
                    default=None,
-                   help="single-projection studies instead of the step: grouped vs capacity-padded "
-                        "BMM over routed-row counts, or throughput vs load imbalance; hbm: the "
-                        "device's write-only, read-only and copy rates on the step's row volume; "
-                        "oracle: the CPU baseline on every workload, all cores and one")
+                   help="studies instead of the step: capacity (grouped vs capacity-padded BMM over "
+                        "routed-row counts), histogram (throughput vs load imbalance), configs "
+                        "(forward and training GEMMs on every workload), precision (the wgrads with "
+                        "and without the low half of the activation operand), oracle (the CPU "
+                        "baseline on every workload, all cores and one)")
     return p.parse_args()
 
 
@@ -354,6 +355,141 @@ def load_traffic():
     return {}
 
 
+def kernel_work(M, T, k, E, d, h):
+    """Per launch of each step kernel on a workload with M routed rows: (useful FLOPs, compulsory
+    DRAM bytes, FLOPs the tensor cores execute). Bytes count every operand read once and every
+    output written once under the library's data contract: bf16 rows and weights, fp32 saved U,
+    bf16 low halves of P and dU (the wgrads' second operand half), fp32 weight gradients, int32
+    indices, fp32 routing weights. The wgrads execute twice their useful FLOPs (both halves)."""
+    mdh = float(M) * d * h
+    np_ = 2 * ((h + 255) // 256)  # routing-gradient partials per row
+    wd = E * h * d * 2.0          # one [E, h, d] bf16 weight
+    w = {
+        "route": (0, T * k * 4 * 4.0, 0),                       # ids read twice, placement + inverse map written
+        "permute": (0, T * d * 2.0 + M * d * 2.0 + M * 4.0, 0),
+        "up_swiglu": (4 * mdh, M * d * 2.0 + 2 * wd + M * h * 2.0 * 2 + M * 2 * h * 4.0 + M * 8.0, 4 * mdh),
+        "down": (2 * mdh, M * h * 2.0 + wd + M * d * 2.0, 2 * mdh),
+        "combine": (0, M * d * 2.0 + T * d * 2.0 + T * k * 4.0, 0),
+        "combine_bwd": (0, T * d * 2.0 + M * d * 2.0 + M * 4.0, 0),
+        "down_dgrad_swiglu": (2 * mdh, M * d * 2.0 + wd + M * 2 * h * 4.0 + M * 2 * h * 2.0 * 2 + M * np_ * 4.0
+                              + M * 8.0, 2 * mdh),
+        "routing_weight_grad": (0, M * np_ * 4.0 + T * k * 8.0, 0),
+        "up_dgrad": (4 * mdh, M * 2 * h * 2.0 + 2 * wd + M * d * 2.0, 4 * mdh),
+        # down: P high + low [M, h], dy [M, d] -> dW_down fp32; up: dU high + low [M, 2h], xp -> dW_ug fp32
+        "wgrad_dual": (6 * mdh, M * h * 4.0 + M * d * 2.0 + E * h * d * 4.0 + M * 2 * h * 4.0 + M * d * 2.0
+                       + E * 2 * h * d * 4.0, 12 * mdh),
+        "permute_bwd": (0, M * d * 2.0 + T * d * 2.0 + T * k * 4.0, 0),
+    }
+    return w
+
+
+def kernel_rooflines(per_call, work, peaks, peak_src):
+    """Each kernel against its roofline. The tensor peak is the measured burst bf16 rate (the
+    timed region is tens of milliseconds, not the seconds-long loop the sustained figure comes
+    from); the memory peak the measured copy rate. A kernel is tensor-bound when its FLOPs per
+    compulsory byte reach the ridge peak_tflops / peak_hbm, else memory-bound; `floor_ms` is
+    the larger of its two floors and `frac` = floor / measured time. Returns (breakdown, the
+    slowest kernel, the roofline object of that kernel)."""
+    peak_tf = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    peak_hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    ridge = peak_tf * 1e12 / (peak_hbm * 1e9)
+    out = {}
+    for name, ms in per_call.items():
+        fl, by, ex = work[name]
+        sec = ms * 1e-3
+        b = {"ms": round(ms, 4), "bytes": int(by), "gbs": round(by / sec / 1e9, 1),
+             "hbm_frac": round(by / sec / 1e9 / peak_hbm, 3)}
+        if fl:
+            b["tflops"] = round(fl / sec / 1e12, 1)
+            b["tensor_frac"] = round(fl / sec / 1e12 / peak_tf, 3)
+            b["intensity"] = round(fl / by, 1)
+            b["bound"] = "tensor" if fl / by >= ridge else "hbm"
+            if ex != fl:
+                b["mma_executed_tflops"] = round(ex / sec / 1e12, 1)
+        else:
+            b["bound"] = "hbm"
+        floor = max(fl / (peak_tf * 1e12), by / (peak_hbm * 1e9))
+        b["floor_ms"] = round(floor * 1e3, 4)
+        b["frac"] = round(floor / sec, 3)
+        out[name] = b
+    dom = max(per_call, key=per_call.get)
+    fl, by, ex = work[dom]
+    sec = per_call[dom] * 1e-3
+    if out[dom]["bound"] == "tensor":
+        roof = {"kernel": dom, "bound": "tensor", "achieved": fl / sec / 1e12, "peak": peak_tf, "unit": "TFLOP/s",
+                "frac": fl / sec / 1e12 / peak_tf, "peak_source": f"bf16_tflops ({peak_src}, burst)"}
+    else:
+        roof = {"kernel": dom, "bound": "hbm", "achieved": by / sec / 1e9, "peak": peak_hbm, "unit": "GB/s",
+                "frac": by / sec / 1e9 / peak_hbm, "peak_source": f"hbm_gbs ({peak_src})"}
+    roof["algorithmic_bytes"] = int(by)
+    roof["useful_flops"] = fl
+    roof["tensor_frac_of_burst"] = fl / sec / 1e12 / peak_tf if fl else 0.0
+    roof["mma_executed_tflops"] = ex / sec / 1e12 if ex else 0.0
+    roof["ridge_flop_per_byte"] = round(ridge, 1)
+    return out, dom, roof
+
+
+VARIANT_CONFIGS = ("balanced", "finegrained", "skew")
+
+
+def config_variants(L, names=VARIANT_CONFIGS):
+    """Forward of the SwiGLU expert on the mid-size workloads: the grouped composite call, the
+    in-library capacity-padded BMM at C = ceil(1.25 M/E) (same kernels, rows beyond C dropped
+    and counted) and the host-scheduled per-expert loop. Grouped and BMM: mean of 20 launches
+    queued in a CUDA graph after 10 warm-ups; loop: wall time of one call (it copies the counts
+    to the host and waits), mean of 3 after one warm-up. Weights and inputs are drawn on the
+    device (values do not change the timing); the routing is the workload's."""
+    import torch
+    from ragged_grouped_gemm_device_gb300 import workloads as W
+    dev, bf, i32 = "cuda", torch.bfloat16, torch.int32
+    res = {}
+    for name in names:
+        wl = W.make(name)
+        T, k, E, d, h, n = wl.T, wl.k, wl.E, wl.d, wl.h, wl.n
+        gen = torch.Generator(device=dev).manual_seed(1)
+        x = torch.randn(T, d, device=dev, generator=gen).to(bf)
+        w_ug = (torch.randn(E, 2 * h, d, device=dev, generator=gen) * d ** -0.5).to(bf)
+        w_down = (torch.randn(E, h, d, device=dev, generator=gen) * h ** -0.5).to(bf)
+        ids = torch.from_numpy(wl.ids).to(dev)
+        counts, offsets = torch.empty(E, dtype=i32, device=dev), torch.empty(E, dtype=i32, device=dev)
+        ss, inv = torch.empty(n, dtype=i32, device=dev), torch.empty(n, dtype=i32, device=dev)
+        rws = torch.empty(max(L.moe_workspace_bytes(L.OP_ROUTE, T, k, E), 1), dtype=torch.uint8, device=dev)
+        xp = torch.empty(n, d, dtype=bf, device=dev)
+        L.moe_route_offsets(ids, T, k, E, counts, offsets, ss, inv, rws)
+        L.moe_permute(x, ss, offsets, None, T, k, E, d, xp)
+        torch.cuda.synchronize()
+        M = int(offsets[-1].item())
+        C = -(-(5 * M) // (4 * E))
+        dropped = int(torch.clamp(counts.long() - C, min=0).sum().item())
+        y = torch.empty(n, d, dtype=bf, device=dev)
+        a = torch.empty(n, h, dtype=bf, device=dev)
+        status = torch.zeros(1, dtype=i32, device=dev)
+        bws = torch.empty(L.moe_workspace_bytes(L.OP_PADDED_BMM, T, k, E, d, h, C), dtype=torch.uint8, device=dev)
+        t_g = queued_mean_ms(lambda: L.moe_grouped_swiglu_fwd(xp, offsets, None, None, E, n, d, h, w_ug, w_down, y,
+                                                               a, None, None, status))
+        t_b = queued_mean_ms(lambda: L.moe_padded_bmm_swiglu_fwd(xp, offsets, E, n, d, h, C, w_ug, w_down, y, bws,
+                                                                  status))
+        loop = lambda: L.moe_loop_swiglu_fwd(xp, offsets, E, n, d, h, w_ug, w_down, y, a, None, status)
+        loop()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(3):
+            loop()
+        torch.cuda.synchronize()
+        t_l = (time.perf_counter() - t0) * 1e3 / 3
+        assert status.item() == 0, f"device status {status.item()}"
+        fl = 6.0 * M * d * h
+        res[name] = {"T": T, "top_k": k, "E": E, "d": d, "h": h, "M": M,
+                     "grouped": {"ms": round(t_g, 4), "tflops": round(fl / t_g / 1e9, 1)},
+                     "padded_bmm": {"ms": round(t_b, 4), "tflops": round(fl / t_b / 1e9, 1), "C": C,
+                                    "rows_multiplied": E * C, "rows_dropped": dropped},
+                     "host_loop": {"ms": round(t_l, 4), "tflops": round(fl / t_l / 1e9, 1)},
+                     "grouped_vs_bmm": round(t_b / t_g, 3), "grouped_vs_loop": round(t_l / t_g, 3)}
+        del x, w_ug, w_down, xp, y, a, bws
+        torch.cuda.empty_cache()
+    return res
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -429,8 +565,9 @@ def run_ours(args):
                                                                              dw_part=dw_part)),
             ("routing_weight_grad", 1, lambda: L.moe_routing_weight_grad(dw_part, inv_map, T, k, h, dw_route)),
             ("up_dgrad", 1, lambda: L.moe_grouped_up_dgrad(du_hi, offsets, E, n, d, h, w_ug, dxp, status)),
-            ("wgrad_down", 1, lambda: L.moe_grouped_wgrad(a, p_lo, h, dy, d, offsets, E, n, dw_down, status)),
-            ("wgrad_up", 1, lambda: L.moe_grouped_wgrad(du_hi, du_lo, 2 * h, xp, d, offsets, E, n, dw_ug, status)),
+            # both weight gradients (down, then up/gate) in one persistent launch
+            ("wgrad_dual", 1, lambda: L.moe_grouped_wgrad_dual(a, p_lo, h, dy, d, dw_down, du_hi, du_lo, 2 * h, xp,
+                                                               d, dw_ug, offsets, E, n, status)),
             ("permute_bwd", 1, lambda: L.moe_unpermute_combine(dxp, inv_map, None, T, k, d, dx)),
         ]
 
@@ -476,26 +613,12 @@ def run_ours(args):
     fwdbwd_flops = 18.0 * M * d * h
     value = job_tflops(world, fwdbwd_flops, ms_step)
     peaks, peak_src = load_peaks()
-    peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
-    peak_hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     mdh = float(M) * d * h
-    algo_flops = {"up_swiglu": 4 * mdh, "down": 2 * mdh, "down_dgrad_swiglu": 2 * mdh, "up_dgrad": 4 * mdh,
-                  "wgrad_down": 2 * mdh, "wgrad_up": 4 * mdh}
-    gemm_ms = {kname: per_call[kname] for kname in algo_flops}
-    dom = max(gemm_ms, key=gemm_ms.get)
-    achieved = algo_flops[dom] / (gemm_ms[dom] * 1e-3) / 1e12
+    breakdown, dom, roofline = kernel_rooflines(per_call, kernel_work(M, T, k, E, d, h), peaks, peak_src)
     traffic = load_traffic().get(dom)
+    roofline["traffic"] = traffic
     fwd_ms = per_call["up_swiglu"] + per_call["down"]
-    breakdown = {kname: {"ms": round(v, 4)} for kname, v in per_call.items()}
-    for kname, fl in algo_flops.items():
-        breakdown[kname]["tflops"] = round(fl / (per_call[kname] * 1e-3) / 1e12, 1)
-        breakdown[kname]["frac_of_sustained_peak"] = round(fl / (per_call[kname] * 1e-3) / 1e12 / peak_sus, 3)
-    # algorithmic bytes: token rows read once (x and dOut fit in L2), expert rows written/read once
-    hbm_bytes = {"permute": M * d * 2 + T * d * 2 + M * 4, "combine": M * d * 2 + T * d * 2 + T * k * 4,
-                 "combine_bwd": M * d * 2 + T * d * 2 + M * 4, "permute_bwd": M * d * 2 + T * d * 2 + T * k * 4}
-    for kname, b in hbm_bytes.items():
-        breakdown[kname]["gbs"] = round(b / (per_call[kname] * 1e-3) / 1e9, 1)
-        breakdown[kname]["frac_of_hbm_peak"] = round(b / (per_call[kname] * 1e-3) / 1e9 / peak_hbm, 3)
+    peak_tf = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
 
     # ---- end to end through the public calls with host buffers (pinned), copies inside. As a
     # training loop would: the inputs of a step go host -> device on one copy stream into one of
@@ -609,19 +732,16 @@ def run_ours(args):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded; random-init weights)",
         "config": workload_config(wl),
         "fwd": {"ms": fwd_ms, "tflops": 6.0 * mdh / (fwd_ms * 1e-3) / 1e12,
-                "frac_of_sustained_peak": 6.0 * mdh / (fwd_ms * 1e-3) / 1e12 / peak_sus},
-        "roofline": {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peak_sus,
-                     "unit": "TFLOP/s", "frac": achieved / peak_sus, "traffic": traffic,
-                     "peak_source": f"bf16_tflops_sustained ({peak_src})",
-                     # context: the wgrads contract both bf16 halves of their activation operand,
-                     # so their tensor cores execute twice the useful FLOPs counted above
-                     "mma_executed_tflops": achieved * (2.0 if dom.startswith("wgrad") else 1.0)},
+                "frac_of_burst_peak": 6.0 * mdh / (fwd_ms * 1e-3) / 1e12 / peak_tf,
+                "peak_source": f"bf16_tflops ({peak_src}, burst: the timed region lasts well under a second)"},
+        "roofline": roofline,
         "e2e": {"value": job_tflops(world, fwdbwd_flops, e2e_ms), "unit": "TFLOP/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
         "breakdown": breakdown,
         "variants": variants,
+        "variants_by_config": config_variants(L) if (not args.no_variants and world == 1) else None,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         flops, el, desc = OracleSampler(wl).run(12.0)
@@ -889,81 +1009,61 @@ def run_sweep_configs(args):
     return 0
 
 
-def run_sweep_partition(args):
-    """Fig. 39 of "Section 09: Grouped GEMM" on one GB300: one dense projection [T, 8192] @
-    [8192, 81920] against its exact split into E = 4 or 8 expert GEMMs (Eq. 17: expert e owns
-    columns [e N/E, (e+1) N/E) of the weight; the grouped input repeats the dense input E
-    times). Same useful FLOPs, weights and outputs; dense = cuBLAS (torch.matmul), grouped = the
-    grouped kernel over the uniform problem list. Mean of 20 launches queued in a CUDA graph."""
+def run_sweep_precision(args):
+    """Price of the wgrads' precision scheme: the dual wgrad launch (dW_down and dW_ug) with both
+    bf16 halves of its activation operand (P = w*A for the down projection, dU for the up/gate
+    projection; two MMAs per K step) against the high half only (one MMA per K step), on the
+    workloads with a backward. Operands come from the library's own forward and dgrad on the
+    workload's routing with device-drawn N(0,1) inputs; mean of 20 launches queued in a CUDA
+    graph after 10 warm-ups. The accuracy side of the trade is a GPU test against the oracle."""
     import torch
     from ragged_grouped_gemm_device_gb300 import _lib as L
-    dev, bf = "cuda", torch.bfloat16
-    K, N = 8192, 81920
-    gen = torch.Generator(device=dev).manual_seed(3)
-    w = (torch.randn(K, N, device=dev, generator=gen) * K ** -0.5).to(bf)
-    status = torch.zeros(1, dtype=torch.int32, device=dev)
-    rows = []
-    for T in (256, 1024, 4096, 8192, 16384, 32768, 65536):
-        x = torch.randn(T, K, device=dev, generator=gen).to(bf)
-        y = torch.empty(T, N, dtype=bf, device=dev)
-        t_dense = queued_mean_ms(lambda: torch.matmul(x, w, out=y))
-        del y
-        row = {"sweep": "partition", "T": T, "K": K, "N": N, "dense_cublas_ms": t_dense,
-               "dense_cublas_tflops": 2.0 * T * K * N / t_dense / 1e9}
-        for E in (4, 8):
-            wg = w.view(K, E, N // E).permute(1, 0, 2).contiguous()   # [E, K, N/E]
-            xr = x.repeat(E, 1)                                          # expert e owns rows [eT, (e+1)T)
-            yg = torch.empty(E * T, N // E, dtype=bf, device=dev)
-            offs = torch.arange(1, E + 1, dtype=torch.int32, device=dev) * T
-            t_g = queued_mean_ms(lambda: L.moe_grouped_down(xr, offs, E, E * T, N // E, K, wg, yg, status))
-            row[f"grouped_{E}_ms"] = t_g
-            row[f"grouped_{E}_tflops"] = 2.0 * T * K * N / t_g / 1e9
-            row[f"grouped_{E}_vs_dense"] = t_dense / t_g
-            del wg, xr, yg
+    from ragged_grouped_gemm_device_gb300 import workloads as W
+    L.load()
+    dev, bf, i32 = "cuda", torch.bfloat16, torch.int32
+    for name in ("finegrained", "skew", "large"):
+        wl = W.make(name)
+        T, k, E, d, h, n = wl.T, wl.k, wl.E, wl.d, wl.h, wl.n
+        gen = torch.Generator(device=dev).manual_seed(2)
+        x = torch.randn(T, d, device=dev, generator=gen).to(bf)
+        w_ug = (torch.randn(E, 2 * h, d, device=dev, generator=gen) * d ** -0.5).to(bf)
+        w_down = (torch.randn(E, h, d, device=dev, generator=gen) * h ** -0.5).to(bf)
+        ids = torch.from_numpy(wl.ids).to(dev)
+        counts, offsets = torch.empty(E, dtype=i32, device=dev), torch.empty(E, dtype=i32, device=dev)
+        ss, inv = torch.empty(n, dtype=i32, device=dev), torch.empty(n, dtype=i32, device=dev)
+        rws = torch.empty(max(L.moe_workspace_bytes(L.OP_ROUTE, T, k, E), 1), dtype=torch.uint8, device=dev)
+        xp = torch.empty(n, d, dtype=bf, device=dev)
+        status = torch.zeros(1, dtype=i32, device=dev)
+        L.moe_route_offsets(ids, T, k, E, counts, offsets, ss, inv, rws)
+        L.moe_permute(x, ss, offsets, None, T, k, E, d, xp)
+        a = torch.empty(n, h, dtype=bf, device=dev)
+        sv = torch.empty(L.moe_workspace_bytes(L.OP_SAVED, T, k, E, d, h), dtype=torch.uint8, device=dev)
+        L.moe_grouped_up_swiglu(xp, offsets, None, None, E, n, d, h, w_ug, a, sv, status)
+        dy = torch.randn(n, d, device=dev, generator=gen).to(bf)
+        du_hi, du_lo = torch.empty(n, 2 * h, dtype=bf, device=dev), torch.empty(n, 2 * h, dtype=bf, device=dev)
+        L.moe_grouped_down_dgrad_swiglu(dy, sv, offsets, None, None, E, n, d, h, w_down, du_hi, du_lo, status)
+        _, p_lo = L.saved_views(sv, n, h)
+        dwd = torch.empty(E, h, d, device=dev)
+        dwu = torch.empty(E, 2 * h, d, device=dev)
+        t_hl = queued_mean_ms(lambda: L.moe_grouped_wgrad_dual(a, p_lo, h, dy, d, dwd, du_hi, du_lo, 2 * h, xp, d,
+                                                               dwu, offsets, E, n, status))
+        t_hi = queued_mean_ms(lambda: L.moe_grouped_wgrad_dual(a, None, h, dy, d, dwd, du_hi, None, 2 * h, xp, d,
+                                                               dwu, offsets, E, n, status))
         torch.cuda.synchronize()
         assert status.item() == 0, f"device status {status.item()}"
-        rows.append(row)
-        print(json.dumps(row), flush=True)
-        del x
+        M = int(offsets[-1].item())
+        fl = 6.0 * M * d * h
+        # bytes the scheme adds per step beyond bf16 saved state: the low half of P written by the
+        # forward and read by the down wgrad, U in fp32 instead of bf16 (written by the forward,
+        # read by the dgrad), the low half of dU written by the dgrad and read by the up wgrad
+        extra = M * h * 2 * 2 + M * 2 * h * 2 * 2 + M * 2 * h * 2 * 2
+        print(json.dumps({"sweep": "precision", "workload": name, "M": M, "E": E, "d": d, "h": h,
+                          "wgrad_hi_lo_ms": t_hl, "wgrad_hi_only_ms": t_hi,
+                          "wgrad_hi_lo_useful_tflops": fl / t_hl / 1e9, "wgrad_hi_only_tflops": fl / t_hi / 1e9,
+                          "extra_state_bytes_per_step": extra,
+                          "timing": "mean of 20 launches queued in a CUDA graph after 10 warm-ups"}), flush=True)
+        del x, w_ug, w_down, xp, a, sv, dy, du_hi, du_lo, dwd, dwu
         torch.cuda.empty_cache()
-    return 0
-
-
-def run_sweep_hbm(args):
-    """HBM rates of plain PyTorch kernels on the volume the row kernels move (one 512 MiB bf16
-    buffer, the size of xp / y / dxp on the large workload): write only (fill), read only (sum),
-    a 1:1 copy, and the gathers' mix of ~8 bytes written per byte read. The gathers and combines
-    are compared with these (they are write- or read-dominated, the measured peak is a 1:1 copy).
-    Mean of 20 calls after 3 warm-ups, CUDA events."""
-    import torch
-    torch.cuda.set_device(0)
-    n = 131072 * 2048
-    a = torch.empty(n, dtype=torch.bfloat16, device="cuda").normal_()
-    b = torch.empty(n, dtype=torch.bfloat16, device="cuda")
-    small = torch.randn(n // 8, dtype=torch.bfloat16, device="cuda")
-    res = {}
-
-    def rate(fn, nbytes, name, reps=20):
-        for _ in range(3):
-            fn()
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        for _ in range(reps):
-            fn()
-        e1.record()
-        torch.cuda.synchronize()
-        ms = e0.elapsed_time(e1) / reps
-        res[name] = {"ms": round(ms, 4), "gbs": round(nbytes / ms / 1e6, 1)}
-
-    rate(lambda: b.fill_(1.0), 2 * n, "write_only_fill")
-    rate(lambda: a.sum(), 2 * n, "read_only_sum")
-    rate(lambda: b.copy_(a), 4 * n, "copy_1to1")
-    bv = b.view(8, n // 8)
-    rate(lambda: bv.copy_(small.expand(8, n // 8)), 2 * n + 2 * n // 8, "write8_read1_broadcast")
-    peaks, src = load_peaks()
-    print(json.dumps({"sweep": "hbm", "bytes_per_buffer": 2 * n, "rates": res,
-                      "measured_copy_peak_gbs": peaks.get("hbm_gbs"), "peak_source": src}), flush=True)
     return 0
 
 
@@ -977,12 +1077,10 @@ def main():
         return run_sweep_histogram(args)
     if args.sweep == "configs":
         return run_sweep_configs(args)
-    if args.sweep == "partition":
-        return run_sweep_partition(args)
-    if args.sweep == "hbm":
-        return run_sweep_hbm(args)
     if args.sweep == "oracle":
         return run_sweep_oracle(args)
+    if args.sweep == "precision":
+        return run_sweep_precision(args)
     return run_ours(args)
 
 

@@ -243,6 +243,21 @@ moe_status_t moe_grouped_wgrad(const moe_bf16* p_hi, const moe_bf16* p_lo, int p
                                int cap, float* dw, int32_t* dev_status, moe_stream_t stream);
 
 /*
+ * moe_grouped_wgrad_dual -- two independent moe_grouped_wgrad problems over the same experts and
+ * rows (the down projection's dW_down = P^T dy and the up/gate projection's dW_ug = dU^T xp of one
+ * backward, Eq. 15 wgrad / Table 15) computed by one persistent launch: the second problem's
+ * tiles follow the first's, so the two gradients share one pipeline fill and one tail. Each
+ * problem's arguments mean what they mean for moe_grouped_wgrad; results are bit-identical to
+ * two moe_grouped_wgrad calls. p1_lo and p2_lo must both be given or both be NULL.
+ */
+moe_status_t moe_grouped_wgrad_dual(const moe_bf16* p1_hi, const moe_bf16* p1_lo, int p1_cols,
+                                    const moe_bf16* q1, int q1_cols, float* dw1,
+                                    const moe_bf16* p2_hi, const moe_bf16* p2_lo, int p2_cols,
+                                    const moe_bf16* q2, int q2_cols, float* dw2,
+                                    const int32_t* offsets, int E, int cap, int32_t* dev_status,
+                                    moe_stream_t stream);
+
+/*
  * moe_unpermute_combine -- atomic-free weighted combine through the inverse map ("grouped_mm"
  * agent doc: the scatter-back becomes a gather plus a reduction):
  *     out[t] = sum_{j : inv_map[t*top_k+j] >= 0} w[t,j] * y[inv_map[t*top_k+j]]
@@ -296,7 +311,9 @@ moe_status_t moe_loop_swiglu_fwd(const moe_bf16* xp, const int32_t* offsets, int
  *  exceeds MOE_NOALLOC_ROUTE_SCRATCH_BYTES.
  *  Calls no cudaMalloc or cudaFree. The first call on each device looks up the array's device
  *  address (cudaGetSymbolAddress) with that device current; make that first call before any
- *  stream capture. Every call shares the one array and every call rewrites each entry before it
+ *  stream capture. The address is kept per device together with the device's current context
+ *  and looked up again when that context changes (after cudaDeviceReset the array may move),
+ *  so the first call after such a change is a set-up call too. Every call shares the one array and every call rewrites each entry before it
  *  reads it, so nothing has to start at zero; but two calls that overlap on the GPU (different
  *  streams, or different host threads) race on it and give wrong results.
  */

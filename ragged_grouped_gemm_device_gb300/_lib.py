@@ -40,6 +40,7 @@ SIGNATURES = {
     "moe_routing_weight_grad": (_I, [_P, _P, _I, _I, _I, _P, _P]),
     "moe_grouped_up_dgrad": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P]),
     "moe_grouped_wgrad": (_I, [_P, _P, _I, _P, _I, _P, _I, _I, _P, _P, _P]),
+    "moe_grouped_wgrad_dual": (_I, [_P, _P, _I, _P, _I, _P, _P, _P, _I, _P, _I, _P, _P, _I, _I, _P, _P]),
     "moe_route_offsets_noalloc": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P]),
     "moe_status_string": (ctypes.c_char_p, [_I]),
     "moe_last_cuda_error": (ctypes.c_char_p, []),
@@ -180,6 +181,13 @@ def moe_grouped_wgrad(p_hi, p_lo, p_cols, q, q_cols, offsets, E, cap, dw, dev_st
     _check("moe_grouped_wgrad", load().moe_grouped_wgrad(
         _ptr(p_hi), _ptr(p_lo), p_cols, _ptr(q), q_cols, _ptr(offsets), E, cap, _ptr(dw), _ptr(dev_status),
         _stream(stream)))
+
+
+def moe_grouped_wgrad_dual(p1_hi, p1_lo, p1_cols, q1, q1_cols, dw1, p2_hi, p2_lo, p2_cols, q2, q2_cols, dw2,
+                           offsets, E, cap, dev_status=None, stream=None):
+    _check("moe_grouped_wgrad_dual", load().moe_grouped_wgrad_dual(
+        _ptr(p1_hi), _ptr(p1_lo), p1_cols, _ptr(q1), q1_cols, _ptr(dw1), _ptr(p2_hi), _ptr(p2_lo), p2_cols,
+        _ptr(q2), q2_cols, _ptr(dw2), _ptr(offsets), E, cap, _ptr(dev_status), _stream(stream)))
 
 
 def saved_views(saved, cap, h):

@@ -102,47 +102,13 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
-// The same copy delivered to the same shared-memory offset in every CTA of `cta_mask` (this
-// GPU's memory only); each destination CTA's mbarrier at offset `bar` receives the bytes.
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* map, int c0, int c1,
-                                               uint32_t bar, uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar), "h"(cta_mask)
-      : "memory");
-}
-
-__device__ __forceinline__ void tma_load_3d_mc(uint32_t dst, const CUtensorMap* map, int c0, int c1,
-                                               int c2, uint32_t bar, uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar), "h"(cta_mask)
-      : "memory");
-}
-
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
-__device__ __forceinline__ uint32_t cluster_id_x() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
-  return r;
-}
-
-__device__ __forceinline__ uint32_t nclusters_x() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
-  return r;
-}
-
-// Every thread of every CTA of the cluster arrives, then waits for all of them.
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+// Untiled bulk copy global -> shared of `bytes` (a multiple of 16; both addresses 16-byte
+// aligned), completing on the mbarrier `bar` like the tensor loads.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   dst),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+               : "memory");
 }
 
 // Shared -> global tensor store (clipped at the tensor's bounds), tracked by a bulk group.
@@ -232,13 +198,26 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
                : "memory");
 }
 
-// As mma_commit, arriving on the mbarrier at offset `bar` of every CTA in `cta_mask`.
-__device__ __forceinline__ void mma_commit_mc(uint32_t bar, uint16_t cta_mask) {
+// Block-scaled D[tmem] (+)= (A * SA) * (B * SB)^T, kind::mxf8f6f4 with one E8M0 scale per 32
+// elements of K (scale_vec::1X): A and B from shared-memory descriptors, the scales of A's
+// rows and B's rows from tensor memory at sfa / sfb; the instruction descriptor's scale ids
+// pick the byte of each 32-bit scale word (the K-step within a 4-step chunk).
+__device__ __forceinline__ void mma_mxf8_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
   asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(bar),
-      "h"(cta_mask)
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
       : "memory");
+}
+
+// Shared -> tensor memory copy of 32 rows x 128 bits, replicated into the four lane quadrants:
+// row i of the source lands in lane i of every quadrant, 4 consecutive columns from `taddr`.
+// Ordered before the tcgen05.mma instructions this thread issues after it.
+__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 
 // 32 lanes x 16 columns of 32-bit words: thread i of the warp gets lane (base lane + i).
@@ -283,6 +262,21 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
          (static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16) |
          (static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
 }
+
+// Shared-memory descriptor of an unswizzled region of 16-byte rows stored back to back (the
+// 8-row core matrices 128 bytes apart in both directions), for tcgen05.cp.
+__device__ __forceinline__ uint64_t smem_desc_rows16(uint32_t saddr) {
+  return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>(128 >> 4) << 16) |
+         (static_cast<uint64_t>(128 >> 4) << 32) | (1ull << 46);
+}
+
+// Instruction descriptor for kind::mxf8f6f4 with block scaling: E4M3 A and B (format 0), both
+// K-major, fp32 accumulator (implied), E8M0 scales (bit 23), N, M; the scale-id fields (bits
+// 29-30 for A, 4-5 for B) are or-ed in per K-step.
+__host__ __device__ constexpr uint32_t idesc_mxf8_e4m3(int M, int N) {
+  return ((static_cast<uint32_t>(N) >> 3) << 17) | (1u << 23) | ((static_cast<uint32_t>(M) >> 4) << 24);
+}
+__host__ __device__ constexpr uint32_t idesc_sf_ids(uint32_t ks) { return (ks << 29) | (ks << 4); }
 
 // Instruction descriptor for kind::f16: fp32 accumulator, bf16 A and B, operand majors, N, M.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_major,

@@ -6,9 +6,9 @@
 // memory, derives each expert's row segment and 128-row tile count, and prefix-sums the tile
 // counts; a tile index then maps to (expert, row block, column block) by binary search. The
 // grid is one CTA per SM; CTA c takes tiles c, c + grid, ... ("thread blocks take tiles in
-// turn"). The wgrad modes launch as clusters of two: cluster c takes pair tiles c, c +
-// clusters, ..., a pair tile being two 128-row tiles that share their B operand, which the two
-// CTAs load half each and multicast to both. The host never learns M.
+// turn"). The host never learns M. A wgrad launch may carry two independent gradients over the
+// same experts (the down and the up/gate projection's): the second one's tiles follow the
+// first's in the same tile sequence, so one persistent launch covers both.
 //
 // Roles (352 threads, warp-specialised):
 //   warp 0      TMA producer of the A operand: 128B-swizzled tiles into a 4-stage
@@ -58,6 +58,14 @@ constexpr int CTL_BYTES = 256;
 // 32-row x 16-column bf16 boxes (dgrad)
 constexpr int STAGE_OUT_BYTES = 32 * 16 * 4;
 constexpr int STAGING_BYTES = EPI_WARPS * STAGE_OUT_BYTES;
+// MXFP8 modes: per stage, the scale atoms of A (512 bytes) and of B's two 128-row halves
+// (2 x 512); in tensor memory each stage's scales take 12 columns of a 16-column slot after
+// the (single) accumulator
+constexpr int SF_STAGE_BYTES = 1536;
+constexpr int SF_RING_BYTES = STAGES * SF_STAGE_BYTES;
+constexpr int SF_TMEM_COL = 256;
+constexpr int MX_BK = 128;                    // K elements per MXFP8 stage (128 bytes of E4M3)
+constexpr int MX_UK = 32;                     // K of one block-scaled MMA
 
 struct Ctl {
   uint64_t full[STAGES];
@@ -71,28 +79,27 @@ struct Ctl {
 static_assert(sizeof(Ctl) <= CTL_BYTES, "control block too large");
 
 constexpr size_t smem_bytes_for(int E) {
-  return 1024 + static_cast<size_t>(RING_BYTES) + STAGING_BYTES + CTL_BYTES +
+  return 1024 + static_cast<size_t>(RING_BYTES) + SF_RING_BYTES + STAGING_BYTES + CTL_BYTES +
          2 * sizeof(int) * static_cast<size_t>(E + 2);
 }
 
 template <int MODE>
 struct ModeTraits {
+  static constexpr bool mx = MODE >= MODE_UP_SWIGLU_MX;
+  // the bf16 mode whose tile shape and epilogue this mode has
+  static constexpr int epi = mx ? MODE - MODE_UP_SWIGLU_MX : MODE;
   static constexpr bool wgrad = (MODE == MODE_WGRAD || MODE == MODE_WGRAD_BF16);
   static constexpr bool a_mn = wgrad;
   static constexpr bool b_mn = (MODE == MODE_PLAIN_BF16 || wgrad);
-  static constexpr int out_cols_per_tile = (MODE == MODE_UP_SWIGLU) ? 128 : BN;
+  static constexpr int out_cols_per_tile = (epi == MODE_UP_SWIGLU) ? 128 : BN;
+  // accumulators in tensor memory: two (a tile's epilogue overlaps the next tile's main loop),
+  // one in the MXFP8 modes, whose scale slots take the other half of the 512 columns
+  static constexpr int nacc = mx ? 1 : 2;
+  static constexpr int bk = mx ? MX_BK : BK;  // K elements per stage
   // MODE_WGRAD stages hold A high, A low and B: 64 KB, three of them; the others 48 KB, four
   static constexpr int a_parts = (MODE == MODE_WGRAD) ? 2 : 1;
   static constexpr int stage_bytes = a_parts * A_BYTES + B_BYTES;
   static constexpr int stages = RING_BYTES / stage_bytes;
-  // Cluster pairs: two CTAs take two row tiles that share the B tile (row tiles 2j and 2j+1 of
-  // one expert, or of one expert's gradient); each loads half of B and multicasts it to both,
-  // so each SM pulls a third fewer operand bytes. An expert with an odd number of row tiles
-  // leaves one CTA of its last pair idle, which cost more than the saved bytes in the
-  // row-grouped modes (measured on the large workload), so only the wgrad modes pair up: a
-  // gradient's row tiles come in even numbers whenever the width is a multiple of 256.
-  static constexpr bool pair = wgrad;
-  static_assert(pair == wgrad, "the producer pairs exactly the wgrad modes");
   // A and B parts of each stage loaded by two producer threads (see the producer role)
   static constexpr bool split_producer = true;
 };
@@ -106,36 +113,41 @@ struct Tile {
   int n0;       // first output column
   int kblocks;  // K blocks of 64
   int kvalid;   // wgrad: contraction length M_e
-  bool active;  // cluster pairs: false when this CTA's half of the pair has no rows
+  int prob;     // wgrad: 0 for the first gradient of the launch, 1 for the second
 };
 
 struct Sched {
   const int* offs;  // offs[e] = first row of expert e, offs[E] = end (E+1 entries)
   const int* pre;   // row-grouped: prefix of 128-row tiles, E+1 entries
   int E;
-  int nt;           // column tiles per problem
-  int mt;           // wgrad: row tiles per expert gradient
-  int mdim;         // wgrad: rows of each expert's gradient
+  int nt;           // column tiles per problem (wgrad: of the first gradient)
+  int mt;           // wgrad: row tiles per expert gradient (first gradient)
+  int nt2, mt2;     // wgrad: the same for the second gradient (0 without one)
+  int total0;       // wgrad: tiles of the first gradient
   int kblocks;      // row-grouped: K blocks
-  int total;        // tiles (pair tiles for cluster pairs)
+  int total;        // tiles
 };
 
 template <int MODE>
-__device__ __forceinline__ Tile decode_tile(const Sched& s, int t, int rank) {
+__device__ __forceinline__ Tile decode_tile(const Sched& s, int t) {
   Tile ti;
-  ti.active = true;
+  ti.prob = 0;
   if constexpr (ModeTraits<MODE>::wgrad) {
-    // (expert, row tile, column tile); with cluster pairs the row index counts pairs of row
-    // tiles and this CTA takes row tile 2 * pair + rank
-    constexpr bool P = ModeTraits<MODE>::pair;
-    const int mp = P ? (s.mt + 1) / 2 : s.mt;
-    const int per = mp * s.nt;
-    ti.e = t / per;
-    const int r = t - ti.e * per;
-    const int mi = r / s.nt;
-    ti.m0 = (P ? 2 * mi + rank : mi) * BM;
-    ti.active = ti.m0 < s.mdim;
-    ti.n0 = (r - mi * s.nt) * BN;
+    // the first gradient's tiles, then the second's; within a gradient (expert, row tile,
+    // column tile), column tile fastest: the CTAs in flight share an expert's A column slice
+    // and its rows of B, which stay in L2
+    int tt = t;
+    if (tt >= s.total0) {
+      tt -= s.total0;
+      ti.prob = 1;
+    }
+    const int nt = ti.prob ? s.nt2 : s.nt;
+    const int per = (ti.prob ? s.mt2 : s.mt) * nt;
+    ti.e = tt / per;
+    const int r = tt - ti.e * per;
+    const int mi = r / nt;
+    ti.m0 = mi * BM;
+    ti.n0 = (r - mi * nt) * BN;
     ti.row0 = s.offs[ti.e];
     ti.kvalid = s.offs[ti.e + 1] - ti.row0;
     ti.kblocks = (ti.kvalid + BK - 1) / BK;
@@ -143,7 +155,7 @@ __device__ __forceinline__ Tile decode_tile(const Sched& s, int t, int rank) {
     ti.g = 0;
   } else {
     // expert e owns tiles [pre[e]*nt, pre[e+1]*nt): largest e with pre[e] <= t/nt (experts
-    // without tiles have pre[e] == pre[e+1]); pre counts 128-row tiles (pairs with clusters)
+    // without tiles have pre[e] == pre[e+1]); pre counts 128-row tiles
     const int nt = s.nt;
     const int gq = t / nt;
     int lo = 0, hi = s.E;
@@ -164,16 +176,8 @@ __device__ __forceinline__ Tile decode_tile(const Sched& s, int t, int rank) {
     const int m_local = grp * RASTER_M + within % gm;
     const int n = within / gm;
     ti.g = s.pre[lo] + m_local;
-    if constexpr (ModeTraits<MODE>::pair) {
-      const int mloc = 2 * m_local + rank;
-      const int me = s.offs[lo + 1] - s.offs[lo];
-      ti.row0 = s.offs[lo] + mloc * BM;
-      ti.rows = min(BM, me - mloc * BM);
-      ti.active = mloc * BM < me;
-    } else {
-      ti.row0 = s.offs[lo] + m_local * BM;
-      ti.rows = min(BM, s.offs[lo + 1] - ti.row0);
-    }
+    ti.row0 = s.offs[lo] + m_local * BM;
+    ti.rows = min(BM, s.offs[lo + 1] - ti.row0);
     ti.n0 = n * ModeTraits<MODE>::out_cols_per_tile;
     ti.m0 = 0;
     ti.kblocks = s.kblocks;
@@ -213,11 +217,7 @@ __device__ __forceinline__ void st_global_v4(void* p, uint32_t a, uint32_t b, ui
 
 template <int MODE>
 __global__ void __launch_bounds__(THREADS, 1)
-    grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
-                        const __grid_constant__ CUtensorMap map_a_lo,
-                        const __grid_constant__ CUtensorMap map_b,
-                        const __grid_constant__ CUtensorMap map_out,
-                        const __grid_constant__ CUtensorMap map_out2, const GemmArgs args) {
+    grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs args) {
   constexpr int NST = ModeTraits<MODE>::stages;
   constexpr int SB = ModeTraits<MODE>::stage_bytes;
   constexpr int APARTS = ModeTraits<MODE>::a_parts;
@@ -225,9 +225,13 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* stages = smem;
-  uint8_t* staging = smem + RING_BYTES;
-  Ctl* ctl = reinterpret_cast<Ctl*>(smem + RING_BYTES + STAGING_BYTES);
-  int* offs = reinterpret_cast<int*>(smem + RING_BYTES + STAGING_BYTES + CTL_BYTES);
+  uint8_t* sf_ring = smem + RING_BYTES;  // MXFP8 scale atoms, one slot per stage
+  uint8_t* staging = smem + RING_BYTES + SF_RING_BYTES;
+  Ctl* ctl = reinterpret_cast<Ctl*>(smem + RING_BYTES + SF_RING_BYTES + STAGING_BYTES);
+  int* offs = reinterpret_cast<int*>(smem + RING_BYTES + SF_RING_BYTES + STAGING_BYTES + CTL_BYTES);
+  constexpr int EPI = ModeTraits<MODE>::epi;
+  constexpr int NACC = ModeTraits<MODE>::nacc;
+  constexpr bool MX = ModeTraits<MODE>::mx;
   const int E = args.E;
   int* pre = offs + (E + 1);
 
@@ -260,22 +264,25 @@ __global__ void __launch_bounds__(THREADS, 1)
   sc.E = E;
   if constexpr (ModeTraits<MODE>::wgrad) {
     sc.mt = (args.Mdim + BM - 1) / BM;
-    sc.mdim = args.Mdim;
     sc.nt = (args.N + BN - 1) / BN;
+    const bool two = args.nprob == 2;
+    sc.mt2 = two ? (args.Mdim2 + BM - 1) / BM : 0;
+    sc.nt2 = two ? (args.N2 + BN - 1) / BN : 0;
     sc.kblocks = 0;
-    sc.total = E * (ModeTraits<MODE>::pair ? (sc.mt + 1) / 2 : sc.mt) * sc.nt;
+    sc.total0 = E * sc.mt * sc.nt;
+    sc.total = sc.total0 + E * sc.mt2 * sc.nt2;
   } else {
     sc.mt = 0;
-    sc.mdim = 0;
+    sc.mt2 = sc.nt2 = sc.total0 = 0;
     sc.nt = (args.N + ModeTraits<MODE>::out_cols_per_tile - 1) / ModeTraits<MODE>::out_cols_per_tile;
-    sc.kblocks = (args.K + BK - 1) / BK;
+    sc.kblocks = (args.K + ModeTraits<MODE>::bk - 1) / ModeTraits<MODE>::bk;
     if (warp == 0) {
       int carry = 0;
       if (lane == 0) pre[0] = 0;
       for (int base = 0; base < E; base += 32) {
         const int e = base + lane;
         const int mt_e = (e < E) ? (offs[e + 1] - offs[e] + BM - 1) / BM : 0;
-        int v = ModeTraits<MODE>::pair ? (mt_e + 1) / 2 : mt_e;
+        int v = mt_e;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
           const int nb = __shfl_up_sync(0xffffffffu, v, o);
@@ -291,7 +298,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (tid == 0) {
     for (int s = 0; s < NST; ++s) {
       mbar_init(smem_u32(&ctl->full[s]), ModeTraits<MODE>::split_producer ? 2 : 1);
-      mbar_init(smem_u32(&ctl->empty[s]), ModeTraits<MODE>::pair ? 2 : 1);
+      mbar_init(smem_u32(&ctl->empty[s]), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&ctl->tfull[b]), 1);
@@ -300,9 +307,14 @@ __global__ void __launch_bounds__(THREADS, 1)
     mbar_init(smem_u32(&ctl->done), 1);
     ctl->abort_flag = 0;
     fence_mbar_init();
-    prefetch_tmap(&map_a);
-    if (APARTS == 2) prefetch_tmap(&map_a_lo);
-    prefetch_tmap(&map_b);
+    prefetch_tmap(&maps.a);
+    if (APARTS == 2) prefetch_tmap(&maps.a_lo);
+    prefetch_tmap(&maps.b);
+    if (ModeTraits<MODE>::wgrad && args.nprob == 2) {
+      prefetch_tmap(&maps.a2);
+      if (APARTS == 2) prefetch_tmap(&maps.a_lo2);
+      prefetch_tmap(&maps.b2);
+    }
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(&ctl->tmem_base), TMEM_COLS);
@@ -311,18 +323,15 @@ __global__ void __launch_bounds__(THREADS, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  // the peer's barriers must exist before any multicast or remote arrive can reach them
-  if constexpr (ModeTraits<MODE>::pair) cluster_sync_all();
   if constexpr (!ModeTraits<MODE>::wgrad) sc.total = pre[E] * sc.nt;
-  constexpr bool PAIR = ModeTraits<MODE>::pair;
-  const int rank = PAIR ? static_cast<int>(cluster_ctarank()) : 0;
-  const int t_first = PAIR ? static_cast<int>(cluster_id_x()) : static_cast<int>(blockIdx.x);
-  const int t_step = PAIR ? static_cast<int>(nclusters_x()) : static_cast<int>(gridDim.x);
+  const int t_first = static_cast<int>(blockIdx.x);
+  const int t_step = static_cast<int>(gridDim.x);
   const uint32_t tmem_base = ctl->tmem_base;
   volatile int* abort_flag = &ctl->abort_flag;
   const long long tmo = args.timeout_ns;
   int32_t* status = args.status;
   const uint32_t stage0 = smem_u32(stages);
+  const uint32_t sf0 = smem_u32(sf_ring);
 
   // Two producer threads fill each stage: lane 0 of warp 0 loads the A part, lane 0 of the last
   // warp the B part. Each arrives on the stage's full barrier (count 2) with the bytes it will
@@ -338,10 +347,11 @@ __global__ void __launch_bounds__(THREADS, 1)
       uint32_t it = 0;
       bool ok = true;
       for (int t = t_first; t < sc.total && ok; t += t_step) {
-        const Tile ti = decode_tile<MODE>(sc, t, rank);
+        const Tile ti = decode_tile<MODE>(sc, t);
         const int eg = ti.e + expert_base;
-        const uint32_t a_bytes = (!PAIR || ti.active) ? static_cast<uint32_t>(APARTS * A_BYTES) : 0u;
-        const uint32_t bytes = (do_a ? a_bytes : 0u) + (do_b ? static_cast<uint32_t>(B_BYTES) : 0u);
+        constexpr uint32_t A_SF = MX ? 512u : 0u, B_SF = MX ? 1024u : 0u;
+        const uint32_t bytes = (do_a ? static_cast<uint32_t>(APARTS * A_BYTES) + A_SF : 0u) +
+                               (do_b ? static_cast<uint32_t>(B_BYTES) + B_SF : 0u);
         for (int kb = 0; kb < ti.kblocks; ++kb, ++it) {
           const int s = it % NST;
           const uint32_t ph = (it / NST) & 1u;
@@ -354,44 +364,71 @@ __global__ void __launch_bounds__(THREADS, 1)
           const uint32_t sa = stage0 + s * SB;
           const uint32_t sb = sa + APARTS * A_BYTES;
           const int k0 = kb * BK;
-          // A: this CTA's own rows. The B tile is loaded whole into this CTA's shared memory,
-          // except with cluster pairs (wgrad), where this CTA loads half `rank` and multicasts it
-          // to both CTAs of the pair (multicast exists only in cluster launches). The issue path
-          // is kept straight-line: it is on the critical path of the MN-major modes.
-          if constexpr (!ModeTraits<MODE>::wgrad) {
-            if (do_a) tma_load_2d(sa, &map_a, k0, ti.row0, fb);
-          }
-          if constexpr (MODE == MODE_UP_SWIGLU) {
+          // A: this CTA's rows; B: the whole tile. The issue path is kept straight-line: it is
+          // on the critical path of the MN-major modes.
+          if constexpr (MX) {
+            // E4M3 codes, 128 bytes of K per row, and the scale atoms of this K chunk: A's by the
+            // row tile of the problem list, B's by expert and 128-row tile (gate and up halves
+            // of W_ug for the up/gate product, else two consecutive tiles of N)
+            const int kc = kb;
+            const int m0 = kb * MX_BK;
+            const uint32_t sfs = sf0 + s * SF_STAGE_BYTES;
+            if (do_a) {
+              tma_load_2d(sa, &maps.a, m0, ti.row0, fb);
+              bulk_load(sfs, args.sfa + ((args.tile_base + ti.g) * args.sf_kc + kc) * 512, 512, fb);
+            }
             if (do_b) {
-              tma_load_3d(sb, &map_b, k0, ti.n0, eg, fb);                            // gate rows
-              tma_load_3d(sb + B_BYTES / 2, &map_b, k0, args.h + ti.n0, eg, fb);     // up rows
+              const long long eb = static_cast<long long>(eg) * args.sfb_ntpad;
+              int nt0, nt1;
+              if constexpr (EPI == MODE_UP_SWIGLU) {
+                tma_load_3d(sb, &maps.b, m0, ti.n0, eg, fb);
+                tma_load_3d(sb + B_BYTES / 2, &maps.b, m0, args.h + ti.n0, eg, fb);
+                nt0 = ti.n0 / 128;
+                nt1 = (args.h + ti.n0) / 128;
+              } else {
+                tma_load_3d(sb, &maps.b, m0, ti.n0, eg, fb);  // 256 rows of B in one box
+                nt0 = ti.n0 / 128;
+                nt1 = nt0 + 1;
+              }
+              bulk_load(sfs + 512, args.sfb + ((eb + nt0) * args.sf_kc + kc) * 512, 512, fb);
+              bulk_load(sfs + 1024, args.sfb + ((eb + nt1) * args.sf_kc + kc) * 512, 512, fb);
+            }
+          } else if constexpr (!ModeTraits<MODE>::wgrad) {
+            if (do_a) tma_load_2d(sa, &maps.a, k0, ti.row0, fb);
+          }
+          if constexpr (MX) {
+          } else if constexpr (MODE == MODE_UP_SWIGLU) {
+            if (do_b) {
+              tma_load_3d(sb, &maps.b, k0, ti.n0, eg, fb);                            // gate rows
+              tma_load_3d(sb + B_BYTES / 2, &maps.b, k0, args.h + ti.n0, eg, fb);     // up rows
             }
           } else if constexpr (MODE == MODE_PLAIN_BF16) {
             if (do_b) {
 #pragma unroll
               for (int i = 0; i < BN / 64; ++i)
-                tma_load_3d(sb + i * ATOM_BYTES, &map_b, ti.n0 + 64 * i, k0, eg, fb);
+                tma_load_3d(sb + i * ATOM_BYTES, &maps.b, ti.n0 + 64 * i, k0, eg, fb);
             }
           } else if constexpr (MODE == MODE_DGRAD_SWIGLU) {
-            if (do_b) tma_load_3d(sb, &map_b, k0, ti.n0, eg, fb);  // 256 rows of W_down in one box
+            if (do_b) tma_load_3d(sb, &maps.b, k0, ti.n0, eg, fb);  // 256 rows of W_down in one box
           } else {
-            static_assert(ModeTraits<MODE>::pair, "the wgrad modes load B as cluster pairs");
+            // MN-major 64 x 64 boxes: two of A (and two of its low half), four of B, from the
+            // operands of this tile's gradient
             const int rk = ti.row0 + k0;  // first contraction row of this K block
-            if (do_a && ti.active) {
+            if (do_a) {
+              const CUtensorMap* ma = ti.prob ? &maps.a2 : &maps.a;
 #pragma unroll
-              for (int i = 0; i < BM / 64; ++i) tma_load_2d(sa + i * ATOM_BYTES, &map_a, ti.m0 + 64 * i, rk, fb);
+              for (int i = 0; i < BM / 64; ++i) tma_load_2d(sa + i * ATOM_BYTES, ma, ti.m0 + 64 * i, rk, fb);
               if constexpr (APARTS == 2) {
+                const CUtensorMap* ml = ti.prob ? &maps.a_lo2 : &maps.a_lo;
 #pragma unroll
                 for (int i = 0; i < BM / 64; ++i)
-                  tma_load_2d(sa + A_BYTES + i * ATOM_BYTES, &map_a_lo, ti.m0 + 64 * i, rk, fb);
+                  tma_load_2d(sa + A_BYTES + i * ATOM_BYTES, ml, ti.m0 + 64 * i, rk, fb);
               }
             }
             if (do_b) {
+              const CUtensorMap* mb = ti.prob ? &maps.b2 : &maps.b;
 #pragma unroll
-              for (int i = 0; i < 2; ++i) {
-                const int box = 2 * rank + i;
-                tma_load_2d_mc(sb + box * ATOM_BYTES, &map_b, ti.n0 + 64 * box, rk, fb, 0x3);
-              }
+              for (int i = 0; i < BN / 64; ++i) tma_load_2d(sb + i * ATOM_BYTES, mb, ti.n0 + 64 * i, rk, fb);
             }
           }
         }
@@ -410,15 +447,12 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint32_t it = 0, acc = 0;
     bool ok = true;
     for (int t = t_first; t < sc.total && ok; t += t_step) {
-      const Tile ti = decode_tile<MODE>(sc, t, rank);
+      const Tile ti = decode_tile<MODE>(sc, t);
       if (ti.kblocks == 0) continue;
-      const uint32_t buf = acc & 1u, use = acc >> 1;
-      const bool act = !PAIR || ti.active;  // compile-time true without cluster pairs
-      if (act) {
-        ok = warp_all(mbar_wait(smem_u32(&ctl->tempty[buf]), (use & 1u) ^ 1u, abort_flag, status, tmo));
-        if (!ok) break;
-        tc_fence_after();
-      }
+      const uint32_t buf = acc % NACC, use = acc / NACC;
+      ok = warp_all(mbar_wait(smem_u32(&ctl->tempty[buf]), (use & 1u) ^ 1u, abort_flag, status, tmo));
+      if (!ok) break;
+      tc_fence_after();
       const uint32_t dtm = tmem_base + buf * BN;
       for (int kb = 0; kb < ti.kblocks; ++kb, ++it) {
         const int s = it % NST;
@@ -429,7 +463,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         uint8_t* sp = stages + s * SB;
         if constexpr (ModeTraits<MODE>::wgrad) {
           const int valid = ti.kvalid - kb * BK;
-          if (valid < BK && act) {
+          if (valid < BK) {
             // rows [valid, 64) of every 64x64 box belong to the next expert: zero them. The
             // swizzle only permutes 16-byte pieces inside a 128-byte row, so those rows are the
             // contiguous bytes [valid * 128, 8192) of each box.
@@ -442,6 +476,31 @@ __global__ void __launch_bounds__(THREADS, 1)
             fence_proxy_async_smem();
           }
           __syncwarp();
+        }
+        if constexpr (MX) {
+          if (lane == 0) {
+            // the stage's scale atoms into this stage's tensor-memory slot (A: 4 columns, B: 8),
+            // then four block-scaled MMAs of K = 32, each reading byte ks of the scale words;
+            // tcgen05.cp and tcgen05.mma from one thread execute in issue order
+            const uint32_t sa = stage0 + s * SB;
+            const uint32_t sb = sa + A_BYTES;
+            const uint32_t sfs = sf0 + s * SF_STAGE_BYTES;
+            const uint32_t sft = tmem_base + SF_TMEM_COL + s * 16;
+            tmem_cp_32x128b_x4(sft, smem_desc_rows16(sfs));
+            tmem_cp_32x128b_x4(sft + 4, smem_desc_rows16(sfs + 512));
+            tmem_cp_32x128b_x4(sft + 8, smem_desc_rows16(sfs + 1024));
+            constexpr uint32_t idesc_mx = idesc_mxf8_e4m3(BM, BN);
+#pragma unroll
+            for (int ks = 0; ks < MX_BK / MX_UK; ++ks) {
+              const uint64_t ad = smem_desc_sw128(sa + ks * MX_UK, 16, 1024);
+              const uint64_t bd = smem_desc_sw128(sb + ks * MX_UK, 16, 1024);
+              mma_mxf8_ss(dtm, ad, bd, idesc_mx | idesc_sf_ids(static_cast<uint32_t>(ks)), sft, sft + 4,
+                          (kb | ks) != 0 ? 1u : 0u);
+            }
+            mma_commit(smem_u32(&ctl->empty[s]));
+          }
+          __syncwarp();
+          continue;
         }
         if (lane == 0) {
           const uint32_t sa = stage0 + s * SB;
@@ -457,21 +516,18 @@ __global__ void __launch_bounds__(THREADS, 1)
               const uint64_t bd = ModeTraits<MODE>::b_mn
                                       ? smem_desc_sw128(sb + ks * (UK * 128), ATOM_BYTES, 1024)
                                       : smem_desc_sw128(sb + ks * (UK * 2), 16, 1024);
-              if (act) mma_bf16_ss(dtm, ad, bd, idesc, (kb | ks | part) != 0 ? 1u : 0u);
+              mma_bf16_ss(dtm, ad, bd, idesc, (kb | ks | part) != 0 ? 1u : 0u);
             }
           }
-          // release the stage (for cluster pairs: in both CTAs, whose producers refill it)
-          if constexpr (PAIR) mma_commit_mc(smem_u32(&ctl->empty[s]), 0x3);
-          else mma_commit(smem_u32(&ctl->empty[s]));
+          // release the stage to the producers once these MMAs have read it
+          mma_commit(smem_u32(&ctl->empty[s]));
         }
         __syncwarp();
       }
       if (!ok) break;
-      if (act) {
-        if (lane == 0) mma_commit(smem_u32(&ctl->tfull[buf]));
-        __syncwarp();
-        ++acc;
-      }
+      if (lane == 0) mma_commit(smem_u32(&ctl->tfull[buf]));
+      __syncwarp();
+      ++acc;
     }
     // every MMA this thread issued must finish before tensor memory is released
     if (lane == 0) mma_commit(smem_u32(&ctl->done));
@@ -485,16 +541,18 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint32_t acc = 0;
     uint32_t box_ctr = 0;             // dgrad: staging boxes this warp has stored
     for (int t = t_first; t < sc.total; t += t_step) {
-      const Tile ti = decode_tile<MODE>(sc, t, rank);
-      if (PAIR && !ti.active) continue;
+      const Tile ti = decode_tile<MODE>(sc, t);
+      // wgrad: the gradient this tile belongs to
+      [[maybe_unused]] const int gN = ti.prob ? args.N2 : args.N;
+      [[maybe_unused]] const int gM = ti.prob ? args.Mdim2 : args.Mdim;
       if constexpr (ModeTraits<MODE>::wgrad) {
         if (ti.kblocks == 0) {
           // empty expert: its gradient is zero
           const int mrow = ti.m0 + r_in;
-          if (mrow < args.Mdim) {
-            float* dst = reinterpret_cast<float*>(args.out) +
-                         (static_cast<long long>(ti.e + expert_base) * args.Mdim + mrow) * args.ldo;
-            for (int c = ti.n0 + half * (BN / 2); c < min(ti.n0 + (half + 1) * (BN / 2), args.N); c += 4)
+          if (mrow < gM) {
+            float* dst = reinterpret_cast<float*>(ti.prob ? args.out_b : args.out) +
+                         (static_cast<long long>(ti.e + expert_base) * gM + mrow) * (ti.prob ? args.ldo_b : args.ldo);
+            for (int c = ti.n0 + half * (BN / 2); c < min(ti.n0 + (half + 1) * (BN / 2), gN); c += 4)
               *reinterpret_cast<float4*>(dst + c) = make_float4(0.f, 0.f, 0.f, 0.f);
           }
           continue;
@@ -503,7 +561,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       // dgrad: the saved U does not depend on the accumulator, so this warp requests its first
       // chunk before waiting for the tile. (An L2 prefetch of the next tile's U measured slower.)
       float4 gcur[4], ucur[4];
-      if constexpr (MODE == MODE_DGRAD_SWIGLU) {
+      if constexpr (EPI == MODE_DGRAD_SWIGLU) {
         const int h16 = (args.h + 15) >> 4;
         const int cw = BN / 32;  // 16-column chunks per warp
         const int c0 = (ti.n0 >> 4) + half * cw;
@@ -522,12 +580,12 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
         }
       }
-      const uint32_t buf = acc & 1u, use = acc >> 1;
+      const uint32_t buf = acc % NACC, use = acc / NACC;
       if (!warp_all(mbar_wait(smem_u32(&ctl->tfull[buf]), use & 1u, abort_flag, status, tmo))) break;
       tc_fence_after();
       const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * BN;
 
-      if constexpr (MODE == MODE_UP_SWIGLU) {
+      if constexpr (EPI == MODE_UP_SWIGLU) {
         const bool rv = r_in < ti.rows;
         const long long row = ti.row0 + r_in;
         const int h = args.h;
@@ -595,7 +653,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           process(c + 1, gb, ub);
           if (more) tmem_ld_wait2(ga, ua);
         }
-      } else if constexpr (MODE == MODE_PLAIN_BF16) {
+      } else if constexpr (EPI == MODE_PLAIN_BF16) {
         const bool rv = r_in < ti.rows;
         const long long row = ti.row0 + r_in;
         bf16* orow = reinterpret_cast<bf16*>(args.out) + row * args.ldo;
@@ -639,7 +697,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           store_pair(c + 2, vc, vd);
           if (more) tmem_ld_wait2(va, vb);
         }
-      } else if constexpr (MODE == MODE_DGRAD_SWIGLU) {
+      } else if constexpr (EPI == MODE_DGRAD_SWIGLU) {
         const bool rv = r_in < ti.rows;
         const long long row = ti.row0 + r_in;
         const int h = args.h;
@@ -724,10 +782,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             ul[j] = pack_bf16x2(du[0] - bf16_lo(uh[j]), du[1] - bf16_hi(uh[j]));
           }
           if (slab_full && two) {
-            stage_store(gh, &map_out, col);
-            stage_store(uh, &map_out, h + col);
-            stage_store(gl, &map_out2, col);
-            stage_store(ul, &map_out2, h + col);
+            stage_store(gh, &maps.out, col);
+            stage_store(uh, &maps.out, h + col);
+            stage_store(gl, &maps.out2, col);
+            stage_store(ul, &maps.out2, h + col);
             return;
           }
           if (args.vec32) {
@@ -793,14 +851,15 @@ __global__ void __launch_bounds__(THREADS, 1)
         uint8_t* sbuf = staging + (warp - 2) * STAGE_OUT_BYTES;
         const uint32_t sbuf_addr = smem_u32(sbuf);
         const int sw = (lane >> 1) & 3;
-        const bool rows_in = ti.m0 + q * 32 < args.Mdim;  // warp-uniform
+        const bool rows_in = ti.m0 + q * 32 < gM;  // warp-uniform
+        const CUtensorMap* mo = ti.prob ? &maps.out2 : &maps.out;
 #pragma unroll 1
         for (int c = half * (BN / 32); c < (half + 1) * (BN / 32); ++c) {
           uint32_t v[16];
           tmem_ld16(tb + c * 16, v);
           tmem_ld_wait(v);
           // a box that would start past the gradient's last row or column is not stored
-          if (!rows_in || ti.n0 + c * 16 >= args.N) continue;
+          if (!rows_in || ti.n0 + c * 16 >= gN) continue;
           if (lane == 0) bulk_wait_group_read0();  // the previous chunk has left the buffer
           __syncwarp();
 #pragma unroll
@@ -810,7 +869,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            tma_store_3d(&map_out, sbuf_addr, ti.n0 + c * 16, ti.m0 + q * 32, ti.e + expert_base);
+            tma_store_3d(mo, sbuf_addr, ti.n0 + c * 16, ti.m0 + q * 32, ti.e + expert_base);
             bulk_commit_group();
           }
         }
@@ -822,11 +881,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 
   // ---- teardown: every role has finished (or given up); release tensor memory
-  if ((ModeTraits<MODE>::wgrad || MODE == MODE_DGRAD_SWIGLU) && warp >= 2 && lane == 0) bulk_wait_group0();
+  if ((ModeTraits<MODE>::wgrad || ModeTraits<MODE>::epi == MODE_DGRAD_SWIGLU) && warp >= 2 && lane == 0)
+    bulk_wait_group0();
   tc_fence_before();
   __syncthreads();
-  // neither CTA of a pair leaves while the other may still write to its shared memory
-  if constexpr (ModeTraits<MODE>::pair) cluster_sync_all();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, TMEM_COLS);
@@ -854,42 +912,15 @@ EncodeTiledFn encode_fn() {
 }
 
 template <int MODE>
-moe_status_t launch_mode(const CUtensorMap& a, const CUtensorMap& a_lo, const CUtensorMap& b,
-                         const CUtensorMap& out, const CUtensorMap& out2, const GemmArgs& args,
-                         long long max_tiles, cudaStream_t stream) {
+moe_status_t launch_mode(const GemmMaps& maps, const GemmArgs& args, long long max_tiles,
+                         cudaStream_t stream) {
   const size_t smem = smem_bytes_for(args.E);
   const cudaError_t attr_err = ensure_max_dynamic_smem(
       reinterpret_cast<const void*>(grouped_gemm_kernel<MODE>), static_cast<int>(smem_bytes_for(MAX_E)));
   if (attr_err != cudaSuccess) return cuda_fail(attr_err);
   const long long sms = device_sm_count();
-  if constexpr (ModeTraits<MODE>::pair) {
-    // clusters of two CTAs, as many as can be resident at once (persistent)
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.blockDim = dim3(THREADS);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    cfg.gridDim = dim3(static_cast<unsigned>(sms & ~1LL));
-    int clusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&clusters, grouped_gemm_kernel<MODE>, &cfg) != cudaSuccess ||
-        clusters < 1) {
-      cudaGetLastError();
-      clusters = static_cast<int>(sms / 2);
-    }
-    const long long pairs = std::max(1LL, std::min<long long>(clusters, (max_tiles + 1) / 2));
-    cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
-    const cudaError_t lerr = cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<MODE>, a, a_lo, b, out, out2, args);
-    if (lerr != cudaSuccess) return cuda_fail(lerr);
-  } else {
-    const int grid = static_cast<int>(std::max(1LL, std::min(sms, max_tiles)));
-    grouped_gemm_kernel<MODE><<<grid, THREADS, smem, stream>>>(a, a_lo, b, out, out2, args);
-  }
+  const int grid = static_cast<int>(std::max(1LL, std::min(sms, max_tiles)));
+  grouped_gemm_kernel<MODE><<<grid, THREADS, smem, stream>>>(maps, args);
   const cudaError_t err = cudaGetLastError();
   return err == cudaSuccess ? MOE_OK : cuda_fail(err);
 }
@@ -897,7 +928,7 @@ moe_status_t launch_mode(const CUtensorMap& a, const CUtensorMap& a_lo, const CU
 }  // namespace
 
 int gemm_tiles_n(int mode, int N) {
-  const int w = (mode == MODE_UP_SWIGLU) ? 128 : BN;
+  const int w = (mode == MODE_UP_SWIGLU || mode == MODE_UP_SWIGLU_MX) ? 128 : BN;
   return (N + w - 1) / w;
 }
 
@@ -955,25 +986,42 @@ bool make_map_weight3d(CUtensorMap* map, const void* ptr, long long E, long long
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-moe_status_t launch_grouped_gemm(int mode, const CUtensorMap& a, const CUtensorMap& a_lo,
-                                 const CUtensorMap& b, const GemmArgs& args, long long max_tiles,
-                                 cudaStream_t stream, const CUtensorMap* out,
-                                 const CUtensorMap* out2) {
+bool make_map_u8_rows2d(CUtensorMap* map, const void* ptr, long long rows, long long cols, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || rows <= 0 || cols <= 0) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols)};
+  const cuuint32_t box[2] = {128u, static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t estr[2] = {1u, 1u};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool make_map_u8_weight3d(CUtensorMap* map, const void* ptr, long long E, long long R, long long C, int box_r) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || E <= 0 || R <= 0 || C <= 0) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(C), static_cast<cuuint64_t>(R), static_cast<cuuint64_t>(E)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(C), static_cast<cuuint64_t>(R) * static_cast<cuuint64_t>(C)};
+  const cuuint32_t box[3] = {128u, static_cast<cuuint32_t>(box_r), 1u};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+moe_status_t launch_grouped_gemm(int mode, const GemmMaps& maps, const GemmArgs& args,
+                                 long long max_tiles, cudaStream_t stream) {
   if (args.E < 1 || args.E > MAX_E) return MOE_ERR_UNSUPPORTED_SHAPE;
-  const CUtensorMap& o = out ? *out : a;
-  const CUtensorMap& o2 = out2 ? *out2 : a;
   switch (mode) {
-    case MODE_UP_SWIGLU: return launch_mode<MODE_UP_SWIGLU>(a, a_lo, b, o, o2, args, max_tiles, stream);
-    case MODE_PLAIN_BF16: return launch_mode<MODE_PLAIN_BF16>(a, a_lo, b, o, o2, args, max_tiles, stream);
-    case MODE_DGRAD_SWIGLU:
-      if (!out || !out2) return MOE_ERR_INVALID_ARG;
-      return launch_mode<MODE_DGRAD_SWIGLU>(a, a_lo, b, o, o2, args, max_tiles, stream);
-    case MODE_WGRAD:
-      if (!out) return MOE_ERR_INVALID_ARG;
-      return launch_mode<MODE_WGRAD>(a, a_lo, b, o, o2, args, max_tiles, stream);
-    case MODE_WGRAD_BF16:
-      if (!out) return MOE_ERR_INVALID_ARG;
-      return launch_mode<MODE_WGRAD_BF16>(a, a_lo, b, o, o2, args, max_tiles, stream);
+    case MODE_UP_SWIGLU: return launch_mode<MODE_UP_SWIGLU>(maps, args, max_tiles, stream);
+    case MODE_PLAIN_BF16: return launch_mode<MODE_PLAIN_BF16>(maps, args, max_tiles, stream);
+    case MODE_DGRAD_SWIGLU: return launch_mode<MODE_DGRAD_SWIGLU>(maps, args, max_tiles, stream);
+    case MODE_WGRAD: return launch_mode<MODE_WGRAD>(maps, args, max_tiles, stream);
+    case MODE_WGRAD_BF16: return launch_mode<MODE_WGRAD_BF16>(maps, args, max_tiles, stream);
+    case MODE_UP_SWIGLU_MX: return launch_mode<MODE_UP_SWIGLU_MX>(maps, args, max_tiles, stream);
+    case MODE_PLAIN_MX: return launch_mode<MODE_PLAIN_MX>(maps, args, max_tiles, stream);
+    case MODE_DGRAD_SWIGLU_MX: return launch_mode<MODE_DGRAD_SWIGLU_MX>(maps, args, max_tiles, stream);
     default: return MOE_ERR_INVALID_ARG;
   }
 }

@@ -27,7 +27,23 @@ enum GemmMode : int {
   // MN-major, two MMAs per K step into one accumulator); fp32 store, zeros for empty experts.
   MODE_WGRAD = 3,
   // as MODE_WGRAD with the high half of P only (plain bf16 activations, one MMA per K step)
-  MODE_WGRAD_BF16 = 4
+  MODE_WGRAD_BF16 = 4,
+  // MXFP8 versions of the row-grouped modes (mode - MODE_UP_SWIGLU_MX is the bf16 mode whose
+  // epilogue they share): E4M3 operands, both K-major (A [cap, K] codes, B [E, N, K] codes), an
+  // E8M0 scale per 32 elements of K in 512-byte atoms (sfa by the problem list's row tile,
+  // sfb by expert and 128-row tile of N), block-scaled MMAs into one accumulator.
+  MODE_UP_SWIGLU_MX = 5,   // B = W_ug codes along d; epilogue of MODE_UP_SWIGLU
+  MODE_PLAIN_MX = 6,       // B = W^T codes [E, N, K]; epilogue of MODE_PLAIN_BF16
+  MODE_DGRAD_SWIGLU_MX = 7 // B = W_down codes along d; epilogue of MODE_DGRAD_SWIGLU
+};
+
+// The tensor maps of one launch. They travel as one __grid_constant__ kernel parameter, so the
+// kernel's TMA instructions read them from parameter space.
+struct GemmMaps {
+  CUtensorMap a, a_lo, b;     // operands; a_lo is the low half of A (MODE_WGRAD only)
+  CUtensorMap out, out2;      // TMA store maps: DGRAD_SWIGLU dU high / low; WGRAD dW of the
+                              // first / second problem
+  CUtensorMap a2, a_lo2, b2;  // WGRAD modes: operands of the second problem
 };
 
 struct GemmArgs {
@@ -67,6 +83,20 @@ struct GemmArgs {
   // unweighted, G = dy W_down^T before the routing weight), one per (column tile, warp half)
   float* dw_part;
   int dw_np;
+  // WGRAD modes: number of independent problems in the launch (1 or 2). The second one has its
+  // own operands (maps a2, a_lo2, b2), gradient shape (Mdim2 x N2), output (out_b / map out2)
+  // and shares the experts and row segments of the first; its tiles follow the first's.
+  int nprob;
+  int N2;
+  int Mdim2;
+  void* out_b;
+  long long ldo_b;
+  // MXFP8 modes: scale atoms of A (by row tile of the problem list) and of B (by expert and
+  // 128-row tile of N, sfb_ntpad tiles per expert), sf_kc 128-element chunks of K per row
+  const uint8_t* sfa;
+  const uint8_t* sfb;
+  int sf_kc;
+  int sfb_ntpad;
   int32_t* status;         // optional device status word
   long long timeout_ns;    // bound of every wait of the main loops
   // bound of the teardown waits that let this CTA's in-flight copies and MMAs finish before it
@@ -74,13 +104,11 @@ struct GemmArgs {
   long long drain_ns;
 };
 
-// Launch one persistent grouped GEMM. `a` and `b` are the operand tensor maps described with
-// each mode; `a_lo` is the low half of the A operand (WGRAD only, else ignored). `max_tiles`
-// bounds the grid (the exact tile count is only known on the device).
-moe_status_t launch_grouped_gemm(int mode, const CUtensorMap& a, const CUtensorMap& a_lo,
-                                 const CUtensorMap& b, const GemmArgs& args, long long max_tiles,
-                                 cudaStream_t stream, const CUtensorMap* out = nullptr,
-                                 const CUtensorMap* out2 = nullptr);
+// Launch one persistent grouped GEMM. `maps` holds the operand tensor maps described with each
+// mode (unused entries are ignored). `max_tiles` bounds the grid (the exact tile count is only
+// known on the device).
+moe_status_t launch_grouped_gemm(int mode, const GemmMaps& maps, const GemmArgs& args,
+                                 long long max_tiles, cudaStream_t stream);
 
 // Tensor maps (bf16, 128-byte swizzle, zero fill outside the tensor).
 //   rows2d: a [rows, cols] row-major matrix; box = 64 columns x box_rows rows.
@@ -94,6 +122,11 @@ bool make_map_weight3d(CUtensorMap* map, const void* ptr, long long E, long long
 //   32B swizzle (cols * 2 bytes a multiple of 16).
 bool make_map_rows2d_store(CUtensorMap* map, const void* ptr, long long rows, long long cols);
 bool make_map_grad3d_f32(CUtensorMap* map, const void* ptr, long long E, long long R, long long C);
+
+//   u8 maps (MXFP8 codes, 128-byte swizzle): rows2d [rows, cols] with 128-byte x box_rows boxes;
+//   weight3d [E, R, C] with 128-byte x box_r x 1 boxes.
+bool make_map_u8_rows2d(CUtensorMap* map, const void* ptr, long long rows, long long cols, int box_rows);
+bool make_map_u8_weight3d(CUtensorMap* map, const void* ptr, long long E, long long R, long long C, int box_r);
 
 int gemm_tiles_n(int mode, int N);  // column tiles of one problem
 
@@ -126,6 +159,15 @@ moe_status_t launch_pitch_repack(const void* src, void* dst, bool fp32, long lon
 // dw[s] = sum of the dw_np partials of row inv_map[s] in index order, 0 for a dropped slot.
 moe_status_t launch_routing_weight_grad(const float* part, int np, const int32_t* inv_map,
                                         int n_slots, float* dw, cudaStream_t s);
+// MXFP8 quantization (layouts in mx_quant.cu). Rows along K: with offsets, the rows p < M of a
+// problem list (scale atoms by its 128-row tiles); else `rows` rows of weights with per_expert
+// rows each (atoms by expert and 128-row tile, tiles padded to even). Columns: a weight
+// [E, R, C] quantized along R into [E, C, R] codes.
+int mx_ntpad(int N);
+int mx_kc(int K);
+moe_status_t launch_mx_quant_rows(const void* src, long long rows, int K, const int32_t* offsets, int E,
+                                  int per_expert, void* q, void* sf, int32_t* status, cudaStream_t s);
+moe_status_t launch_mx_quant_cols(const void* w, int E, int R, int C, void* q, void* sf, cudaStream_t s);
 moe_status_t launch_unpad_rows(const void* src, const int32_t* offsets, int E, int C, int cap,
                                int cols, void* dst, cudaStream_t s);
 

@@ -129,9 +129,9 @@ moe_status_t repack_weight(const void* src, void* dst, bool fp32, int E, int nsu
 moe_status_t run_up_swiglu(const GemmArgs& src, long long rows, long long tiles_bound, int E, int d,
                            int h, const void* xp, const void* w_ug, void* a_save, void* saved,
                            cudaStream_t s) {
-  CUtensorMap ma, mb;
-  if (!make_map_rows2d(&ma, xp, rows, d, 128)) return map_fail("xp");
-  if (!make_map_weight3d(&mb, w_ug, E, 2LL * h, d, 128)) return map_fail("w_ug");
+  GemmMaps m{};
+  if (!make_map_rows2d(&m.a, xp, rows, d, 128)) return map_fail("xp");
+  if (!make_map_weight3d(&m.b, w_ug, E, 2LL * h, d, 128)) return map_fail("w_ug");
   GemmArgs a = src;
   a.N = h;
   a.K = d;
@@ -144,16 +144,15 @@ moe_status_t run_up_swiglu(const GemmArgs& src, long long rows, long long tiles_
     a.ldo3 = h;
   }
   a.vec32 = (h % 16 == 0 && aligned32(a_save) && (saved == nullptr || aligned32(saved))) ? 1 : 0;
-  return launch_grouped_gemm(MODE_UP_SWIGLU, ma, ma, mb, a,
-                             tiles_bound * gemm_tiles_n(MODE_UP_SWIGLU, h), s);
+  return launch_grouped_gemm(MODE_UP_SWIGLU, m, a, tiles_bound * gemm_tiles_n(MODE_UP_SWIGLU, h), s);
 }
 
 // a7: y = A W_down.
 moe_status_t run_down(const GemmArgs& src, long long rows, long long tiles_bound, int E, int d,
                       int h, const void* a_in, const void* w_down, void* y, cudaStream_t s) {
-  CUtensorMap ma, mb;
-  if (!make_map_rows2d(&ma, a_in, rows, h, 128)) return map_fail("a");
-  if (!make_map_weight3d(&mb, w_down, E, h, d, 64)) return map_fail("w_down");
+  GemmMaps m{};
+  if (!make_map_rows2d(&m.a, a_in, rows, h, 128)) return map_fail("a");
+  if (!make_map_weight3d(&m.b, w_down, E, h, d, 64)) return map_fail("w_down");
   GemmArgs a = src;
   a.N = d;
   a.K = h;
@@ -161,17 +160,16 @@ moe_status_t run_down(const GemmArgs& src, long long rows, long long tiles_bound
   a.out = y;
   a.ldo = d;
   a.vec32 = (d % 16 == 0 && aligned32(y)) ? 1 : 0;
-  return launch_grouped_gemm(MODE_PLAIN_BF16, ma, ma, mb, a,
-                             tiles_bound * gemm_tiles_n(MODE_PLAIN_BF16, d), s);
+  return launch_grouped_gemm(MODE_PLAIN_BF16, m, a, tiles_bound * gemm_tiles_n(MODE_PLAIN_BF16, d), s);
 }
 
 // a10: dA = dy W_down^T with the SwiGLU backward -> dU high and low halves.
 moe_status_t run_down_dgrad_swiglu(const GemmArgs& src, long long rows, int E, int d, int h,
                                    const void* dy, const void* saved, const void* w_down,
                                    void* du_hi, void* du_lo, float* dw_part, cudaStream_t s) {
-  CUtensorMap ma, mb;
-  if (!make_map_rows2d(&ma, dy, rows, d, 128)) return map_fail("dy");
-  if (!make_map_weight3d(&mb, w_down, E, h, d, 256)) return map_fail("w_down");
+  GemmMaps m{};
+  if (!make_map_rows2d(&m.a, dy, rows, d, 128)) return map_fail("dy");
+  if (!make_map_weight3d(&m.b, w_down, E, h, d, 256)) return map_fail("w_down");
   GemmArgs a = src;
   a.N = h;
   a.K = d;
@@ -184,20 +182,18 @@ moe_status_t run_down_dgrad_swiglu(const GemmArgs& src, long long rows, int E, i
   a.vec32 = (h % 16 == 0 && aligned32(du_hi) && aligned32(du_lo)) ? 1 : 0;
   a.dw_part = dw_part;
   a.dw_np = route_grad_parts(h);
-  CUtensorMap mhi, mlo;
-  if (!make_map_rows2d_store(&mhi, du_hi, rows, 2LL * h)) return map_fail("du_hi");
-  if (!make_map_rows2d_store(&mlo, du_lo, rows, 2LL * h)) return map_fail("du_lo");
-  return launch_grouped_gemm(MODE_DGRAD_SWIGLU, ma, ma, mb, a,
-                             row_tiles_bound(rows, src.E) * gemm_tiles_n(MODE_DGRAD_SWIGLU, h), s,
-                             &mhi, &mlo);
+  if (!make_map_rows2d_store(&m.out, du_hi, rows, 2LL * h)) return map_fail("du_hi");
+  if (!make_map_rows2d_store(&m.out2, du_lo, rows, 2LL * h)) return map_fail("du_lo");
+  return launch_grouped_gemm(MODE_DGRAD_SWIGLU, m, a,
+                             row_tiles_bound(rows, src.E) * gemm_tiles_n(MODE_DGRAD_SWIGLU, h), s);
 }
 
 // a12: dxp = dU W_ug.
 moe_status_t run_up_dgrad(const GemmArgs& src, long long rows, int E, int d, int h,
                           const void* du_hi, const void* w_ug, void* dxp, cudaStream_t s) {
-  CUtensorMap ma, mb;
-  if (!make_map_rows2d(&ma, du_hi, rows, 2LL * h, 128)) return map_fail("dU");
-  if (!make_map_weight3d(&mb, w_ug, E, 2LL * h, d, 64)) return map_fail("w_ug");
+  GemmMaps m{};
+  if (!make_map_rows2d(&m.a, du_hi, rows, 2LL * h, 128)) return map_fail("dU");
+  if (!make_map_weight3d(&m.b, w_ug, E, 2LL * h, d, 64)) return map_fail("w_ug");
   GemmArgs a = src;
   a.N = d;
   a.K = 2 * h;
@@ -205,29 +201,62 @@ moe_status_t run_up_dgrad(const GemmArgs& src, long long rows, int E, int d, int
   a.out = dxp;
   a.ldo = d;
   a.vec32 = (d % 16 == 0 && aligned32(dxp)) ? 1 : 0;
-  return launch_grouped_gemm(MODE_PLAIN_BF16, ma, ma, mb, a,
+  return launch_grouped_gemm(MODE_PLAIN_BF16, m, a,
                              row_tiles_bound(rows, src.E) * gemm_tiles_n(MODE_PLAIN_BF16, d), s);
 }
 
-// a11 / a13: dW_e = (P_hi + P_lo)_e^T Q_e over each expert's rows.
-moe_status_t run_wgrad(const GemmArgs& src, long long rows, int E, const void* p_hi,
-                       const void* p_lo, int p_cols, const void* q, int q_cols, float* dw,
-                       cudaStream_t s) {
-  // with no rows every expert is empty: the maps then describe a one-row placeholder
+// One wgrad problem: dW_e = (P_hi + P_lo)_e^T Q_e over each expert's rows (P_lo may be null).
+struct WgradProblem {
+  const void* p_hi;
+  const void* p_lo;
+  int p_cols;
+  const void* q;
+  int q_cols;
+  float* dw;
+};
+
+// Operand and gradient maps of one problem (with no rows every expert is empty: the maps then
+// describe a one-row placeholder).
+moe_status_t wgrad_maps(const WgradProblem& w, long long rows, int E, CUtensorMap* a, CUtensorMap* a_lo,
+                        CUtensorMap* b, CUtensorMap* out) {
   const long long r = std::max(rows, 1LL);
-  CUtensorMap ma, ml, mb;
-  if (!make_map_rows2d(&ma, p_hi, r, p_cols, 64)) return map_fail("p_hi");
-  if (!make_map_rows2d(&ml, p_lo ? p_lo : p_hi, r, p_cols, 64)) return map_fail("p_lo");
-  if (!make_map_rows2d(&mb, q, r, q_cols, 64)) return map_fail("q");
+  if (!make_map_rows2d(a, w.p_hi, r, w.p_cols, 64)) return map_fail("p_hi");
+  if (!make_map_rows2d(a_lo, w.p_lo ? w.p_lo : w.p_hi, r, w.p_cols, 64)) return map_fail("p_lo");
+  if (!make_map_rows2d(b, w.q, r, w.q_cols, 64)) return map_fail("q");
+  if (!make_map_grad3d_f32(out, w.dw, E, w.p_cols, w.q_cols)) return map_fail("dw");
+  return MOE_OK;
+}
+
+long long wgrad_tiles(const WgradProblem& w, int E) {
+  return static_cast<long long>(E) * ((w.p_cols + 127) / 128) * ((w.q_cols + 255) / 256);
+}
+
+// a11 / a13: one or two wgrad problems over the same experts in one persistent launch (the
+// second one's tiles follow the first's). Both must agree on whether P has a low half.
+moe_status_t run_wgrad(const GemmArgs& src, long long rows, int E, const WgradProblem& w1,
+                       const WgradProblem* w2, cudaStream_t s) {
+  GemmMaps m{};
+  moe_status_t st = wgrad_maps(w1, rows, E, &m.a, &m.a_lo, &m.b, &m.out);
+  if (st != MOE_OK) return st;
   GemmArgs a = src;
-  a.N = q_cols;
-  a.Mdim = p_cols;
-  a.out = dw;
-  a.ldo = q_cols;
-  CUtensorMap mo;
-  if (!make_map_grad3d_f32(&mo, dw, E, p_cols, q_cols)) return map_fail("dw");
-  const long long tiles = static_cast<long long>(E) * ((p_cols + 127) / 128) * ((q_cols + 255) / 256);
-  return launch_grouped_gemm(p_lo ? MODE_WGRAD : MODE_WGRAD_BF16, ma, ml, mb, a, tiles, s, &mo);
+  a.N = w1.q_cols;
+  a.Mdim = w1.p_cols;
+  a.out = w1.dw;
+  a.ldo = w1.q_cols;
+  a.nprob = 1;
+  long long tiles = wgrad_tiles(w1, E);
+  if (w2 != nullptr) {
+    if ((w2->p_lo == nullptr) != (w1.p_lo == nullptr)) return MOE_ERR_INVALID_ARG;
+    st = wgrad_maps(*w2, rows, E, &m.a2, &m.a_lo2, &m.b2, &m.out2);
+    if (st != MOE_OK) return st;
+    a.nprob = 2;
+    a.N2 = w2->q_cols;
+    a.Mdim2 = w2->p_cols;
+    a.out_b = w2->dw;
+    a.ldo_b = w2->q_cols;
+    tiles += wgrad_tiles(*w2, E);
+  }
+  return launch_grouped_gemm(w1.p_lo ? MODE_WGRAD : MODE_WGRAD_BF16, m, a, tiles, s);
 }
 
 moe_status_t check_grouped_common(int E, int cap, int d, int h) {
@@ -487,8 +516,32 @@ moe_status_t moe_grouped_wgrad(const moe_bf16* p_hi, const moe_bf16* p_lo, int p
   if (st != MOE_OK) return st;
   GemmArgs src = base_args(E, cap, dev_status);
   src.offsets = offsets;
-  return run_wgrad(src, cap, E, p_hi, p_lo, p_cols, q, q_cols, dw,
-                   reinterpret_cast<cudaStream_t>(stream));
+  const WgradProblem w{p_hi, p_lo, p_cols, q, q_cols, dw};
+  return run_wgrad(src, cap, E, w, nullptr, reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_grouped_wgrad_dual(const moe_bf16* p1_hi, const moe_bf16* p1_lo, int p1_cols,
+                                    const moe_bf16* q1, int q1_cols, float* dw1,
+                                    const moe_bf16* p2_hi, const moe_bf16* p2_lo, int p2_cols,
+                                    const moe_bf16* q2, int q2_cols, float* dw2,
+                                    const int32_t* offsets, int E, int cap, int32_t* dev_status,
+                                    moe_stream_t stream) {
+  if (cap < 0 || E < 1 || p1_cols <= 0 || q1_cols <= 0 || p2_cols <= 0 || q2_cols <= 0)
+    return MOE_ERR_INVALID_ARG;
+  if (E > MAX_E || !dim_ok(p1_cols) || !dim_ok(q1_cols) || !dim_ok(p2_cols) || !dim_ok(q2_cols))
+    return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!p1_hi || !q1 || !dw1 || !p2_hi || !q2 || !dw2 || !offsets) return MOE_ERR_INVALID_ARG;
+  if ((p1_lo == nullptr) != (p2_lo == nullptr)) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(p1_hi) || !aligned16(p1_lo) || !aligned16(q1) || !aligned16(dw1) || !aligned16(p2_hi) ||
+      !aligned16(p2_lo) || !aligned16(q2) || !aligned16(dw2))
+    return MOE_ERR_INVALID_ARG;
+  moe_status_t st = check_device();
+  if (st != MOE_OK) return st;
+  GemmArgs src = base_args(E, cap, dev_status);
+  src.offsets = offsets;
+  const WgradProblem w1{p1_hi, p1_lo, p1_cols, q1, q1_cols, dw1};
+  const WgradProblem w2{p2_hi, p2_lo, p2_cols, q2, q2_cols, dw2};
+  return run_wgrad(src, cap, E, w1, &w2, reinterpret_cast<cudaStream_t>(stream));
 }
 
 // ------------------------------------------------------------------ composite calls
@@ -573,11 +626,11 @@ moe_status_t grouped_bwd_core(const void* dy, const void* xp, const void* a_save
     st = run_up_dgrad(src, cap, E, d, h, du_hi, w_ug, dxp, s);
     if (st != MOE_OK) return st;
   }
-  // wgrads contract over each expert's rows; empty experts get zeros
-  st = run_wgrad(src, cap, E, p_hi, cap > 0 ? p_lo : p_hi, h, dy, d, dw_down, s);
-  if (st != MOE_OK) return st;
-  return run_wgrad(src, cap, E, cap > 0 ? du_hi : a_save, cap > 0 ? du_lo : a_save, 2 * h, xp, d,
-                   dw_ug, s);
+  // both wgrads in one launch; they contract over each expert's rows, empty experts get zeros
+  // (with no rows the operands are never read: a_save stands in for the unwritten dU)
+  const WgradProblem wd{p_hi, cap > 0 ? p_lo : p_hi, h, dy, d, dw_down};
+  const WgradProblem wu{cap > 0 ? du_hi : a_save, cap > 0 ? du_lo : a_save, 2 * h, xp, d, dw_ug};
+  return run_wgrad(src, cap, E, wd, &wu, s);
 }
 
 }  // namespace

@@ -218,21 +218,48 @@ namespace {
 constexpr int NOALLOC_MAX_DEVICES = 64;
 static __device__ __align__(256) int32_t g_route_scratch[MOE_NOALLOC_ROUTE_SCRATCH_BYTES / sizeof(int32_t)];
 
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+
+// cuCtxGetCurrent through the runtime's driver entry-point query (the library does not link
+// libcuda directly)
+CtxGetCurrentFn ctx_get_current() {
+  static CtxGetCurrentFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(p);
+  });
+  return fn;
+}
+
 std::mutex g_scratch_mu;
 void* g_scratch_addr[NOALLOC_MAX_DEVICES] = {};
+CUcontext g_scratch_ctx[NOALLOC_MAX_DEVICES] = {};
 
-// Device address of g_route_scratch on the current device, looked up on first use.
+// Device address of g_route_scratch on the current device. It is looked up on the first call
+// with that device current, and looked up again whenever the device's current context is not
+// the one of the last lookup (after cudaDeviceReset the module is loaded again and the array
+// may sit at another address).
 moe_status_t route_scratch_address(void** addr) {
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return cuda_fail(err);
   if (dev < 0 || dev >= NOALLOC_MAX_DEVICES) return MOE_ERR_UNSUPPORTED_DEVICE;
+  const CtxGetCurrentFn get = ctx_get_current();
+  if (get == nullptr) return cuda_fail(cudaErrorNotSupported);
+  CUcontext ctx = nullptr;
+  if (get(&ctx) != CUDA_SUCCESS) ctx = nullptr;  // no context current yet: look up below
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (g_scratch_addr[dev] == nullptr) {
+  if (g_scratch_addr[dev] == nullptr || ctx == nullptr || g_scratch_ctx[dev] != ctx) {
     void* p = nullptr;
-    err = cudaGetSymbolAddress(&p, g_route_scratch);
+    err = cudaGetSymbolAddress(&p, g_route_scratch);  // makes the device's context current
     if (err != cudaSuccess) return cuda_fail(err);
+    if (get(&ctx) != CUDA_SUCCESS || ctx == nullptr) return cuda_fail(cudaErrorDeviceUninitialized);
     g_scratch_addr[dev] = p;
+    g_scratch_ctx[dev] = ctx;
   }
   *addr = g_scratch_addr[dev];
   return MOE_OK;

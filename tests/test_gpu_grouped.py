@@ -129,8 +129,9 @@ def test_bad_offsets_flag_and_no_work(lib):
 
 def test_single_kernel_entry_points_equal_composites(lib):
     """The per-step entry points (one kernel each) reproduce the composite forward and backward
-    bit for bit, with routing weights folded in; the bf16-only wgrad (no low half) stays within
-    the normalised tolerance."""
+    bit for bit, with routing weights folded in (the composite backward runs both wgrads in one
+    launch, as moe_grouped_wgrad_dual does); the bf16-only wgrad (no low half) stays within the
+    normalised tolerance."""
     from ragged_grouped_gemm_device_gb300 import _lib as L
     wl = W.custom(T=300, k=4, E=7, d=136, h=200, seed=31, invalid_frac=0.05, empty_experts=(3,))
     run = G.DevicePipeline(wl).route().permute()
@@ -165,6 +166,15 @@ def test_single_kernel_entry_points_equal_composites(lib):
     L.moe_grouped_wgrad(a2, p_lo, h, dy, d, run.offsets, E, n, dwd2, run.status)
     L.moe_grouped_wgrad(du_hi, du_lo, 2 * h, run.xp, d, run.offsets, E, n, dwu2, run.status)
     L.moe_grouped_wgrad(du_hi, None, 2 * h, run.xp, d, run.offsets, E, n, dwu3, run.status)
+    # both gradients from one launch, with and without the low halves
+    dwd4, dwu4 = torch.full_like(dwd1, float("nan")), torch.full_like(dwu1, float("nan"))
+    L.moe_grouped_wgrad_dual(a2, p_lo, h, dy, d, dwd4, du_hi, du_lo, 2 * h, run.xp, d, dwu4, run.offsets, E, n,
+                             run.status)
+    dwd5, dwu5 = torch.full_like(dwd1, float("nan")), torch.full_like(dwu1, float("nan"))
+    L.moe_grouped_wgrad_dual(a2, None, h, dy, d, dwd5, du_hi, None, 2 * h, run.xp, d, dwu5, run.offsets, E, n,
+                             run.status)
+    dwd6 = torch.full_like(dwd1, float("nan"))
+    L.moe_grouped_wgrad(a2, None, h, dy, d, run.offsets, E, n, dwd6, run.status)
     torch.cuda.synchronize()
     assert run.status.item() == 0
     M = int(run.offsets[-1].item())
@@ -173,6 +183,8 @@ def test_single_kernel_entry_points_equal_composites(lib):
     # saved compared as bytes: bit for bit, whatever values it holds
     assert torch.equal(sv2.view(torch.uint8), sv1.view(torch.uint8))
     assert torch.equal(dwu2, dwu1) and torch.equal(dwd2, dwd1)
+    assert torch.equal(dwu4, dwu1) and torch.equal(dwd4, dwd1)
+    assert torch.equal(dwu5, dwu3) and torch.equal(dwd5, dwd6)
     assert torch.equal(dwr2, dwr1) and torch.isfinite(dwr1).all()
     err = (dwu3 - dwu1).double().norm() / dwu1.double().norm()
     assert err <= G.REL_NORM_TOL, f"bf16-only wgrad normalised error {err:.2e}"
