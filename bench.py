@@ -469,6 +469,20 @@ def config_variants(L, names=VARIANT_CONFIGS):
                                                                a, None, None, status))
         t_b = queued_mean_ms(lambda: L.moe_padded_bmm_swiglu_fwd(xp, offsets, E, n, d, h, C, w_ug, w_down, y, bws,
                                                                   status))
+        top1 = None
+        if k == 1:
+            # the layer forward after the permute: grouped forward + combine, against the down
+            # projection writing the token rows itself
+            out = torch.empty(T, d, dtype=bf, device=dev)
+            wts = torch.from_numpy(wl.weights.reshape(-1)).to(dev)
+            t_sep = queued_mean_ms(lambda: (L.moe_grouped_swiglu_fwd(xp, offsets, ss, wts, E, n, d, h, w_ug, w_down, y,
+                                                                     a, None, None, status),
+                                            L.moe_unpermute_combine(y, inv, None, T, k, d, out)))
+            t_fus = queued_mean_ms(lambda: L.moe_grouped_swiglu_fwd_top1_combine(xp, offsets, ss, inv, wts, E, T, d, h,
+                                                                                 w_ug, w_down, out, a, None, status))
+            top1 = {"forward_then_combine_ms": round(t_sep, 4), "fused_combine_ms": round(t_fus, 4),
+                    "speedup": round(t_sep / t_fus, 3)}
+            del out, wts
         loop = lambda: L.moe_loop_swiglu_fwd(xp, offsets, E, n, d, h, w_ug, w_down, y, a, None, status)
         loop()
         torch.cuda.synchronize()
@@ -485,6 +499,8 @@ def config_variants(L, names=VARIANT_CONFIGS):
                                     "rows_multiplied": E * C, "rows_dropped": dropped},
                      "host_loop": {"ms": round(t_l, 4), "tflops": round(fl / t_l / 1e9, 1)},
                      "grouped_vs_bmm": round(t_b / t_g, 3), "grouped_vs_loop": round(t_l / t_g, 3)}
+        if top1 is not None:
+            res[name]["top1_fused_combine"] = top1
         del x, w_ug, w_down, xp, y, a, bws
         torch.cuda.empty_cache()
     return res
@@ -717,11 +733,36 @@ def run_ours(args):
         l_dev, l_wall = time_fn(lambda: L.moe_loop_swiglu_fwd(xp, offsets, E, n, d, h, w_ug, w_down, y2, a, None,
                                                               status), reps=5)
         fw = 6.0 * mdh
+        # MXFP8 variant (scaled forward and dgrad, BF16 wgrads) against the bf16 training calls:
+        # the forward includes its activation quantizations; the weight preparation (once per
+        # weight update) is timed on its own
+        mxw = torch.empty(L.moe_workspace_bytes(L.OP_MX_WEIGHTS, T, k, E, d, h), dtype=torch.uint8, device=dev)
+        mfws = torch.empty(L.moe_workspace_bytes(L.OP_MX_FWD, T, k, E, d, h), dtype=torch.uint8, device=dev)
+        mbws = torch.empty(L.moe_workspace_bytes(L.OP_MX_BWD, T, k, E, d, h), dtype=torch.uint8, device=dev)
+        bbws = torch.empty(L.moe_workspace_bytes(L.OP_BWD, T, k, E, d, h), dtype=torch.uint8, device=dev)
+        wp_ms, _ = time_fn(lambda: L.moe_mx_prepare_weights(w_ug, w_down, E, d, h, mxw))
+        mf_ms, _ = time_fn(lambda: L.moe_grouped_swiglu_fwd_mxfp8(xp, offsets, sorted_src, wts, E, n, d, h, mxw, y2,
+                                                                 a, saved, mfws, status))
+        mb_ms, _ = time_fn(lambda: L.moe_grouped_bwd_mxfp8(dy, xp, a, saved, offsets, sorted_src, wts, E, n, d, h,
+                                                           mxw, dxp, dw_ug, dw_down, mbws, status))
+        tf_ms, _ = time_fn(lambda: L.moe_grouped_swiglu_fwd(xp, offsets, sorted_src, wts, E, n, d, h, w_ug, w_down,
+                                                            y2, a, saved, None, status))
+        tb_ms, _ = time_fn(lambda: L.moe_grouped_bwd(dy, xp, a, saved, offsets, sorted_src, wts, E, n, d, h, w_ug,
+                                                     w_down, dxp, dw_ug, dw_down, bbws, status))
+        mxfp8 = {"weight_prep_ms": wp_ms, "fwd_ms": mf_ms, "fwd_tflops": fw / (mf_ms * 1e-3) / 1e12,
+                 "bwd_ms": mb_ms, "fwd_bwd_tflops": 3 * fw / ((mf_ms + mb_ms) * 1e-3) / 1e12,
+                 "bf16_training_fwd_ms": tf_ms, "bf16_bwd_ms": tb_ms,
+                 "bf16_fwd_bwd_tflops": 3 * fw / ((tf_ms + tb_ms) * 1e-3) / 1e12,
+                 "note": "composite calls, saved state written; MXFP8 forward = quantize xp, scaled up/gate "
+                         "GEMM, quantize P, scaled down GEMM; backward = quantize dy, scaled dgrad, quantize "
+                         "dU, scaled up dgrad, BF16 wgrads"}
+        del mxw, mfws, mbws, bbws
         variants = {"grouped_fwd": {"ms": g_ms, "tflops": fw / (g_ms * 1e-3) / 1e12},
                     "padded_bmm_fwd": {"ms": b_ms, "tflops": fw / (b_ms * 1e-3) / 1e12, "C": C,
                                        "rows_multiplied": E * C, "rho_pad": 1 - M / (E * C)},
                     "host_loop_fwd": {"ms": l_wall, "tflops": fw / (l_wall * 1e-3) / 1e12,
-                                      "note": "wall time incl. the D2H count copy and host wait"}}
+                                      "note": "wall time incl. the D2H count copy and host wait"},
+                    "mxfp8": mxfp8}
         del bmm_ws, y2
         torch.cuda.synchronize()
         assert status.item() == 0, f"device status {status.item()}"

@@ -72,7 +72,11 @@ typedef enum {
   MOE_OP_BWD = 2,         /* moe_grouped_bwd (dU halves, routing-gradient partials) */
   MOE_OP_PADDED_BMM = 3,  /* moe_padded_bmm_swiglu_fwd (uses capacity_C) */
   MOE_OP_LOOP = 4,        /* moe_loop_swiglu_fwd */
-  MOE_OP_SAVED = 5        /* size of the `saved` buffer the forward fills for the backward */
+  MOE_OP_SAVED = 5,       /* size of the `saved` buffer the forward fills for the backward */
+  MOE_OP_MX_WEIGHTS = 6,  /* moe_mx_prepare_weights: the prepared MXFP8 weights */
+  MOE_OP_MX_FWD = 7,      /* moe_grouped_swiglu_fwd_mxfp8 */
+  MOE_OP_MX_BWD = 8,      /* moe_grouped_bwd_mxfp8 */
+  MOE_OP_MX_ROW_SCALES = 9 /* moe_mx_quantize_rows: scale bytes for T*top_k rows of K = d */
 } moe_op_t;
 
 /* Bytes of caller workspace that `op` needs for these sizes (0 when none). Pure host
@@ -271,6 +275,26 @@ moe_status_t moe_unpermute_combine(const moe_bf16* y, const int32_t* inv_map, co
                                    int T, int top_k, int d, moe_bf16* out, moe_stream_t stream);
 
 /*
+ * moe_grouped_swiglu_fwd_top1_combine -- for top_k = 1, the forward and the combine in one pass:
+ * the down projection stores row p straight into token row sorted_src[p] of `out`, the
+ * direct-access write into the combine buffer of "Section 09: Grouped GEMM", §9.4. With one slot
+ * per token the combine has no reduction to do (out[t] = y[inv[t]], the routing weight being
+ * folded into the SwiGLU output as in moe_grouped_swiglu_fwd), so no scatter-add and no atomics
+ * are needed; tokens whose slot was dropped (inv_map[t] = -1) get zero rows. Results are
+ * bit-identical to moe_grouped_swiglu_fwd followed by moe_unpermute_combine with weights = NULL.
+ *
+ *  xp [T, d], offsets [E], sorted_src and inv_map [T] as moe_route_offsets wrote them for
+ *  top_k = 1; weights nullable [T] fp32; out [T, d] bf16 (every row written); a_save [T, h] and
+ *  saved (nullable) as moe_grouped_swiglu_fwd. d and h multiples of 8 (no zero-padded copies).
+ */
+moe_status_t moe_grouped_swiglu_fwd_top1_combine(const moe_bf16* xp, const int32_t* offsets,
+                                                 const int32_t* sorted_src, const int32_t* inv_map,
+                                                 const float* weights, int E, int T, int d, int h,
+                                                 const moe_bf16* w_ug, const moe_bf16* w_down, moe_bf16* out,
+                                                 moe_bf16* a_save, void* saved, int32_t* dev_status,
+                                                 moe_stream_t stream);
+
+/*
  * moe_padded_bmm_swiglu_fwd -- comparison variant: capacity-padded batched GEMM ("Section 09",
  * Eq. 14 and Fig. 35). Every expert is padded to capacity_C rows ([E, C, d], zero rows added),
  * the same tcgen05 kernels run the E uniform problems (all E*C rows are multiplied), and the
@@ -295,6 +319,64 @@ moe_status_t moe_loop_swiglu_fwd(const moe_bf16* xp, const int32_t* offsets, int
                                  int d, int h, const moe_bf16* w_ug, const moe_bf16* w_down,
                                  moe_bf16* y, moe_bf16* a_save, void* saved,
                                  int32_t* dev_status, moe_stream_t stream);
+
+/*
+ * MXFP8 variant -- "Section 09: Grouped GEMM", §9.5 (last paragraph): the routed MXFP8 path
+ * runs the forward and the Dgrad as scaled grouped GEMMs and the Wgrad as BF16 grouped GEMM.
+ * Format: OCP Microscaling MXFP8 -- blocks of 32 consecutive elements along the contraction
+ * dimension share one power-of-two scale 2^s stored as E8M0 (s + 127), each element is FP8
+ * E4M3; s = floor(log2(max |v|)) - 8 clamped to [-127, 127] (-127 for an all-zero block);
+ * elements are v / 2^s rounded to nearest, ties to even, saturated to +-448. Every operand is
+ * quantized along its own contraction dimension from its bf16 value: x and dy along d, the
+ * SwiGLU output (a_save, bf16 P = w*A) along h, dU (its bf16 high half) along 2h, W_ug along d
+ * (forward) and along 2h (dgrad), W_down along h (forward) and along d (dgrad). Products of
+ * the block-scaled operands accumulate in fp32 in tensor memory (tcgen05.mma
+ * kind::mxf8f6f4.block_scale). Shapes: d a multiple of 32, h a multiple of 128 (the gate and
+ * up halves of W_ug then start on a 128-row scale tile), 1 <= E <= 1024; others return
+ * MOE_ERR_UNSUPPORTED_SHAPE.
+ *
+ * Layouts. Codes of an operand [rows, K] are bytes, row-major. Scales come in 512-byte atoms,
+ * one per (128-row tile, 128-element chunk of K): the scale of row r of the tile (0..127) and
+ * 32-block kb of the chunk (0..3) is byte (r % 32) * 16 + (r / 32) * 4 + kb of atom
+ * tile * ceil(K / 128) + chunk. For an activation the tiles are the problem list's 128-row
+ * tiles (each expert's segment cut from its start; tile index = row tiles of the experts
+ * before it + (p - start) / 128, at most (rows + 127 E) / 128 tiles); for a weight [E, N, K]
+ * the tile of row n of expert e is e * NTp + n / 128 with NTp = ceil(N / 128) rounded up to even.
+ *
+ * moe_mx_prepare_weights -- quantize W_ug [E, 2h, d] and W_down [E, h, d] (bf16) into `mxw`
+ *   (moe_workspace_bytes(MOE_OP_MX_WEIGHTS, 0, 1, E, d, h, 0) bytes, 256-byte aligned): four
+ *   (codes, scales) pairs, each piece starting on a 256-byte boundary, in this order: W_ug
+ *   along d (codes [E, 2h, d]); W_down along h (codes [E, d, h], the transpose); W_down along d
+ *   (codes [E, h, d]); W_ug along 2h (codes [E, d, 2h], the transpose). Run once per weight
+ *   update; the forward and the backward read it.
+ * moe_mx_quantize_rows -- quantize rows p < M = offsets[E-1] of x [cap, K] (bf16) into codes
+ *   q [cap, K] and scale atoms sf (moe_workspace_bytes(MOE_OP_MX_ROW_SCALES, T, top_k, E, K, h,
+ *   0) bytes for cap = T*top_k; h is ignored beyond its own check) by the problem list's tiles.
+ *   Offsets that decrease or exceed cap set MOE_DEV_BAD_OFFSETS and nothing is written.
+ * moe_grouped_swiglu_fwd_mxfp8 -- Eq. 13 with scaled GEMMs: U = q(xp) q(W_ug)^T, P = w*SwiGLU(U)
+ *   in the up/gate epilogue (a_save = bf16(P), saved as in moe_grouped_swiglu_fwd), then
+ *   y = q(a_save) q(W_down). Arguments as moe_grouped_swiglu_fwd plus mxw; ws holds the codes
+ *   and scales of xp and a_save (moe_workspace_bytes(MOE_OP_MX_FWD, ...), 256-byte aligned).
+ * moe_grouped_bwd_mxfp8 -- Eq. 15: dA = w * q(dy) q(W_down)^T with the SwiGLU backward (dU high
+ *   and low halves, routing-weight partials), dxp = q(dU_hi) q(W_ug) (scaled GEMMs); dW_down =
+ *   P^T dy and dW_ug = dU^T xp as BF16 grouped GEMMs on both halves (one launch). Arguments as
+ *   moe_grouped_bwd plus mxw; ws = moe_workspace_bytes(MOE_OP_MX_BWD, ...) bytes (256-byte
+ *   aligned): dU high, dU low, routing partials, then the codes and scales of dy and dU.
+ */
+moe_status_t moe_mx_prepare_weights(const moe_bf16* w_ug, const moe_bf16* w_down, int E, int d, int h, void* mxw,
+                                    size_t mxw_bytes, moe_stream_t stream);
+moe_status_t moe_mx_quantize_rows(const moe_bf16* x, const int32_t* offsets, int E, int cap, int K, uint8_t* q,
+                                  uint8_t* sf, int32_t* dev_status, moe_stream_t stream);
+moe_status_t moe_grouped_swiglu_fwd_mxfp8(const moe_bf16* xp, const int32_t* offsets, const int32_t* sorted_src,
+                                          const float* weights, int E, int cap, int d, int h, const void* mxw,
+                                          moe_bf16* y, moe_bf16* a_save, void* saved, void* ws, size_t ws_bytes,
+                                          int32_t* dev_status, moe_stream_t stream);
+moe_status_t moe_grouped_bwd_mxfp8(const moe_bf16* dy, const moe_bf16* xp, const moe_bf16* a_save,
+                                   const void* saved, const int32_t* offsets, const int32_t* sorted_src,
+                                   const float* weights, int E, int cap, int d, int h, const void* mxw,
+                                   moe_bf16* dxp, float* dw_ug, float* dw_down, const int32_t* inv_map,
+                                   float* dw_route, void* ws, size_t ws_bytes, int32_t* dev_status,
+                                   moe_stream_t stream);
 
 /*
  * moe_route_offsets_noalloc -- moe_route_offsets for callers that cannot allocate device memory.

@@ -200,7 +200,10 @@ def mx_expert_backward(dy: np.ndarray, xp: np.ndarray, u: np.ndarray, p: np.ndar
         dU  = [dA v s (1 + g (1 - s)), dA silu(g)]
         dX  = q(bf16(dU)) q(W_ug,e)               (dU along 2h; W_ug [2h, d] along 2h)
         dW_ug = dU^T X_e,  dW_down = P^T dY_e     (BF16 wgrads of the unquantized operands)
-    Returns (dxp [n, d], dw_ug [E, 2h, d], dw_down [E, h, d], du [n, 2h])."""
+    and, per row, the routing-weight term <SwiGLU(U)_p, (q(dY_e) q(W_down,e)^T)_p>: the gradient of
+    the combine with respect to the row's routing weight, <y~_p, dOut[t]> with the unweighted
+    expert output y~, evaluated through the scaled Dgrad product (dY the plain gather of dOut).
+    Returns (dxp [n, d], dw_ug [E, 2h, d], dw_down [E, h, d], du [n, 2h], g_dot [n])."""
     dy = np.asarray(dy, np.float64)
     xp = np.asarray(xp, np.float64)
     u = np.asarray(u, np.float64)
@@ -209,7 +212,7 @@ def mx_expert_backward(dy: np.ndarray, xp: np.ndarray, u: np.ndarray, p: np.ndar
     h = u.shape[1] // 2
     segs = segments(offsets)
     E = len(segs)
-    dxp, du = np.zeros((n, d)), np.zeros((n, 2 * h))
+    dxp, du, g_dot = np.zeros((n, d)), np.zeros((n, 2 * h)), np.zeros(n)
     dw_ug, dw_down = np.zeros((E, 2 * h, d)), np.zeros((E, h, d))
     for e in (range(E) if experts is None else experts):
         s, t = segs[e]
@@ -219,10 +222,12 @@ def mx_expert_backward(dy: np.ndarray, xp: np.ndarray, u: np.ndarray, p: np.ndar
         w = np.ones(t - s) if row_weight is None else np.asarray(row_weight, np.float64)[s:t]
         g, v = u[s:t, :h], u[s:t, h:]
         sg = 1.0 / (1.0 + np.exp(-g))
-        da = w[:, None] * (mx_round_trip(dy[s:t]) @ mx_round_trip(wd).T)
+        ge = mx_round_trip(dy[s:t]) @ mx_round_trip(wd).T
+        da = w[:, None] * ge
+        g_dot[s:t] = np.einsum("ph,ph->p", g * sg * v, ge)
         due = np.concatenate([da * v * sg * (1.0 + g * (1.0 - sg)), da * g * sg], axis=1)
         dxp[s:t] = mx_round_trip(bf16_round(due)) @ mx_round_trip(wu, axis=0)
         dw_ug[e] = due.T @ xp[s:t]
         dw_down[e] = p[s:t].T @ dy[s:t]
         du[s:t] = due
-    return dxp, dw_ug, dw_down, du
+    return dxp, dw_ug, dw_down, du, g_dot

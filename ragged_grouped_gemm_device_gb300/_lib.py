@@ -21,7 +21,8 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED_SHAPE",
           6: "MOE_ERR_UNSUPPORTED_DEVICE"}
 MOE_DEV_TIMEOUT = 0x1
 MOE_DEV_BAD_OFFSETS = 0x2
-OP_ROUTE, OP_FWD, OP_BWD, OP_PADDED_BMM, OP_LOOP, OP_SAVED = range(6)
+OP_ROUTE, OP_FWD, OP_BWD, OP_PADDED_BMM, OP_LOOP, OP_SAVED, OP_MX_WEIGHTS, OP_MX_FWD, OP_MX_BWD, OP_MX_ROW_SCALES = \
+    range(10)
 
 _P, _I, _S = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
 SIGNATURES = {
@@ -41,6 +42,13 @@ SIGNATURES = {
     "moe_grouped_up_dgrad": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P]),
     "moe_grouped_wgrad": (_I, [_P, _P, _I, _P, _I, _P, _I, _I, _P, _P, _P]),
     "moe_grouped_wgrad_dual": (_I, [_P, _P, _I, _P, _I, _P, _P, _P, _I, _P, _I, _P, _P, _I, _I, _P, _P]),
+    "moe_mx_prepare_weights": (_I, [_P, _P, _I, _I, _I, _P, _S, _P]),
+    "moe_mx_quantize_rows": (_I, [_P, _P, _I, _I, _I, _P, _P, _P, _P]),
+    "moe_grouped_swiglu_fwd_mxfp8": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _S, _P, _P]),
+    "moe_grouped_bwd_mxfp8": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _S,
+                                   _P, _P]),
+    "moe_grouped_swiglu_fwd_top1_combine": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P,
+                                                 _P]),
     "moe_route_offsets_noalloc": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P]),
     "moe_status_string": (ctypes.c_char_p, [_I]),
     "moe_last_cuda_error": (ctypes.c_char_p, []),
@@ -190,6 +198,35 @@ def moe_grouped_wgrad_dual(p1_hi, p1_lo, p1_cols, q1, q1_cols, dw1, p2_hi, p2_lo
         _ptr(q2), q2_cols, _ptr(dw2), _ptr(offsets), E, cap, _ptr(dev_status), _stream(stream)))
 
 
+def _nbytes(t):
+    return 0 if t is None else t.numel() * t.element_size()
+
+
+def moe_mx_prepare_weights(w_ug, w_down, E, d, h, mxw, stream=None):
+    _check("moe_mx_prepare_weights", load().moe_mx_prepare_weights(
+        _ptr(w_ug), _ptr(w_down), E, d, h, _ptr(mxw), _nbytes(mxw), _stream(stream)))
+
+
+def moe_mx_quantize_rows(x, offsets, E, cap, K, q, sf, dev_status=None, stream=None):
+    _check("moe_mx_quantize_rows", load().moe_mx_quantize_rows(
+        _ptr(x), _ptr(offsets), E, cap, K, _ptr(q), _ptr(sf), _ptr(dev_status), _stream(stream)))
+
+
+def moe_grouped_swiglu_fwd_mxfp8(xp, offsets, sorted_src, weights, E, cap, d, h, mxw, y, a_save, saved, ws,
+                                 dev_status=None, stream=None):
+    _check("moe_grouped_swiglu_fwd_mxfp8", load().moe_grouped_swiglu_fwd_mxfp8(
+        _ptr(xp), _ptr(offsets), _ptr(sorted_src), _ptr(weights), E, cap, d, h, _ptr(mxw), _ptr(y), _ptr(a_save),
+        _ptr(saved), _ptr(ws), _nbytes(ws), _ptr(dev_status), _stream(stream)))
+
+
+def moe_grouped_bwd_mxfp8(dy, xp, a_save, saved, offsets, sorted_src, weights, E, cap, d, h, mxw, dxp, dw_ug,
+                          dw_down, ws, dev_status=None, stream=None, inv_map=None, dw_route=None):
+    _check("moe_grouped_bwd_mxfp8", load().moe_grouped_bwd_mxfp8(
+        _ptr(dy), _ptr(xp), _ptr(a_save), _ptr(saved), _ptr(offsets), _ptr(sorted_src), _ptr(weights), E, cap, d,
+        h, _ptr(mxw), _ptr(dxp), _ptr(dw_ug), _ptr(dw_down), _ptr(inv_map), _ptr(dw_route), _ptr(ws), _nbytes(ws),
+        _ptr(dev_status), _stream(stream)))
+
+
 def saved_views(saved, cap, h):
     """The parts of the forward's `saved` buffer (a contiguous tensor of any dtype, read as bytes):
     the low half of P = w*A (bf16 [cap, h8]; the high half is a_save) at byte 0, then fp32 U in
@@ -209,6 +246,13 @@ def saved_views(saved, cap, h):
 def moe_unpermute_combine(y, inv_map, weights, T, top_k, d, out, stream=None):
     _check("moe_unpermute_combine", load().moe_unpermute_combine(
         _ptr(y), _ptr(inv_map), _ptr(weights), T, top_k, d, _ptr(out), _stream(stream)))
+
+
+def moe_grouped_swiglu_fwd_top1_combine(xp, offsets, sorted_src, inv_map, weights, E, T, d, h, w_ug, w_down, out,
+                                        a_save, saved=None, dev_status=None, stream=None):
+    _check("moe_grouped_swiglu_fwd_top1_combine", load().moe_grouped_swiglu_fwd_top1_combine(
+        _ptr(xp), _ptr(offsets), _ptr(sorted_src), _ptr(inv_map), _ptr(weights), E, T, d, h, _ptr(w_ug),
+        _ptr(w_down), _ptr(out), _ptr(a_save), _ptr(saved), _ptr(dev_status), _stream(stream)))
 
 
 def moe_padded_bmm_swiglu_fwd(xp, offsets, E, cap, d, h, capacity_C, w_ug, w_down, y, ws,

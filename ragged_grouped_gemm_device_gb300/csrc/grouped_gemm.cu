@@ -656,7 +656,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       } else if constexpr (EPI == MODE_PLAIN_BF16) {
         const bool rv = r_in < ti.rows;
         const long long row = ti.row0 + r_in;
-        bf16* orow = reinterpret_cast<bf16*>(args.out) + row * args.ldo;
+        const long long orow_idx = (args.row_dst != nullptr && rv) ? __ldg(args.row_dst + row) : row;
+        bf16* orow = reinterpret_cast<bf16*>(args.out) + orow_idx * args.ldo;
         // 32 columns (two 16-column chunks) at a time; the next pair's accumulator columns are
         // in flight while this pair is converted and stored
         auto store_pair = [&](int c, const uint32_t (&v0)[16], const uint32_t (&v1)[16]) {

@@ -79,6 +79,9 @@ struct GemmArgs {
   // aligned; h % 16 == 0 for UP_SWIGLU and DGRAD_SWIGLU, N % 16 == 0 for PLAIN_BF16), so a chunk
   // row is one 32-byte store
   int vec32;
+  // PLAIN_BF16, optional: row p of the output is written to row row_dst[p] of `out` instead of
+  // row p (the down projection storing straight into token rows when top_k = 1)
+  const int32_t* row_dst;
   // DGRAD_SWIGLU, optional: per row p, dw_np fp32 partial sums of <A_p, G_p> (A = SwiGLU(U)
   // unweighted, G = dy W_down^T before the routing weight), one per (column tile, warp half)
   float* dw_part;
@@ -145,6 +148,8 @@ moe_status_t launch_route(const int32_t* ids, int n, int E, int32_t* counts, int
 moe_status_t launch_permute(const void* x, const int32_t* sorted_src, const int32_t* offsets,
                             const float* row_scale, int n, int k, int E, int d, void* xp,
                             cudaStream_t s);
+// out[t] = 0 for the tokens with inv_map[t] < 0 (top_k = 1); d a multiple of 8
+moe_status_t launch_zero_dropped_rows(const int32_t* inv_map, int T, int d, void* out, cudaStream_t s);
 moe_status_t launch_combine(const void* y, const int32_t* inv_map, const float* weights, int T,
                             int k, int d, void* out, cudaStream_t s);
 moe_status_t launch_pad_rows(const void* src, const int32_t* offsets, int E, int C, int cols,
@@ -167,6 +172,7 @@ int mx_ntpad(int N);
 int mx_kc(int K);
 moe_status_t launch_mx_quant_rows(const void* src, long long rows, int K, const int32_t* offsets, int E,
                                   int per_expert, void* q, void* sf, int32_t* status, cudaStream_t s);
+size_t mx_workspace_bytes(int op, long long n, int E, int d, int h);  // the MOE_OP_MX_* sizes
 moe_status_t launch_mx_quant_cols(const void* w, int E, int R, int C, void* q, void* sf, cudaStream_t s);
 moe_status_t launch_unpad_rows(const void* src, const int32_t* offsets, int E, int C, int cap,
                                int cols, void* dst, cudaStream_t s);

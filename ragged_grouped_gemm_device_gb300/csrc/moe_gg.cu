@@ -371,6 +371,10 @@ size_t moe_workspace_bytes(int op, int T, int top_k, int E, int d, int h, int ca
       return round256(rows * d * 2) * 2 + round256(rows * h * 2);
     }
     case MOE_OP_LOOP: return 0;
+    case MOE_OP_MX_WEIGHTS:
+    case MOE_OP_MX_FWD:
+    case MOE_OP_MX_BWD:
+    case MOE_OP_MX_ROW_SCALES: return mx_workspace_bytes(op, n, E, d, h);
   }
   return 0;
 }
@@ -690,6 +694,35 @@ moe_status_t moe_grouped_bwd(const moe_bf16* dy, const moe_bf16* xp, const moe_b
   return repack_weight(dwdn8, dw_down, true, E, 1, h, d, false, s);
 }
 
+moe_status_t moe_grouped_swiglu_fwd_top1_combine(const moe_bf16* xp, const int32_t* offsets,
+                                                 const int32_t* sorted_src, const int32_t* inv_map,
+                                                 const float* weights, int E, int T, int d, int h,
+                                                 const moe_bf16* w_ug, const moe_bf16* w_down, moe_bf16* out,
+                                                 moe_bf16* a_save, void* saved, int32_t* dev_status,
+                                                 moe_stream_t stream) {
+  moe_status_t st = check_grouped_common(E, T, d, h);
+  if (st != MOE_OK) return st;
+  if (!xp || !offsets || !sorted_src || !inv_map || !w_ug || !w_down || !out || !a_save) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(xp) || !aligned16(w_ug) || !aligned16(w_down) || !aligned16(out) || !aligned16(a_save) ||
+      !aligned16(saved))
+    return MOE_ERR_INVALID_ARG;
+  if ((st = check_device()) != MOE_OK || T == 0) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int cap = T;  // one slot per token
+  // tokens whose only slot was dropped get zero rows; every other row is the down projection's
+  if ((st = launch_zero_dropped_rows(inv_map, T, d, out, s)) != MOE_OK) return st;
+  GemmArgs src = base_args(E, cap, dev_status);
+  src.offsets = offsets;
+  src.row_src = sorted_src;
+  src.row_weight = weights;
+  const long long tb = row_tiles_bound(cap, E);
+  if ((st = run_up_swiglu(src, cap, tb, E, d, h, xp, w_ug, a_save, saved, s)) != MOE_OK) return st;
+  GemmArgs dsrc = base_args(E, cap, dev_status);  // the weight is already in a_save
+  dsrc.offsets = offsets;
+  dsrc.row_dst = sorted_src;                      // flat slot = token when top_k = 1
+  return run_down(dsrc, cap, tb, E, d, h, a_save, w_down, out, s);
+}
+
 moe_status_t moe_padded_bmm_swiglu_fwd(const moe_bf16* xp, const int32_t* offsets, int E, int cap,
                                        int d, int h, int capacity_C, const moe_bf16* w_ug,
                                        const moe_bf16* w_down, moe_bf16* y, void* ws,
@@ -765,6 +798,276 @@ moe_status_t moe_loop_swiglu_fwd(const moe_bf16* xp, const int32_t* offsets, int
     prev = off[e];
   }
   return MOE_OK;
+}
+
+}  // extern "C"
+
+// ------------------------------------------------------------------ MXFP8 variant
+// "Section 09: Grouped GEMM", §9.5: the routed MXFP8 path runs the forward and the Dgrad as
+// scaled grouped GEMMs and keeps the Wgrad in BF16. Operands are quantized along their
+// contraction dimension (E4M3 codes, one E8M0 scale per 32 elements; layouts in mx_quant.cu).
+namespace moe {
+namespace {
+
+bool mx_shape_ok(int E, int d, int h) {
+  return E >= 1 && E <= MAX_E && d > 0 && h > 0 && d % 32 == 0 && h % 128 == 0 && d <= (1 << 20) &&
+         h <= (1 << 20);
+}
+size_t mx_codes_bytes(long long rows, int K) { return round256(static_cast<size_t>(rows) * K); }
+size_t mx_wsf_bytes(int E, int N, int K) {
+  return round256(static_cast<size_t>(E) * mx_ntpad(N) * mx_kc(K) * 512);
+}
+size_t mx_asf_bytes(long long cap, int E, int K) {
+  return round256(static_cast<size_t>(saved_u_tiles(cap, E)) * mx_kc(K) * 512);
+}
+
+// The prepared weights: four (codes, scales) pairs, each piece 256-byte aligned, in order.
+struct MxWeights {
+  const uint8_t *ug_q, *ug_sf;    // W_ug along d:       codes [E, 2h, d]  (up/gate forward)
+  const uint8_t *dnT_q, *dnT_sf;  // W_down along h:     codes [E, d, h]   (down forward)
+  const uint8_t *dn_q, *dn_sf;    // W_down along d:     codes [E, h, d]   (down dgrad)
+  const uint8_t *ugT_q, *ugT_sf;  // W_ug along 2h:      codes [E, d, 2h]  (up/gate dgrad)
+};
+
+size_t mx_weights_bytes(int E, int d, int h) {
+  const long long e = E;
+  return mx_codes_bytes(e * 2 * h, d) + mx_wsf_bytes(E, 2 * h, d) + mx_codes_bytes(e * d, h) +
+         mx_wsf_bytes(E, d, h) + mx_codes_bytes(e * h, d) + mx_wsf_bytes(E, h, d) +
+         mx_codes_bytes(e * d, 2 * h) + mx_wsf_bytes(E, d, 2 * h);
+}
+
+MxWeights carve_mx_weights(const void* base, int E, int d, int h) {
+  const uint8_t* p = static_cast<const uint8_t*>(base);
+  const long long e = E;
+  MxWeights w;
+  w.ug_q = p;    p += mx_codes_bytes(e * 2 * h, d);
+  w.ug_sf = p;   p += mx_wsf_bytes(E, 2 * h, d);
+  w.dnT_q = p;   p += mx_codes_bytes(e * d, h);
+  w.dnT_sf = p;  p += mx_wsf_bytes(E, d, h);
+  w.dn_q = p;    p += mx_codes_bytes(e * h, d);
+  w.dn_sf = p;   p += mx_wsf_bytes(E, h, d);
+  w.ugT_q = p;   p += mx_codes_bytes(e * d, 2 * h);
+  w.ugT_sf = p;
+  return w;
+}
+
+size_t mx_fwd_ws_bytes(long long cap, int E, int d, int h) {
+  return mx_codes_bytes(cap, d) + mx_asf_bytes(cap, E, d) + mx_codes_bytes(cap, h) + mx_asf_bytes(cap, E, h);
+}
+size_t mx_bwd_ws_bytes(long long cap, int E, int d, int h) {
+  return bwd_core_bytes(cap, h) + mx_codes_bytes(cap, d) + mx_asf_bytes(cap, E, d) + mx_codes_bytes(cap, 2 * h) +
+         mx_asf_bytes(cap, E, 2 * h);
+}
+
+void set_mx(GemmArgs& a, const void* sfa, const void* sfb, int K, int N_b) {
+  a.sfa = static_cast<const uint8_t*>(sfa);
+  a.sfb = static_cast<const uint8_t*>(sfb);
+  a.sf_kc = mx_kc(K);
+  a.sfb_ntpad = mx_ntpad(N_b);
+}
+
+// U = q(xp) q(W_ug)^T with the up/gate epilogue of the BF16 path (a_save, optional saved).
+moe_status_t run_up_swiglu_mx(const GemmArgs& src, long long rows, long long tiles_bound, int E, int d, int h,
+                              const void* xq, const void* xsf, const MxWeights& w, void* a_save, void* saved,
+                              cudaStream_t s) {
+  GemmMaps m{};
+  if (!make_map_u8_rows2d(&m.a, xq, rows, d, 128)) return map_fail("xq");
+  if (!make_map_u8_weight3d(&m.b, w.ug_q, E, 2LL * h, d, 128)) return map_fail("w_ug codes");
+  GemmArgs a = src;
+  a.N = h;
+  a.K = d;
+  a.h = h;
+  a.out = a_save;
+  a.ldo = h;
+  if (saved != nullptr) {
+    a.out2 = const_cast<void*>(saved_u(saved, rows, h));
+    a.out3 = saved;
+    a.ldo3 = h;
+  }
+  a.vec32 = (h % 16 == 0 && aligned32(a_save) && (saved == nullptr || aligned32(saved))) ? 1 : 0;
+  set_mx(a, xsf, w.ug_sf, d, 2 * h);
+  return launch_grouped_gemm(MODE_UP_SWIGLU_MX, m, a, tiles_bound * gemm_tiles_n(MODE_UP_SWIGLU_MX, h), s);
+}
+
+// out = q(A) q(B)^T for a codes operand A [rows, K] and weight codes B [E, N, K]; bf16 out.
+moe_status_t run_plain_mx(const GemmArgs& src, long long rows, long long tiles_bound, int E, int K, int N,
+                          const void* aq, const void* asf, const void* bq, const void* bsf, void* out,
+                          cudaStream_t s) {
+  GemmMaps m{};
+  if (!make_map_u8_rows2d(&m.a, aq, rows, K, 128)) return map_fail("a codes");
+  if (!make_map_u8_weight3d(&m.b, bq, E, N, K, 256)) return map_fail("b codes");
+  GemmArgs a = src;
+  a.N = N;
+  a.K = K;
+  a.out = out;
+  a.ldo = N;
+  a.vec32 = (N % 16 == 0 && aligned32(out)) ? 1 : 0;
+  set_mx(a, asf, bsf, K, N);
+  return launch_grouped_gemm(MODE_PLAIN_MX, m, a, tiles_bound * gemm_tiles_n(MODE_PLAIN_MX, N), s);
+}
+
+// dA = w * q(dy) q(W_down)^T with the SwiGLU backward of the BF16 path (dU high / low).
+moe_status_t run_dgrad_mx(const GemmArgs& src, long long rows, int E, int d, int h, const void* dyq,
+                          const void* dysf, const void* saved, const MxWeights& w, void* du_hi, void* du_lo,
+                          float* dw_part, cudaStream_t s) {
+  GemmMaps m{};
+  if (!make_map_u8_rows2d(&m.a, dyq, rows, d, 128)) return map_fail("dy codes");
+  if (!make_map_u8_weight3d(&m.b, w.dn_q, E, h, d, 256)) return map_fail("w_down codes");
+  if (!make_map_rows2d_store(&m.out, du_hi, rows, 2LL * h)) return map_fail("du_hi");
+  if (!make_map_rows2d_store(&m.out2, du_lo, rows, 2LL * h)) return map_fail("du_lo");
+  GemmArgs a = src;
+  a.N = h;
+  a.K = d;
+  a.h = h;
+  a.out = du_hi;
+  a.ldo = 2LL * h;
+  a.out2 = du_lo;
+  a.ldo2 = 2LL * h;
+  a.aux = saved_u(saved, rows, h);
+  a.vec32 = (h % 16 == 0 && aligned32(du_hi) && aligned32(du_lo)) ? 1 : 0;
+  a.dw_part = dw_part;
+  a.dw_np = route_grad_parts(h);
+  set_mx(a, dysf, w.dn_sf, d, h);
+  return launch_grouped_gemm(MODE_DGRAD_SWIGLU_MX, m, a,
+                             row_tiles_bound(rows, src.E) * gemm_tiles_n(MODE_DGRAD_SWIGLU_MX, h), s);
+}
+
+}  // namespace
+
+size_t mx_workspace_bytes(int op, long long n, int E, int d, int h) {
+  if (!mx_shape_ok(E, d, h)) return 0;
+  switch (op) {
+    case MOE_OP_MX_WEIGHTS: return mx_weights_bytes(E, d, h);
+    case MOE_OP_MX_FWD: return mx_fwd_ws_bytes(n, E, d, h);
+    case MOE_OP_MX_BWD: return mx_bwd_ws_bytes(n, E, d, h);
+    case MOE_OP_MX_ROW_SCALES: return mx_asf_bytes(n, E, d);
+  }
+  return 0;
+}
+
+}  // namespace moe
+
+extern "C" {
+
+moe_status_t moe_mx_prepare_weights(const moe_bf16* w_ug, const moe_bf16* w_down, int E, int d, int h, void* mxw,
+                                    size_t mxw_bytes, moe_stream_t stream) {
+  if (E < 1 || d <= 0 || h <= 0) return MOE_ERR_INVALID_ARG;
+  if (!mx_shape_ok(E, d, h)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!w_ug || !w_down || !mxw) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(w_ug) || !aligned16(w_down) || (reinterpret_cast<uintptr_t>(mxw) & 255u)) return MOE_ERR_INVALID_ARG;
+  if (mxw_bytes < mx_weights_bytes(E, d, h)) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  moe_status_t st = check_device();
+  if (st != MOE_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const MxWeights w = carve_mx_weights(mxw, E, d, h);
+  auto mut = [](const uint8_t* p) { return const_cast<uint8_t*>(p); };
+  const long long e = E;
+  if ((st = launch_mx_quant_rows(w_ug, e * 2 * h, d, nullptr, E, 2 * h, mut(w.ug_q), mut(w.ug_sf), nullptr, s)) !=
+      MOE_OK)
+    return st;
+  if ((st = launch_mx_quant_cols(w_down, E, h, d, mut(w.dnT_q), mut(w.dnT_sf), s)) != MOE_OK) return st;
+  if ((st = launch_mx_quant_rows(w_down, e * h, d, nullptr, E, h, mut(w.dn_q), mut(w.dn_sf), nullptr, s)) != MOE_OK)
+    return st;
+  return launch_mx_quant_cols(w_ug, E, 2 * h, d, mut(w.ugT_q), mut(w.ugT_sf), s);
+}
+
+moe_status_t moe_mx_quantize_rows(const moe_bf16* x, const int32_t* offsets, int E, int cap, int K, uint8_t* q,
+                                  uint8_t* sf, int32_t* dev_status, moe_stream_t stream) {
+  if (cap < 0 || K <= 0 || E < 1) return MOE_ERR_INVALID_ARG;
+  if (E > MAX_E || K % 32 != 0 || K > (1 << 20)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!offsets || (cap > 0 && (!x || !q || !sf))) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(q) || !aligned16(sf)) return MOE_ERR_INVALID_ARG;
+  moe_status_t st = check_device();
+  if (st != MOE_OK || cap == 0) return st;
+  return launch_mx_quant_rows(x, cap, K, offsets, E, 0, q, sf, dev_status, reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status_t moe_grouped_swiglu_fwd_mxfp8(const moe_bf16* xp, const int32_t* offsets, const int32_t* sorted_src,
+                                          const float* weights, int E, int cap, int d, int h, const void* mxw,
+                                          moe_bf16* y, moe_bf16* a_save, void* saved, void* ws, size_t ws_bytes,
+                                          int32_t* dev_status, moe_stream_t stream) {
+  if (cap < 0 || d <= 0 || h <= 0 || E < 1) return MOE_ERR_INVALID_ARG;
+  if (!mx_shape_ok(E, d, h)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!xp || !offsets || !mxw || !y || !a_save || !ws || (weights && !sorted_src)) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(xp) || !aligned16(y) || !aligned16(a_save) || !aligned16(saved) ||
+      (reinterpret_cast<uintptr_t>(mxw) & 255u) || (reinterpret_cast<uintptr_t>(ws) & 255u))
+    return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < mx_fwd_ws_bytes(cap, E, d, h)) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  moe_status_t st = check_device();
+  if (st != MOE_OK || cap == 0) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const MxWeights w = carve_mx_weights(mxw, E, d, h);
+  Carver cv{static_cast<uint8_t*>(ws)};
+  void* xq = cv.take(mx_codes_bytes(cap, d));
+  void* xsf = cv.take(mx_asf_bytes(cap, E, d));
+  void* pq = cv.take(mx_codes_bytes(cap, h));
+  void* psf = cv.take(mx_asf_bytes(cap, E, h));
+  GemmArgs src = base_args(E, cap, dev_status);
+  src.offsets = offsets;
+  src.row_src = sorted_src;
+  src.row_weight = weights;
+  GemmArgs dsrc = base_args(E, cap, dev_status);  // the weight is already in a_save
+  dsrc.offsets = offsets;
+  const long long tb = row_tiles_bound(cap, E);
+  if ((st = launch_mx_quant_rows(xp, cap, d, offsets, E, 0, xq, xsf, dev_status, s)) != MOE_OK) return st;
+  if ((st = run_up_swiglu_mx(src, cap, tb, E, d, h, xq, xsf, w, a_save, saved, s)) != MOE_OK) return st;
+  // the down projection's input is P as the BF16 path stores it (bf16), quantized along h
+  if ((st = launch_mx_quant_rows(a_save, cap, h, offsets, E, 0, pq, psf, dev_status, s)) != MOE_OK) return st;
+  return run_plain_mx(dsrc, cap, tb, E, h, d, pq, psf, w.dnT_q, w.dnT_sf, y, s);
+}
+
+moe_status_t moe_grouped_bwd_mxfp8(const moe_bf16* dy, const moe_bf16* xp, const moe_bf16* a_save,
+                                   const void* saved, const int32_t* offsets, const int32_t* sorted_src,
+                                   const float* weights, int E, int cap, int d, int h, const void* mxw,
+                                   moe_bf16* dxp, float* dw_ug, float* dw_down, const int32_t* inv_map,
+                                   float* dw_route, void* ws, size_t ws_bytes, int32_t* dev_status,
+                                   moe_stream_t stream) {
+  if (cap < 0 || d <= 0 || h <= 0 || E < 1) return MOE_ERR_INVALID_ARG;
+  if (!mx_shape_ok(E, d, h)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!dy || !xp || !a_save || !saved || !offsets || !mxw || !dxp || !dw_ug || !dw_down || !ws ||
+      (weights && !sorted_src) || (dw_route && !inv_map))
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(dy) || !aligned16(xp) || !aligned16(a_save) || !aligned16(saved) || !aligned16(dxp) ||
+      !aligned16(dw_ug) || !aligned16(dw_down) || (reinterpret_cast<uintptr_t>(mxw) & 255u) ||
+      (reinterpret_cast<uintptr_t>(ws) & 255u))
+    return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < mx_bwd_ws_bytes(cap, E, d, h)) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  moe_status_t st = check_device();
+  if (st != MOE_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const MxWeights w = carve_mx_weights(mxw, E, d, h);
+  Carver cv{static_cast<uint8_t*>(ws)};
+  moe_bf16* du_hi = static_cast<moe_bf16*>(cv.take(bwd_ws_half(cap, h)));
+  moe_bf16* du_lo = static_cast<moe_bf16*>(cv.take(bwd_ws_half(cap, h)));
+  float* dw_part = static_cast<float*>(cv.take(route_grad_part_bytes(cap, h)));
+  void* dyq = cv.take(mx_codes_bytes(cap, d));
+  void* dysf = cv.take(mx_asf_bytes(cap, E, d));
+  void* duq = cv.take(mx_codes_bytes(cap, 2 * h));
+  void* dusf = cv.take(mx_asf_bytes(cap, E, 2 * h));
+  GemmArgs src = base_args(E, cap, dev_status);
+  src.offsets = offsets;
+  if (cap > 0) {
+    GemmArgs wsrc = src;
+    wsrc.row_src = sorted_src;
+    wsrc.row_weight = weights;
+    const long long tb = row_tiles_bound(cap, E);
+    if ((st = launch_mx_quant_rows(dy, cap, d, offsets, E, 0, dyq, dysf, dev_status, s)) != MOE_OK) return st;
+    if ((st = run_dgrad_mx(wsrc, cap, E, d, h, dyq, dysf, saved, w, du_hi, du_lo, dw_route ? dw_part : nullptr,
+                           s)) != MOE_OK)
+      return st;
+    if (dw_route) {
+      if ((st = launch_routing_weight_grad(dw_part, route_grad_parts(h), inv_map, cap, dw_route, s)) != MOE_OK)
+        return st;
+    }
+    // the up/gate dgrad's input is dU as the BF16 path stores it (its bf16 high half), along 2h
+    if ((st = launch_mx_quant_rows(du_hi, cap, 2 * h, offsets, E, 0, duq, dusf, dev_status, s)) != MOE_OK)
+      return st;
+    if ((st = run_plain_mx(src, cap, tb, E, 2 * h, d, duq, dusf, w.ugT_q, w.ugT_sf, dxp, s)) != MOE_OK) return st;
+  }
+  // BF16 wgrads of both projections in one launch (both halves of P and dU)
+  const WgradProblem wd{a_save, cap > 0 ? saved : a_save, h, dy, d, dw_down};
+  const WgradProblem wu{cap > 0 ? du_hi : a_save, cap > 0 ? du_lo : a_save, 2 * h, xp, d, dw_ug};
+  return run_wgrad(src, cap, E, wd, &wu, s);
 }
 
 }  // extern "C"

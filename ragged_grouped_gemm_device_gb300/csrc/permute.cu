@@ -53,6 +53,19 @@ __global__ void __launch_bounds__(THREADS) permute_kernel(
   }
 }
 
+// out[t] = 0 for every token whose single slot (top_k = 1) was dropped (inv[t] < 0): the rows the
+// down projection does not write when it stores straight into the token rows.
+__global__ void __launch_bounds__(THREADS) zero_dropped_rows_kernel(const int32_t* __restrict__ inv, int T,
+                                                                    int vec, uint4* __restrict__ out) {
+  const int lane = threadIdx.x & 31;
+  const int gw = blockIdx.x * WARPS + (threadIdx.x >> 5);
+  const int nw = gridDim.x * WARPS;
+  for (int t = gw; t < T; t += nw) {
+    if (__ldg(inv + t) >= 0) continue;  // warp-uniform
+    for (int v = lane; v < vec; v += 32) out[static_cast<size_t>(t) * vec + v] = make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
 // out[t] = sum_j w[t,j] * y[inv[t,j]] over slots with inv >= 0, fp32 in slot order, one bf16
 // rounding (gather + reduction in place of the scatter-add, "grouped_mm" agent doc).
 __global__ void __launch_bounds__(THREADS) combine_kernel(const uint4* __restrict__ y,
@@ -289,6 +302,14 @@ moe_status_t launch_permute(const void* x, const int32_t* sorted_src, const int3
       static_cast<const uint4*>(x), sorted_src, offsets, row_scale, n, k, E, d / 8,
       static_cast<uint4*>(xp));
   return last_launch();
+}
+
+moe_status_t launch_zero_dropped_rows(const int32_t* inv_map, int T, int d, void* out, cudaStream_t s) {
+  if (T == 0) return MOE_OK;
+  const int blocks = std::max(1, std::min((T + WARPS - 1) / WARPS, 8 * device_sm_count()));
+  zero_dropped_rows_kernel<<<blocks, THREADS, 0, s>>>(inv_map, T, d / 8, static_cast<uint4*>(out));
+  const cudaError_t err = cudaGetLastError();
+  return err == cudaSuccess ? MOE_OK : cuda_fail(err);
 }
 
 moe_status_t launch_combine(const void* y, const int32_t* inv_map, const float* weights, int T,

@@ -61,7 +61,14 @@ class ExpertLayer:
         _lib.moe_route_offsets(ids, T, k, E, self.counts, self.offsets, self.sorted_src, self.inv_map,
                                self.route_ws, stream)
         _lib.moe_permute(x, self.sorted_src, self.offsets, None, T, k, E, d, self.xp, stream)
-        # the routing weight is applied in the down projection's epilogue; the combine sums
+        if k == 1 and d % 8 == 0 and h % 8 == 0:
+            # one slot per token: the down projection writes the token rows itself (no y, no
+            # combine pass); the routing weight is folded into the SwiGLU output
+            _lib.moe_grouped_swiglu_fwd_top1_combine(self.xp, self.offsets, self.sorted_src, self.inv_map, weights,
+                                                     E, T, d, h, self.w_ug, self.w_down, self.out, self.a,
+                                                     self.saved, self.status, stream)
+            return self.out
+        # the routing weight is applied in the up/gate projection's epilogue; the combine sums
         _lib.moe_grouped_swiglu_fwd(self.xp, self.offsets, self.sorted_src, weights, E, n, d, h, self.w_ug,
                                     self.w_down, self.y, self.a, self.saved, self.fwd_ws, self.status, stream)
         _lib.moe_unpermute_combine(self.y, self.inv_map, None, T, k, d, self.out, stream)

@@ -177,7 +177,7 @@ def test_mx_backward_dgrad_exact_where_representable_and_bf16_wgrads():
     dy = np.zeros((wl.n, wl.d))
     dy[:M] = _representable(rng, (M, wl.d), 1.0)
     y, u, p = X.mx_expert_forward(xp, r["offsets"], wug, wdn, w_row)
-    dxp, dwu, dwd, du = X.mx_expert_backward(dy, xp, u, p, r["offsets"], wug, wdn, w_row)
+    dxp, dwu, dwd, du, g_dot = X.mx_expert_backward(dy, xp, u, p, r["offsets"], wug, wdn, w_row)
     # dy and W_down are representable: dU is the plain oracle's with dY = w * dy at the boundary
     dxp0, dwu0, dwd0, du0 = O.expert_backward(w_row[:, None] * dy, xp, u, r["offsets"], wug, wdn)
     assert np.allclose(du[:M], du0[:M], rtol=1e-12, atol=1e-14)
@@ -195,6 +195,18 @@ def test_mx_backward_dgrad_exact_where_representable_and_bf16_wgrads():
         assert (np.abs(dxp[s:t] - dxp0[s:t]) <= bound * (1 + 1e-9)).all()
     # empty experts: no arithmetic, zero gradients
     assert not dwu[2].any() and not dwd[2].any()
+    # the routing-weight term through the exact (representable) dgrad is the plain oracle's
+    # routing-weight gradient <y~, dOut> (dy is the unweighted gather of dOut here)
+    y0, _, _, _ = O.expert_forward(xp, r["offsets"], wug, wdn)
+    T, k = wl.T, wl.k
+    dout = np.zeros((T, wl.d))
+    src = r["sorted_src"][:M]
+    dout[src // k] = dy[:M]          # a dOut whose gather is dy (each token's slots share one row)
+    dwr_plain = O.routing_weight_grad(dout, y0, r["inv_map"], T, k)
+    dwr = np.where(r["inv_map"] >= 0, g_dot[np.maximum(r["inv_map"], 0)], 0.0).reshape(T, k)
+    tok = np.unique(src // k)
+    one_slot = np.bincount(src // k, minlength=T)[tok] == 1
+    assert np.allclose(dwr[tok[one_slot]], dwr_plain[tok[one_slot]], rtol=1e-12, atol=1e-12)
 
 
 def test_mx_forward_planted_mistakes_fail_the_bound():
