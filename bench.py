@@ -341,18 +341,24 @@ def kernel_source_hash():
 
 
 def load_traffic():
-    """DRAM bytes per launch (large workload) from the committed ncu summary, if the kernels are
-    unchanged since the capture: the summary's `traffic_per_launch_large:` line holds a JSON
-    object with the source hash and the bytes per kernel."""
-    path = os.path.join(ROOT, "profiles", "ncu_full_grouped_gemm_medium.md")
-    if not os.path.exists(path):
-        return {}
-    with open(path) as f:
-        for line in f:
-            if line.startswith("traffic_per_launch_large:"):
-                t = json.loads(line.split(":", 1)[1])
-                return t.get("kernels", {}) if t.get("source_hash") == kernel_source_hash() else {}
-    return {}
+    """DRAM bytes per launch (large workload) from the committed ncu summaries, for the kernels
+    unchanged since their capture: a summary's `traffic_per_launch_large:` line holds a JSON
+    object with the source hash and the bytes per kernel; lines whose hash is not the current
+    one are ignored."""
+    out = {}
+    pdir = os.path.join(ROOT, "profiles")
+    if not os.path.isdir(pdir):
+        return out
+    for fn in sorted(os.listdir(pdir)):
+        if not fn.endswith(".md"):
+            continue
+        with open(os.path.join(pdir, fn)) as f:
+            for line in f:
+                if line.startswith("traffic_per_launch_large:"):
+                    t = json.loads(line.split(":", 1)[1])
+                    if t.get("source_hash") == kernel_source_hash():
+                        out.update(t.get("kernels", {}))
+    return out
 
 
 def kernel_work(M, T, k, E, d, h):

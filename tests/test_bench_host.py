@@ -30,3 +30,25 @@ def test_oracle_rates_time_forward_and_backward_separately():
     assert set(r) == {"fwd", "fwd_bwd"}
     for mode in r.values():
         assert mode["experts"] == 4 and mode["rows"] == 10 and mode["tflops"] > 0
+
+
+def test_kernel_rooflines_bound_by_intensity_against_the_ridge():
+    peaks = {"bf16_tflops": 2000.0, "hbm_gbs": 8000.0}      # ridge 250 FLOP/B
+    work = {"gemm": (1e12, 1e9, 1e12),                     # 1000 FLOP/B: tensor-bound
+            "wgrad": (8e11, 5e9, 1.6e12),                  # 160 FLOP/B: memory-bound
+            "gather": (0, 6e8, 0)}
+    per_call = {"gemm": 1.0, "wgrad": 1.25, "gather": 0.1}
+    br, dom, roof = bench.kernel_rooflines(per_call, work, peaks, "test")
+    assert br["gemm"]["bound"] == "tensor" and br["wgrad"]["bound"] == "hbm" and br["gather"]["bound"] == "hbm"
+    assert dom == "wgrad" and roof["bound"] == "hbm" and roof["unit"] == "GB/s"
+    assert abs(roof["achieved"] - 5e9 / 1.25e-3 / 1e9) < 1e-6 and abs(roof["frac"] - 0.5) < 1e-9
+    assert abs(roof["mma_executed_tflops"] - 1280.0) < 1e-6       # both halves executed
+    assert abs(br["gemm"]["floor_ms"] - 0.5) < 1e-9 and abs(br["gemm"]["frac"] - 0.5) < 1e-9
+    w = bench.kernel_work(131072, 16384, 8, 256, 2048, 512)
+    assert w["wgrad_dual"][0] == 6.0 * 131072 * 2048 * 512 and w["wgrad_dual"][2] == 2 * w["wgrad_dual"][0]
+
+
+def test_traffic_is_taken_only_from_captures_of_the_current_sources():
+    t = bench.load_traffic()
+    assert set(t) <= {"up_swiglu", "down", "down_dgrad_swiglu", "up_dgrad", "wgrad_dual"}
+    assert all(v > 0 for v in t.values())
