@@ -747,21 +747,45 @@ def run_ours(args):
         mbws = torch.empty(L.moe_workspace_bytes(L.OP_MX_BWD, T, k, E, d, h), dtype=torch.uint8, device=dev)
         bbws = torch.empty(L.moe_workspace_bytes(L.OP_BWD, T, k, E, d, h), dtype=torch.uint8, device=dev)
         wp_ms, _ = time_fn(lambda: L.moe_mx_prepare_weights(w_ug, w_down, E, d, h, mxw))
-        mf_ms, _ = time_fn(lambda: L.moe_grouped_swiglu_fwd_mxfp8(xp, offsets, sorted_src, wts, E, n, d, h, mxw, y2,
-                                                                 a, saved, mfws, status))
-        mb_ms, _ = time_fn(lambda: L.moe_grouped_bwd_mxfp8(dy, xp, a, saved, offsets, sorted_src, wts, E, n, d, h,
-                                                           mxw, dxp, dw_ug, dw_down, mbws, status))
-        tf_ms, _ = time_fn(lambda: L.moe_grouped_swiglu_fwd(xp, offsets, sorted_src, wts, E, n, d, h, w_ug, w_down,
-                                                            y2, a, saved, None, status))
-        tb_ms, _ = time_fn(lambda: L.moe_grouped_bwd(dy, xp, a, saved, offsets, sorted_src, wts, E, n, d, h, w_ug,
-                                                     w_down, dxp, dw_ug, dw_down, bbws, status))
+        # each side from token rows: the gather (fused with the quantization on the MXFP8 side)
+        # and the composite call; the backward from dOut through its gather
+        sfb = L.moe_workspace_bytes(L.OP_MX_ROW_SCALES, T, k, E, d, h)
+        xq, xsf = (torch.empty(n, d, dtype=torch.uint8, device=dev), torch.empty(sfb, dtype=torch.uint8, device=dev))
+        dyq, dysf = (torch.empty(n, d, dtype=torch.uint8, device=dev), torch.empty(sfb, dtype=torch.uint8, device=dev))
+
+        def mx_fwd():
+            L.moe_permute_mxfp8(x, sorted_src, offsets, T, k, E, d, xp, xq, xsf, status)
+            L.moe_grouped_swiglu_fwd_mxfp8(None, offsets, sorted_src, wts, E, n, d, h, mxw, y2, a, saved, mfws, status,
+                                           xq=xq, xsf=xsf)
+
+        def mx_bwd():
+            L.moe_permute_mxfp8(dout, sorted_src, offsets, T, k, E, d, dy, dyq, dysf, status)
+            L.moe_grouped_bwd_mxfp8(dy, xp, a, saved, offsets, sorted_src, wts, E, n, d, h, mxw, dxp, dw_ug, dw_down,
+                                    mbws, status, dyq=dyq, dysf=dysf)
+
+        def bf_fwd():
+            L.moe_permute(x, sorted_src, offsets, None, T, k, E, d, xp)
+            L.moe_grouped_swiglu_fwd(xp, offsets, sorted_src, wts, E, n, d, h, w_ug, w_down, y2, a, saved, None,
+                                     status)
+
+        def bf_bwd():
+            L.moe_permute(dout, sorted_src, offsets, None, T, k, E, d, dy)
+            L.moe_grouped_bwd(dy, xp, a, saved, offsets, sorted_src, wts, E, n, d, h, w_ug, w_down, dxp, dw_ug,
+                              dw_down, bbws, status)
+
+        mf_ms, _ = time_fn(mx_fwd)
+        mb_ms, _ = time_fn(mx_bwd)
+        tf_ms, _ = time_fn(bf_fwd)
+        tb_ms, _ = time_fn(bf_bwd)
+        del xq, xsf, dyq, dysf
         mxfp8 = {"weight_prep_ms": wp_ms, "fwd_ms": mf_ms, "fwd_tflops": fw / (mf_ms * 1e-3) / 1e12,
                  "bwd_ms": mb_ms, "fwd_bwd_tflops": 3 * fw / ((mf_ms + mb_ms) * 1e-3) / 1e12,
                  "bf16_training_fwd_ms": tf_ms, "bf16_bwd_ms": tb_ms,
                  "bf16_fwd_bwd_tflops": 3 * fw / ((tf_ms + tb_ms) * 1e-3) / 1e12,
-                 "note": "composite calls, saved state written; MXFP8 forward = quantize xp, scaled up/gate "
-                         "GEMM, quantize P, scaled down GEMM; backward = quantize dy, scaled dgrad, quantize "
-                         "dU, scaled up dgrad, BF16 wgrads"}
+                 "note": "from token rows, saved state written; MXFP8 forward = gather fused with the "
+                         "quantization of xp, scaled up/gate GEMM quantizing P in its epilogue, scaled down "
+                         "GEMM; backward = gather of dOut fused with its quantization, scaled dgrad quantizing "
+                         "dU in its epilogue, scaled up dgrad, BF16 wgrads; bf16 = gather + the composite"}
         del mxw, mfws, mbws, bbws
         variants = {"grouped_fwd": {"ms": g_ms, "tflops": fw / (g_ms * 1e-3) / 1e12},
                     "padded_bmm_fwd": {"ms": b_ms, "tflops": fw / (b_ms * 1e-3) / 1e12, "C": C,

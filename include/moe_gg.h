@@ -349,30 +349,47 @@ moe_status_t moe_loop_swiglu_fwd(const moe_bf16* xp, const int32_t* offsets, int
  *   along d (codes [E, 2h, d]); W_down along h (codes [E, d, h], the transpose); W_down along d
  *   (codes [E, h, d]); W_ug along 2h (codes [E, d, 2h], the transpose). Run once per weight
  *   update; the forward and the backward read it.
+ * moe_permute_mxfp8 -- the permute's gather and the quantization of the gathered rows along d in
+ *   one pass: for p < M, codes q[p] [d] and the scale atoms sf (by the problem list's tiles;
+ *   moe_workspace_bytes(MOE_OP_MX_ROW_SCALES, T, top_k, E, d, h, 0) bytes) of x[sorted_src[p] /
+ *   top_k], and, when xp is non-NULL, the bf16 row itself (what moe_permute writes). Gives the
+ *   scaled forward its xp operand (and the scaled dgrad its dy: the gather of dOut) without a
+ *   separate pass over the rows. d a multiple of 32.
  * moe_mx_quantize_rows -- quantize rows p < M = offsets[E-1] of x [cap, K] (bf16) into codes
  *   q [cap, K] and scale atoms sf (moe_workspace_bytes(MOE_OP_MX_ROW_SCALES, T, top_k, E, K, h,
  *   0) bytes for cap = T*top_k; h is ignored beyond its own check) by the problem list's tiles.
  *   Offsets that decrease or exceed cap set MOE_DEV_BAD_OFFSETS and nothing is written.
  * moe_grouped_swiglu_fwd_mxfp8 -- Eq. 13 with scaled GEMMs: U = q(xp) q(W_ug)^T, P = w*SwiGLU(U)
- *   in the up/gate epilogue (a_save = bf16(P), saved as in moe_grouped_swiglu_fwd), then
- *   y = q(a_save) q(W_down). Arguments as moe_grouped_swiglu_fwd plus mxw; ws holds the codes
- *   and scales of xp and a_save (moe_workspace_bytes(MOE_OP_MX_FWD, ...), 256-byte aligned).
+ *   in the up/gate epilogue (a_save = bf16(P), saved as in moe_grouped_swiglu_fwd; the same
+ *   epilogue quantizes bf16(P) along h), then y = q(a_save) q(W_down). Arguments as
+ *   moe_grouped_swiglu_fwd plus mxw and the nullable pair xq, xsf: the codes and scales of xp
+ *   (from moe_permute_mxfp8 or moe_mx_quantize_rows); when they are NULL, xp is quantized here
+ *   (xp may be NULL when they are given). ws holds the codes and scales of xp (unused when
+ *   given) and of P (moe_workspace_bytes(MOE_OP_MX_FWD, ...), 256-byte aligned).
  * moe_grouped_bwd_mxfp8 -- Eq. 15: dA = w * q(dy) q(W_down)^T with the SwiGLU backward (dU high
- *   and low halves, routing-weight partials), dxp = q(dU_hi) q(W_ug) (scaled GEMMs); dW_down =
- *   P^T dy and dW_ug = dU^T xp as BF16 grouped GEMMs on both halves (one launch). Arguments as
- *   moe_grouped_bwd plus mxw; ws = moe_workspace_bytes(MOE_OP_MX_BWD, ...) bytes (256-byte
- *   aligned): dU high, dU low, routing partials, then the codes and scales of dy and dU.
+ *   and low halves, routing-weight partials; the same epilogue quantizes dU's high half along
+ *   2h), dxp = q(dU_hi) q(W_ug) (scaled GEMMs); dW_down = P^T dy and dW_ug = dU^T xp as BF16
+ *   grouped GEMMs on both halves (one launch). Arguments as moe_grouped_bwd plus mxw and the
+ *   nullable pair dyq, dysf: the codes and scales of dy (moe_permute_mxfp8 of dOut); when NULL,
+ *   dy is quantized here (dy itself is always required: the BF16 wgrad reads it).
+ *   ws = moe_workspace_bytes(MOE_OP_MX_BWD, ...) bytes (256-byte aligned): dU high, dU low,
+ *   routing partials, then the codes and scales of dy (unused when given) and of dU.
  */
 moe_status_t moe_mx_prepare_weights(const moe_bf16* w_ug, const moe_bf16* w_down, int E, int d, int h, void* mxw,
                                     size_t mxw_bytes, moe_stream_t stream);
+moe_status_t moe_permute_mxfp8(const moe_bf16* x, const int32_t* sorted_src, const int32_t* offsets, int T,
+                               int top_k, int E, int d, moe_bf16* xp, uint8_t* q, uint8_t* sf, int32_t* dev_status,
+                               moe_stream_t stream);
 moe_status_t moe_mx_quantize_rows(const moe_bf16* x, const int32_t* offsets, int E, int cap, int K, uint8_t* q,
                                   uint8_t* sf, int32_t* dev_status, moe_stream_t stream);
-moe_status_t moe_grouped_swiglu_fwd_mxfp8(const moe_bf16* xp, const int32_t* offsets, const int32_t* sorted_src,
-                                          const float* weights, int E, int cap, int d, int h, const void* mxw,
-                                          moe_bf16* y, moe_bf16* a_save, void* saved, void* ws, size_t ws_bytes,
+moe_status_t moe_grouped_swiglu_fwd_mxfp8(const moe_bf16* xp, const uint8_t* xq, const uint8_t* xsf,
+                                          const int32_t* offsets, const int32_t* sorted_src, const float* weights,
+                                          int E, int cap, int d, int h, const void* mxw, moe_bf16* y,
+                                          moe_bf16* a_save, void* saved, void* ws, size_t ws_bytes,
                                           int32_t* dev_status, moe_stream_t stream);
-moe_status_t moe_grouped_bwd_mxfp8(const moe_bf16* dy, const moe_bf16* xp, const moe_bf16* a_save,
-                                   const void* saved, const int32_t* offsets, const int32_t* sorted_src,
+moe_status_t moe_grouped_bwd_mxfp8(const moe_bf16* dy, const uint8_t* dyq, const uint8_t* dysf, const moe_bf16* xp,
+                                   const moe_bf16* a_save, const void* saved, const int32_t* offsets,
+                                   const int32_t* sorted_src,
                                    const float* weights, int E, int cap, int d, int h, const void* mxw,
                                    moe_bf16* dxp, float* dw_ug, float* dw_down, const int32_t* inv_map,
                                    float* dw_route, void* ws, size_t ws_bytes, int32_t* dev_status,

@@ -44,9 +44,10 @@ SIGNATURES = {
     "moe_grouped_wgrad_dual": (_I, [_P, _P, _I, _P, _I, _P, _P, _P, _I, _P, _I, _P, _P, _I, _I, _P, _P]),
     "moe_mx_prepare_weights": (_I, [_P, _P, _I, _I, _I, _P, _S, _P]),
     "moe_mx_quantize_rows": (_I, [_P, _P, _I, _I, _I, _P, _P, _P, _P]),
-    "moe_grouped_swiglu_fwd_mxfp8": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _S, _P, _P]),
-    "moe_grouped_bwd_mxfp8": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _S,
-                                   _P, _P]),
+    "moe_permute_mxfp8": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P]),
+    "moe_grouped_swiglu_fwd_mxfp8": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _S, _P, _P]),
+    "moe_grouped_bwd_mxfp8": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P,
+                                   _S, _P, _P]),
     "moe_grouped_swiglu_fwd_top1_combine": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P,
                                                  _P]),
     "moe_route_offsets_noalloc": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P]),
@@ -207,22 +208,28 @@ def moe_mx_prepare_weights(w_ug, w_down, E, d, h, mxw, stream=None):
         _ptr(w_ug), _ptr(w_down), E, d, h, _ptr(mxw), _nbytes(mxw), _stream(stream)))
 
 
+def moe_permute_mxfp8(x, sorted_src, offsets, T, top_k, E, d, xp, q, sf, dev_status=None, stream=None):
+    _check("moe_permute_mxfp8", load().moe_permute_mxfp8(
+        _ptr(x), _ptr(sorted_src), _ptr(offsets), T, top_k, E, d, _ptr(xp), _ptr(q), _ptr(sf), _ptr(dev_status),
+        _stream(stream)))
+
+
 def moe_mx_quantize_rows(x, offsets, E, cap, K, q, sf, dev_status=None, stream=None):
     _check("moe_mx_quantize_rows", load().moe_mx_quantize_rows(
         _ptr(x), _ptr(offsets), E, cap, K, _ptr(q), _ptr(sf), _ptr(dev_status), _stream(stream)))
 
 
 def moe_grouped_swiglu_fwd_mxfp8(xp, offsets, sorted_src, weights, E, cap, d, h, mxw, y, a_save, saved, ws,
-                                 dev_status=None, stream=None):
+                                 dev_status=None, stream=None, xq=None, xsf=None):
     _check("moe_grouped_swiglu_fwd_mxfp8", load().moe_grouped_swiglu_fwd_mxfp8(
-        _ptr(xp), _ptr(offsets), _ptr(sorted_src), _ptr(weights), E, cap, d, h, _ptr(mxw), _ptr(y), _ptr(a_save),
+        _ptr(xp), _ptr(xq), _ptr(xsf), _ptr(offsets), _ptr(sorted_src), _ptr(weights), E, cap, d, h, _ptr(mxw), _ptr(y), _ptr(a_save),
         _ptr(saved), _ptr(ws), _nbytes(ws), _ptr(dev_status), _stream(stream)))
 
 
 def moe_grouped_bwd_mxfp8(dy, xp, a_save, saved, offsets, sorted_src, weights, E, cap, d, h, mxw, dxp, dw_ug,
-                          dw_down, ws, dev_status=None, stream=None, inv_map=None, dw_route=None):
+                          dw_down, ws, dev_status=None, stream=None, inv_map=None, dw_route=None, dyq=None, dysf=None):
     _check("moe_grouped_bwd_mxfp8", load().moe_grouped_bwd_mxfp8(
-        _ptr(dy), _ptr(xp), _ptr(a_save), _ptr(saved), _ptr(offsets), _ptr(sorted_src), _ptr(weights), E, cap, d,
+        _ptr(dy), _ptr(dyq), _ptr(dysf), _ptr(xp), _ptr(a_save), _ptr(saved), _ptr(offsets), _ptr(sorted_src), _ptr(weights), E, cap, d,
         h, _ptr(mxw), _ptr(dxp), _ptr(dw_ug), _ptr(dw_down), _ptr(inv_map), _ptr(dw_route), _ptr(ws), _nbytes(ws),
         _ptr(dev_status), _stream(stream)))
 

@@ -9,6 +9,7 @@
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
 #include "../../include/moe_gg.h"
@@ -286,6 +287,32 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_ma
          ((static_cast<uint32_t>(M) >> 4) << 24);
 }
 
+// ---------------------------------------------------------------------------------- MXFP8
+// OCP MXFP8 element and scale encoding, shared by every kernel that quantizes (so that the
+// codes agree bit for bit whichever kernel produced them).
+// Shared exponent of a block from its largest magnitude (fp32, exact for bf16 inputs).
+__device__ __forceinline__ int mx_exponent(float amax) {
+  const int eb = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu);
+  if (eb == 0) return -127;               // zero or subnormal max: floor(log2) - 8 < -127
+  return max(eb - 127 - 8, -127);         // normal: floor(log2(amax)) = eb - 127
+}
+
+// 1 / 2^s for s in [-127, 126]: a normal fp32 power of two
+__device__ __forceinline__ float mx_inv_scale(int s) { return __uint_as_float(static_cast<uint32_t>(127 - s) << 23); }
+
+// a in the low byte, b in the high byte (memory order of two consecutive elements)
+__device__ __forceinline__ uint32_t e4m3x2(float a, float b) {
+  const uint32_t ca = __nv_cvt_float_to_fp8(a, __NV_SATFINITE, __NV_E4M3);
+  const uint32_t cb = __nv_cvt_float_to_fp8(b, __NV_SATFINITE, __NV_E4M3);
+  return (ca & 0xFFu) | ((cb & 0xFFu) << 8);
+}
+
+// Byte of the scale of row r (0..127 of its 128-row tile G) and 32-block kb (counted from the
+// row's start) in the atoms of an operand with KC 128-element chunks per row.
+__device__ __forceinline__ size_t atom_byte(long long G, int KC, int kb_global, int r) {
+  return static_cast<size_t>(G * KC + (kb_global >> 2)) * 512 + (r & 31) * 16 + (r >> 5) * 4 + (kb_global & 3);
+}
+
 // ---------------------------------------------------------------------------------- bf16 packing
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -294,5 +321,28 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+
+// One MXFP8 block of 32 bf16 values given as 16 packed pairs (elements 0..15 in p0, 16..31 in
+// p1, lower element of a pair in the low half): 32 E4M3 codes in memory order and the E8M0
+// scale code. The same arithmetic as every other quantizer of the library.
+__device__ __forceinline__ uint8_t mx_block_bf16(const uint32_t (&p0)[8], const uint32_t (&p1)[8],
+                                                 uint32_t (&codes)[8]) {
+  float amax = 0.f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(p0[j])), fabsf(bf16_hi(p0[j]))));
+    amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(p1[j])), fabsf(bf16_hi(p1[j]))));
+  }
+  const int s = mx_exponent(amax);
+  const float inv = mx_inv_scale(s);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    codes[j] = e4m3x2(bf16_lo(p0[2 * j]) * inv, bf16_hi(p0[2 * j]) * inv) |
+               (e4m3x2(bf16_lo(p0[2 * j + 1]) * inv, bf16_hi(p0[2 * j + 1]) * inv) << 16);
+    codes[4 + j] = e4m3x2(bf16_lo(p1[2 * j]) * inv, bf16_hi(p1[2 * j]) * inv) |
+                   (e4m3x2(bf16_lo(p1[2 * j + 1]) * inv, bf16_hi(p1[2 * j + 1]) * inv) << 16);
+  }
+  return static_cast<uint8_t>(s + 127);
+}
 
 }  // namespace moe

@@ -597,8 +597,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         // input, P - bf16(P) its low half for the down wgrad
         const float wrow =
             (args.row_weight != nullptr && rv) ? __ldg(args.row_weight + __ldg(args.row_src + row)) : 1.0f;
-        // chunk c's gate and up columns: U (blocked), then bf16(P) and its low half
-        auto process = [&](int c, const uint32_t (&g)[16], const uint32_t (&u)[16]) {
+        // chunk c's gate and up columns: U (blocked), then bf16(P) and its low half; bf16(P) is
+        // also left in pout for the MXFP8 quantization of the pair of chunks
+        auto process = [&](int c, const uint32_t (&g)[16], const uint32_t (&u)[16], uint32_t (&pout)[8]) {
           const int col = ti.n0 + c * 16;
           if (!rv || col >= h) return;
           if (args.out2 != nullptr) {
@@ -618,6 +619,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             const float p1 = wrow * (silu_f(__uint_as_float(g[2 * j + 1])) * __uint_as_float(u[2 * j + 1]));
             pa[j] = pack_bf16x2(p0, p1);
             pl[j] = pack_bf16x2(p0 - bf16_lo(pa[j]), p1 - bf16_hi(pa[j]));
+            pout[j] = pa[j];
           }
           const bool two = col + 16 <= h;
           if (args.vec32) {
@@ -636,6 +638,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         // processed
         const int cb = half * 4;
         uint32_t ga[16], ua[16], gb[16], ub[16];
+        uint32_t pq0[8], pq1[8];
         tmem_ld16(tb + cb * 16, ga);
         tmem_ld16(tb + 128 + cb * 16, ua);
         tmem_ld_wait2(ga, ua);
@@ -643,14 +646,24 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int c = cb; c < cb + 4; c += 2) {
           tmem_ld16(tb + (c + 1) * 16, gb);
           tmem_ld16(tb + 128 + (c + 1) * 16, ub);
-          process(c, ga, ua);
+          process(c, ga, ua, pq0);
           tmem_ld_wait2(gb, ub);
           const bool more = c + 2 < cb + 4;
           if (more) {
             tmem_ld16(tb + (c + 2) * 16, ga);
             tmem_ld16(tb + 128 + (c + 2) * 16, ua);
           }
-          process(c + 1, gb, ub);
+          process(c + 1, gb, ub, pq1);
+          if constexpr (MX) {
+            // the down projection's A operand: bf16(P) of these 32 columns as one MXFP8 block
+            const int col = ti.n0 + c * 16;
+            if (args.mxq != nullptr && rv && col < h) {
+              uint32_t codes[8];
+              const uint8_t sc = mx_block_bf16(pq0, pq1, codes);
+              st_global_v8(args.mxq + row * args.mx_ldq + col, codes);
+              args.mxsf[atom_byte(G, args.mx_kc, col >> 5, r_in)] = sc;
+            }
+          }
           if (more) tmem_ld_wait2(ga, ua);
         }
       } else if constexpr (EPI == MODE_PLAIN_BF16) {
@@ -753,7 +766,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         // routing-weight gradient, A = silu(gate) * up unweighted and acc = dy W_down^T before w
         // (<A, dy W_down^T> = <A W_down, dy>: the unweighted expert output against dOut).
         float dw_acc = 0.f;
-        auto process = [&](int c, const uint32_t (&v)[16]) {
+        auto process = [&](int c, const uint32_t (&v)[16], uint32_t (&gout)[8], uint32_t (&uout)[8]) {
           const int col = ti.n0 + c * 16;
           if (!rv || col >= h) return;
           const bool two = col + 16 <= h;
@@ -781,6 +794,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             uh[j] = pack_bf16x2(du[0], du[1]);
             gl[j] = pack_bf16x2(dg[0] - bf16_lo(gh[j]), dg[1] - bf16_hi(gh[j]));
             ul[j] = pack_bf16x2(du[0] - bf16_lo(uh[j]), du[1] - bf16_hi(uh[j]));
+            if constexpr (MX) {
+              gout[j] = gh[j];
+              uout[j] = uh[j];
+            }
           }
           if (slab_full && two) {
             stage_store(gh, &maps.out, col);
@@ -811,6 +828,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int cb = half * (BN / 32), ce = cb + BN / 32;  // an even number of chunks
         float4 gnxt[4], unxt[4];
         uint32_t v0[16], v1[16];
+        // MXFP8 dgrad: dU's high half of a pair of chunks, kept for its quantization
+        [[maybe_unused]] uint32_t qg0[8], qu0[8], qg1[8], qu1[8];
         tmem_ld16(tb + cb * 16, v0);
         tmem_ld_wait(v0);
         // two chunks per iteration: the accumulator columns and saved U of the next chunk are
@@ -819,7 +838,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int c = cb; c < ce; c += 2) {
           tmem_ld16(tb + (c + 1) * 16, v1);
           load_u(c + 1, gnxt, unxt);
-          process(c, v0);
+          process(c, v0, qg0, qu0);
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             gcur[j] = gnxt[j];
@@ -831,7 +850,22 @@ __global__ void __launch_bounds__(THREADS, 1)
             tmem_ld16(tb + (c + 2) * 16, v0);
             load_u(c + 2, gnxt, unxt);
           }
-          process(c + 1, v1);
+          process(c + 1, v1, qg1, qu1);
+          if constexpr (MX) {
+            // the up/gate dgrad's A operand: dU's high half of these 32 gate and 32 up columns
+            // as two MXFP8 blocks along 2h
+            const int col = ti.n0 + c * 16;
+            if (args.mxq != nullptr && rv && col < h) {
+              uint32_t codes[8];
+              uint8_t* qrow = args.mxq + row * args.mx_ldq;
+              uint8_t sc = mx_block_bf16(qg0, qg1, codes);
+              st_global_v8(qrow + col, codes);
+              args.mxsf[atom_byte(G, args.mx_kc, col >> 5, r_in)] = sc;
+              sc = mx_block_bf16(qu0, qu1, codes);
+              st_global_v8(qrow + h + col, codes);
+              args.mxsf[atom_byte(G, args.mx_kc, (h + col) >> 5, r_in)] = sc;
+            }
+          }
           if (more) {
 #pragma unroll
             for (int j = 0; j < 4; ++j) {

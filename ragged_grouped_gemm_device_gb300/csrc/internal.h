@@ -94,6 +94,13 @@ struct GemmArgs {
   int Mdim2;
   void* out_b;
   long long ldo_b;
+  // MXFP8 up/gate and dgrad modes, optional (mxq non-null): the next scaled GEMM's A operand
+  // quantized in the epilogue from the bf16 values it stores (P = a_save; dU's high half):
+  // codes [cap, mx_ldq] and scale atoms by the problem list's row tile, mx_kc 128-column chunks
+  uint8_t* mxq;
+  uint8_t* mxsf;
+  int mx_ldq;
+  int mx_kc;
   // MXFP8 modes: scale atoms of A (by row tile of the problem list) and of B (by expert and
   // 128-row tile of N, sfb_ntpad tiles per expert), sf_kc 128-element chunks of K per row
   const uint8_t* sfa;
@@ -173,6 +180,11 @@ int mx_kc(int K);
 moe_status_t launch_mx_quant_rows(const void* src, long long rows, int K, const int32_t* offsets, int E,
                                   int per_expert, void* q, void* sf, int32_t* status, cudaStream_t s);
 size_t mx_workspace_bytes(int op, long long n, int E, int d, int h);  // the MOE_OP_MX_* sizes
+// The permute's gather fused with the quantization of the gathered rows along d (xp nullable:
+// the bf16 copy is written only when given).
+moe_status_t launch_mx_permute_quant(const void* x, const int32_t* sorted_src, const int32_t* offsets, int E,
+                                    int n, int k, int d, void* xp, void* q, void* sf, int32_t* status,
+                                    cudaStream_t s);
 moe_status_t launch_mx_quant_cols(const void* w, int E, int R, int C, void* q, void* sf, cudaStream_t s);
 moe_status_t launch_unpad_rows(const void* src, const int32_t* offsets, int E, int C, int cap,
                                int cols, void* dst, cudaStream_t s);

@@ -866,10 +866,11 @@ void set_mx(GemmArgs& a, const void* sfa, const void* sfb, int K, int N_b) {
   a.sfb_ntpad = mx_ntpad(N_b);
 }
 
-// U = q(xp) q(W_ug)^T with the up/gate epilogue of the BF16 path (a_save, optional saved).
+// U = q(xp) q(W_ug)^T with the up/gate epilogue of the BF16 path (a_save, optional saved); the
+// epilogue also quantizes bf16(P) into pq / psf, the down projection's A operand.
 moe_status_t run_up_swiglu_mx(const GemmArgs& src, long long rows, long long tiles_bound, int E, int d, int h,
                               const void* xq, const void* xsf, const MxWeights& w, void* a_save, void* saved,
-                              cudaStream_t s) {
+                              void* pq, void* psf, cudaStream_t s) {
   GemmMaps m{};
   if (!make_map_u8_rows2d(&m.a, xq, rows, d, 128)) return map_fail("xq");
   if (!make_map_u8_weight3d(&m.b, w.ug_q, E, 2LL * h, d, 128)) return map_fail("w_ug codes");
@@ -886,6 +887,10 @@ moe_status_t run_up_swiglu_mx(const GemmArgs& src, long long rows, long long til
   }
   a.vec32 = (h % 16 == 0 && aligned32(a_save) && (saved == nullptr || aligned32(saved))) ? 1 : 0;
   set_mx(a, xsf, w.ug_sf, d, 2 * h);
+  a.mxq = static_cast<uint8_t*>(pq);
+  a.mxsf = static_cast<uint8_t*>(psf);
+  a.mx_ldq = h;
+  a.mx_kc = mx_kc(h);
   return launch_grouped_gemm(MODE_UP_SWIGLU_MX, m, a, tiles_bound * gemm_tiles_n(MODE_UP_SWIGLU_MX, h), s);
 }
 
@@ -906,10 +911,11 @@ moe_status_t run_plain_mx(const GemmArgs& src, long long rows, long long tiles_b
   return launch_grouped_gemm(MODE_PLAIN_MX, m, a, tiles_bound * gemm_tiles_n(MODE_PLAIN_MX, N), s);
 }
 
-// dA = w * q(dy) q(W_down)^T with the SwiGLU backward of the BF16 path (dU high / low).
+// dA = w * q(dy) q(W_down)^T with the SwiGLU backward of the BF16 path (dU high / low); the
+// epilogue also quantizes dU's high half into duq / dusf, the up/gate dgrad's A operand.
 moe_status_t run_dgrad_mx(const GemmArgs& src, long long rows, int E, int d, int h, const void* dyq,
                           const void* dysf, const void* saved, const MxWeights& w, void* du_hi, void* du_lo,
-                          float* dw_part, cudaStream_t s) {
+                          float* dw_part, void* duq, void* dusf, cudaStream_t s) {
   GemmMaps m{};
   if (!make_map_u8_rows2d(&m.a, dyq, rows, d, 128)) return map_fail("dy codes");
   if (!make_map_u8_weight3d(&m.b, w.dn_q, E, h, d, 256)) return map_fail("w_down codes");
@@ -928,6 +934,10 @@ moe_status_t run_dgrad_mx(const GemmArgs& src, long long rows, int E, int d, int
   a.dw_part = dw_part;
   a.dw_np = route_grad_parts(h);
   set_mx(a, dysf, w.dn_sf, d, h);
+  a.mxq = static_cast<uint8_t*>(duq);
+  a.mxsf = static_cast<uint8_t*>(dusf);
+  a.mx_ldq = 2 * h;
+  a.mx_kc = mx_kc(2 * h);
   return launch_grouped_gemm(MODE_DGRAD_SWIGLU_MX, m, a,
                              row_tiles_bound(rows, src.E) * gemm_tiles_n(MODE_DGRAD_SWIGLU_MX, h), s);
 }
@@ -971,6 +981,21 @@ moe_status_t moe_mx_prepare_weights(const moe_bf16* w_ug, const moe_bf16* w_down
   return launch_mx_quant_cols(w_ug, E, 2 * h, d, mut(w.ugT_q), mut(w.ugT_sf), s);
 }
 
+moe_status_t moe_permute_mxfp8(const moe_bf16* x, const int32_t* sorted_src, const int32_t* offsets, int T,
+                               int top_k, int E, int d, moe_bf16* xp, uint8_t* q, uint8_t* sf, int32_t* dev_status,
+                               moe_stream_t stream) {
+  if (T < 0 || top_k < 1 || d <= 0 || E < 1) return MOE_ERR_INVALID_ARG;
+  if (top_k > MAX_TOPK || E > MAX_E || d % 32 != 0 || d > (1 << 20)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  const long long n = static_cast<long long>(T) * top_k;
+  if (n >= (1LL << 31)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!offsets || (n > 0 && (!x || !sorted_src || !q || !sf))) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(xp) || !aligned16(q) || !aligned16(sf)) return MOE_ERR_INVALID_ARG;
+  moe_status_t st = check_device();
+  if (st != MOE_OK || n == 0) return st;
+  return launch_mx_permute_quant(x, sorted_src, offsets, E, static_cast<int>(n), top_k, d, xp, q, sf, dev_status,
+                                 reinterpret_cast<cudaStream_t>(stream));
+}
+
 moe_status_t moe_mx_quantize_rows(const moe_bf16* x, const int32_t* offsets, int E, int cap, int K, uint8_t* q,
                                   uint8_t* sf, int32_t* dev_status, moe_stream_t stream) {
   if (cap < 0 || K <= 0 || E < 1) return MOE_ERR_INVALID_ARG;
@@ -982,14 +1007,16 @@ moe_status_t moe_mx_quantize_rows(const moe_bf16* x, const int32_t* offsets, int
   return launch_mx_quant_rows(x, cap, K, offsets, E, 0, q, sf, dev_status, reinterpret_cast<cudaStream_t>(stream));
 }
 
-moe_status_t moe_grouped_swiglu_fwd_mxfp8(const moe_bf16* xp, const int32_t* offsets, const int32_t* sorted_src,
-                                          const float* weights, int E, int cap, int d, int h, const void* mxw,
-                                          moe_bf16* y, moe_bf16* a_save, void* saved, void* ws, size_t ws_bytes,
+moe_status_t moe_grouped_swiglu_fwd_mxfp8(const moe_bf16* xp, const uint8_t* xq, const uint8_t* xsf,
+                                          const int32_t* offsets, const int32_t* sorted_src, const float* weights,
+                                          int E, int cap, int d, int h, const void* mxw, moe_bf16* y,
+                                          moe_bf16* a_save, void* saved, void* ws, size_t ws_bytes,
                                           int32_t* dev_status, moe_stream_t stream) {
   if (cap < 0 || d <= 0 || h <= 0 || E < 1) return MOE_ERR_INVALID_ARG;
   if (!mx_shape_ok(E, d, h)) return MOE_ERR_UNSUPPORTED_SHAPE;
-  if (!xp || !offsets || !mxw || !y || !a_save || !ws || (weights && !sorted_src)) return MOE_ERR_INVALID_ARG;
-  if (!aligned16(xp) || !aligned16(y) || !aligned16(a_save) || !aligned16(saved) ||
+  if ((!xp && !xq) || (!xq != !xsf) || !offsets || !mxw || !y || !a_save || !ws || (weights && !sorted_src))
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(xp) || !aligned16(xq) || !aligned16(xsf) || !aligned16(y) || !aligned16(a_save) || !aligned16(saved) ||
       (reinterpret_cast<uintptr_t>(mxw) & 255u) || (reinterpret_cast<uintptr_t>(ws) & 255u))
     return MOE_ERR_INVALID_ARG;
   if (ws_bytes < mx_fwd_ws_bytes(cap, E, d, h)) return MOE_ERR_WORKSPACE_TOO_SMALL;
@@ -998,8 +1025,8 @@ moe_status_t moe_grouped_swiglu_fwd_mxfp8(const moe_bf16* xp, const int32_t* off
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const MxWeights w = carve_mx_weights(mxw, E, d, h);
   Carver cv{static_cast<uint8_t*>(ws)};
-  void* xq = cv.take(mx_codes_bytes(cap, d));
-  void* xsf = cv.take(mx_asf_bytes(cap, E, d));
+  void* xq_ws = cv.take(mx_codes_bytes(cap, d));
+  void* xsf_ws = cv.take(mx_asf_bytes(cap, E, d));
   void* pq = cv.take(mx_codes_bytes(cap, h));
   void* psf = cv.take(mx_asf_bytes(cap, E, h));
   GemmArgs src = base_args(E, cap, dev_status);
@@ -1009,15 +1036,19 @@ moe_status_t moe_grouped_swiglu_fwd_mxfp8(const moe_bf16* xp, const int32_t* off
   GemmArgs dsrc = base_args(E, cap, dev_status);  // the weight is already in a_save
   dsrc.offsets = offsets;
   const long long tb = row_tiles_bound(cap, E);
-  if ((st = launch_mx_quant_rows(xp, cap, d, offsets, E, 0, xq, xsf, dev_status, s)) != MOE_OK) return st;
-  if ((st = run_up_swiglu_mx(src, cap, tb, E, d, h, xq, xsf, w, a_save, saved, s)) != MOE_OK) return st;
-  // the down projection's input is P as the BF16 path stores it (bf16), quantized along h
-  if ((st = launch_mx_quant_rows(a_save, cap, h, offsets, E, 0, pq, psf, dev_status, s)) != MOE_OK) return st;
+  if (xq == nullptr) {  // the caller passed bf16 rows: quantize them here
+    if ((st = launch_mx_quant_rows(xp, cap, d, offsets, E, 0, xq_ws, xsf_ws, dev_status, s)) != MOE_OK) return st;
+    xq = static_cast<const uint8_t*>(xq_ws);
+    xsf = static_cast<const uint8_t*>(xsf_ws);
+  }
+  // the up/gate epilogue quantizes P as the BF16 path stores it (bf16) along h for the down GEMM
+  if ((st = run_up_swiglu_mx(src, cap, tb, E, d, h, xq, xsf, w, a_save, saved, pq, psf, s)) != MOE_OK) return st;
   return run_plain_mx(dsrc, cap, tb, E, h, d, pq, psf, w.dnT_q, w.dnT_sf, y, s);
 }
 
-moe_status_t moe_grouped_bwd_mxfp8(const moe_bf16* dy, const moe_bf16* xp, const moe_bf16* a_save,
-                                   const void* saved, const int32_t* offsets, const int32_t* sorted_src,
+moe_status_t moe_grouped_bwd_mxfp8(const moe_bf16* dy, const uint8_t* dyq, const uint8_t* dysf, const moe_bf16* xp,
+                                   const moe_bf16* a_save, const void* saved, const int32_t* offsets,
+                                   const int32_t* sorted_src,
                                    const float* weights, int E, int cap, int d, int h, const void* mxw,
                                    moe_bf16* dxp, float* dw_ug, float* dw_down, const int32_t* inv_map,
                                    float* dw_route, void* ws, size_t ws_bytes, int32_t* dev_status,
@@ -1025,9 +1056,9 @@ moe_status_t moe_grouped_bwd_mxfp8(const moe_bf16* dy, const moe_bf16* xp, const
   if (cap < 0 || d <= 0 || h <= 0 || E < 1) return MOE_ERR_INVALID_ARG;
   if (!mx_shape_ok(E, d, h)) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (!dy || !xp || !a_save || !saved || !offsets || !mxw || !dxp || !dw_ug || !dw_down || !ws ||
-      (weights && !sorted_src) || (dw_route && !inv_map))
+      (weights && !sorted_src) || (dw_route && !inv_map) || (!dyq != !dysf))
     return MOE_ERR_INVALID_ARG;
-  if (!aligned16(dy) || !aligned16(xp) || !aligned16(a_save) || !aligned16(saved) || !aligned16(dxp) ||
+  if (!aligned16(dy) || !aligned16(dyq) || !aligned16(dysf) || !aligned16(xp) || !aligned16(a_save) || !aligned16(saved) || !aligned16(dxp) ||
       !aligned16(dw_ug) || !aligned16(dw_down) || (reinterpret_cast<uintptr_t>(mxw) & 255u) ||
       (reinterpret_cast<uintptr_t>(ws) & 255u))
     return MOE_ERR_INVALID_ARG;
@@ -1040,8 +1071,8 @@ moe_status_t moe_grouped_bwd_mxfp8(const moe_bf16* dy, const moe_bf16* xp, const
   moe_bf16* du_hi = static_cast<moe_bf16*>(cv.take(bwd_ws_half(cap, h)));
   moe_bf16* du_lo = static_cast<moe_bf16*>(cv.take(bwd_ws_half(cap, h)));
   float* dw_part = static_cast<float*>(cv.take(route_grad_part_bytes(cap, h)));
-  void* dyq = cv.take(mx_codes_bytes(cap, d));
-  void* dysf = cv.take(mx_asf_bytes(cap, E, d));
+  void* dyq_ws = cv.take(mx_codes_bytes(cap, d));
+  void* dysf_ws = cv.take(mx_asf_bytes(cap, E, d));
   void* duq = cv.take(mx_codes_bytes(cap, 2 * h));
   void* dusf = cv.take(mx_asf_bytes(cap, E, 2 * h));
   GemmArgs src = base_args(E, cap, dev_status);
@@ -1051,17 +1082,20 @@ moe_status_t moe_grouped_bwd_mxfp8(const moe_bf16* dy, const moe_bf16* xp, const
     wsrc.row_src = sorted_src;
     wsrc.row_weight = weights;
     const long long tb = row_tiles_bound(cap, E);
-    if ((st = launch_mx_quant_rows(dy, cap, d, offsets, E, 0, dyq, dysf, dev_status, s)) != MOE_OK) return st;
+    if (dyq == nullptr) {  // the caller passed bf16 rows only: quantize them here
+      if ((st = launch_mx_quant_rows(dy, cap, d, offsets, E, 0, dyq_ws, dysf_ws, dev_status, s)) != MOE_OK)
+        return st;
+      dyq = static_cast<const uint8_t*>(dyq_ws);
+      dysf = static_cast<const uint8_t*>(dysf_ws);
+    }
+    // the dgrad epilogue quantizes dU's high half along 2h for the up/gate dgrad
     if ((st = run_dgrad_mx(wsrc, cap, E, d, h, dyq, dysf, saved, w, du_hi, du_lo, dw_route ? dw_part : nullptr,
-                           s)) != MOE_OK)
+                           duq, dusf, s)) != MOE_OK)
       return st;
     if (dw_route) {
       if ((st = launch_routing_weight_grad(dw_part, route_grad_parts(h), inv_map, cap, dw_route, s)) != MOE_OK)
         return st;
     }
-    // the up/gate dgrad's input is dU as the BF16 path stores it (its bf16 high half), along 2h
-    if ((st = launch_mx_quant_rows(du_hi, cap, 2 * h, offsets, E, 0, duq, dusf, dev_status, s)) != MOE_OK)
-      return st;
     if ((st = run_plain_mx(src, cap, tb, E, 2 * h, d, duq, dusf, w.ugT_q, w.ugT_sf, dxp, s)) != MOE_OK) return st;
   }
   // BF16 wgrads of both projections in one launch (both halves of P and dU)

@@ -25,8 +25,6 @@
 //   TMA zero fill), so every scale a valid output reads is defined.
 #include <algorithm>
 
-#include <cuda_fp8.h>
-
 #include "common.cuh"
 #include "internal.h"
 
@@ -35,23 +33,6 @@ namespace {
 
 constexpr int MXB = 32;        // elements per scale block
 constexpr int MAX_E = 1024;
-
-// Shared exponent of a block from its largest magnitude (fp32, exact for bf16 inputs).
-__device__ __forceinline__ int mx_exponent(float amax) {
-  const int eb = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu);
-  if (eb == 0) return -127;               // zero or subnormal max: floor(log2) - 8 < -127
-  return max(eb - 127 - 8, -127);         // normal: floor(log2(amax)) = eb - 127
-}
-
-// 1 / 2^s for s in [-127, 126]: a normal fp32 power of two
-__device__ __forceinline__ float mx_inv_scale(int s) { return __uint_as_float(static_cast<uint32_t>(127 - s) << 23); }
-
-// a in the low byte, b in the high byte (memory order of two consecutive elements)
-__device__ __forceinline__ uint32_t e4m3x2(float a, float b) {
-  const uint32_t ca = __nv_cvt_float_to_fp8(a, __NV_SATFINITE, __NV_E4M3);
-  const uint32_t cb = __nv_cvt_float_to_fp8(b, __NV_SATFINITE, __NV_E4M3);
-  return (ca & 0xFFu) | ((cb & 0xFFu) << 8);
-}
 
 // Quantize 32 fp32 values (already loaded) into 32 codes; returns the scale code.
 __device__ __forceinline__ uint8_t mx_block(const float (&v)[MXB], uint32_t (&codes)[8]) {
@@ -69,13 +50,71 @@ __device__ __forceinline__ uint8_t mx_block(const float (&v)[MXB], uint32_t (&co
   return static_cast<uint8_t>(s + 127);
 }
 
-__device__ __forceinline__ size_t atom_byte(long long G, int KC, int kb_global, int r) {
-  return static_cast<size_t>(G * KC + (kb_global >> 2)) * 512 + (r & 31) * 16 + (r >> 5) * 4 + (kb_global & 3);
-}
-
 // After the last block of a row: scales of the chunk's 32-blocks past K are 2^0.
 __device__ __forceinline__ void fill_chunk_tail(uint8_t* sf, long long G, int KC, int nb, int r) {
   for (int kb = nb; kb < ((nb + 3) & ~3); ++kb) sf[atom_byte(G, KC, kb, r)] = 127;
+}
+
+// The problem list as the grouped GEMM derives it from the offsets: s_end[e] = inclusive end of
+// expert e's rows, s_pre[e] = 128-row tiles of the experts before e (block-wide scan, 256
+// threads). Offsets that decrease or end past `rows` would place rows outside the scale atoms:
+// they are flagged (MOE_DEV_BAD_OFFSETS) and the function returns false in every thread.
+__device__ bool load_problem_tiles(const int32_t* __restrict__ offsets, int E, long long rows, int* s_end,
+                                   int* s_pre, int32_t* status) {
+  __shared__ int s_carry;
+  __shared__ int wsum[8];
+  if (threadIdx.x == 0) s_carry = 0;
+  __syncthreads();
+  for (int base = 0; base < E; base += blockDim.x) {
+    const int e = base + threadIdx.x;
+    int tiles = 0;
+    if (e < E) {
+      const int end = __ldg(offsets + e);
+      const int start = e > 0 ? __ldg(offsets + e - 1) : 0;
+      s_end[e] = end;
+      tiles = (end - start + 127) / 128;
+    }
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int incl = tiles;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int nb = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += nb;
+    }
+    if (lane == 31) wsum[warp] = incl;
+    __syncthreads();
+    int before = s_carry;
+    for (int w = 0; w < warp; ++w) before += wsum[w];
+    if (e < E) s_pre[e] = before + incl - tiles;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      int tot = 0;
+      for (int w = 0; w < 8; ++w) tot += wsum[w];
+      s_carry += tot;
+    }
+    __syncthreads();
+  }
+  bool bad = false;
+  for (int e = threadIdx.x; e < E; e += blockDim.x)
+    bad |= (s_end[e] < (e > 0 ? s_end[e - 1] : 0)) || (e == E - 1 && s_end[e] > rows);
+  if (__syncthreads_or(bad)) {
+    if (threadIdx.x == 0 && blockIdx.x == 0) record_status(status, MOE_DEV_BAD_OFFSETS);
+    return false;
+  }
+  return true;
+}
+
+// Tile (G) and row within the tile (r) of row p of the problem list.
+__device__ __forceinline__ void row_tile(const int* s_end, const int* s_pre, int E, long long p, long long& G,
+                                         int& r) {
+  int lo = 0, hi = E - 1;  // first expert whose segment ends after p
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (s_end[mid] > p) hi = mid; else lo = mid + 1;
+  }
+  const long long start = lo > 0 ? s_end[lo - 1] : 0;
+  G = s_pre[lo] + (p - start) / 128;
+  r = static_cast<int>((p - start) % 128);
 }
 
 // Rows along K (the contraction), one thread per (row, 32-block). With offsets: rows p < M of a
@@ -87,53 +126,8 @@ __global__ void __launch_bounds__(256) mx_quant_rows_kernel(const bf16* __restri
                                                             int32_t* status) {
   __shared__ int s_end[MAX_E];   // inclusive offsets
   __shared__ int s_pre[MAX_E];   // 128-row tiles of the experts before e
-  __shared__ int s_carry;
   const bool act = offsets != nullptr;
-  if (act) {
-    // the problem list's tile prefix, as the grouped GEMM derives it from the offsets
-    if (threadIdx.x == 0) s_carry = 0;
-    __syncthreads();
-    for (int base = 0; base < E; base += blockDim.x) {
-      const int e = base + threadIdx.x;
-      int tiles = 0;
-      if (e < E) {
-        const int end = __ldg(offsets + e);
-        const int start = e > 0 ? __ldg(offsets + e - 1) : 0;
-        s_end[e] = end;
-        tiles = (end - start + 127) / 128;
-      }
-      // block-wide exclusive scan of `tiles` (256 threads: warp scans, then warp totals)
-      __shared__ int wsum[8];
-      const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-      int incl = tiles;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int nb = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += nb;
-      }
-      if (lane == 31) wsum[warp] = incl;
-      __syncthreads();
-      int before = s_carry;
-      for (int w = 0; w < warp; ++w) before += wsum[w];
-      if (e < E) s_pre[e] = before + incl - tiles;
-      __syncthreads();
-      if (threadIdx.x == 0) {
-        int tot = 0;
-        for (int w = 0; w < 8; ++w) tot += wsum[w];
-        s_carry += tot;
-      }
-      __syncthreads();
-    }
-    // offsets that decrease or end past the buffer would place rows outside the scale atoms:
-    // flag them and quantize nothing
-    bool bad = false;
-    for (int e = threadIdx.x; e < E; e += blockDim.x)
-      bad |= (s_end[e] < (e > 0 ? s_end[e - 1] : 0)) || (e == E - 1 && s_end[e] > rows);
-    if (__syncthreads_or(bad)) {
-      if (threadIdx.x == 0 && blockIdx.x == 0) record_status(status, MOE_DEV_BAD_OFFSETS);
-      return;
-    }
-  }
+  if (act && !load_problem_tiles(offsets, E, rows, s_end, s_pre, status)) return;
   const int nb = K / MXB;
   const int KC = (K + 127) / 128;
   const long long M = act ? s_end[E - 1] : rows;
@@ -145,14 +139,7 @@ __global__ void __launch_bounds__(256) mx_quant_rows_kernel(const bf16* __restri
     long long G;
     int r;
     if (act) {
-      int lo = 0, hi = E - 1;  // first expert whose segment ends after p
-      while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        if (s_end[mid] > p) hi = mid; else lo = mid + 1;
-      }
-      const long long start = lo > 0 ? s_end[lo - 1] : 0;
-      G = s_pre[lo] + (p - start) / 128;
-      r = static_cast<int>((p - start) % 128);
+      row_tile(s_end, s_pre, E, p, G, r);
     } else {
       const long long e = p / per_expert, n = p - e * per_expert;
       G = e * ntpad + n / 128;
@@ -177,6 +164,63 @@ __global__ void __launch_bounds__(256) mx_quant_rows_kernel(const bf16* __restri
     d4[1] = make_uint4(c[4], c[5], c[6], c[7]);
     sf[atom_byte(G, KC, b, r)] = code;
     if (b == nb - 1) fill_chunk_tail(sf, G, KC, nb, r);
+  }
+}
+
+// The gather of the permute (xp[p] = x[sorted_src[p] / k]) and the quantization of the gathered
+// row along d in one pass: one warp per row p < M; lane l moves 16-byte pieces l, l + 32, ...
+// (8 elements each), four consecutive lanes hold one 32-element block and agree on its scale
+// by two shuffles. Optionally also writes the bf16 row (the BF16 wgrad's operand).
+__global__ void __launch_bounds__(256) mx_permute_quant_kernel(const uint4* __restrict__ x,
+                                                               const int32_t* __restrict__ sorted_src,
+                                                               const int32_t* __restrict__ offsets, int E,
+                                                               int n, int k, int d, uint4* __restrict__ xp,
+                                                               uint8_t* __restrict__ q, uint8_t* __restrict__ sf,
+                                                               int32_t* status) {
+  __shared__ int s_end[MAX_E];
+  __shared__ int s_pre[MAX_E];
+  if (!load_problem_tiles(offsets, E, n, s_end, s_pre, status)) return;
+  const int M = s_end[E - 1];
+  const int vec = d / 8, nb = d / MXB, KC = (d + 127) / 128;
+  const int lane = threadIdx.x & 31;
+  const int gw = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int nw = gridDim.x * 8;
+  for (int p = gw; p < M; p += nw) {
+    const int src = __ldg(sorted_src + p);
+    if (src < 0 || src >= n) continue;  // warp-uniform
+    long long G;
+    int r;
+    row_tile(s_end, s_pre, E, p, G, r);
+    const uint4* xr = x + static_cast<size_t>(src / k) * vec;
+    for (int v0 = 0; v0 < vec; v0 += 32) {  // every lane runs every pass: the shuffles need the warp
+      const int v = v0 + lane;
+      const bool act = v < vec;                // vec % 4 == 0: a block's four lanes agree
+      const uint4 w4 = act ? __ldg(xr + v) : make_uint4(0u, 0u, 0u, 0u);
+      if (act && xp != nullptr) __stcs(xp + static_cast<size_t>(p) * vec + v, w4);
+      const uint32_t ww[4] = {w4.x, w4.y, w4.z, w4.w};
+      float f[8];
+      float amax = 0.f;
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        f[2 * t] = bf16_lo(ww[t]);
+        f[2 * t + 1] = bf16_hi(ww[t]);
+        amax = fmaxf(amax, fmaxf(fabsf(f[2 * t]), fabsf(f[2 * t + 1])));
+      }
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+      const int e8 = mx_exponent(amax);
+      const float inv = mx_inv_scale(e8);
+      if (act) {
+        const uint32_t lo = e4m3x2(f[0] * inv, f[1] * inv) | (e4m3x2(f[2] * inv, f[3] * inv) << 16);
+        const uint32_t hi = e4m3x2(f[4] * inv, f[5] * inv) | (e4m3x2(f[6] * inv, f[7] * inv) << 16);
+        *reinterpret_cast<uint2*>(q + static_cast<size_t>(p) * d + v * 8) = make_uint2(lo, hi);
+        if ((lane & 3) == 0) {
+          const int b = v >> 2;
+          sf[atom_byte(G, KC, b, r)] = static_cast<uint8_t>(e8 + 127);
+          if (b == nb - 1) fill_chunk_tail(sf, G, KC, nb, r);
+        }
+      }
+    }
   }
 }
 
@@ -229,6 +273,19 @@ moe_status_t launch_mx_quant_rows(const void* src, long long rows, int K, const 
   mx_quant_rows_kernel<<<grid_for(items), 256, 0, s>>>(static_cast<const bf16*>(src), rows, K, offsets, E,
                                                        per_expert, ntpad, static_cast<uint8_t*>(q),
                                                        static_cast<uint8_t*>(sf), status);
+  const cudaError_t err = cudaGetLastError();
+  return err == cudaSuccess ? MOE_OK : cuda_fail(err);
+}
+
+moe_status_t launch_mx_permute_quant(const void* x, const int32_t* sorted_src, const int32_t* offsets, int E,
+                                    int n, int k, int d, void* xp, void* q, void* sf, int32_t* status,
+                                    cudaStream_t s) {
+  if (d % MXB != 0 || E < 1 || E > MAX_E) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (n == 0) return MOE_OK;
+  const int blocks = std::max(1, std::min((n + 7) / 8, 8 * device_sm_count()));
+  mx_permute_quant_kernel<<<blocks, 256, 0, s>>>(static_cast<const uint4*>(x), sorted_src, offsets, E, n, k, d,
+                                                 static_cast<uint4*>(xp), static_cast<uint8_t*>(q),
+                                                 static_cast<uint8_t*>(sf), status);
   const cudaError_t err = cudaGetLastError();
   return err == cudaSuccess ? MOE_OK : cuda_fail(err);
 }

@@ -103,17 +103,23 @@ def test_invalid_arguments_rejected_before_any_cuda_call(lib):
     assert lib.moe_grouped_wgrad_dual(p, p, 64, p, 64, p, p, None, 64, p, 64, p, p, 4, 10, None, None) == INVALID
     # MXFP8: d a multiple of 32, h of 128; 256-byte aligned prepared weights and workspace
     p256 = ctypes.c_void_p(256)
-    mxf = lib.moe_grouped_swiglu_fwd_mxfp8
+    mxf = lambda *a: lib.moe_grouped_swiglu_fwd_mxfp8(a[0], None, None, *a[1:])
     assert mxf(p, p, None, None, 4, 10, 64, 96, p256, p, p, None, p256, 1 << 30, None, None) == SHAPE   # h % 128
     assert mxf(p, p, None, None, 4, 10, 48, 128, p256, p, p, None, p256, 1 << 30, None, None) == SHAPE  # d % 32
     assert mxf(p, p, None, None, 4, 10, 64, 128, p, p, p, None, p256, 1 << 30, None, None) == INVALID   # mxw align
     need = _lib.moe_workspace_bytes(_lib.OP_MX_FWD, 10, 1, 4, 64, 128)
     assert need > 0 and mxf(p, p, None, None, 4, 10, 64, 128, p256, p, p, None, p256, need - 1, None, None) == WS
+    # codes without their scales, or neither xp nor codes
+    assert lib.moe_grouped_swiglu_fwd_mxfp8(None, p, None, p, None, None, 4, 10, 64, 128, p256, p, p, None, p256,
+                                            1 << 30, None, None) == INVALID
+    assert lib.moe_grouped_swiglu_fwd_mxfp8(None, None, None, p, None, None, 4, 10, 64, 128, p256, p, p, None, p256,
+                                            1 << 30, None, None) == INVALID
+    assert lib.moe_permute_mxfp8(p, p, p, 10, 1, 4, 40, None, p, p, None, None) == SHAPE               # d % 32
     assert lib.moe_mx_prepare_weights(p, p, 4, 64, 128, p256, 16, None) == WS
     assert lib.moe_mx_quantize_rows(p, p, 4, 10, 40, p, p, None, None) == SHAPE                     # K % 32
     mxb = lib.moe_grouped_bwd_mxfp8
-    assert mxb(p, p, p, None, p, None, None, 4, 10, 64, 128, p256, p, p, p, None, None, p256, 1 << 30, None,
-               None) == INVALID                                                                      # saved
+    assert mxb(p, None, None, p, p, None, p, None, None, 4, 10, 64, 128, p256, p, p, p, None, None, p256, 1 << 30,
+               None, None) == INVALID                                                                # saved
 
 
 def test_binding_argument_counts_match_header():

@@ -223,3 +223,60 @@ def test_mx_large_sampled_experts(lib):
     G.assert_close(G.host(g["dxp"])[rows], o["dxp"][rows], "dxp[large]")
     G.assert_close(G.host(g["dwu"][experts]), o["dwu"][experts], "dW_ug[large]")
     G.assert_close(G.host(g["dwd"][experts]), o["dwd"][experts], "dW_down[large]")
+
+
+@pytest.mark.parametrize("name", ["toy", "edge", "finegrained"])
+def test_mx_permute_equals_permute_then_quantize(lib, name):
+    """The gather fused with the quantization writes the same bytes as the gather followed by
+    the standalone quantizer: bf16 rows, codes and every scale atom byte."""
+    wl = CASES[name]()
+    run = G.DevicePipeline(wl, with_u=False).route().permute()
+    n, d, E = wl.n, wl.d, wl.E
+    sfb = L.moe_workspace_bytes(L.OP_MX_ROW_SCALES, wl.T, wl.k, E, d, 128)
+    q1 = torch.full((n, d), 0xEE, dtype=torch.uint8, device="cuda")
+    sf1 = torch.full((sfb,), 0xEE, dtype=torch.uint8, device="cuda")
+    L.moe_mx_quantize_rows(run.xp, run.offsets, E, n, d, q1, sf1, run.status)
+    xp2 = G.nan_filled((n, d))
+    q2, sf2 = torch.full_like(q1, 0xEE), torch.full_like(sf1, 0xEE)
+    L.moe_permute_mxfp8(run.x, run.sorted_src, run.offsets, wl.T, wl.k, E, d, xp2, q2, sf2, run.status)
+    torch.cuda.synchronize()
+    assert run.status.item() == 0
+    M = int(run.offsets[-1].item())
+    assert torch.equal(xp2[:M].view(torch.int16), run.xp[:M].view(torch.int16))
+    assert torch.equal(q2, q1) and torch.equal(sf2, sf1)
+
+
+def test_mx_layer_with_fused_gathers_is_bit_identical(lib):
+    """The scaled forward fed with the codes of moe_permute_mxfp8, and the scaled backward fed
+    with the codes of the dOut gather, give exactly what the calls that quantize internally give."""
+    wl = CASES["edge_tiles"]()
+    run, g = _mx_run(wl, backward=True)
+    E, d, h, n, T, k = wl.E, wl.d, wl.h, wl.n, wl.T, wl.k
+    mxw = _prepared(wl)
+    sfb = L.moe_workspace_bytes(L.OP_MX_ROW_SCALES, T, k, E, d, h)
+    xq = torch.empty(n, d, dtype=torch.uint8, device="cuda")
+    xsf = torch.empty(sfb, dtype=torch.uint8, device="cuda")
+    L.moe_permute_mxfp8(run.x, run.sorted_src, run.offsets, T, k, E, d, None, xq, xsf, run.status)
+    y2, a2 = G.nan_filled((n, d)), G.nan_filled((n, h))
+    sv2 = torch.full_like(run.saved, float("nan"))
+    ws = torch.empty(L.moe_workspace_bytes(L.OP_MX_FWD, T, k, E, d, h), dtype=torch.uint8, device="cuda")
+    L.moe_grouped_swiglu_fwd_mxfp8(None, run.offsets, run.sorted_src, run.weights, E, n, d, h, mxw, y2, a2, sv2, ws,
+                                   run.status, xq=xq, xsf=xsf)
+    dy = G.nan_filled((n, d))
+    dyq = torch.empty(n, d, dtype=torch.uint8, device="cuda")
+    dysf = torch.empty(sfb, dtype=torch.uint8, device="cuda")
+    L.moe_permute_mxfp8(G.dev_bf16(g["dout"]), run.sorted_src, run.offsets, T, k, E, d, dy, dyq, dysf, run.status)
+    dxp2 = G.nan_filled((n, d))
+    dwu2, dwd2 = torch.empty_like(g["dwu"]), torch.empty_like(g["dwd"])
+    dwr2 = torch.full_like(g["dwr"], float("nan"))
+    bws = torch.empty(L.moe_workspace_bytes(L.OP_MX_BWD, T, k, E, d, h), dtype=torch.uint8, device="cuda")
+    L.moe_grouped_bwd_mxfp8(dy, run.xp, a2, sv2, run.offsets, run.sorted_src, run.weights, E, n, d, h, mxw, dxp2,
+                            dwu2, dwd2, bws, run.status, inv_map=run.inv_map, dw_route=dwr2, dyq=dyq, dysf=dysf)
+    torch.cuda.synchronize()
+    assert run.status.item() == 0
+    M = int(run.offsets[-1].item())
+    bits = lambda t: t.view(torch.int16) if t.dtype == torch.bfloat16 else t.view(torch.int32)
+    assert torch.equal(bits(y2[:M]), bits(run.y[:M])) and torch.equal(bits(a2[:M]), bits(run.a[:M]))
+    assert torch.equal(bits(dxp2[:M]), bits(g["dxp"][:M]))
+    assert torch.equal(bits(dwu2), bits(g["dwu"])) and torch.equal(bits(dwd2), bits(g["dwd"]))
+    assert torch.equal(bits(dwr2), bits(g["dwr"]))
