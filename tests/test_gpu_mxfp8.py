@@ -280,3 +280,36 @@ def test_mx_layer_with_fused_gathers_is_bit_identical(lib):
     assert torch.equal(bits(dxp2[:M]), bits(g["dxp"][:M]))
     assert torch.equal(bits(dwu2), bits(g["dwu"])) and torch.equal(bits(dwd2), bits(g["dwd"]))
     assert torch.equal(bits(dwr2), bits(g["dwr"]))
+
+
+def test_mx_edge_problem_lists(lib):
+    """The largest expert count (1024 experts of a few rows, every 37th empty: one ragged tile
+    per expert, scale atoms indexed up to the problem list's last tile) and a problem with no
+    routed rows at all (nothing launched, zero gradients)."""
+    wl = W.custom(T=400, k=4, E=1024, d=64, h=128, seed=63, invalid_frac=0.02,
+                  empty_experts=tuple(range(0, 1024, 37)))
+    run, g = _mx_run(wl, backward=True)
+    o = _oracle(wl, True, g["dout"])
+    M = o["r"]["M"]
+    G.assert_close(G.host(run.y)[:M], o["y"][:M], "y[E=1024]")
+    G.assert_close(G.host(g["dxp"])[:M], o["dxp"][:M], "dxp[E=1024]")
+    nz = o["r"]["counts"] > 0
+    G.assert_close(G.host(g["dwu"])[nz], o["dwu"][nz], "dW_ug[E=1024]")
+    assert not G.host(g["dwd"])[~nz].any()
+
+    wl0 = W.custom(T=0, k=2, E=5, d=64, h=128, seed=64)
+    E, d, h = wl0.E, wl0.d, wl0.h
+    offs = torch.zeros(E, dtype=torch.int32, device="cuda")
+    mxw = _prepared(wl0)
+    one = lambda *s: torch.zeros(*s, dtype=torch.bfloat16, device="cuda")
+    dwu = torch.full((E, 2 * h, d), float("nan"), device="cuda")
+    dwd = torch.full((E, h, d), float("nan"), device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = torch.empty(max(L.moe_workspace_bytes(L.OP_MX_BWD, 0, 2, E, d, h), 256), dtype=torch.uint8, device="cuda")
+    sv = torch.zeros(max(L.moe_workspace_bytes(L.OP_SAVED, 0, 2, E, d, h), 256), dtype=torch.uint8, device="cuda")
+    L.moe_grouped_swiglu_fwd_mxfp8(one(1, d), offs, None, None, E, 0, d, h, mxw, one(1, d), one(1, h), sv, ws, status)
+    L.moe_grouped_bwd_mxfp8(one(1, d), one(1, d), one(1, h), sv, offs, None, None, E, 0, d, h, mxw, one(1, d), dwu,
+                            dwd, ws, status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    assert not dwu.any() and not dwd.any()

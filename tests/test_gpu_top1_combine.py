@@ -48,3 +48,21 @@ def test_top1_fused_combine_equals_forward_then_combine(lib, name):
     assert not G.host(out2)[dropped].any()
     r, xp, yo, u, a = G.oracle_run(wl)
     G.assert_close(G.host(out2), O.combine(yo, r["inv_map"], wl.weights, T, 1), f"out[{name}]")
+
+
+def test_top1_fused_combine_max_experts_and_no_tokens(lib):
+    wl = W.custom(T=900, k=1, E=1024, d=64, h=64, seed=72, invalid_frac=0.05,
+                  empty_experts=tuple(range(0, 1024, 29)))
+    run = G.DevicePipeline(wl).route().permute()
+    T, E, d, h = wl.T, wl.E, wl.d, wl.h
+    out = G.nan_filled((T, d))
+    L.moe_grouped_swiglu_fwd_top1_combine(run.xp, run.offsets, run.sorted_src, run.inv_map, run.weights, E, T, d, h,
+                                          run.w_ug, run.w_down, out, G.nan_filled((T, h)), None, run.status)
+    torch.cuda.synchronize()
+    assert run.status.item() == 0
+    r, xp, yo, u, a = G.oracle_run(wl)
+    G.assert_close(G.host(out), O.combine(yo, r["inv_map"], wl.weights, T, 1), "out[E=1024]")
+    # no tokens: nothing to launch, status OK
+    z = torch.zeros(1, dtype=torch.int32, device="cuda")
+    L.moe_grouped_swiglu_fwd_top1_combine(run.xp, run.offsets, run.sorted_src, run.inv_map, None, E, 0, d, h,
+                                          run.w_ug, run.w_down, out, G.nan_filled((1, h)), None, z)
