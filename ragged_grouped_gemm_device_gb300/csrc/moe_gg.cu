@@ -9,6 +9,7 @@
 #include <vector>
 
 #include "internal.h"
+#include "trace.h"
 
 namespace moe {
 
@@ -382,6 +383,7 @@ size_t moe_workspace_bytes(int op, int T, int top_k, int E, int d, int h, int ca
 moe_status_t moe_route_offsets(const int32_t* ids, int T, int top_k, int E, int32_t* counts,
                                int32_t* offsets, int32_t* sorted_src, int32_t* inv_map,
                                void* ws, size_t ws_bytes, moe_stream_t stream) {
+  MOE_TRACE_CALL();
   if (T < 0 || top_k < 1) return MOE_ERR_INVALID_ARG;
   if (top_k > MAX_TOPK || E < 1 || E > MAX_E) return MOE_ERR_UNSUPPORTED_SHAPE;
   const long long n = static_cast<long long>(T) * top_k;
@@ -400,6 +402,7 @@ moe_status_t moe_route_offsets(const int32_t* ids, int T, int top_k, int E, int3
 moe_status_t moe_permute(const moe_bf16* x, const int32_t* sorted_src, const int32_t* offsets,
                          const float* row_scale, int T, int top_k, int E, int d, moe_bf16* xp,
                          moe_stream_t stream) {
+  MOE_TRACE_CALL();
   if (T < 0 || top_k < 1 || d <= 0) return MOE_ERR_INVALID_ARG;
   if (top_k > MAX_TOPK || E < 1 || E > MAX_E || !any_width_ok(d)) return MOE_ERR_UNSUPPORTED_SHAPE;
   const long long n = static_cast<long long>(T) * top_k;
@@ -415,6 +418,7 @@ moe_status_t moe_permute(const moe_bf16* x, const int32_t* sorted_src, const int
 
 moe_status_t moe_unpermute_combine(const moe_bf16* y, const int32_t* inv_map, const float* weights,
                                    int T, int top_k, int d, moe_bf16* out, moe_stream_t stream) {
+  MOE_TRACE_CALL();
   if (T < 0 || top_k < 1 || d <= 0) return MOE_ERR_INVALID_ARG;
   if (top_k > MAX_TOPK || !any_width_ok(d)) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (static_cast<long long>(T) * top_k >= (1LL << 31)) return MOE_ERR_UNSUPPORTED_SHAPE;
@@ -431,6 +435,7 @@ moe_status_t moe_grouped_up_swiglu(const moe_bf16* xp, const int32_t* offsets,
                                    const int32_t* sorted_src, const float* weights, int E, int cap,
                                    int d, int h, const moe_bf16* w_ug, moe_bf16* a_save,
                                    void* saved, int32_t* dev_status, moe_stream_t stream) {
+  MOE_TRACE_CALL();
   moe_status_t st = check_grouped_common(E, cap, d, h);
   if (st != MOE_OK) return st;
   if (!xp || !offsets || !w_ug || !a_save || (weights && !sorted_src)) return MOE_ERR_INVALID_ARG;
@@ -448,6 +453,7 @@ moe_status_t moe_grouped_up_swiglu(const moe_bf16* xp, const int32_t* offsets,
 moe_status_t moe_grouped_down(const moe_bf16* a, const int32_t* offsets, int E, int cap, int d,
                               int h, const moe_bf16* w_down, moe_bf16* y, int32_t* dev_status,
                               moe_stream_t stream) {
+  MOE_TRACE_CALL();
   moe_status_t st = check_grouped_common(E, cap, d, h);
   if (st != MOE_OK) return st;
   if (!a || !offsets || !w_down || !y) return MOE_ERR_INVALID_ARG;
@@ -465,6 +471,7 @@ moe_status_t moe_grouped_down_dgrad_swiglu(const moe_bf16* dy, const void* saved
                                            const moe_bf16* w_down, moe_bf16* du_hi,
                                            moe_bf16* du_lo, float* dw_part, int32_t* dev_status,
                                            moe_stream_t stream) {
+  MOE_TRACE_CALL();
   moe_status_t st = check_grouped_common(E, cap, d, h);
   if (st != MOE_OK) return st;
   if (!dy || !saved || !offsets || !w_down || !du_hi || !du_lo || (weights && !sorted_src))
@@ -483,6 +490,7 @@ moe_status_t moe_grouped_down_dgrad_swiglu(const moe_bf16* dy, const void* saved
 
 moe_status_t moe_routing_weight_grad(const float* dw_part, const int32_t* inv_map, int T,
                                      int top_k, int h, float* dw_route, moe_stream_t stream) {
+  MOE_TRACE_CALL();
   if (T < 0 || top_k < 1 || h <= 0) return MOE_ERR_INVALID_ARG;
   if (top_k > MAX_TOPK) return MOE_ERR_UNSUPPORTED_SHAPE;
   const long long n = static_cast<long long>(T) * top_k;
@@ -498,6 +506,7 @@ moe_status_t moe_routing_weight_grad(const float* dw_part, const int32_t* inv_ma
 moe_status_t moe_grouped_up_dgrad(const moe_bf16* du_hi, const int32_t* offsets, int E, int cap,
                                   int d, int h, const moe_bf16* w_ug, moe_bf16* dxp,
                                   int32_t* dev_status, moe_stream_t stream) {
+  MOE_TRACE_CALL();
   moe_status_t st = check_grouped_common(E, cap, d, h);
   if (st != MOE_OK) return st;
   if (!du_hi || !offsets || !w_ug || !dxp) return MOE_ERR_INVALID_ARG;
@@ -511,6 +520,7 @@ moe_status_t moe_grouped_up_dgrad(const moe_bf16* du_hi, const int32_t* offsets,
 moe_status_t moe_grouped_wgrad(const moe_bf16* p_hi, const moe_bf16* p_lo, int p_cols,
                                const moe_bf16* q, int q_cols, const int32_t* offsets, int E,
                                int cap, float* dw, int32_t* dev_status, moe_stream_t stream) {
+  MOE_TRACE_CALL();
   if (cap < 0 || E < 1 || p_cols <= 0 || q_cols <= 0) return MOE_ERR_INVALID_ARG;
   if (E > MAX_E || !dim_ok(p_cols) || !dim_ok(q_cols)) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (!p_hi || !q || !offsets || !dw) return MOE_ERR_INVALID_ARG;
@@ -530,6 +540,7 @@ moe_status_t moe_grouped_wgrad_dual(const moe_bf16* p1_hi, const moe_bf16* p1_lo
                                     const moe_bf16* q2, int q2_cols, float* dw2,
                                     const int32_t* offsets, int E, int cap, int32_t* dev_status,
                                     moe_stream_t stream) {
+  MOE_TRACE_CALL();
   if (cap < 0 || E < 1 || p1_cols <= 0 || q1_cols <= 0 || p2_cols <= 0 || q2_cols <= 0)
     return MOE_ERR_INVALID_ARG;
   if (E > MAX_E || !dim_ok(p1_cols) || !dim_ok(q1_cols) || !dim_ok(p2_cols) || !dim_ok(q2_cols))
@@ -555,6 +566,7 @@ moe_status_t moe_grouped_swiglu_fwd(const moe_bf16* xp, const int32_t* offsets,
                                     const moe_bf16* w_down, moe_bf16* y, moe_bf16* a_save,
                                     void* saved, void* ws, size_t ws_bytes, int32_t* dev_status,
                                     moe_stream_t stream) {
+  MOE_TRACE_CALL();
   moe_status_t st = check_grouped_any_width(E, cap, d, h);
   if (st != MOE_OK) return st;
   if (!xp || !offsets || !w_ug || !w_down || !y || !a_save || (weights && !sorted_src))
@@ -649,6 +661,7 @@ moe_status_t moe_grouped_bwd(const moe_bf16* dy, const moe_bf16* xp, const moe_b
                              float* dw_ug, float* dw_down, const int32_t* inv_map,
                              float* dw_route, void* ws, size_t ws_bytes, int32_t* dev_status,
                              moe_stream_t stream) {
+  MOE_TRACE_CALL();
   moe_status_t st = check_grouped_any_width(E, cap, d, h);
   if (st != MOE_OK) return st;
   if (!dy || !xp || !a_save || !saved || !offsets || !w_ug || !w_down || !dxp || !dw_ug ||
@@ -700,6 +713,7 @@ moe_status_t moe_grouped_swiglu_fwd_top1_combine(const moe_bf16* xp, const int32
                                                  const moe_bf16* w_ug, const moe_bf16* w_down, moe_bf16* out,
                                                  moe_bf16* a_save, void* saved, int32_t* dev_status,
                                                  moe_stream_t stream) {
+  MOE_TRACE_CALL();
   moe_status_t st = check_grouped_common(E, T, d, h);
   if (st != MOE_OK) return st;
   if (!xp || !offsets || !sorted_src || !inv_map || !w_ug || !w_down || !out || !a_save) return MOE_ERR_INVALID_ARG;
@@ -727,6 +741,7 @@ moe_status_t moe_padded_bmm_swiglu_fwd(const moe_bf16* xp, const int32_t* offset
                                        int d, int h, int capacity_C, const moe_bf16* w_ug,
                                        const moe_bf16* w_down, moe_bf16* y, void* ws,
                                        size_t ws_bytes, int32_t* dev_status, moe_stream_t stream) {
+  MOE_TRACE_CALL();
   if (cap < 0 || d <= 0 || h <= 0 || E < 1 || capacity_C < 1) return MOE_ERR_INVALID_ARG;
   if (!shape_ok(E, d, h)) return MOE_ERR_UNSUPPORTED_SHAPE;
   const long long rows = static_cast<long long>(E) * capacity_C;
@@ -760,6 +775,7 @@ moe_status_t moe_loop_swiglu_fwd(const moe_bf16* xp, const int32_t* offsets, int
                                  int d, int h, const moe_bf16* w_ug, const moe_bf16* w_down,
                                  moe_bf16* y, moe_bf16* a_save, void* saved,
                                  int32_t* dev_status, moe_stream_t stream) {
+  MOE_TRACE_CALL();
   moe_status_t st = check_grouped_common(E, cap, d, h);
   if (st != MOE_OK) return st;
   if (!xp || !offsets || !w_ug || !w_down || !y || !a_save) return MOE_ERR_INVALID_ARG;
@@ -961,6 +977,7 @@ extern "C" {
 
 moe_status_t moe_mx_prepare_weights(const moe_bf16* w_ug, const moe_bf16* w_down, int E, int d, int h, void* mxw,
                                     size_t mxw_bytes, moe_stream_t stream) {
+  MOE_TRACE_CALL();
   if (E < 1 || d <= 0 || h <= 0) return MOE_ERR_INVALID_ARG;
   if (!mx_shape_ok(E, d, h)) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (!w_ug || !w_down || !mxw) return MOE_ERR_INVALID_ARG;
@@ -984,6 +1001,7 @@ moe_status_t moe_mx_prepare_weights(const moe_bf16* w_ug, const moe_bf16* w_down
 moe_status_t moe_permute_mxfp8(const moe_bf16* x, const int32_t* sorted_src, const int32_t* offsets, int T,
                                int top_k, int E, int d, moe_bf16* xp, uint8_t* q, uint8_t* sf, int32_t* dev_status,
                                moe_stream_t stream) {
+  MOE_TRACE_CALL();
   if (T < 0 || top_k < 1 || d <= 0 || E < 1) return MOE_ERR_INVALID_ARG;
   if (top_k > MAX_TOPK || E > MAX_E || d % 32 != 0 || d > (1 << 20)) return MOE_ERR_UNSUPPORTED_SHAPE;
   const long long n = static_cast<long long>(T) * top_k;
@@ -998,6 +1016,7 @@ moe_status_t moe_permute_mxfp8(const moe_bf16* x, const int32_t* sorted_src, con
 
 moe_status_t moe_mx_quantize_rows(const moe_bf16* x, const int32_t* offsets, int E, int cap, int K, uint8_t* q,
                                   uint8_t* sf, int32_t* dev_status, moe_stream_t stream) {
+  MOE_TRACE_CALL();
   if (cap < 0 || K <= 0 || E < 1) return MOE_ERR_INVALID_ARG;
   if (E > MAX_E || K % 32 != 0 || K > (1 << 20)) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (!offsets || (cap > 0 && (!x || !q || !sf))) return MOE_ERR_INVALID_ARG;
@@ -1012,6 +1031,7 @@ moe_status_t moe_grouped_swiglu_fwd_mxfp8(const moe_bf16* xp, const uint8_t* xq,
                                           int E, int cap, int d, int h, const void* mxw, moe_bf16* y,
                                           moe_bf16* a_save, void* saved, void* ws, size_t ws_bytes,
                                           int32_t* dev_status, moe_stream_t stream) {
+  MOE_TRACE_CALL();
   if (cap < 0 || d <= 0 || h <= 0 || E < 1) return MOE_ERR_INVALID_ARG;
   if (!mx_shape_ok(E, d, h)) return MOE_ERR_UNSUPPORTED_SHAPE;
   if ((!xp && !xq) || (!xq != !xsf) || !offsets || !mxw || !y || !a_save || !ws || (weights && !sorted_src))
@@ -1053,6 +1073,7 @@ moe_status_t moe_grouped_bwd_mxfp8(const moe_bf16* dy, const uint8_t* dyq, const
                                    moe_bf16* dxp, float* dw_ug, float* dw_down, const int32_t* inv_map,
                                    float* dw_route, void* ws, size_t ws_bytes, int32_t* dev_status,
                                    moe_stream_t stream) {
+  MOE_TRACE_CALL();
   if (cap < 0 || d <= 0 || h <= 0 || E < 1) return MOE_ERR_INVALID_ARG;
   if (!mx_shape_ok(E, d, h)) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (!dy || !xp || !a_save || !saved || !offsets || !mxw || !dxp || !dw_ug || !dw_down || !ws ||
