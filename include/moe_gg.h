@@ -430,6 +430,33 @@ const char* moe_last_cuda_error(void);
 /* Version of this ABI (incremented on incompatible change). */
 int moe_abi_version(void);
 
+/*
+ * Debug build. The same sources compiled with -DMOE_GG_DEBUG (build.build(debug=True) ->
+ * libmoe_gg_debug.so, the same ABI) stand in for a memory checker: each kernel checks the
+ * global accesses whose index comes from device data (offsets, slot and inverse maps, tile
+ * decoding) against the extent of the buffer it addresses, skips an access that fails (or
+ * redirects a copy a barrier waits for to the buffer's first element) and records it; and each
+ * entry point waits for its stream when it returns (not while the stream is being captured),
+ * so that an asynchronous CUDA error is reported by the call that queued the faulting work.
+ * Release builds compile the checks away.
+ *
+ * moe_debug_build -- 1 for a debug build, else 0.
+ * moe_debug_report -- waits for the device (cudaDeviceSynchronize), then writes
+ *   *site_mask   bit s set when check site s failed since the last reset; bit
+ *                MOE_DEBUG_CALL_ERROR_BIT when an entry point found a CUDA error on its
+ *                stream as it returned (moe_last_cuda_error() then names the call);
+ *   *first_site  the first failing site (-1: none), *index its index, *limit the bound the
+ *                index had to stay below (each pointer nullable),
+ *   and clears the record when reset != 0. A release build writes 0 and -1 and returns MOE_OK.
+ *   Returns MOE_ERR_CUDA when the device cannot be read.
+ * moe_debug_site_name -- name of check site s ("?" when out of range; static storage).
+ */
+#define MOE_DEBUG_CALL_ERROR_BIT 30
+int moe_debug_build(void);
+moe_status_t moe_debug_report(int32_t* site_mask, int32_t* first_site, long long* index,
+                              long long* limit, int reset);
+const char* moe_debug_site_name(int site);
+
 #ifdef __cplusplus
 }
 #endif

@@ -13,6 +13,7 @@ import re
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libmoe_gg.so")
+DEBUG_LIB_PATH = os.path.join(_HERE, "libmoe_gg_debug.so")  # same ABI, built with MOE_GG_DEBUG
 HEADER = os.path.join(os.path.dirname(_HERE), "include", "moe_gg.h")
 
 MOE_OK = 0
@@ -25,6 +26,7 @@ OP_ROUTE, OP_FWD, OP_BWD, OP_PADDED_BMM, OP_LOOP, OP_SAVED, OP_MX_WEIGHTS, OP_MX
     range(10)
 
 _P, _I, _S = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+_PI32, _PI64 = ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_longlong)
 SIGNATURES = {
     "moe_workspace_bytes": (_S, [_I, _I, _I, _I, _I, _I, _I]),
     "moe_route_offsets": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P, _S, _P]),
@@ -54,7 +56,11 @@ SIGNATURES = {
     "moe_status_string": (ctypes.c_char_p, [_I]),
     "moe_last_cuda_error": (ctypes.c_char_p, []),
     "moe_abi_version": (_I, []),
+    "moe_debug_build": (_I, []),
+    "moe_debug_report": (_I, [_PI32, _PI32, _PI64, _PI64, _I]),
+    "moe_debug_site_name": (ctypes.c_char_p, [_I]),
 }
+MOE_DEBUG_CALL_ERROR_BIT = 30
 
 _lib = None
 
@@ -76,18 +82,24 @@ def header_functions(path: str = HEADER):
     return sorted(set(re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", text)))
 
 
+def open_library(path: str):
+    """A ctypes handle of a build of the library at `path`, every entry point declared."""
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is not built: run __graft_entry__.build() (nvcc, sm_103a)")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
 def load(path: str = LIB_PATH):
-    """Load the library (once) and declare every entry point's C signature."""
+    """Load the library (once; the first call's path wins, so a process that wants the debug
+    build calls load(DEBUG_LIB_PATH) before anything else) and return its handle."""
     global _lib
     if _lib is None:
-        if not os.path.exists(path):
-            raise RuntimeError(f"{path} is not built: run __graft_entry__.build() (nvcc, sm_103a)")
-        lib = ctypes.CDLL(path)
-        for name, (res, args) in SIGNATURES.items():
-            fn = getattr(lib, name)
-            fn.restype = res
-            fn.argtypes = args
-        _lib = lib
+        _lib = open_library(path)
     return _lib
 
 
@@ -283,3 +295,21 @@ def moe_status_string(status: int) -> str:
 
 def moe_abi_version() -> int:
     return int(load().moe_abi_version())
+
+
+def moe_debug_build() -> bool:
+    return bool(load().moe_debug_build())
+
+
+def moe_debug_report(reset: bool = True, lib=None):
+    """(site_mask, first_site, index, limit) of the debug build's bounds checks since the last
+    reset (waits for the device); (0, -1, 0, 0) from a release build."""
+    L = lib if lib is not None else load()
+    m, s, i, l = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_longlong(), ctypes.c_longlong()
+    _check("moe_debug_report", L.moe_debug_report(ctypes.byref(m), ctypes.byref(s), ctypes.byref(i),
+                                                  ctypes.byref(l), int(reset)))
+    return m.value, s.value, i.value, l.value
+
+
+def moe_debug_site_name(site: int) -> str:
+    return load().moe_debug_site_name(site).decode()

@@ -1,6 +1,10 @@
 """Build libmoe_gg.so in place: every .cu under csrc/ compiled for sm_103a by nvcc, in parallel,
 then linked into one shared library next to this file. Rebuilds only when a source or header is
-newer than the library (or when forced)."""
+newer than the library (or when forced).
+
+build(debug=True) compiles the same sources with -DMOE_GG_DEBUG into libmoe_gg_debug.so (same
+ABI): device-side bounds checks at the data-dependent global accesses and a wait for the stream
+at the end of every entry point, read back with moe_debug_report()."""
 from __future__ import annotations
 
 import concurrent.futures as cf
@@ -14,6 +18,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libmoe_gg.so")
+DEBUG_LIB = os.path.join(PKG, "libmoe_gg_debug.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include")]
@@ -35,21 +40,25 @@ def _inputs():
         glob.glob(os.path.join(ROOT, "include", "*.h")) + [os.path.abspath(__file__)]
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(p) <= t for p in _inputs())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    if not force and up_to_date():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags=(), debug: bool = False) -> str:
+    lib = DEBUG_LIB if debug else LIB
+    if not force and up_to_date(lib):
+        return lib
+    objdir = os.path.join(BUILD, "debug") if debug else BUILD
+    os.makedirs(objdir, exist_ok=True)
     cc = nvcc()
+    if debug:
+        extra_flags = (*extra_flags, "-DMOE_GG_DEBUG")
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src) + ".o")
+        obj = os.path.join(objdir, os.path.basename(src) + ".o")
         cmd = [cc, *ARCH, *FLAGS, *extra_flags, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -61,15 +70,15 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     srcs = sources()
     with cf.ThreadPoolExecutor(max_workers=max(1, min(len(srcs), os.cpu_count() or 4))) as ex:
         objs = list(ex.map(compile_one, srcs))
-    tmp = LIB + ".tmp"
+    tmp = lib + ".tmp"
     cmd = [cc, *ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
     import sys
-    print(build(force="--force" in sys.argv, verbose=True))
+    print(build(force="--force" in sys.argv, verbose=True, debug="--debug" in sys.argv))

@@ -13,6 +13,7 @@
 #include <cuda_runtime.h>
 
 #include "../../include/moe_gg.h"
+#include "debug.cuh"
 
 namespace moe {
 

@@ -375,7 +375,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             const uint32_t sfs = sf0 + s * SF_STAGE_BYTES;
             if (do_a) {
               tma_load_2d(sa, &maps.a, m0, ti.row0, fb);
-              bulk_load(sfs, args.sfa + ((args.tile_base + ti.g) * args.sf_kc + kc) * 512, 512, fb);
+              long long ta = args.tile_base + ti.g;
+              if (!MOE_DBG_IN(DBG_GG_SFA, ta, args.dbg_sfa_tiles)) ta = 0;
+              bulk_load(sfs, args.sfa + (ta * args.sf_kc + kc) * 512, 512, fb);
             }
             if (do_b) {
               const long long eb = static_cast<long long>(eg) * args.sfb_ntpad;
@@ -390,8 +392,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                 nt0 = ti.n0 / 128;
                 nt1 = nt0 + 1;
               }
-              bulk_load(sfs + 512, args.sfb + ((eb + nt0) * args.sf_kc + kc) * 512, 512, fb);
-              bulk_load(sfs + 1024, args.sfb + ((eb + nt1) * args.sf_kc + kc) * 512, 512, fb);
+              long long tb0 = eb + nt0, tb1 = eb + nt1;
+              if (!MOE_DBG_IN(DBG_GG_SFB, tb0, args.dbg_sfb_tiles)) tb0 = 0;
+              if (!MOE_DBG_IN(DBG_GG_SFB, tb1, args.dbg_sfb_tiles)) tb1 = 0;
+              bulk_load(sfs + 512, args.sfb + (tb0 * args.sf_kc + kc) * 512, 512, fb);
+              bulk_load(sfs + 1024, args.sfb + (tb1 * args.sf_kc + kc) * 512, 512, fb);
             }
           } else if constexpr (!ModeTraits<MODE>::wgrad) {
             if (do_a) tma_load_2d(sa, &maps.a, k0, ti.row0, fb);
@@ -570,7 +575,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           gcur[j] = make_float4(0.f, 0.f, 0.f, 0.f);
           ucur[j] = gcur[j];
         }
-        if (r_in < ti.rows && c0 < h16) {
+        if (r_in < ti.rows && c0 < h16 && MOE_DBG_IN(DBG_GG_TILE, args.tile_base + ti.g, args.dbg_u_tiles)) {
           const float4* bg = u_block(args.aux, args.tile_base + ti.g, q, c0, 2 * h16);
           const float4* bu = u_block(args.aux, args.tile_base + ti.g, q, h16 + c0, 2 * h16);
 #pragma unroll
@@ -586,23 +591,28 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * BN;
 
       if constexpr (EPI == MODE_UP_SWIGLU) {
-        const bool rv = r_in < ti.rows;
+        bool rv = r_in < ti.rows;
         const long long row = ti.row0 + r_in;
+        if (rv && !MOE_DBG_IN(DBG_GG_ROW, row, args.cap)) rv = false;
         const int h = args.h;
         bf16* arow = reinterpret_cast<bf16*>(args.out) + row * args.ldo;
         bf16* lrow = args.out3 ? reinterpret_cast<bf16*>(args.out3) + row * args.ldo3 : nullptr;
         const long long G = args.tile_base + ti.g;
+        const bool u_out = args.out2 != nullptr && MOE_DBG_IN(DBG_GG_TILE, G, args.dbg_u_tiles);
         const int h16 = (h + 15) >> 4;
         // P = w*A with the row's routing weight (else P = A): bf16(P) is the down projection's
         // input, P - bf16(P) its low half for the down wgrad
-        const float wrow =
-            (args.row_weight != nullptr && rv) ? __ldg(args.row_weight + __ldg(args.row_src + row)) : 1.0f;
+        float wrow = 1.0f;
+        if (args.row_weight != nullptr && rv) {
+          const int slot = __ldg(args.row_src + row);
+          if (MOE_DBG_IN(DBG_GG_SLOT, slot, args.cap)) wrow = __ldg(args.row_weight + slot);
+        }
         // chunk c's gate and up columns: U (blocked), then bf16(P) and its low half; bf16(P) is
         // also left in pout for the MXFP8 quantization of the pair of chunks
         auto process = [&](int c, const uint32_t (&g)[16], const uint32_t (&u)[16], uint32_t (&pout)[8]) {
           const int col = ti.n0 + c * 16;
           if (!rv || col >= h) return;
-          if (args.out2 != nullptr) {
+          if (u_out) {
             // U in its blocked layout: 512 contiguous bytes per warp-wide store
             uint32_t* bg = reinterpret_cast<uint32_t*>(u_block(args.out2, G, q, col >> 4, 2 * h16));
             uint32_t* bu = reinterpret_cast<uint32_t*>(u_block(args.out2, G, q, h16 + (col >> 4), 2 * h16));
@@ -657,7 +667,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           if constexpr (MX) {
             // the down projection's A operand: bf16(P) of these 32 columns as one MXFP8 block
             const int col = ti.n0 + c * 16;
-            if (args.mxq != nullptr && rv && col < h) {
+            if (args.mxq != nullptr && rv && col < h && MOE_DBG_IN(DBG_GG_MXSF, G, args.dbg_mxsf_tiles)) {
               uint32_t codes[8];
               const uint8_t sc = mx_block_bf16(pq0, pq1, codes);
               st_global_v8(args.mxq + row * args.mx_ldq + col, codes);
@@ -667,9 +677,14 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (more) tmem_ld_wait2(ga, ua);
         }
       } else if constexpr (EPI == MODE_PLAIN_BF16) {
-        const bool rv = r_in < ti.rows;
+        bool rv = r_in < ti.rows;
         const long long row = ti.row0 + r_in;
-        const long long orow_idx = (args.row_dst != nullptr && rv) ? __ldg(args.row_dst + row) : row;
+        if (rv && !MOE_DBG_IN(DBG_GG_ROW, row, args.cap)) rv = false;
+        long long orow_idx = row;
+        if (args.row_dst != nullptr && rv) {
+          orow_idx = __ldg(args.row_dst + row);
+          if (!MOE_DBG_IN(DBG_GG_DST, orow_idx, args.dbg_dst_rows)) rv = false;
+        }
         bf16* orow = reinterpret_cast<bf16*>(args.out) + orow_idx * args.ldo;
         // 32 columns (two 16-column chunks) at a time; the next pair's accumulator columns are
         // in flight while this pair is converted and stored
@@ -712,15 +727,20 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (more) tmem_ld_wait2(va, vb);
         }
       } else if constexpr (EPI == MODE_DGRAD_SWIGLU) {
-        const bool rv = r_in < ti.rows;
+        bool rv = r_in < ti.rows;
         const long long row = ti.row0 + r_in;
+        if (rv && !MOE_DBG_IN(DBG_GG_ROW, row, args.cap)) rv = false;
         const int h = args.h;
         const int h16 = (h + 15) >> 4;
         const long long G = args.tile_base + ti.g;
+        const bool u_in = MOE_DBG_IN(DBG_GG_TILE, G, args.dbg_u_tiles);
         bf16* hrow = reinterpret_cast<bf16*>(args.out) + row * args.ldo;
         bf16* lrow = reinterpret_cast<bf16*>(args.out2) + row * args.ldo2;
-        const float wrow =
-            (args.row_weight != nullptr && rv) ? __ldg(args.row_weight + __ldg(args.row_src + row)) : 1.0f;
+        float wrow = 1.0f;
+        if (args.row_weight != nullptr && rv) {
+          const int slot = __ldg(args.row_src + row);
+          if (MOE_DBG_IN(DBG_GG_SLOT, slot, args.cap)) wrow = __ldg(args.row_weight + slot);
+        }
         // A warp whose 32 rows all belong to the tile's expert sends whole 16-column chunks out
         // through two 1 KB staging boxes (32-byte swizzle: lane r's 16-byte piece j at piece
         // j ^ ((r >> 2) & 1), conflict-free) and TMA tensor stores: full sectors from the copy
@@ -751,7 +771,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             gq[j] = make_float4(0.f, 0.f, 0.f, 0.f);
             uq[j] = gq[j];
           }
-          if (rv && ci < h16) {
+          if (rv && ci < h16 && u_in) {
             const float4* bg = u_block(args.aux, G, q, ci, 2 * h16);
             const float4* bu = u_block(args.aux, G, q, h16 + ci, 2 * h16);
 #pragma unroll
@@ -855,7 +875,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             // the up/gate dgrad's A operand: dU's high half of these 32 gate and 32 up columns
             // as two MXFP8 blocks along 2h
             const int col = ti.n0 + c * 16;
-            if (args.mxq != nullptr && rv && col < h) {
+            if (args.mxq != nullptr && rv && col < h && MOE_DBG_IN(DBG_GG_MXSF, G, args.dbg_mxsf_tiles)) {
               uint32_t codes[8];
               uint8_t* qrow = args.mxq + row * args.mx_ldq;
               uint8_t sc = mx_block_bf16(qg0, qg1, codes);
@@ -961,6 +981,8 @@ moe_status_t launch_mode(const GemmMaps& maps, const GemmArgs& args, long long m
 }
 
 }  // namespace
+
+MOE_DBG_DEFINE_COLLECTOR(dbg_collect_grouped)
 
 int gemm_tiles_n(int mode, int N) {
   const int w = (mode == MODE_UP_SWIGLU || mode == MODE_UP_SWIGLU_MX) ? 128 : BN;

@@ -107,6 +107,15 @@ struct GemmArgs {
   const uint8_t* sfb;
   int sf_kc;
   int sfb_ntpad;
+  // Debug builds (MOE_GG_DEBUG) only: the extents the bounds checks compare against -- row
+  // tiles of the blocked saved U (read or written), of the activation scale atoms read (sfa) and
+  // of those the epilogue writes (mxsf), tiles of the weight scale atoms (sfb), and the rows of
+  // the row_dst output
+  long long dbg_u_tiles;
+  long long dbg_sfa_tiles;
+  long long dbg_mxsf_tiles;
+  long long dbg_sfb_tiles;
+  long long dbg_dst_rows;
   int32_t* status;         // optional device status word
   long long timeout_ns;    // bound of every wait of the main loops
   // bound of the teardown waits that let this CTA's in-flight copies and MMAs finish before it
@@ -139,6 +148,37 @@ bool make_map_u8_rows2d(CUtensorMap* map, const void* ptr, long long rows, long 
 bool make_map_u8_weight3d(CUtensorMap* map, const void* ptr, long long E, long long R, long long C, int box_r);
 
 int gemm_tiles_n(int mode, int N);  // column tiles of one problem
+
+// ------------------------------------------------------------------ debug build (debug.cuh)
+// Check sites of the bounds checks; the names moe_debug_site_name() returns follow this order.
+enum DbgSite : int {
+  DBG_GG_ROW = 0,       // grouped kernel: an epilogue row against the row buffers' rows (cap)
+  DBG_GG_TILE = 1,      // grouped kernel: a row tile of the blocked saved U
+  DBG_GG_SLOT = 2,      // grouped kernel: a row's flat slot (row_src) against cap
+  DBG_GG_DST = 3,       // grouped kernel: a destination row (row_dst) against the output's rows
+  DBG_GG_SFA = 4,       // grouped kernel (MXFP8): a row tile of the activation scale atoms read
+  DBG_GG_SFB = 5,       // grouped kernel (MXFP8): a tile of the weight scale atoms read
+  DBG_GG_MXSF = 6,      // grouped kernel (MXFP8): a row tile of the scale atoms the epilogue writes
+  DBG_COMBINE_ROW = 7,  // combine: an inverse-map row against T*top_k
+  DBG_RWG_ROW = 8,      // routing-weight gradient: an inverse-map row against the slots
+  DBG_ROUTE_POS = 9,    // route scatter: a slot's placed row against T*top_k
+  DBG_MX_TILE = 10,     // MXFP8 quantization: a scale-atom tile against the atoms buffer
+  DBG_SITES = 11
+};
+
+struct DbgRecord {
+  int mask;         // bit s: check site s failed at least once
+  int site;         // first failing site (-1: none)
+  long long index;  // its index
+  long long limit;  // and the bound the index had to stay below
+};
+
+// One per kernel translation unit: merge its record into *acc, clear it when `reset` (no-ops in
+// release builds).
+cudaError_t dbg_collect_grouped(DbgRecord* acc, bool reset);
+cudaError_t dbg_collect_permute(DbgRecord* acc, bool reset);
+cudaError_t dbg_collect_route(DbgRecord* acc, bool reset);
+cudaError_t dbg_collect_mx(DbgRecord* acc, bool reset);
 
 // ------------------------------------------------------------------ helpers
 int device_sm_count();              // SMs of the current device (cached per device)

@@ -2,6 +2,7 @@
 // construction and stream-ordered launches. No entry point allocates device memory; only
 // moe_loop_swiglu_fwd synchronises (by design, it is the host-scheduled comparison variant).
 #include <algorithm>
+#include <atomic>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
@@ -143,6 +144,7 @@ moe_status_t run_up_swiglu(const GemmArgs& src, long long rows, long long tiles_
     a.out2 = const_cast<void*>(saved_u(saved, rows, h));
     a.out3 = saved;
     a.ldo3 = h;
+    a.dbg_u_tiles = saved_u_tiles(rows, E);
   }
   a.vec32 = (h % 16 == 0 && aligned32(a_save) && (saved == nullptr || aligned32(saved))) ? 1 : 0;
   return launch_grouped_gemm(MODE_UP_SWIGLU, m, a, tiles_bound * gemm_tiles_n(MODE_UP_SWIGLU, h), s);
@@ -180,6 +182,7 @@ moe_status_t run_down_dgrad_swiglu(const GemmArgs& src, long long rows, int E, i
   a.out2 = du_lo;
   a.ldo2 = 2LL * h;
   a.aux = saved_u(saved, rows, h);
+  a.dbg_u_tiles = saved_u_tiles(rows, E);
   a.vec32 = (h % 16 == 0 && aligned32(du_hi) && aligned32(du_lo)) ? 1 : 0;
   a.dw_part = dw_part;
   a.dw_np = route_grad_parts(h);
@@ -331,6 +334,22 @@ moe_status_t check_device() {
   return ok_cache[dev] == 1 ? MOE_OK : MOE_ERR_UNSUPPORTED_DEVICE;
 }
 
+#ifdef MOE_GG_DEBUG
+namespace {
+std::atomic<bool> g_dbg_call_error{false};
+}  // namespace
+
+void dbg_after_call(const char* name, cudaStream_t stream) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) return;
+  const cudaError_t err = cudaStreamSynchronize(stream);
+  if (err == cudaSuccess) return;
+  g_dbg_call_error = true;
+  std::snprintf(g_last_error, sizeof(g_last_error), "%s: %s: %s", name, cudaGetErrorName(err),
+                cudaGetErrorString(err));
+}
+#endif
+
 }  // namespace moe
 
 using namespace moe;
@@ -338,6 +357,45 @@ using namespace moe;
 extern "C" {
 
 int moe_abi_version(void) { return 2; }
+
+int moe_debug_build(void) {
+#ifdef MOE_GG_DEBUG
+  return 1;
+#else
+  return 0;
+#endif
+}
+
+moe_status_t moe_debug_report(int32_t* site_mask, int32_t* first_site, long long* index, long long* limit,
+                              int reset) {
+  DbgRecord acc = {0, -1, 0, 0};
+#ifdef MOE_GG_DEBUG
+  cudaError_t err = cudaDeviceSynchronize();
+  if (err == cudaSuccess) err = dbg_collect_grouped(&acc, reset != 0);
+  if (err == cudaSuccess) err = dbg_collect_permute(&acc, reset != 0);
+  if (err == cudaSuccess) err = dbg_collect_route(&acc, reset != 0);
+  if (err == cudaSuccess) err = dbg_collect_mx(&acc, reset != 0);
+  if (err != cudaSuccess) return cuda_fail(err);
+  if (g_dbg_call_error) acc.mask |= 1 << MOE_DEBUG_CALL_ERROR_BIT;
+  if (reset) g_dbg_call_error = false;
+#else
+  (void)reset;
+#endif
+  if (site_mask) *site_mask = acc.mask;
+  if (first_site) *first_site = acc.site;
+  if (index) *index = acc.index;
+  if (limit) *limit = acc.limit;
+  return MOE_OK;
+}
+
+const char* moe_debug_site_name(int site) {
+  static const char* const names[DBG_SITES] = {
+      "grouped: epilogue row", "grouped: saved U row tile", "grouped: row slot",
+      "grouped: destination row", "grouped: activation scale tile", "grouped: weight scale tile",
+      "grouped: written scale tile", "combine: inverse-map row", "routing-weight grad: inverse-map row",
+      "route: placed row", "mxfp8 quantization: scale tile"};
+  return (site >= 0 && site < DBG_SITES) ? names[site] : "?";
+}
 
 const char* moe_last_cuda_error(void) { return g_last_error; }
 
@@ -734,6 +792,7 @@ moe_status_t moe_grouped_swiglu_fwd_top1_combine(const moe_bf16* xp, const int32
   GemmArgs dsrc = base_args(E, cap, dev_status);  // the weight is already in a_save
   dsrc.offsets = offsets;
   dsrc.row_dst = sorted_src;                      // flat slot = token when top_k = 1
+  dsrc.dbg_dst_rows = T;
   return run_down(dsrc, cap, tb, E, d, h, a_save, w_down, out, s);
 }
 
@@ -875,11 +934,14 @@ size_t mx_bwd_ws_bytes(long long cap, int E, int d, int h) {
          mx_asf_bytes(cap, E, 2 * h);
 }
 
-void set_mx(GemmArgs& a, const void* sfa, const void* sfb, int K, int N_b) {
+void set_mx(GemmArgs& a, const void* sfa, const void* sfb, int K, int N_b, long long rows, int E) {
   a.sfa = static_cast<const uint8_t*>(sfa);
   a.sfb = static_cast<const uint8_t*>(sfb);
   a.sf_kc = mx_kc(K);
   a.sfb_ntpad = mx_ntpad(N_b);
+  a.dbg_sfa_tiles = saved_u_tiles(rows, E);
+  a.dbg_sfb_tiles = static_cast<long long>(E) * mx_ntpad(N_b);
+  a.dbg_mxsf_tiles = saved_u_tiles(rows, E);
 }
 
 // U = q(xp) q(W_ug)^T with the up/gate epilogue of the BF16 path (a_save, optional saved); the
@@ -900,9 +962,10 @@ moe_status_t run_up_swiglu_mx(const GemmArgs& src, long long rows, long long til
     a.out2 = const_cast<void*>(saved_u(saved, rows, h));
     a.out3 = saved;
     a.ldo3 = h;
+    a.dbg_u_tiles = saved_u_tiles(rows, E);
   }
   a.vec32 = (h % 16 == 0 && aligned32(a_save) && (saved == nullptr || aligned32(saved))) ? 1 : 0;
-  set_mx(a, xsf, w.ug_sf, d, 2 * h);
+  set_mx(a, xsf, w.ug_sf, d, 2 * h, rows, E);
   a.mxq = static_cast<uint8_t*>(pq);
   a.mxsf = static_cast<uint8_t*>(psf);
   a.mx_ldq = h;
@@ -923,7 +986,7 @@ moe_status_t run_plain_mx(const GemmArgs& src, long long rows, long long tiles_b
   a.out = out;
   a.ldo = N;
   a.vec32 = (N % 16 == 0 && aligned32(out)) ? 1 : 0;
-  set_mx(a, asf, bsf, K, N);
+  set_mx(a, asf, bsf, K, N, rows, E);
   return launch_grouped_gemm(MODE_PLAIN_MX, m, a, tiles_bound * gemm_tiles_n(MODE_PLAIN_MX, N), s);
 }
 
@@ -946,10 +1009,11 @@ moe_status_t run_dgrad_mx(const GemmArgs& src, long long rows, int E, int d, int
   a.out2 = du_lo;
   a.ldo2 = 2LL * h;
   a.aux = saved_u(saved, rows, h);
+  a.dbg_u_tiles = saved_u_tiles(rows, E);
   a.vec32 = (h % 16 == 0 && aligned32(du_hi) && aligned32(du_lo)) ? 1 : 0;
   a.dw_part = dw_part;
   a.dw_np = route_grad_parts(h);
-  set_mx(a, dysf, w.dn_sf, d, h);
+  set_mx(a, dysf, w.dn_sf, d, h, rows, E);
   a.mxq = static_cast<uint8_t*>(duq);
   a.mxsf = static_cast<uint8_t*>(dusf);
   a.mx_ldq = 2 * h;

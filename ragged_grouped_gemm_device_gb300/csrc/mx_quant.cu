@@ -123,7 +123,7 @@ __global__ void __launch_bounds__(256) mx_quant_rows_kernel(const bf16* __restri
                                                             int K, const int32_t* __restrict__ offsets,
                                                             int E, int per_expert, int ntpad,
                                                             uint8_t* __restrict__ q, uint8_t* __restrict__ sf,
-                                                            int32_t* status) {
+                                                            long long sf_tiles, int32_t* status) {
   __shared__ int s_end[MAX_E];   // inclusive offsets
   __shared__ int s_pre[MAX_E];   // 128-row tiles of the experts before e
   const bool act = offsets != nullptr;
@@ -162,6 +162,7 @@ __global__ void __launch_bounds__(256) mx_quant_rows_kernel(const bf16* __restri
     uint4* d4 = reinterpret_cast<uint4*>(q + p * K + b * MXB);
     d4[0] = make_uint4(c[0], c[1], c[2], c[3]);
     d4[1] = make_uint4(c[4], c[5], c[6], c[7]);
+    if (!MOE_DBG_IN(DBG_MX_TILE, G, sf_tiles)) continue;
     sf[atom_byte(G, KC, b, r)] = code;
     if (b == nb - 1) fill_chunk_tail(sf, G, KC, nb, r);
   }
@@ -176,7 +177,7 @@ __global__ void __launch_bounds__(256) mx_permute_quant_kernel(const uint4* __re
                                                                const int32_t* __restrict__ offsets, int E,
                                                                int n, int k, int d, uint4* __restrict__ xp,
                                                                uint8_t* __restrict__ q, uint8_t* __restrict__ sf,
-                                                               int32_t* status) {
+                                                               long long sf_tiles, int32_t* status) {
   __shared__ int s_end[MAX_E];
   __shared__ int s_pre[MAX_E];
   if (!load_problem_tiles(offsets, E, n, s_end, s_pre, status)) return;
@@ -214,7 +215,7 @@ __global__ void __launch_bounds__(256) mx_permute_quant_kernel(const uint4* __re
         const uint32_t lo = e4m3x2(f[0] * inv, f[1] * inv) | (e4m3x2(f[2] * inv, f[3] * inv) << 16);
         const uint32_t hi = e4m3x2(f[4] * inv, f[5] * inv) | (e4m3x2(f[6] * inv, f[7] * inv) << 16);
         *reinterpret_cast<uint2*>(q + static_cast<size_t>(p) * d + v * 8) = make_uint2(lo, hi);
-        if ((lane & 3) == 0) {
+        if ((lane & 3) == 0 && MOE_DBG_IN(DBG_MX_TILE, G, sf_tiles)) {
           const int b = v >> 2;
           sf[atom_byte(G, KC, b, r)] = static_cast<uint8_t>(e8 + 127);
           if (b == nb - 1) fill_chunk_tail(sf, G, KC, nb, r);
@@ -249,6 +250,7 @@ __global__ void __launch_bounds__(256) mx_quant_cols_kernel(const bf16* __restri
     d4[0] = make_uint4(cd[0], cd[1], cd[2], cd[3]);
     d4[1] = make_uint4(cd[4], cd[5], cd[6], cd[7]);
     const long long G = static_cast<long long>(e) * ntpad + c / 128;
+    if (!MOE_DBG_IN(DBG_MX_TILE, G, static_cast<long long>(E) * ntpad)) continue;
     sf[atom_byte(G, KC, b, c % 128)] = code;
     if (b == nb - 1) fill_chunk_tail(sf, G, KC, nb, c % 128);
   }
@@ -259,7 +261,13 @@ int grid_for(long long items) {
   return static_cast<int>(std::max(1LL, std::min<long long>(blocks, 16LL * device_sm_count())));
 }
 
+// scale-atom tiles of a problem list of at most `rows` rows over E experts (each expert's segment
+// starts a tile): the size the activation scale buffers are given
+long long activation_sf_tiles(long long rows, int E) { return (rows + 127LL * E) / 128; }
+
 }  // namespace
+
+MOE_DBG_DEFINE_COLLECTOR(dbg_collect_mx)
 
 int mx_ntpad(int N) { return 2 * ((((N + 127) / 128) + 1) / 2); }
 int mx_kc(int K) { return (K + 127) / 128; }
@@ -270,9 +278,10 @@ moe_status_t launch_mx_quant_rows(const void* src, long long rows, int K, const 
   const long long items = rows * (K / MXB);
   if (items == 0) return MOE_OK;
   const int ntpad = offsets ? 0 : mx_ntpad(per_expert);
+  const long long sf_tiles = offsets ? activation_sf_tiles(rows, E) : (rows / per_expert) * ntpad;
   mx_quant_rows_kernel<<<grid_for(items), 256, 0, s>>>(static_cast<const bf16*>(src), rows, K, offsets, E,
                                                        per_expert, ntpad, static_cast<uint8_t*>(q),
-                                                       static_cast<uint8_t*>(sf), status);
+                                                       static_cast<uint8_t*>(sf), sf_tiles, status);
   const cudaError_t err = cudaGetLastError();
   return err == cudaSuccess ? MOE_OK : cuda_fail(err);
 }
@@ -285,7 +294,7 @@ moe_status_t launch_mx_permute_quant(const void* x, const int32_t* sorted_src, c
   const int blocks = std::max(1, std::min((n + 7) / 8, 8 * device_sm_count()));
   mx_permute_quant_kernel<<<blocks, 256, 0, s>>>(static_cast<const uint4*>(x), sorted_src, offsets, E, n, k, d,
                                                  static_cast<uint4*>(xp), static_cast<uint8_t*>(q),
-                                                 static_cast<uint8_t*>(sf), status);
+                                                 static_cast<uint8_t*>(sf), activation_sf_tiles(n, E), status);
   const cudaError_t err = cudaGetLastError();
   return err == cudaSuccess ? MOE_OK : cuda_fail(err);
 }

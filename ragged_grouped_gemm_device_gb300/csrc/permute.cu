@@ -101,7 +101,7 @@ __global__ void __launch_bounds__(THREADS) combine_kernel(const uint4* __restric
           const int j = j0 + jj;
           const int p = __shfl_sync(0xffffffffu, my_p, j & 31);
           wj[jj] = __shfl_sync(0xffffffffu, my_w, j & 31);
-          ok[jj] = active && j < k && p >= 0;
+          ok[jj] = active && j < k && p >= 0 && MOE_DBG_IN(DBG_COMBINE_ROW, p, static_cast<long long>(T) * k);
           q[jj] = ok[jj] ? __ldg(y + static_cast<size_t>(p) * vec + v) : make_uint4(0u, 0u, 0u, 0u);
         }
 #pragma unroll
@@ -132,7 +132,7 @@ __global__ void __launch_bounds__(THREADS) routing_weight_grad_kernel(
   for (int sl = blockIdx.x * THREADS + threadIdx.x; sl < n_slots; sl += gridDim.x * THREADS) {
     const int p = __ldg(inv + sl);
     float acc = 0.f;
-    if (p >= 0)
+    if (p >= 0 && MOE_DBG_IN(DBG_RWG_ROW, p, n_slots))
       for (int i = 0; i < np; ++i) acc += __ldg(part + static_cast<size_t>(p) * np + i);
     dw[sl] = acc;
   }
@@ -172,7 +172,7 @@ __global__ void __launch_bounds__(THREADS) combine_scalar_kernel(const bf16* __r
       float acc = 0.f;
       for (int j = 0; j < k; ++j) {
         const int p = __ldg(inv + static_cast<size_t>(t) * k + j);
-        if (p < 0) continue;
+        if (p < 0 || !MOE_DBG_IN(DBG_COMBINE_ROW, p, static_cast<long long>(T) * k)) continue;
         const float wj = weights ? __ldg(weights + static_cast<size_t>(t) * k + j) : 1.0f;
         acc = fmaf(wj, __bfloat162float(y[static_cast<size_t>(p) * d + c]), acc);
       }
@@ -288,6 +288,8 @@ moe_status_t last_launch() {
 }
 
 }  // namespace
+
+MOE_DBG_DEFINE_COLLECTOR(dbg_collect_permute)
 
 moe_status_t launch_permute(const void* x, const int32_t* sorted_src, const int32_t* offsets,
                             const float* row_scale, int n, int k, int E, int d, void* xp,

@@ -21,6 +21,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "trace.h"
 
 namespace moe {
 namespace {
@@ -153,8 +154,10 @@ __global__ void __launch_bounds__(256) route_scatter_kernel(
       const unsigned peers = __match_any_sync(0xffffffffu, key);
       if (valid) {
         const int pos = run[e] + __popc(peers & ((1u << lane) - 1u));
-        sorted_src[pos] = i;
-        inv_map[i] = pos;
+        if (MOE_DBG_IN(DBG_ROUTE_POS, pos, n)) {
+          sorted_src[pos] = i;
+          inv_map[i] = pos;
+        }
       } else if (i < n) {
         inv_map[i] = -1;
       }
@@ -169,6 +172,8 @@ __global__ void __launch_bounds__(256) route_scatter_kernel(
 }
 
 }  // namespace
+
+MOE_DBG_DEFINE_COLLECTOR(dbg_collect_route)
 
 size_t route_workspace_bytes(long long n, int E) {
   const long long W = (n + CHUNK - 1) / CHUNK;
@@ -273,6 +278,7 @@ extern "C" moe_status_t moe_route_offsets_noalloc(const int32_t* ids, int T, int
                                                   int32_t* sorted_src, int32_t* inv_map,
                                                   moe_stream_t stream) {
   using namespace moe;
+  MOE_TRACE_CALL();
   if (T < 0 || top_k < 1) return MOE_ERR_INVALID_ARG;
   if (top_k > 32 || E < 1 || E > MAX_E) return MOE_ERR_UNSUPPORTED_SHAPE;
   const long long n = static_cast<long long>(T) * top_k;

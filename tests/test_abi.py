@@ -132,3 +132,22 @@ def test_binding_argument_counts_match_header():
         params = m.group(1).strip()
         n = 0 if params in ("", "void") else params.count(",") + 1
         assert len(args) == n, (name, len(args), n)
+
+
+def test_debug_build_loads_with_the_same_abi(lib):
+    """libmoe_gg_debug.so (MOE_GG_DEBUG: device-side bounds checks, a wait at the end of each
+    call) exports the same functions, says it is the debug build, and validates arguments on the
+    host exactly as the release build does. A release build reports no failed check without
+    touching CUDA."""
+    dbg = _lib.open_library(build.build(debug=True))
+    for name in _lib.header_functions():
+        assert hasattr(dbg, name), name
+    assert dbg.moe_debug_build() == 1 and lib.moe_debug_build() == 0
+    assert dbg.moe_abi_version() == lib.moe_abi_version()
+    assert _lib.moe_debug_report(lib=lib) == (0, -1, 0, 0)
+    p = ctypes.c_void_p(16)
+    for L in (lib, dbg):
+        assert L.moe_route_offsets(p, 10, 1, 0, p, p, p, p, p, 1 << 20, None) == 2      # E = 0
+        assert L.moe_permute(ctypes.c_void_p(18), p, p, None, 10, 1, 4, 16, p, None) == 1  # misaligned
+    names = [dbg.moe_debug_site_name(s).decode() for s in range(11)]
+    assert len(set(names)) == 11 and "?" not in names and dbg.moe_debug_site_name(11) == b"?"
