@@ -10,6 +10,14 @@ import torch
 from . import _lib
 
 
+def _dense(t: torch.Tensor) -> torch.Tensor:
+    """The library reads row-major contiguous rows. A view with other strides -- notably the
+    zero-stride gradient a scalar loss broadcasts back (`out.sum().backward()` hands over an
+    expanded [T, d] tensor with strides (0, 0)), which "Grouped expert GEMM" lists as an edge case
+    of the grouped GEMM's backward -- is materialised once here; dense tensors pass through."""
+    return t if t.is_contiguous() else t.contiguous()
+
+
 class ExpertLayer:
     """Holds the expert weights W_ug [E, 2h, d] and W_down [E, h, d] (bf16, on the device)."""
 
@@ -54,6 +62,7 @@ class ExpertLayer:
 
     def forward(self, x: torch.Tensor, ids: torch.Tensor, weights: torch.Tensor, stream=None):
         """x [T, d] bf16, ids [T, k] int32, weights [T, k] fp32 -> out [T, d] bf16."""
+        x, ids, weights = _dense(x), _dense(ids), _dense(weights)
         T, k = ids.shape
         self._buffers(T, k)
         self.T, self.k, self.weights = T, k, weights
@@ -78,6 +87,7 @@ class ExpertLayer:
         """dout [T, d] bf16 -> (dx [T, d] bf16, dW_ug [E, 2h, d] fp32, dW_down [E, h, d] fp32,
         d_weights [T, k] fp32: the gradient of the routing weights, 0 for dropped slots)."""
         T, k, E, d, h, n = self.T, self.k, self.E, self.d, self.h, self.T * self.k
+        dout = _dense(dout)
         _lib.moe_permute(dout, self.sorted_src, self.offsets, None, T, k, E, d, self.dy, stream)
         _lib.moe_grouped_bwd(self.dy, self.xp, self.a, self.saved, self.offsets, self.sorted_src, self.weights,
                              E, n, d, h, self.w_ug,

@@ -91,3 +91,39 @@ def test_layer_is_deterministic(lib):
     for a, b in zip(*runs):
         assert torch.equal(a.view(torch.uint8) if a.dtype == torch.bfloat16 else a.view(torch.int32),
                            b.view(torch.uint8) if b.dtype == torch.bfloat16 else b.view(torch.int32))
+
+
+def test_zero_stride_upstream_gradient(lib):
+    """A scalar loss broadcasts its gradient back as an expanded [T, d] view with strides (0, 0)
+    ("Grouped expert GEMM": zero-stride gradients from .sum() reach the grouped GEMM's backward).
+    The layer takes it and gives the same bits as for the dense tensor of the same values; a
+    transposed (non-contiguous) input x likewise."""
+    wl = W.custom(T=96, k=2, E=5, d=128, h=64, seed=31, empty_experts=(1,))
+    w_ug, w_down = G.device_weights(wl)
+    ids, w = G.dev_i32(wl.ids), G.dev_f32(wl.weights)
+    x = G.dev_bf16(wl.x())
+    results = []
+    for variant in ("dense", "strided"):
+        layer = ExpertLayer(w_ug, w_down)
+        xin = x if variant == "dense" else x.t().contiguous().t()  # same values, column-major
+        assert variant == "dense" or not xin.is_contiguous()
+        out = layer.forward(xin, ids, w).clone()
+        g = torch.full((), 0.75, dtype=torch.bfloat16, device="cuda").expand(wl.T, wl.d)
+        assert g.stride() == (0, 0)
+        dout = g.contiguous() if variant == "dense" else g
+        res = [t.clone() for t in layer.backward(dout)]
+        torch.cuda.synchronize()
+        assert layer.status.item() == 0
+        results.append([out] + res)
+    for a, b in zip(*results):
+        assert torch.equal(a, b)
+    # and the values are the oracle's for that constant gradient
+    doutn = np.full((wl.T, wl.d), 0.75, np.float32)
+    o_out, o_dx, o_ug, o_dn, o_dwr = _oracle_layer(wl, doutn)
+    out, dx, dw_ug, dw_down, dwr = results[1]
+    G.assert_close(G.host(out), o_out, "out[zero-stride]")
+    G.assert_close(G.host(dx), o_dx, "dx[zero-stride]")
+    G.assert_close(G.host(dwr), o_dwr, "d_weights[zero-stride]")
+    nz = np.bincount(wl.ids.ravel(), minlength=wl.E) > 0
+    G.assert_close(G.host(dw_ug)[nz], o_ug[nz], "dW_ug[zero-stride]")
+    G.assert_close(G.host(dw_down)[nz], o_dn[nz], "dW_down[zero-stride]")
