@@ -144,6 +144,19 @@ else:
     dw = torch.empty(n, device=dev)
     L.moe_routing_weight_grad(part, bad_inv, T, k, 128, dw)
     found["rwg"] = L.moe_debug_report(reset=True)
+    # (4) top_k = 1: the down projection meets a destination token row past T (and the up/gate
+    # epilogue, reading the same slot map for the weight, a slot past cap = T)
+    w1 = W.custom(T=80, k=1, E=4, d=128, h=128, seed=78)
+    offs1, ss1, inv1 = route(w1)
+    bad1 = ss1.clone()
+    bad1[3] = w1.T + 9
+    xp1 = torch.empty(w1.n, w1.d, dtype=bf16, device=dev)
+    L.moe_permute(bf(w1.x()), ss1, offs1, None, w1.T, 1, w1.E, w1.d, xp1)
+    o1 = torch.empty(w1.T, w1.d, dtype=bf16, device=dev)
+    a1 = torch.empty(w1.T, w1.h, dtype=bf16, device=dev)
+    L.moe_grouped_swiglu_fwd_top1_combine(xp1, offs1, bad1, inv1, torch.from_numpy(w1.weights).to(dev), w1.E,
+                                          w1.T, w1.d, w1.h, bf(w1.w_ug_all()), bf(w1.w_down_all()), o1, a1)
+    found["dst"] = L.moe_debug_report(reset=True)
     found["clean"] = L.moe_debug_report(reset=True)
     print(json.dumps({k: list(v) for k, v in found.items()}), flush=True)
 """
@@ -183,5 +196,8 @@ def test_debug_build_catches_planted_indices(debug_lib, tmp_path):
     assert got["combine"] == [1 << sites["combine_row"], sites["combine_row"], n + 5, n]
     assert got["slot"] == [1 << sites["gg_slot"], sites["gg_slot"], n + 7, cap]
     assert got["rwg"] == [1 << sites["rwg_row"], sites["rwg_row"], n + 5, n]
+    # both the slot read for the weight (up/gate) and the destination row (down) are caught; the
+    # up/gate launch runs first, so its site is the first failure
+    assert got["dst"] == [(1 << sites["gg_slot"]) | (1 << sites["gg_dst"]), sites["gg_slot"], 80 + 9, 80]
     assert got["clean"] == [0, -1, 0, 0]
     assert L.moe_debug_site_name(sites["combine_row"]).startswith("combine")
