@@ -640,6 +640,8 @@ def run_ours(args):
     traffic = load_traffic().get(dom)
     roofline["traffic"] = traffic
     fwd_ms = per_call["up_swiglu"] + per_call["down"]
+    # the forward layer a1-a8: routing, gather, both projections and the combine
+    fwd_layer_ms = sum(per_call[c] for c in ("route", "permute", "up_swiglu", "down", "combine"))
     peak_tf = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
 
     # ---- end to end through the public calls with host buffers (pinned), copies inside. As a
@@ -805,6 +807,8 @@ def run_ours(args):
         "fwd": {"ms": fwd_ms, "tflops": 6.0 * mdh / (fwd_ms * 1e-3) / 1e12,
                 "frac_of_burst_peak": 6.0 * mdh / (fwd_ms * 1e-3) / 1e12 / peak_tf,
                 "peak_source": f"bf16_tflops ({peak_src}, burst: the timed region lasts well under a second)"},
+        "fwd_layer": {"ms": fwd_layer_ms, "tflops": 6.0 * mdh / (fwd_layer_ms * 1e-3) / 1e12,
+                      "span": "route, permute, up/gate + SwiGLU, down, combine (in the training step)"},
         "roofline": roofline,
         "e2e": {"value": job_tflops(world, fwdbwd_flops, e2e_ms), "unit": "TFLOP/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
