@@ -512,6 +512,69 @@ def config_variants(L, names=VARIANT_CONFIGS):
     return res
 
 
+class TrainingStep:
+    """One training step of the hot path as the benchmark times it: every row a1-a14 as one C-ABI
+    call per kernel (13 launches), on buffers allocated once for T tokens, top_k slots, E experts
+    and widths d, h. `calls(x, ids, weights, dout)` lists (name, launches, thunk) in step order:
+    route, gather, up/gate + SwiGLU, down, combine, dOut gather, down dgrad + SwiGLU backward with
+    the routing-gradient partials, their reduction, up/gate dgrad, both wgrads in one launch,
+    input-gradient combine. The full-size parity test runs these same calls."""
+
+    def __init__(self, L, T, k, E, d, h, w_ug, w_down, dev):
+        import torch
+        self.L, self.T, self.k, self.E, self.d, self.h = L, T, k, E, d, h
+        self.n = n = T * k
+        self.w_ug, self.w_down = w_ug, w_down
+        bf, i32, f32, u8 = torch.bfloat16, torch.int32, torch.float32, torch.uint8
+        self.counts = torch.empty(E, dtype=i32, device=dev)
+        self.offsets = torch.empty(E, dtype=i32, device=dev)
+        self.sorted_src = torch.empty(n, dtype=i32, device=dev)
+        self.inv_map = torch.empty(n, dtype=i32, device=dev)
+        self.route_ws = torch.empty(max(L.moe_workspace_bytes(L.OP_ROUTE, T, k, E), 1), dtype=u8, device=dev)
+        self.xp = torch.empty(n, d, dtype=bf, device=dev)
+        self.a = torch.empty(n, h, dtype=bf, device=dev)
+        self.y = torch.empty(n, d, dtype=bf, device=dev)
+        self.saved = torch.empty(L.moe_workspace_bytes(L.OP_SAVED, T, k, E, d, h), dtype=u8, device=dev)
+        self.out = torch.empty(T, d, dtype=bf, device=dev)
+        self.dy = torch.empty(n, d, dtype=bf, device=dev)
+        self.du_hi = torch.empty(n, 2 * h, dtype=bf, device=dev)
+        self.du_lo = torch.empty(n, 2 * h, dtype=bf, device=dev)
+        self.dxp = torch.empty(n, d, dtype=bf, device=dev)
+        self.dx = torch.empty(T, d, dtype=bf, device=dev)
+        self.dw_ug = torch.empty(E, 2 * h, d, dtype=f32, device=dev)
+        self.dw_down = torch.empty(E, h, d, dtype=f32, device=dev)
+        self.dw_part = torch.empty(n, L.routing_grad_parts(h), dtype=f32, device=dev)
+        self.dw_route = torch.empty(T, k, dtype=f32, device=dev)
+        self.status = torch.zeros(1, dtype=i32, device=dev)
+        _, self.p_lo = L.saved_views(self.saved, n, h)
+
+    def calls(self, xin, idin, win, doin):
+        L, T, k, E, d, h, n = self.L, self.T, self.k, self.E, self.d, self.h, self.n
+        w_ug, w_down, status = self.w_ug, self.w_down, self.status
+        counts, offsets, sorted_src, inv_map = self.counts, self.offsets, self.sorted_src, self.inv_map
+        xp, a, y, saved, out, dy = self.xp, self.a, self.y, self.saved, self.out, self.dy
+        du_hi, du_lo, dxp, dx, dw_part = self.du_hi, self.du_lo, self.dxp, self.dx, self.dw_part
+        return [
+            ("route", 3, lambda: L.moe_route_offsets(idin, T, k, E, counts, offsets, sorted_src, inv_map,
+                                                     self.route_ws)),
+            ("permute", 1, lambda: L.moe_permute(xin, sorted_src, offsets, None, T, k, E, d, xp)),
+            ("up_swiglu", 1, lambda: L.moe_grouped_up_swiglu(xp, offsets, sorted_src, win, E, n, d, h, w_ug, a,
+                                                             saved, status)),
+            ("down", 1, lambda: L.moe_grouped_down(a, offsets, E, n, d, h, w_down, y, status)),
+            ("combine", 1, lambda: L.moe_unpermute_combine(y, inv_map, None, T, k, d, out)),
+            ("combine_bwd", 1, lambda: L.moe_permute(doin, sorted_src, offsets, None, T, k, E, d, dy)),
+            ("down_dgrad_swiglu", 1, lambda: L.moe_grouped_down_dgrad_swiglu(dy, saved, offsets, sorted_src, win, E,
+                                                                             n, d, h, w_down, du_hi, du_lo, status,
+                                                                             dw_part=dw_part)),
+            ("routing_weight_grad", 1, lambda: L.moe_routing_weight_grad(dw_part, inv_map, T, k, h, self.dw_route)),
+            ("up_dgrad", 1, lambda: L.moe_grouped_up_dgrad(du_hi, offsets, E, n, d, h, w_ug, dxp, status)),
+            # both weight gradients (down, then up/gate) in one persistent launch
+            ("wgrad_dual", 1, lambda: L.moe_grouped_wgrad_dual(a, self.p_lo, h, dy, d, self.dw_down, du_hi, du_lo,
+                                                               2 * h, xp, d, self.dw_ug, offsets, E, n, status)),
+            ("permute_bwd", 1, lambda: L.moe_unpermute_combine(dxp, inv_map, None, T, k, d, dx)),
+        ]
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -546,52 +609,17 @@ def run_ours(args):
         w_down[e].copy_(torch.from_numpy(wl.w_down(e)).to(bf))
     x, dout, ids, wts = x_h.to(dev), dout_h.to(dev), ids_h.to(dev), wts_h.to(dev)
 
-    i32 = torch.int32
-    counts = torch.empty(E, dtype=i32, device=dev)
-    offsets = torch.empty(E, dtype=i32, device=dev)
-    sorted_src = torch.empty(n, dtype=i32, device=dev)
-    inv_map = torch.empty(n, dtype=i32, device=dev)
-    route_ws = torch.empty(L.moe_workspace_bytes(L.OP_ROUTE, T, k, E), dtype=torch.uint8, device=dev)
-    xp = torch.empty(n, d, dtype=bf, device=dev)
-    a = torch.empty(n, h, dtype=bf, device=dev)
-    y = torch.empty(n, d, dtype=bf, device=dev)
-    saved = torch.empty(L.moe_workspace_bytes(L.OP_SAVED, T, k, E, d, h), dtype=torch.uint8, device=dev)
-    out = torch.empty(T, d, dtype=bf, device=dev)
-    dy = torch.empty(n, d, dtype=bf, device=dev)
-    du_hi = torch.empty(n, 2 * h, dtype=bf, device=dev)
-    du_lo = torch.empty(n, 2 * h, dtype=bf, device=dev)
-    dxp = torch.empty(n, d, dtype=bf, device=dev)
-    dx = torch.empty(T, d, dtype=bf, device=dev)
-    dw_ug = torch.empty(E, 2 * h, d, dtype=torch.float32, device=dev)
-    dw_down = torch.empty(E, h, d, dtype=torch.float32, device=dev)
-    dw_part = torch.empty(n, L.routing_grad_parts(h), dtype=torch.float32, device=dev)
-    dw_route = torch.empty(T, k, dtype=torch.float32, device=dev)
-    status = torch.zeros(1, dtype=i32, device=dev)
-    _, p_lo = L.saved_views(saved, n, h)
+    step = TrainingStep(L, T, k, E, d, h, w_ug, w_down, dev)
+    counts, offsets, sorted_src, inv_map = step.counts, step.offsets, step.sorted_src, step.inv_map
+    xp, a, y, saved, out, dy = step.xp, step.a, step.y, step.saved, step.out, step.dy
+    du_hi, du_lo, dxp, dx, dw_ug, dw_down = step.du_hi, step.du_lo, step.dxp, step.dx, step.dw_ug, step.dw_down
+    dw_part, dw_route, status = step.dw_part, step.dw_route, step.status
     stream = torch.cuda.current_stream()
 
     def inputs():
         return x, ids, wts, dout
 
-    def step_calls(xin, idin, win, doin):
-        return [
-            ("route", 3, lambda: L.moe_route_offsets(idin, T, k, E, counts, offsets, sorted_src, inv_map, route_ws)),
-            ("permute", 1, lambda: L.moe_permute(xin, sorted_src, offsets, None, T, k, E, d, xp)),
-            ("up_swiglu", 1, lambda: L.moe_grouped_up_swiglu(xp, offsets, sorted_src, win, E, n, d, h, w_ug, a,
-                                                             saved, status)),
-            ("down", 1, lambda: L.moe_grouped_down(a, offsets, E, n, d, h, w_down, y, status)),
-            ("combine", 1, lambda: L.moe_unpermute_combine(y, inv_map, None, T, k, d, out)),
-            ("combine_bwd", 1, lambda: L.moe_permute(doin, sorted_src, offsets, None, T, k, E, d, dy)),
-            ("down_dgrad_swiglu", 1, lambda: L.moe_grouped_down_dgrad_swiglu(dy, saved, offsets, sorted_src, win, E,
-                                                                             n, d, h, w_down, du_hi, du_lo, status,
-                                                                             dw_part=dw_part)),
-            ("routing_weight_grad", 1, lambda: L.moe_routing_weight_grad(dw_part, inv_map, T, k, h, dw_route)),
-            ("up_dgrad", 1, lambda: L.moe_grouped_up_dgrad(du_hi, offsets, E, n, d, h, w_ug, dxp, status)),
-            # both weight gradients (down, then up/gate) in one persistent launch
-            ("wgrad_dual", 1, lambda: L.moe_grouped_wgrad_dual(a, p_lo, h, dy, d, dw_down, du_hi, du_lo, 2 * h, xp,
-                                                               d, dw_ug, offsets, E, n, status)),
-            ("permute_bwd", 1, lambda: L.moe_unpermute_combine(dxp, inv_map, None, T, k, d, dx)),
-        ]
+    step_calls = step.calls
 
     calls = step_calls(*inputs())
     launches_per_step = sum(c[1] for c in calls)

@@ -3,7 +3,8 @@ the expert groups.
 
 The large workload (T = 16384 tokens, E = 256 experts, top-8, d = 2048, h = 512) runs through
 the public layer (route -> permute -> grouped forward with the routing weights -> combine, then
-the backward). Every routed row of the saved SwiGLU output, the expert output and the
+the backward), and through the benchmark's own sequence of single-kernel calls, which must give
+the same bits. Every routed row of the saved SwiGLU output, the expert output and the
 input-row gradient, every expert's two weight gradients and every token's output, input
 gradient and routing-weight gradient are compared with the oracle at the task tolerance. The
 oracle runs expert chunk by expert chunk: a chunk is the sub-problem made of the chunk's
@@ -34,6 +35,30 @@ def _rows_f32(t: torch.Tensor, M: int) -> np.ndarray:
     return t[:M].float().cpu().numpy()
 
 
+def _bench_step_matches_layer(wl, w_ug, w_down, layer, out, dx, dw_ug, dw_down, dwr):
+    """The benchmark times the step as one C-ABI call per kernel (`bench.TrainingStep`); the layer
+    runs the composite forward and backward. On the same inputs every result of the timed calls
+    equals the layer's bit for bit, so the parity below holds for the benchmarked sequence too."""
+    import bench
+    from ragged_grouped_gemm_device_gb300 import _lib as L
+    step = bench.TrainingStep(L, wl.T, wl.k, wl.E, wl.d, wl.h, w_ug, w_down, w_ug.device)
+    for _, _, fn in step.calls(G.dev_bf16(wl.x()), G.dev_i32(wl.ids), G.dev_f32(wl.weights),
+                               G.dev_bf16(wl.dout())):
+        fn()
+    torch.cuda.synchronize()
+    assert step.status.item() == 0
+    M = int(layer.offsets[-1].item())
+    assert torch.equal(step.offsets, layer.offsets) and torch.equal(step.inv_map, layer.inv_map[: wl.n])
+    assert torch.equal(step.sorted_src[:M], layer.sorted_src[:M])
+    for got, want, what in ((step.a[:M], layer.a[:M], "a"), (step.y[:M], layer.y[:M], "y"),
+                            (step.dxp[:M], layer.dxp[:M], "dxp"), (step.out, out, "out"), (step.dx, dx, "dx"),
+                            (step.dw_ug, dw_ug, "dW_ug"), (step.dw_down, dw_down, "dW_down"),
+                            (step.dw_route, dwr, "d_weights")):
+        assert torch.equal(got, want), what
+    del step
+    torch.cuda.empty_cache()
+
+
 @pytest.mark.slow
 def test_large_workload_full_parity(lib):
     wl = W.make("large")
@@ -45,6 +70,7 @@ def test_large_workload_full_parity(lib):
     dx, dw_ug, dw_down, dwr = layer.backward(G.dev_bf16(doutn))
     torch.cuda.synchronize()
     assert layer.status.item() == 0
+    _bench_step_matches_layer(wl, w_ug, w_down, layer, out, dx, dw_ug, dw_down, dwr)
 
     r = O.route_offsets(wl.ids, E)
     M = r["M"]
