@@ -94,11 +94,15 @@ def open_library(path: str):
     return lib
 
 
-def load(path: str = LIB_PATH):
+def load(path: str = None):
     """Load the library (once; the first call's path wins, so a process that wants the debug
-    build calls load(DEBUG_LIB_PATH) before anything else) and return its handle."""
+    build calls load(DEBUG_LIB_PATH) before anything else) and return its handle. Without a
+    path: the release build, or the debug build when MOE_GG_DEBUG_LIB=1 is set in the
+    environment (to run a whole program or test suite with the debug build's bounds checks)."""
     global _lib
     if _lib is None:
+        if path is None:
+            path = DEBUG_LIB_PATH if os.environ.get("MOE_GG_DEBUG_LIB") == "1" else LIB_PATH
         _lib = open_library(path)
     return _lib
 

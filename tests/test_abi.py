@@ -140,13 +140,14 @@ def test_debug_build_loads_with_the_same_abi(lib):
     host exactly as the release build does. A release build reports no failed check without
     touching CUDA."""
     dbg = _lib.open_library(build.build(debug=True))
+    rel = _lib.open_library(_lib.LIB_PATH)
     for name in _lib.header_functions():
         assert hasattr(dbg, name), name
-    assert dbg.moe_debug_build() == 1 and lib.moe_debug_build() == 0
-    assert dbg.moe_abi_version() == lib.moe_abi_version()
-    assert _lib.moe_debug_report(lib=lib) == (0, -1, 0, 0)
+    assert dbg.moe_debug_build() == 1 and rel.moe_debug_build() == 0
+    assert dbg.moe_abi_version() == rel.moe_abi_version()
+    assert _lib.moe_debug_report(lib=rel) == (0, -1, 0, 0)
     p = ctypes.c_void_p(16)
-    for L in (lib, dbg):
+    for L in (rel, dbg):
         assert L.moe_route_offsets(p, 10, 1, 0, p, p, p, p, p, 1 << 20, None) == 2      # E = 0
         assert L.moe_permute(ctypes.c_void_p(18), p, p, None, 10, 1, 4, 16, p, None) == 1  # misaligned
     names = [dbg.moe_debug_site_name(s).decode() for s in range(11)]
