@@ -256,6 +256,21 @@ __device__ __forceinline__ void tmem_ld_wait2(uint32_t (&a)[16], uint32_t (&b)[1
                : "memory");
 }
 
+// 16 consecutive 32-bit columns of this warp's 32 TMEM lanes from registers (lane i of the warp
+// writes lane i of its quadrant), and the wait for this thread's outstanding tcgen05.st.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_wait() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 // Shared-memory matrix descriptor (tcgen05 format): start address, leading and stride byte
 // offsets (16-byte units), descriptor version 1 at bit 46, 128-byte swizzle (mode 2) at bit 61.
 __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo_bytes,

@@ -54,6 +54,15 @@ constexpr int TMEM_COLS = 512;                // two 256-column accumulators
 constexpr int MAX_E = 1024;
 constexpr int RASTER_M = 16;                  // row tiles per raster group (see decode_tile)
 constexpr int CTL_BYTES = 256;
+// The tensor core adds each MMA's products into the fp32 accumulator without rounding to
+// nearest: measured on GB300, the error of one accumulator grows with the number of K steps
+// like truncation (an rms error of 1.2 on sums of rms 990 after 2^20 products, against 0.005
+// for round-to-nearest fp32). A tile whose contraction is longer than SEG_KB K blocks therefore
+// accumulates in segments of SEG_KB blocks: the first into its own accumulator R, each later one
+// into the other tensor-memory buffer P, which the epilogue adds into R in fp32 (round to
+// nearest) before the next segment starts. Shorter contractions (every K up to 8192 here) keep
+// the double-buffered pipeline unchanged.
+constexpr int SEG_KB = 128;
 // per epilogue warp, one 32-row x 16-column fp32 chunk staged for a TMA store (wgrad), or two
 // 32-row x 16-column bf16 boxes (dgrad)
 constexpr int STAGE_OUT_BYTES = 32 * 16 * 4;
@@ -81,6 +90,14 @@ static_assert(sizeof(Ctl) <= CTL_BYTES, "control block too large");
 constexpr size_t smem_bytes_for(int E) {
   return 1024 + static_cast<size_t>(RING_BYTES) + SF_RING_BYTES + STAGING_BYTES + CTL_BYTES +
          2 * sizeof(int) * static_cast<size_t>(E + 2);
+}
+
+// Segments of a tile's contraction: one unless the tile is longer than SEG_KB K blocks and the
+// mode has two accumulators (the MXFP8 modes hold their scales in the second half of tensor
+// memory and keep one accumulator).
+template <int NACC>
+__device__ __forceinline__ int num_segments(int kblocks) {
+  return (NACC == 2 && kblocks > SEG_KB) ? (kblocks + SEG_KB - 1) / SEG_KB : 1;
 }
 
 template <int MODE>
@@ -449,90 +466,100 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else if (warp == 1) {
     // =========================================================== MMA issuer
     constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, ModeTraits<MODE>::a_mn, ModeTraits<MODE>::b_mn);
-    uint32_t it = 0, acc = 0;
+    uint32_t it = 0, turn = 0;
+    uint32_t use0 = 0, use1 = 0;  // completed uses of accumulator buffers 0 and 1 (registers)
     bool ok = true;
     for (int t = t_first; t < sc.total && ok; t += t_step) {
       const Tile ti = decode_tile<MODE>(sc, t);
       if (ti.kblocks == 0) continue;
-      const uint32_t buf = acc % NACC, use = acc / NACC;
-      ok = warp_all(mbar_wait(smem_u32(&ctl->tempty[buf]), (use & 1u) ^ 1u, abort_flag, status, tmo));
-      if (!ok) break;
-      tc_fence_after();
-      const uint32_t dtm = tmem_base + buf * BN;
-      for (int kb = 0; kb < ti.kblocks; ++kb, ++it) {
-        const int s = it % NST;
-        const uint32_t ph = (it / NST) & 1u;
-        ok = warp_all(mbar_wait(smem_u32(&ctl->full[s]), ph, abort_flag, status, tmo));
+      // segment 0 into this tile's buffer (turn), later segments into the other one (SEG_KB)
+      const int nseg = num_segments<NACC>(ti.kblocks);
+      const int seg_len = nseg == 1 ? ti.kblocks : SEG_KB;
+      for (int sg = 0; sg < nseg && ok; ++sg) {
+        const uint32_t buf = sg == 0 ? turn : (turn ^ 1u);
+        ok = warp_all(mbar_wait(smem_u32(&ctl->tempty[buf]), ((buf ? use1 : use0) & 1u) ^ 1u, abort_flag, status,
+                                tmo));
         if (!ok) break;
         tc_fence_after();
-        uint8_t* sp = stages + s * SB;
-        if constexpr (ModeTraits<MODE>::wgrad) {
-          const int valid = ti.kvalid - kb * BK;
-          if (valid < BK) {
-            // rows [valid, 64) of every 64x64 box belong to the next expert: zero them. The
-            // swizzle only permutes 16-byte pieces inside a 128-byte row, so those rows are the
-            // contiguous bytes [valid * 128, 8192) of each box.
-            const int pieces = (BK - valid) * 8;
-#pragma unroll
-            for (int atom = 0; atom < SB / ATOM_BYTES; ++atom) {
-              uint4* base = reinterpret_cast<uint4*>(sp + atom * ATOM_BYTES + valid * 128);
-              for (int c = lane; c < pieces; c += 32) base[c] = make_uint4(0u, 0u, 0u, 0u);
+        const uint32_t dtm = tmem_base + buf * BN;
+        const int kb0 = sg * seg_len, kb1 = min(ti.kblocks, kb0 + seg_len);
+        for (int kb = kb0; kb < kb1; ++kb, ++it) {
+          const int s = it % NST;
+          const uint32_t ph = (it / NST) & 1u;
+          ok = warp_all(mbar_wait(smem_u32(&ctl->full[s]), ph, abort_flag, status, tmo));
+          if (!ok) break;
+          tc_fence_after();
+          uint8_t* sp = stages + s * SB;
+          if constexpr (ModeTraits<MODE>::wgrad) {
+            const int valid = ti.kvalid - kb * BK;
+            if (valid < BK) {
+              // rows [valid, 64) of every 64x64 box belong to the next expert: zero them. The
+              // swizzle only permutes 16-byte pieces inside a 128-byte row, so those rows are the
+              // contiguous bytes [valid * 128, 8192) of each box.
+              const int pieces = (BK - valid) * 8;
+  #pragma unroll
+              for (int atom = 0; atom < SB / ATOM_BYTES; ++atom) {
+                uint4* base = reinterpret_cast<uint4*>(sp + atom * ATOM_BYTES + valid * 128);
+                for (int c = lane; c < pieces; c += 32) base[c] = make_uint4(0u, 0u, 0u, 0u);
+              }
+              fence_proxy_async_smem();
             }
-            fence_proxy_async_smem();
+            __syncwarp();
           }
-          __syncwarp();
-        }
-        if constexpr (MX) {
-          if (lane == 0) {
-            // the stage's scale atoms into this stage's tensor-memory slot (A: 4 columns, B: 8),
-            // then four block-scaled MMAs of K = 32, each reading byte ks of the scale words;
-            // tcgen05.cp and tcgen05.mma from one thread execute in issue order
-            const uint32_t sa = stage0 + s * SB;
-            const uint32_t sb = sa + A_BYTES;
-            const uint32_t sfs = sf0 + s * SF_STAGE_BYTES;
-            const uint32_t sft = tmem_base + SF_TMEM_COL + s * 16;
-            tmem_cp_32x128b_x4(sft, smem_desc_rows16(sfs));
-            tmem_cp_32x128b_x4(sft + 4, smem_desc_rows16(sfs + 512));
-            tmem_cp_32x128b_x4(sft + 8, smem_desc_rows16(sfs + 1024));
-            constexpr uint32_t idesc_mx = idesc_mxf8_e4m3(BM, BN);
-#pragma unroll
-            for (int ks = 0; ks < MX_BK / MX_UK; ++ks) {
-              const uint64_t ad = smem_desc_sw128(sa + ks * MX_UK, 16, 1024);
-              const uint64_t bd = smem_desc_sw128(sb + ks * MX_UK, 16, 1024);
-              mma_mxf8_ss(dtm, ad, bd, idesc_mx | idesc_sf_ids(static_cast<uint32_t>(ks)), sft, sft + 4,
-                          (kb | ks) != 0 ? 1u : 0u);
+          if constexpr (MX) {
+            if (lane == 0) {
+              // the stage's scale atoms into this stage's tensor-memory slot (A: 4 columns, B: 8),
+              // then four block-scaled MMAs of K = 32, each reading byte ks of the scale words;
+              // tcgen05.cp and tcgen05.mma from one thread execute in issue order
+              const uint32_t sa = stage0 + s * SB;
+              const uint32_t sb = sa + A_BYTES;
+              const uint32_t sfs = sf0 + s * SF_STAGE_BYTES;
+              const uint32_t sft = tmem_base + SF_TMEM_COL + s * 16;
+              tmem_cp_32x128b_x4(sft, smem_desc_rows16(sfs));
+              tmem_cp_32x128b_x4(sft + 4, smem_desc_rows16(sfs + 512));
+              tmem_cp_32x128b_x4(sft + 8, smem_desc_rows16(sfs + 1024));
+              constexpr uint32_t idesc_mx = idesc_mxf8_e4m3(BM, BN);
+  #pragma unroll
+              for (int ks = 0; ks < MX_BK / MX_UK; ++ks) {
+                const uint64_t ad = smem_desc_sw128(sa + ks * MX_UK, 16, 1024);
+                const uint64_t bd = smem_desc_sw128(sb + ks * MX_UK, 16, 1024);
+                mma_mxf8_ss(dtm, ad, bd, idesc_mx | idesc_sf_ids(static_cast<uint32_t>(ks)), sft, sft + 4,
+                            ((kb - kb0) | ks) != 0 ? 1u : 0u);
+              }
+              mma_commit(smem_u32(&ctl->empty[s]));
             }
+            __syncwarp();
+            continue;
+          }
+          if (lane == 0) {
+            const uint32_t sa = stage0 + s * SB;
+            const uint32_t sb = sa + APARTS * A_BYTES;
+  #pragma unroll
+            for (int part = 0; part < APARTS; ++part) {
+  #pragma unroll
+              for (int ks = 0; ks < BK / UK; ++ks) {
+                const uint32_t ap = sa + part * A_BYTES;
+                const uint64_t ad = ModeTraits<MODE>::a_mn
+                                        ? smem_desc_sw128(ap + ks * (UK * 128), ATOM_BYTES, 1024)
+                                        : smem_desc_sw128(ap + ks * (UK * 2), 16, 1024);
+                const uint64_t bd = ModeTraits<MODE>::b_mn
+                                        ? smem_desc_sw128(sb + ks * (UK * 128), ATOM_BYTES, 1024)
+                                        : smem_desc_sw128(sb + ks * (UK * 2), 16, 1024);
+                mma_bf16_ss(dtm, ad, bd, idesc, ((kb - kb0) | ks | part) != 0 ? 1u : 0u);
+              }
+            }
+            // release the stage to the producers once these MMAs have read it
             mma_commit(smem_u32(&ctl->empty[s]));
           }
           __syncwarp();
-          continue;
         }
-        if (lane == 0) {
-          const uint32_t sa = stage0 + s * SB;
-          const uint32_t sb = sa + APARTS * A_BYTES;
-#pragma unroll
-          for (int part = 0; part < APARTS; ++part) {
-#pragma unroll
-            for (int ks = 0; ks < BK / UK; ++ks) {
-              const uint32_t ap = sa + part * A_BYTES;
-              const uint64_t ad = ModeTraits<MODE>::a_mn
-                                      ? smem_desc_sw128(ap + ks * (UK * 128), ATOM_BYTES, 1024)
-                                      : smem_desc_sw128(ap + ks * (UK * 2), 16, 1024);
-              const uint64_t bd = ModeTraits<MODE>::b_mn
-                                      ? smem_desc_sw128(sb + ks * (UK * 128), ATOM_BYTES, 1024)
-                                      : smem_desc_sw128(sb + ks * (UK * 2), 16, 1024);
-              mma_bf16_ss(dtm, ad, bd, idesc, (kb | ks | part) != 0 ? 1u : 0u);
-            }
-          }
-          // release the stage to the producers once these MMAs have read it
-          mma_commit(smem_u32(&ctl->empty[s]));
-        }
+        if (!ok) break;
+        if (lane == 0) mma_commit(smem_u32(&ctl->tfull[buf]));
         __syncwarp();
+        if (buf) ++use1; else ++use0;
       }
       if (!ok) break;
-      if (lane == 0) mma_commit(smem_u32(&ctl->tfull[buf]));
-      __syncwarp();
-      ++acc;
+      if constexpr (NACC == 2) turn ^= 1u;
     }
     // every MMA this thread issued must finish before tensor memory is released
     if (lane == 0) mma_commit(smem_u32(&ctl->done));
@@ -543,7 +570,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int q = warp & 3;           // TMEM lane quadrant this warp may access
     const int half = (warp - 2) >> 2; // which half of the tile's columns this warp stores
     const int r_in = q * 32 + lane;   // accumulator row = TMEM lane
-    uint32_t acc = 0;
+    uint32_t turn = 0;
+    uint32_t use0 = 0, use1 = 0;      // completed uses of accumulator buffers 0 and 1
     uint32_t box_ctr = 0;             // dgrad: staging boxes this warp has stored
     for (int t = t_first; t < sc.total; t += t_step) {
       const Tile ti = decode_tile<MODE>(sc, t);
@@ -585,10 +613,45 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
         }
       }
-      const uint32_t buf = acc % NACC, use = acc / NACC;
-      if (!warp_all(mbar_wait(smem_u32(&ctl->tfull[buf]), use & 1u, abort_flag, status, tmo))) break;
+      const uint32_t buf = turn;
+      if (!warp_all(mbar_wait(smem_u32(&ctl->tfull[buf]), (buf ? use1 : use0) & 1u, abort_flag, status, tmo))) break;
       tc_fence_after();
       const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * BN;
+      const int nseg = num_segments<NACC>(ti.kblocks);
+      if (nseg > 1) {
+        // a segmented contraction (SEG_KB): add each later segment's partial sums (the other
+        // buffer) into this tile's accumulator, fp32 round to nearest, over exactly the columns
+        // this warp reads below, then hand the buffer back for the next segment
+        const uint32_t pb = turn ^ 1u;
+        const uint32_t tp = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + pb * BN;
+        bool seg_ok = true;
+        for (int sg = 1; sg < nseg; ++sg) {
+          if (!warp_all(mbar_wait(smem_u32(&ctl->tfull[pb]), (pb ? use1 : use0) & 1u, abort_flag, status, tmo))) {
+            seg_ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll 1
+          for (int i = 0; i < 8; ++i) {
+            // UP_SWIGLU: gate chunks half*4.. and the matching up chunks 128 columns on; else
+            // chunks half*8..half*8+7
+            const int col = (EPI == MODE_UP_SWIGLU) ? (i < 4 ? (half * 4 + i) * 16 : 128 + (half * 4 + i - 4) * 16)
+                                                    : (half * 8 + i) * 16;
+            uint32_t vr[16], vp[16];
+            tmem_ld16(tb + col, vr);
+            tmem_ld16(tp + col, vp);
+            tmem_ld_wait2(vr, vp);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) vr[j] = __float_as_uint(__uint_as_float(vr[j]) + __uint_as_float(vp[j]));
+            tmem_st16(tb + col, vr);
+          }
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(smem_u32(&ctl->tempty[pb]));
+          if (pb) ++use1; else ++use0;
+        }
+        if (!seg_ok) break;
+      }
 
       if constexpr (EPI == MODE_UP_SWIGLU) {
         bool rv = r_in < ti.rows;
@@ -931,7 +994,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       tc_fence_before();
       mbar_arrive(smem_u32(&ctl->tempty[buf]));
-      ++acc;
+      if (buf) ++use1; else ++use0;
+      if constexpr (NACC == 2) turn ^= 1u;
     }
   }
 

@@ -32,13 +32,25 @@ FWD_CASES = {
     "edge_odd_width": lambda: W.custom(T=150, k=3, E=6, d=60, h=44, seed=13, invalid_frac=0.05,
                                        empty_experts=(1,)),
     "edge_odd_width2": lambda: W.custom(T=90, k=2, E=5, d=77, h=33, seed=14),
+    # the widest rows the header allows: d = 2^20 (a contraction of 16384 K blocks in one tile,
+    # 4096 column tiles in the down projection and the wgrads) and h = 2^20 (8192 column tiles of
+    # the up/gate projection, a 2 GB saved U, 16384 gradient row tiles per expert). With
+    # W_down ~ N(0, 1/sqrt(h)) the down dgrad's sums over d = 2^20 products have an rms of
+    # sqrt(d/h); h = 64 keeps them at ~128, where fp32 accumulation (even rounded to nearest at
+    # every step) still meets the elementwise bound on the gradients' near-zero elements -- at
+    # h = 16 (sums of ~256) it does not, whatever the order of the additions.
+    "edge_max_d": lambda: W.custom(T=24, k=1, E=2, d=1 << 20, h=64, seed=15),
+    "edge_max_h": lambda: W.custom(T=24, k=2, E=1, d=32, h=1 << 20, seed=16),
+    # one expert with 20000 rows: a wgrad contraction of 313 K blocks, accumulated in segments
+    "edge_long_expert": lambda: W.custom(T=20000, k=1, E=2, d=64, h=64, seed=17, empty_experts=(1,)),
     "balanced": lambda: W.make("balanced"),
     "finegrained": lambda: W.make("finegrained"),
     "skew": lambda: W.make("skew"),
 }
 
 BWD_CASES = ["toy", "edge_small", "edge_wide", "edge_one_expert", "edge_sparse", "edge_max_experts",
-             "edge_odd_width", "edge_odd_width2", "finegrained", "skew"]
+             "edge_odd_width", "edge_odd_width2", "edge_max_d", "edge_max_h", "edge_long_expert", "finegrained",
+             "skew"]
 
 
 def _dy(wl, M):
@@ -221,3 +233,28 @@ def test_outputs_at_16_byte_alignment_match_32_byte_aligned(lib):
         results.append((a[:M].clone(), saved.clone(), du_hi[:M].clone(), du_lo[:M].clone()))
     for x0, x1 in zip(*results):
         assert torch.equal(x0.view(torch.uint8), x1.view(torch.uint8))
+
+
+def test_long_contraction_keeps_fp32_accuracy(lib):
+    """A contraction of 2^20 products in one tile (the wgrad over one expert's 2^20 rows, fp32
+    out). The tensor core's accumulator does not round each addition to nearest: left alone, its
+    error grows like a truncating sum (rms 1.2 on sums of rms ~1000 here). Contractions longer
+    than 8192 are accumulated in segments folded in round-to-nearest fp32, which keeps the error
+    at the level of an fp32 sum."""
+    from ragged_grouped_gemm_device_gb300 import _lib as L
+    K, P, Q = 1 << 20, 16, 16
+    rng = np.random.default_rng(5)
+    a = torch.from_numpy(rng.standard_normal((K, P)).astype(np.float32)).to(torch.bfloat16)
+    b = torch.from_numpy(rng.standard_normal((K, Q)).astype(np.float32)).to(torch.bfloat16)
+    ref = a.double().numpy().T @ b.double().numpy()
+    offs = torch.tensor([K], dtype=torch.int32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    dw = torch.full((1, P, Q), float("nan"), device="cuda")
+    L.moe_grouped_wgrad(a.cuda(), None, P, b.cuda(), Q, offs, 1, K, dw, st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    err = dw[0].cpu().double().numpy() - ref
+    rms_ref = np.sqrt((ref ** 2).mean())
+    assert rms_ref > 500
+    # an fp32 sum rounded to nearest at every step has an rms error of ~0.005 here
+    assert np.sqrt((err ** 2).mean()) < 0.05 and np.abs(err).max() < 0.25, (np.sqrt((err ** 2).mean()), np.abs(err).max())
