@@ -29,6 +29,11 @@
  *    MOE_DEV_TIMEOUT when a bounded wait inside a kernel gave up (the kernel then stops early
  *    instead of hanging), MOE_DEV_BAD_OFFSETS when offsets decrease or exceed the buffer rows
  *    (the affected kernel then computes nothing).
+ *  - Accumulation: products of bf16 operands are summed in fp32 in tensor memory. A contraction
+ *    longer than 8192 (K = d or h in the projections and dgrads, the rows of an expert in the
+ *    wgrads) is summed in segments of 8192 whose partial sums are added in round-to-nearest
+ *    fp32, which keeps its error at the level of an fp32 sum (the tensor core's own
+ *    accumulator truncates). The MXFP8 calls do not segment.
  *  - Limits: 1 <= E <= 1024, 1 <= top_k <= 32, 1 <= d, h <= 2^20, T*top_k < 2^31. The
  *    grouped kernels read operands by TMA, which needs 16-byte row pitches (d and h multiples
  *    of 8). moe_permute, moe_unpermute_combine, moe_grouped_swiglu_fwd and moe_grouped_bwd also
