@@ -24,12 +24,15 @@ def _oracle_layer(wl, dout):
     return out, dx, dw_ug, dw_down, dwr
 
 
-@pytest.mark.parametrize("name", ["toy", "edge", "edge_odd_width", "finegrained"])
+@pytest.mark.parametrize("name", ["toy", "edge", "edge_odd_width", "edge_top32", "finegrained"])
 def test_layer_forward_backward(lib, name):
     if name == "edge":
         wl = W.custom(T=211, k=4, E=11, d=72, h=40, seed=21, invalid_frac=0.1, empty_experts=(2, 7))
     elif name == "edge_odd_width":
         wl = W.custom(T=120, k=3, E=5, d=60, h=37, seed=22, invalid_frac=0.05, empty_experts=(3,))
+    elif name == "edge_top32":
+        # the largest top_k: 32 slots per token, combined and routing-weight gradients of 32 slots
+        wl = W.custom(T=96, k=32, E=40, d=64, h=64, seed=23, invalid_frac=0.05, empty_experts=(5,))
     else:
         wl = W.make(name)
     w_ug, w_down = G.device_weights(wl)
