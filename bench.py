@@ -15,6 +15,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import os
 import statistics
@@ -328,15 +329,22 @@ class ClockSampler:
 GEMM_SOURCES = ("common.cuh", "grouped_gemm.cu", "internal.h", "moe_gg.cu")
 
 
+def _code_only(text):
+    """C++ source without its comments and blank lines: what the compiler sees."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+
+
 def kernel_source_hash():
-    """Hash of the grouped GEMM's sources (device code, launch arguments and tensor maps): DRAM
-    traffic taken by the profiler is valid only for them. The routing and row-movement kernels
-    (route.cu, permute.cu) do not enter it."""
+    """Hash of the grouped GEMM's code (device code, launch arguments and tensor maps; comments
+    left out): DRAM traffic taken by the profiler is valid only for it. The routing and
+    row-movement kernels (route.cu, permute.cu) do not enter it."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "ragged_grouped_gemm_device_gb300", "csrc")
     for name in GEMM_SOURCES:
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(csrc, name)) as f:
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -16,12 +16,14 @@
 //   warp 10     TMA producer of the B operand into the same stages.
 //   warp 1      tensor-memory allocator and MMA issuer: tcgen05.mma 128x256x16 (bf16 in, fp32
 //               accumulate) into one of two 256-column TMEM accumulators, so the epilogue of a
-//               tile overlaps the main loop of the next.
+//               tile overlaps the main loop of the next. A contraction longer than SEG_KB K
+//               blocks takes both: its later segments go to the second one.
 //   warps 2..9  epilogue, two warps per TMEM lane quadrant (each takes half of the tile's
 //               columns): tcgen05.ld of the accumulator, fused SwiGLU (forward or backward),
 //               conversion and row/column-masked stores. A tile that runs past its expert's
 //               segment still multiplies the neighbouring rows (rows of a product are
-//               independent) but never stores them.
+//               independent) but never stores them. For a segmented contraction they first
+//               add each later segment into the tile's accumulator (fp32, tcgen05.st).
 // The wgrad mode contracts over the M_e rows of an expert (Table 15): its operands are
 // MN-major and the rows of the last K block that belong to the next expert are zeroed in
 // shared memory before the MMA reads them. Its A operand comes as a bf16 high/low pair (the
