@@ -372,7 +372,8 @@ def load_traffic():
 def kernel_work(M, T, k, E, d, h):
     """Per launch of each step kernel on a workload with M routed rows: (useful FLOPs, compulsory
     DRAM bytes, FLOPs the tensor cores execute). Bytes count every operand read once and every
-    output written once under the library's data contract: bf16 rows and weights, fp32 saved U,
+    output written once under the library's data contract: bf16 rows and weights, the saved U at
+    3 bytes a value,
     bf16 low halves of P and dU (the wgrads' second operand half), fp32 weight gradients, int32
     indices, fp32 routing weights. The wgrads execute twice their useful FLOPs (both halves)."""
     mdh = float(M) * d * h
@@ -381,11 +382,11 @@ def kernel_work(M, T, k, E, d, h):
     w = {
         "route": (0, T * k * 4 * 4.0, 0),                       # ids read twice, placement + inverse map written
         "permute": (0, T * d * 2.0 + M * d * 2.0 + M * 4.0, 0),
-        "up_swiglu": (4 * mdh, M * d * 2.0 + 2 * wd + M * h * 2.0 * 2 + M * 2 * h * 4.0 + M * 8.0, 4 * mdh),
+        "up_swiglu": (4 * mdh, M * d * 2.0 + 2 * wd + M * h * 2.0 * 2 + M * 2 * h * 3.0 + M * 8.0, 4 * mdh),
         "down": (2 * mdh, M * h * 2.0 + wd + M * d * 2.0, 2 * mdh),
         "combine": (0, M * d * 2.0 + T * d * 2.0 + T * k * 4.0, 0),
         "combine_bwd": (0, T * d * 2.0 + M * d * 2.0 + M * 4.0, 0),
-        "down_dgrad_swiglu": (2 * mdh, M * d * 2.0 + wd + M * 2 * h * 4.0 + M * 2 * h * 2.0 * 2 + M * np_ * 4.0
+        "down_dgrad_swiglu": (2 * mdh, M * d * 2.0 + wd + M * 2 * h * 3.0 + M * 2 * h * 2.0 * 2 + M * np_ * 4.0
                               + M * 8.0, 2 * mdh),
         "routing_weight_grad": (0, M * np_ * 4.0 + T * k * 8.0, 0),
         "up_dgrad": (4 * mdh, M * 2 * h * 2.0 + 2 * wd + M * d * 2.0, 4 * mdh),
@@ -1165,9 +1166,9 @@ def run_sweep_precision(args):
         M = int(offsets[-1].item())
         fl = 6.0 * M * d * h
         # bytes the scheme adds per step beyond bf16 saved state: the low half of P written by the
-        # forward and read by the down wgrad, U in fp32 instead of bf16 (written by the forward,
+        # forward and read by the down wgrad, U at 3 bytes instead of 2 (written by the forward,
         # read by the dgrad), the low half of dU written by the dgrad and read by the up wgrad
-        extra = M * h * 2 * 2 + M * 2 * h * 2 * 2 + M * 2 * h * 2 * 2
+        extra = M * h * 2 * 2 + M * 2 * h * 1 * 2 + M * 2 * h * 2 * 2
         print(json.dumps({"sweep": "precision", "workload": name, "M": M, "E": E, "d": d, "h": h,
                           "wgrad_hi_lo_ms": t_hl, "wgrad_hi_only_ms": t_hi,
                           "wgrad_hi_lo_useful_tflops": fl / t_hl / 1e9, "wgrad_hi_only_tflops": fl / t_hi / 1e9,

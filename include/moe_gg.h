@@ -144,17 +144,20 @@ moe_status_t moe_permute(const moe_bf16* x, const int32_t* sorted_src, const int
  *  saved      nullable, moe_workspace_bytes(MOE_OP_SAVED, T, top_k, E, d, h) bytes for
  *             cap = T*top_k: what the backward needs beyond a_save, written when non-NULL
  *             (training). Byte 0: P - bf16(P), bf16 [cap, h] row-major. Byte
- *             round_up(cap*h*2, 256): U in fp32, blocked as the kernels' epilogues hold it --
- *             for the G-th 128-row tile of the problem list (experts in order, ceil(M_e/128)
- *             tiles each, at most (cap + 127 E)/128), lane quadrant q (tile rows 32q..32q+31)
- *             and 16-column chunk ci (ci < H = ceil(h/16): gate columns 16ci..; else up columns
- *             16(ci-H)..), a 2 KB block at float offset ((G*4 + q)*2H + ci)*512 holding float4
- *             j (columns 4j..4j+3 of the chunk) of tile row 32q+l at float4 j*32 + l. The
- *             slots of tile rows past the expert's segment are left unwritten. Keeping U in
- *             fp32 and P as a bf16 high+low pair (a_save + the low half) lets the wgrads
- *             contract over long expert segments without the bf16 rounding of saved
- *             activations dominating the result; the blocked U makes each warp's store (and
- *             the dgrad's load) of it one contiguous 512-byte access.
+ *             round_up(cap*h*2, 256): U rounded to nearest even at 24 bits (the upper 24 bits
+ *             of its fp32 pattern: 16 significant bits), blocked as the kernels' epilogues hold
+ *             it -- for the G-th 128-row tile of the problem list (experts in order,
+ *             ceil(M_e/128) tiles each, at most (cap + 127 E)/128), lane quadrant q (tile rows
+ *             32q..32q+31) and 16-column chunk ci (ci < H = ceil(h/16): gate columns 16ci..;
+ *             else up columns 16(ci-H)..), a 1536-byte block at byte ((G*4 + q)*2H + ci)*1536
+ *             of three 512-byte planes: for tile row 32q+l and column j of the chunk, the upper
+ *             16 of the 24 bits are the little-endian 16-bit word at byte (j/8)*512 + l*16 +
+ *             (j%8)*2 and the lower 8 bits the byte at 1024 + l*16 + j. The slots of tile rows
+ *             past the expert's segment are left unwritten. Keeping U to 16 significant bits and
+ *             P as a bf16 high+low pair (a_save + the low half) lets the wgrads contract over
+ *             long expert segments without the bf16 rounding of saved activations dominating
+ *             the result; the blocked U makes each warp's store (and the dgrad's load) of one
+ *             plane one contiguous 512-byte access.
  *  ws         moe_workspace_bytes(MOE_OP_FWD, ...) bytes: 0 (ws may be NULL) when d and h are
  *             multiples of 8, else the zero-padded copies of xp, y, a, W_ug, W_down. With h not
  *             a multiple of 8, `saved` holds the padded width round_up(h, 8) in place of h.

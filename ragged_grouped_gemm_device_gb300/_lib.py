@@ -252,17 +252,16 @@ def moe_grouped_bwd_mxfp8(dy, xp, a_save, saved, offsets, sorted_src, weights, E
 
 def saved_views(saved, cap, h):
     """The parts of the forward's `saved` buffer (a contiguous tensor of any dtype, read as bytes):
-    the low half of P = w*A (bf16 [cap, h8]; the high half is a_save) at byte 0, then fp32 U in
-    the kernels' blocked layout (a flat fp32 view; see the header for the block order). h8 = h
-    rounded up to a multiple of 8: widths that are not are stored zero-padded."""
+    the low half of P = w*A (bf16 [cap, h8]; the high half is a_save) at byte 0, then U rounded to
+    24 bits in the kernels' blocked layout (a flat byte view; see the header for the block
+    order). h8 = h rounded up to a multiple of 8: widths that are not are stored zero-padded."""
     import torch
     saved = saved.reshape(-1).view(torch.uint8)
     h = (h + 7) // 8 * 8
     pb = cap * h * 2
     off = (pb + 255) // 256 * 256
     p_lo = saved[:pb].view(torch.bfloat16).view(cap, h)
-    ub = (saved.numel() - off) // 4 * 4
-    u = saved[off:off + ub].view(torch.float32)
+    u = saved[off:]
     return u, p_lo
 
 

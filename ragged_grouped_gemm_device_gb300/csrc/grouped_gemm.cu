@@ -212,14 +212,48 @@ __device__ __forceinline__ bool warp_all(bool v) { return __all_sync(0xffffffffu
 __device__ __forceinline__ float silu_f(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 __device__ __forceinline__ float sigmoid_f(float g) { return __fdividef(1.0f, 1.0f + __expf(-g)); }
 
-// The saved fp32 U, blocked the way the epilogue holds it: for row tile G (of the problem
-// list), TMEM lane quadrant q and 16-column chunk ci (ci < H16 = ceil(h/16): gate columns
-// 16ci.., else up columns 16(ci - H16)..), one 2 KB block of 4 x 32 float4 with float4 j of
-// lane l at j * 32 + l. A warp's load or store of one float4 per lane is then one contiguous
-// 512 bytes, and the chunks of one (G, q) are contiguous. Each row tile owns its blocks; the
-// slots of its rows past the expert's segment are neither written nor read.
-__device__ __forceinline__ float4* u_block(const void* base, long long G, int q, int ci, int c2) {
-  return const_cast<float4*>(reinterpret_cast<const float4*>(base)) + ((G * 4 + q) * c2 + ci) * 128;
+// The saved U, blocked the way the epilogue holds it: for row tile G (of the problem list), TMEM
+// lane quadrant q and 16-column chunk ci (ci < H16 = ceil(h/16): gate columns 16ci.., else up
+// columns 16(ci - H16)..), one 1536-byte block of three 512-byte planes, lane l's 16 bytes of
+// plane p at byte p * 512 + l * 16. Each value is the fp32 U rounded to nearest even at 24 bits
+// (sign, 8 exponent and 15 mantissa bits: 16 significant bits); plane 0 holds the upper 16 bits
+// of columns 0..7 of the chunk, plane 1 those of columns 8..15 and plane 2 the lower 8 bits of
+// all 16. A warp's store or load of one plane is one contiguous 512 bytes, and the chunks of one
+// (G, q) are contiguous. Each row tile owns its blocks; the slots of its rows past the expert's
+// segment are neither written nor read.
+constexpr int U_BLOCK_BYTES = 1536;
+
+__device__ __forceinline__ uint4* u_block(const void* base, long long G, int q, int ci, int c2) {
+  return const_cast<uint4*>(reinterpret_cast<const uint4*>(base)) + ((G * 4 + q) * c2 + ci) * (U_BLOCK_BYTES / 16);
+}
+
+// 16 fp32 values (as bits) -> the three 16-byte planes of this lane
+__device__ __forceinline__ void u24_pack(const uint32_t (&x)[16], uint4& p0, uint4& p1, uint4& p2) {
+  uint32_t v[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) v[j] = (x[j] + 0x7Fu + ((x[j] >> 8) & 1u)) >> 8;  // 24 bits, to nearest even
+  p0 = make_uint4((v[0] >> 8) | ((v[1] >> 8) << 16), (v[2] >> 8) | ((v[3] >> 8) << 16),
+                  (v[4] >> 8) | ((v[5] >> 8) << 16), (v[6] >> 8) | ((v[7] >> 8) << 16));
+  p1 = make_uint4((v[8] >> 8) | ((v[9] >> 8) << 16), (v[10] >> 8) | ((v[11] >> 8) << 16),
+                  (v[12] >> 8) | ((v[13] >> 8) << 16), (v[14] >> 8) | ((v[15] >> 8) << 16));
+  uint32_t w[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+    w[k] = (v[4 * k] & 0xFFu) | ((v[4 * k + 1] & 0xFFu) << 8) | ((v[4 * k + 2] & 0xFFu) << 16) |
+           ((v[4 * k + 3] & 0xFFu) << 24);
+  p2 = make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// the three planes of one lane -> its 16 values (all-zero planes give +0)
+__device__ __forceinline__ void u24_unpack(const uint4 (&p)[3], float (&f)[16]) {
+  const uint32_t hi[8] = {p[0].x, p[0].y, p[0].z, p[0].w, p[1].x, p[1].y, p[1].z, p[1].w};
+  const uint32_t lo[4] = {p[2].x, p[2].y, p[2].z, p[2].w};
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const uint32_t h16 = (j & 1) ? (hi[j >> 1] >> 16) : (hi[j >> 1] & 0xFFFFu);
+    const uint32_t l8 = (lo[j >> 2] >> (8 * (j & 3))) & 0xFFu;
+    f[j] = __uint_as_float((h16 << 16) | (l8 << 8));
+  }
 }
 
 // 32-byte store (sm_100+ global vector width); the address must be 32-byte aligned
@@ -595,21 +629,21 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       // dgrad: the saved U does not depend on the accumulator, so this warp requests its first
       // chunk before waiting for the tile. (An L2 prefetch of the next tile's U measured slower.)
-      float4 gcur[4], ucur[4];
+      uint4 gcur[3], ucur[3];  // the three planes of this lane's gate and up values (u_block)
       if constexpr (EPI == MODE_DGRAD_SWIGLU) {
         const int h16 = (args.h + 15) >> 4;
         const int cw = BN / 32;  // 16-column chunks per warp
         const int c0 = (ti.n0 >> 4) + half * cw;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          gcur[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int j = 0; j < 3; ++j) {
+          gcur[j] = make_uint4(0u, 0u, 0u, 0u);
           ucur[j] = gcur[j];
         }
         if (r_in < ti.rows && c0 < h16 && MOE_DBG_IN(DBG_GG_TILE, args.tile_base + ti.g, args.dbg_u_tiles)) {
-          const float4* bg = u_block(args.aux, args.tile_base + ti.g, q, c0, 2 * h16);
-          const float4* bu = u_block(args.aux, args.tile_base + ti.g, q, h16 + c0, 2 * h16);
+          const uint4* bg = u_block(args.aux, args.tile_base + ti.g, q, c0, 2 * h16);
+          const uint4* bu = u_block(args.aux, args.tile_base + ti.g, q, h16 + c0, 2 * h16);
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
+          for (int j = 0; j < 3; ++j) {
             gcur[j] = __ldg(bg + j * 32 + lane);
             ucur[j] = __ldg(bu + j * 32 + lane);
           }
@@ -678,14 +712,18 @@ __global__ void __launch_bounds__(THREADS, 1)
           const int col = ti.n0 + c * 16;
           if (!rv || col >= h) return;
           if (u_out) {
-            // U in its blocked layout: 512 contiguous bytes per warp-wide store
-            uint32_t* bg = reinterpret_cast<uint32_t*>(u_block(args.out2, G, q, col >> 4, 2 * h16));
-            uint32_t* bu = reinterpret_cast<uint32_t*>(u_block(args.out2, G, q, h16 + (col >> 4), 2 * h16));
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              st_global_v4(bg + (j * 32 + lane) * 4, g[4 * j], g[4 * j + 1], g[4 * j + 2], g[4 * j + 3]);
-              st_global_v4(bu + (j * 32 + lane) * 4, u[4 * j], u[4 * j + 1], u[4 * j + 2], u[4 * j + 3]);
-            }
+            // U in its blocked 24-bit layout: 512 contiguous bytes per warp-wide store
+            uint4* bg = u_block(args.out2, G, q, col >> 4, 2 * h16);
+            uint4* bu = u_block(args.out2, G, q, h16 + (col >> 4), 2 * h16);
+            uint4 p0, p1, p2;
+            u24_pack(g, p0, p1, p2);
+            bg[lane] = p0;
+            bg[32 + lane] = p1;
+            bg[64 + lane] = p2;
+            u24_pack(u, p0, p1, p2);
+            bu[lane] = p0;
+            bu[32 + lane] = p1;
+            bu[64 + lane] = p2;
           }
           uint32_t pa[8], pl[8];
 #pragma unroll
@@ -828,19 +866,20 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
           ++box_ctr;
         };
-        // saved U of chunk c (zeros past the last column chunk), one coalesced float4 per lane
-        auto load_u = [&](int c, float4 (&gq)[4], float4 (&uq)[4]) {
+        // saved U of chunk c (zeros past the last column chunk): this lane's three planes of
+        // the gate and of the up values, each load one coalesced 512 bytes per warp
+        auto load_u = [&](int c, uint4 (&gq)[3], uint4 (&uq)[3]) {
           const int ci = (ti.n0 >> 4) + c;
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            gq[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int j = 0; j < 3; ++j) {
+            gq[j] = make_uint4(0u, 0u, 0u, 0u);
             uq[j] = gq[j];
           }
           if (rv && ci < h16 && u_in) {
-            const float4* bg = u_block(args.aux, G, q, ci, 2 * h16);
-            const float4* bu = u_block(args.aux, G, q, h16 + ci, 2 * h16);
+            const uint4* bg = u_block(args.aux, G, q, ci, 2 * h16);
+            const uint4* bu = u_block(args.aux, G, q, h16 + ci, 2 * h16);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
+            for (int j = 0; j < 3; ++j) {
               gq[j] = __ldg(bg + j * 32 + lane);
               uq[j] = __ldg(bu + j * 32 + lane);
             }
@@ -855,12 +894,9 @@ __global__ void __launch_bounds__(THREADS, 1)
           const int col = ti.n0 + c * 16;
           if (!rv || col >= h) return;
           const bool two = col + 16 <= h;
-          const float gv[16] = {gcur[0].x, gcur[0].y, gcur[0].z, gcur[0].w, gcur[1].x, gcur[1].y,
-                                gcur[1].z, gcur[1].w, gcur[2].x, gcur[2].y, gcur[2].z, gcur[2].w,
-                                gcur[3].x, gcur[3].y, gcur[3].z, gcur[3].w};
-          const float uv[16] = {ucur[0].x, ucur[0].y, ucur[0].z, ucur[0].w, ucur[1].x, ucur[1].y,
-                                ucur[1].z, ucur[1].w, ucur[2].x, ucur[2].y, ucur[2].z, ucur[2].w,
-                                ucur[3].x, ucur[3].y, ucur[3].z, ucur[3].w};
+          float gv[16], uv[16];
+          u24_unpack(gcur, gv);
+          u24_unpack(ucur, uv);
           uint32_t gh[8], gl[8], uh[8], ul[8];
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
@@ -911,7 +947,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
         };
         const int cb = half * (BN / 32), ce = cb + BN / 32;  // an even number of chunks
-        float4 gnxt[4], unxt[4];
+        uint4 gnxt[3], unxt[3];
         uint32_t v0[16], v1[16];
         // MXFP8 dgrad: dU's high half of a pair of chunks, kept for its quantization
         [[maybe_unused]] uint32_t qg0[8], qu0[8], qg1[8], qu1[8];
@@ -925,7 +961,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           load_u(c + 1, gnxt, unxt);
           process(c, v0, qg0, qu0);
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
+          for (int j = 0; j < 3; ++j) {
             gcur[j] = gnxt[j];
             ucur[j] = unxt[j];
           }
@@ -953,7 +989,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
           if (more) {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
+            for (int j = 0; j < 3; ++j) {
               gcur[j] = gnxt[j];
               ucur[j] = unxt[j];
             }

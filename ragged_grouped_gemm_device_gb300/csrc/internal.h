@@ -14,13 +14,13 @@ namespace moe {
 enum GemmMode : int {
   // U = X W_ug^T per row segment, gate and up column blocks in one accumulator; the epilogue
   // writes bf16(P) for P = w * silu(gate) * up (w = 1 without routing weights), and optionally
-  // U (fp32) and P - bf16(P) (bf16).
+  // U (24 bits) and P - bf16(P) (bf16).
   // A: rows [cap, d] K-major; B: W_ug [E, 2h, d].
   MODE_UP_SWIGLU = 0,
   // Y = P W per row segment with W [E, K, N] (N contiguous, MN-major B); bf16 store.
   MODE_PLAIN_BF16 = 1,
   // dA = dY W_down^T per row segment (W_down [E, h, d] K-major B); the epilogue applies the
-  // SwiGLU backward with the saved fp32 U and writes dU = [dgate, dup] as a bf16 high/low pair
+  // SwiGLU backward with the saved U (24-bit) and writes dU = [dgate, dup] as a bf16 high/low pair
   // (out/out2, with their rows2d_store maps as the kernel's two output maps).
   MODE_DGRAD_SWIGLU = 2,
   // dW_e = (P_hi + P_lo)_e^T Q_e, contraction over the M_e rows of expert e (all operands
@@ -60,7 +60,7 @@ struct GemmArgs {
   int h;                   // SwiGLU half width
   void* out;               // row-grouped bf16 output, or WGRAD fp32 [E, Mdim, N]
   long long ldo;           // elements per output row
-  void* out2;              // UP_SWIGLU: optional fp32 U, blocked by row tile (see u_block);
+  void* out2;              // UP_SWIGLU: optional U rounded to 24 bits, blocked by row tile (see u_block);
                            // DGRAD_SWIGLU: dU low half
   long long ldo2;
   void* out3;              // UP_SWIGLU: optional low half of P [cap, h] (P = w*A, or A)
@@ -70,7 +70,7 @@ struct GemmArgs {
   // SwiGLU backward.
   const int32_t* row_src;
   const float* row_weight;
-  const void* aux;         // DGRAD_SWIGLU: the saved fp32 U in the blocked layout of out2
+  const void* aux;         // DGRAD_SWIGLU: the saved U in the blocked layout of out2
   long long ld_aux;
   // First row tile of this problem list in the blocked U: 0 for a whole problem list, the row
   // tiles of the experts before it for one expert (single_expert)

@@ -55,14 +55,14 @@ GemmArgs base_args(int E, int cap, int32_t* status) {
   return a;
 }
 
-// saved = low half of P [rows, h] bf16 (P = w*A, or A; the high half is a_save) | fp32 U in
-// blocks of 32 rows x 16 columns per (row tile, lane quadrant, column chunk). The row tiles of
-// any problem list with at most `rows` rows number at most sum_e ceil(M_e / 128) <=
-// (rows + 127 E) / 128; each holds 4 quadrants x 2 ceil(h/16) chunks of 2 KB.
+// saved = low half of P [rows, h] bf16 (P = w*A, or A; the high half is a_save) | U rounded to
+// 24 bits in blocks of 32 rows x 16 columns per (row tile, lane quadrant, column chunk). The row
+// tiles of any problem list with at most `rows` rows number at most sum_e ceil(M_e / 128) <=
+// (rows + 127 E) / 128; each holds 4 quadrants x 2 ceil(h/16) chunks of 1536 bytes.
 size_t saved_p_bytes(long long rows, int h) { return round256(static_cast<size_t>(rows) * h * 2); }
 long long saved_u_tiles(long long rows, int E) { return (rows + 127LL * E) / 128; }
 size_t saved_u_bytes(long long rows, int h, int E) {
-  return round256(static_cast<size_t>(saved_u_tiles(rows, E)) * 4 * (2 * ((h + 15) / 16)) * 2048);
+  return round256(static_cast<size_t>(saved_u_tiles(rows, E)) * 4 * (2 * ((h + 15) / 16)) * 1536);
 }
 size_t saved_bytes(long long rows, int h, int E) {
   return saved_p_bytes(rows, h) + saved_u_bytes(rows, h, E);
@@ -127,7 +127,7 @@ moe_status_t repack_weight(const void* src, void* dst, bool fp32, int E, int nsu
 // one expert), `rows` the rows of the row buffers, `tiles_bound` an upper bound of row tiles.
 
 // a6: U = xp W_ug^T, P = w*SwiGLU(U) (w = 1 without row weights) into a_save as bf16; saved
-// (nullable) receives fp32 U and the low half of P.
+// (nullable) receives U (rounded to 24 bits, blocked) and the low half of P.
 moe_status_t run_up_swiglu(const GemmArgs& src, long long rows, long long tiles_bound, int E, int d,
                            int h, const void* xp, const void* w_ug, void* a_save, void* saved,
                            cudaStream_t s) {

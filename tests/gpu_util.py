@@ -67,13 +67,15 @@ def assert_close(got, ref, what: str):
         f"{what}: |err| {np.abs(err).flat[worst]:.3e} > bound {bound.flat[worst]:.3e} at {np.unravel_index(worst, err.shape)}")
 
 
-def unblock_u(u_flat: torch.Tensor, offsets: np.ndarray, h: int) -> torch.Tensor:
-    """Rows [M, 2h] of the saved U from its blocked layout, as the header states it: row p of
-    expert e (the segment starting at s_e) is row r = p - s_e of row tile G = (row tiles of the
-    experts before e) + r // 128, lane l = r % 32 of quadrant q = (r % 128) // 32; column c is
-    in 16-column chunk ci = c // 16 for gate columns and ceil(h/16) + (c - h) // 16 for up
-    columns, in float4 j = (c % 16) // 4 at float ((((G*4 + q)*C2 + ci)*4 + j)*32 + l)*4 + c % 4,
-    C2 = 2 ceil(h/16)."""
+def unblock_u(u_bytes: torch.Tensor, offsets: np.ndarray, h: int) -> torch.Tensor:
+    """Rows [M, 2h] (fp32) of the saved U from its blocked 24-bit layout, as the header states it:
+    row p of expert e (the segment starting at s_e) is row r = p - s_e of row tile G = (row tiles
+    of the experts before e) + r // 128, lane l = r % 32 of quadrant q = (r % 128) // 32; column
+    c is in 16-column chunk ci = c // 16 for gate columns and ceil(h/16) + (c - h) // 16 for up
+    columns, position j = c % 16 in it. The chunk's block starts at byte ((G*4 + q)*C2 + ci)*1536
+    (C2 = 2 ceil(h/16)); the upper 16 bits of value j are the little-endian 16-bit word
+    (j // 8)*256 + l*8 + j % 8 of the block, its lower 8 bits byte 1024 + l*16 + j, and the fp32
+    value is those 24 bits followed by 8 zero bits."""
     h16 = (h + 15) // 16
     c2 = 2 * h16
     starts = np.concatenate([[0], offsets[:-1]])
@@ -89,10 +91,17 @@ def unblock_u(u_flat: torch.Tensor, offsets: np.ndarray, h: int) -> torch.Tensor
     c = np.arange(2 * h)
     cc = np.where(c < h, c, c - h)
     ci = cc // 16 + np.where(c < h, 0, h16)
-    j = (cc % 16) // 4
-    idx = ((((g[:, None] * 4 + q[:, None]) * c2 + ci[None, :]) * 4 + j[None, :]) * 32 + lane[:, None]) * 4 \
-        + (cc % 4)[None, :]
-    return u_flat[torch.from_numpy(idx).to(u_flat.device)]
+    j = cc % 16
+    block = ((g[:, None] * 4 + q[:, None]) * c2 + ci[None, :]) * 1536
+    hi_at = block + (j // 8)[None, :] * 512 + lane[:, None] * 16 + (j % 8)[None, :] * 2
+    lo_at = block + 1024 + lane[:, None] * 16 + j[None, :]
+    b = u_bytes.reshape(-1).view(torch.uint8)
+    dev = b.device
+    hi = b[torch.from_numpy(hi_at).to(dev)].to(torch.int64) | (b[torch.from_numpy(hi_at + 1).to(dev)].to(torch.int64) << 8)
+    lo = b[torch.from_numpy(lo_at).to(dev)].to(torch.int64)
+    v = (hi << 16) | (lo << 8)
+    bits = torch.where(v >= 2 ** 31, v - 2 ** 32, v).to(torch.int32)  # the same 32 bits as int32
+    return bits.view(torch.float32)
 
 
 class DevicePipeline:
@@ -117,7 +126,7 @@ class DevicePipeline:
         self.xp = nan_filled((max(n, 1), d))
         self.y = nan_filled((max(n, 1), d))
         self.a = nan_filled((max(n, 1), h))
-        # saved state for the backward: fp32 U [n, 2h] then the low half of A [n, h]
+        # saved state for the backward: the low half of P [n, h], then U (24 bits, blocked)
         sv = _lib.moe_workspace_bytes(_lib.OP_SAVED, T, k, E, d, h)
         self.saved = nan_filled((max(sv, 4) // 4,), torch.float32) if with_u else None
 
@@ -154,7 +163,7 @@ class DevicePipeline:
 
     @property
     def u(self):
-        """The fp32 U the forward saved, as [M, 2h] rows (unblocked)."""
+        """The U the forward saved (24 bits of each fp32 value), as [M, 2h] fp32 rows (unblocked)."""
         h = self.wl.h
         h8 = (h + 7) // 8 * 8  # widths that are not multiples of 8 are stored zero-padded
         u_flat, _ = _lib.saved_views(self.saved, max(self.cap, 1), h)

@@ -45,15 +45,15 @@ def test_workspace_sizes_are_host_arithmetic(lib):
     assert _lib.moe_workspace_bytes(_lib.OP_BWD, 16384, 8, 256, 2048, 512) == \
         2 * 16384 * 8 * 1024 * 2 + 16384 * 8 * 4 * 4
     assert _lib.routing_grad_parts(512) == 4 and _lib.routing_grad_parts(1000) == 8
-    # saved state: the low bf16 half of P [n, h], then fp32 U in 2 KB blocks (32 rows x 16
-    # columns) for each of at most (n + 127 E) / 128 row tiles, 4 lane quadrants and 2 ceil(h/16)
-    # column chunks
+    # saved state: the low bf16 half of P [n, h], then U at 24 bits in 1536-byte blocks (32 rows
+    # x 16 columns x 3 bytes) for each of at most (n + 127 E) / 128 row tiles, 4 lane quadrants and
+    # 2 ceil(h/16) column chunks
     n = 16384 * 8
     tiles = (n + 127 * 256) // 128
     assert tiles == 1278
-    assert _lib.moe_workspace_bytes(_lib.OP_SAVED, 16384, 8, 256, 2048, 512) == n * 512 * 2 + tiles * 4 * 64 * 2048
+    assert _lib.moe_workspace_bytes(_lib.OP_SAVED, 16384, 8, 256, 2048, 512) == n * 512 * 2 + tiles * 4 * 64 * 1536
     tiles = (20000 + 127 * 64) // 128  # h = 1000: 63 chunks per half, the last one partial
-    assert _lib.moe_workspace_bytes(_lib.OP_SAVED, 20000, 1, 64, 1000, 1000) == 20000 * 1000 * 2 + tiles * 4 * 126 * 2048
+    assert _lib.moe_workspace_bytes(_lib.OP_SAVED, 20000, 1, 64, 1000, 1000) == 20000 * 1000 * 2 + tiles * 4 * 126 * 1536
     bmm = _lib.moe_workspace_bytes(_lib.OP_PADDED_BMM, 10, 1, 4, 64, 128, 4)
     assert bmm == 2 * (16 * 64 * 2) + 16 * 128 * 2  # [16, 64] bf16 x2 and [16, 128] bf16
     assert _lib.moe_workspace_bytes(_lib.OP_ROUTE, 10, 1, 0) == 0      # invalid E
