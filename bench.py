@@ -741,7 +741,7 @@ def run_ours(args):
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e2e_run(3, e0)
     torch.cuda.synchronize()
-    e_steps = max(10, args.steps // 4)
+    e_steps = max(20, args.steps)  # as many steps as the device-timed loop: one host stall weighs less
     e2e_run(e_steps, e0)
     e1.record(stream)
     torch.cuda.synchronize()
