@@ -189,8 +189,8 @@ moe_status_t moe_grouped_swiglu_fwd(const moe_bf16* xp, const int32_t* offsets,
  *          cap = T*top_k) is given, it receives the routing-weight gradient of the combine,
  *          dw_route[t*top_k+j] = <dOut[t], y~_p> with p = inv_map[t*top_k+j] and y~_p = A_p
  *          W_down,e the unweighted expert output (0 for a dropped slot). It is computed as
- *          <A_p, dy_p W_down,e^T> in the dgrad epilogue (dy = the gather of dOut), from fp32
- *          U and the fp32 accumulator, and summed over fixed partial slots in index order:
+ *          <A_p, dy_p W_down,e^T> in the dgrad epilogue (dy = the gather of dOut), from the
+ *          saved U and the fp32 accumulator, and summed over fixed partial slots in index order:
  *          deterministic.
  *  ws      moe_workspace_bytes(MOE_OP_BWD, ...) bytes: dU high and low (2 x [cap, 2h] bf16),
  *          then the routing-gradient partials ([cap, 2 ceil(h/256)] fp32, used with dw_route);
