@@ -41,13 +41,14 @@ def parse_args():
     p.add_argument("--workload", default="large")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-variants", action="store_true")
-    p.add_argument("--sweep", choices=["capacity", "histogram", "configs", "precision", "oracle"],
+    p.add_argument("--sweep", choices=["capacity", "histogram", "configs", "precision", "oracle", "accumulation"],
                    default=None,
                    help="studies instead of the step: capacity (grouped vs capacity-padded BMM over "
                         "routed-row counts), histogram (throughput vs load imbalance), configs "
                         "(forward and training GEMMs on every workload), precision (the wgrads with "
                         "and without the low half of the activation operand), oracle (the CPU "
-                        "baseline on every workload, all cores and one)")
+                        "baseline on every workload, all cores and one), accumulation (the error of "
+                        "long contractions against fp32 sums rounded to nearest and toward zero)")
     return p.parse_args()
 
 
@@ -1179,6 +1180,51 @@ def run_sweep_precision(args):
     return 0
 
 
+def run_sweep_accumulation(args):
+    """How the fp32 accumulation of long contractions behaves: one expert of K rows through the
+    bf16 wgrad (fp32 out, K = the rows), N(0,1) bf16 operands, against the exact sum (fp64) and
+    two fp32 emulations that add each 16-product MMA step's partial sum into the accumulator
+    rounded to nearest (RN) or toward zero (RZ). Up to K = 8192 the library's accumulator is the
+    tensor core's own; longer contractions are summed in segments of 8192 added in RN fp32."""
+    import numpy as np
+    import torch
+    from ragged_grouped_gemm_device_gb300 import _lib as L
+    L.load()
+    dev = "cuda"
+    P = Q = 16
+    rng = np.random.default_rng(1)
+    for lg in (10, 12, 13, 14, 16, 18, 20):
+        K = 1 << lg
+        ta = torch.from_numpy(rng.standard_normal((K, P)).astype(np.float32)).to(torch.bfloat16)
+        tb = torch.from_numpy(rng.standard_normal((K, Q)).astype(np.float32)).to(torch.bfloat16)
+        a64, b64 = ta.double().numpy(), tb.double().numpy()
+        offs = torch.tensor([K], dtype=torch.int32, device=dev)
+        st = torch.zeros(1, dtype=torch.int32, device=dev)
+        dw = torch.full((1, P, Q), float("nan"), device=dev)
+        L.moe_grouped_wgrad(ta.to(dev), None, P, tb.to(dev), Q, offs, 1, K, dw, st)
+        torch.cuda.synchronize()
+        assert st.item() == 0, f"device status {st.item()}"
+        got = dw[0].cpu().double().numpy()
+        ref = a64.T @ b64
+        rn = np.zeros((P, Q), np.float32)
+        rz = np.zeros((P, Q), np.float32)
+        for k0 in range(0, K, 16):
+            part = a64[k0:k0 + 16].T @ b64[k0:k0 + 16]
+            rn = (rn.astype(np.float64) + part).astype(np.float32)
+            s_ = rz.astype(np.float64) + part
+            f = s_.astype(np.float32)
+            over = np.abs(f.astype(np.float64)) > np.abs(s_)
+            f[over] = np.nextafter(f[over], np.float32(0))
+            rz = f
+        rms = lambda e: float(np.sqrt((e ** 2).mean()))
+        print(json.dumps({"sweep": "accumulation", "K": K, "segmented": K > 8192,
+                          "ref_rms": rms(ref), "gpu_err_rms": rms(got - ref),
+                          "fp32_rn_err_rms": rms(rn.astype(np.float64) - ref),
+                          "fp32_rz_err_rms": rms(rz.astype(np.float64) - ref),
+                          "gpu_err_max": float(np.abs(got - ref).max())}), flush=True)
+    return 0
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
@@ -1193,6 +1239,8 @@ def main():
         return run_sweep_oracle(args)
     if args.sweep == "precision":
         return run_sweep_precision(args)
+    if args.sweep == "accumulation":
+        return run_sweep_accumulation(args)
     return run_ours(args)
 
 
