@@ -186,7 +186,7 @@ __global__ void __launch_bounds__(256) mx_permute_quant_kernel(const uint4* __re
   const int lane = threadIdx.x & 31;
   const int gw = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int nw = gridDim.x * 8;
-  for (int p = gw; p < M; p += nw) {
+  for (long long p = gw; p < M; p += nw) {
     const int src = __ldg(sorted_src + p);
     if (src < 0 || src >= n) continue;  // warp-uniform
     long long G;
@@ -291,7 +291,8 @@ moe_status_t launch_mx_permute_quant(const void* x, const int32_t* sorted_src, c
                                     cudaStream_t s) {
   if (d % MXB != 0 || E < 1 || E > MAX_E) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (n == 0) return MOE_OK;
-  const int blocks = std::max(1, std::min((n + 7) / 8, 8 * device_sm_count()));
+  const int blocks = static_cast<int>(std::max(1LL, std::min((static_cast<long long>(n) + 7) / 8,
+                                                            8LL * device_sm_count())));
   mx_permute_quant_kernel<<<blocks, 256, 0, s>>>(static_cast<const uint4*>(x), sorted_src, offsets, E, n, k, d,
                                                  static_cast<uint4*>(xp), static_cast<uint8_t*>(q),
                                                  static_cast<uint8_t*>(sf), activation_sf_tiles(n, E), status);

@@ -34,7 +34,7 @@ __global__ void __launch_bounds__(THREADS) permute_kernel(
   const int lane = threadIdx.x & 31;
   const int gw = blockIdx.x * WARPS + (threadIdx.x >> 5);
   const int nw = gridDim.x * WARPS;
-  for (int p = gw; p < M; p += nw) {
+  for (long long p = gw; p < M; p += nw) {
     const int src = __ldg(sorted_src + p);
     if (src < 0 || src >= n) continue;
     const uint4* xr = x + static_cast<size_t>(src / k) * vec;
@@ -60,7 +60,7 @@ __global__ void __launch_bounds__(THREADS) zero_dropped_rows_kernel(const int32_
   const int lane = threadIdx.x & 31;
   const int gw = blockIdx.x * WARPS + (threadIdx.x >> 5);
   const int nw = gridDim.x * WARPS;
-  for (int t = gw; t < T; t += nw) {
+  for (long long t = gw; t < T; t += nw) {
     if (__ldg(inv + t) >= 0) continue;  // warp-uniform
     for (int v = lane; v < vec; v += 32) out[static_cast<size_t>(t) * vec + v] = make_uint4(0u, 0u, 0u, 0u);
   }
@@ -76,7 +76,7 @@ __global__ void __launch_bounds__(THREADS) combine_kernel(const uint4* __restric
   const int lane = threadIdx.x & 31;
   const int gw = blockIdx.x * WARPS + (threadIdx.x >> 5);
   const int nw = gridDim.x * WARPS;
-  for (int t = gw; t < T; t += nw) {
+  for (long long t = gw; t < T; t += nw) {
     // lane j < k holds slot j's row and weight
     int my_p = -1;
     float my_w = 0.f;
@@ -129,7 +129,8 @@ __global__ void __launch_bounds__(THREADS) combine_kernel(const uint4* __restric
 __global__ void __launch_bounds__(THREADS) routing_weight_grad_kernel(
     const float* __restrict__ part, int np, const int32_t* __restrict__ inv, int n_slots,
     float* __restrict__ dw) {
-  for (int sl = blockIdx.x * THREADS + threadIdx.x; sl < n_slots; sl += gridDim.x * THREADS) {
+  for (long long sl = static_cast<long long>(blockIdx.x) * THREADS + threadIdx.x; sl < n_slots;
+       sl += static_cast<long long>(gridDim.x) * THREADS) {
     const int p = __ldg(inv + sl);
     float acc = 0.f;
     if (p >= 0 && MOE_DBG_IN(DBG_RWG_ROW, p, n_slots))
@@ -148,7 +149,7 @@ __global__ void __launch_bounds__(THREADS) permute_scalar_kernel(
   const int lane = threadIdx.x & 31;
   const int gw = blockIdx.x * WARPS + (threadIdx.x >> 5);
   const int nw = gridDim.x * WARPS;
-  for (int p = gw; p < M; p += nw) {
+  for (long long p = gw; p < M; p += nw) {
     const int src = __ldg(sorted_src + p);
     if (src < 0 || src >= n) continue;
     const bf16* xr = x + static_cast<size_t>(src / k) * d;
@@ -167,7 +168,7 @@ __global__ void __launch_bounds__(THREADS) combine_scalar_kernel(const bf16* __r
   const int lane = threadIdx.x & 31;
   const int gw = blockIdx.x * WARPS + (threadIdx.x >> 5);
   const int nw = gridDim.x * WARPS;
-  for (int t = gw; t < T; t += nw) {
+  for (long long t = gw; t < T; t += nw) {
     for (int c = lane; c < d; c += 32) {
       float acc = 0.f;
       for (int j = 0; j < k; ++j) {
@@ -249,7 +250,7 @@ __global__ void __launch_bounds__(THREADS) unpad_rows_kernel(const uint4* __rest
   const int lane = threadIdx.x & 31;
   const int gw = blockIdx.x * WARPS + (threadIdx.x >> 5);
   const int nw = gridDim.x * WARPS;
-  for (int p = gw; p < M; p += nw) {
+  for (long long p = gw; p < M; p += nw) {
     int lo = 0, hi = E - 1;  // first e with offsets[e] > p
     while (lo < hi) {
       const int mid = (lo + hi) >> 1;

@@ -168,7 +168,8 @@ __global__ void __launch_bounds__(256) route_scatter_kernel(
   }
   // rows past the final offset hold no slot
   const int stride = gridDim.x * blockDim.x;
-  for (int p = M + blockIdx.x * blockDim.x + threadIdx.x; p < n; p += stride) sorted_src[p] = -1;
+  for (long long p = M + static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; p < n; p += stride)
+    sorted_src[p] = -1;
 }
 
 }  // namespace
@@ -184,7 +185,7 @@ size_t route_workspace_bytes(long long n, int E) {
 moe_status_t launch_route(const int32_t* ids, int n, int E, int32_t* counts, int32_t* offsets,
                           int32_t* sorted_src, int32_t* inv_map, void* ws, cudaStream_t s) {
   if (E < 1 || E > MAX_E) return MOE_ERR_UNSUPPORTED_SHAPE;
-  const int W = (n + CHUNK - 1) / CHUNK;
+  const int W = static_cast<int>((static_cast<long long>(n) + CHUNK - 1) / CHUNK);  // n < 2^31
   int32_t* hist = static_cast<int32_t*>(ws);
   if (W == 0) {
     // no slots: zero counts and offsets

@@ -105,3 +105,45 @@ def test_permute_then_combine_is_k_times_identity(lib, k):
     _lib.moe_unpermute_combine(run.xp, run.inv_map, None, wl.T, k, wl.d, out)
     torch.cuda.synchronize()
     assert torch.equal(out, run.x * k)
+
+
+@pytest.mark.slow
+def test_route_permute_combine_at_the_slot_limit(lib):
+    """T*top_k = 2^31 - 8, just below the header's limit of 2^31 slots (int32 indices): routing,
+    the gather and the combine keep every index in range. Checked on the device: the counts
+    against a direct count, the placement and the inverse map on a million sampled rows, the
+    gathered rows bit for bit, and the combine of small integers (exact in bf16) against
+    top_k * x. About 75 GB of device memory."""
+    from ragged_grouped_gemm_device_gb300 import _lib as L
+    k, E, d = 8, 4, 8
+    T = (1 << 28) - 1
+    n = T * k
+    assert n == (1 << 31) - 8
+    dev, i32 = "cuda", torch.int32
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(3)
+    ids = torch.randint(0, E, (n,), dtype=i32, device=dev, generator=gen)
+    counts, offsets = torch.empty(E, dtype=i32, device=dev), torch.empty(E, dtype=i32, device=dev)
+    sorted_src, inv = torch.empty(n, dtype=i32, device=dev), torch.empty(n, dtype=i32, device=dev)
+    ws = torch.empty(L.moe_workspace_bytes(L.OP_ROUTE, T, k, E), dtype=torch.uint8, device=dev)
+    L.moe_route_offsets(ids, T, k, E, counts, offsets, sorted_src, inv, ws)
+    ref_counts = torch.stack([(ids == e).sum() for e in range(E)])
+    assert torch.equal(counts.long(), ref_counts)
+    assert torch.equal(offsets.long(), ref_counts.cumsum(0)) and int(offsets[-1]) == n
+    p = torch.randint(0, n, (1 << 20,), dtype=torch.int64, device=dev, generator=gen)
+    p = torch.cat([p, torch.tensor([0, n - 2, n - 1], device=dev)])
+    src = sorted_src[p].long()
+    assert torch.equal(ids[src].long(), torch.searchsorted(offsets.long(), p, right=True))
+    assert torch.equal(inv[src].long(), p)
+    # stable placement: within a segment the slots keep increasing flat-index order
+    q = p[p + 1 < n]
+    same = torch.searchsorted(offsets.long(), q, right=True) == torch.searchsorted(offsets.long(), q + 1, right=True)
+    assert (sorted_src[q[same]] < sorted_src[q[same] + 1]).all()
+    del ids, ws
+    x = torch.randint(-3, 4, (T, d), dtype=i32, device=dev, generator=gen).to(torch.bfloat16)
+    xp = torch.empty(n, d, dtype=torch.bfloat16, device=dev)
+    L.moe_permute(x, sorted_src, offsets, None, T, k, E, d, xp)
+    assert torch.equal(xp[p], x[src // k])
+    out = torch.empty(T, d, dtype=torch.bfloat16, device=dev)
+    L.moe_unpermute_combine(xp, inv, None, T, k, d, out)
+    assert torch.equal(out, x * k)
