@@ -41,6 +41,10 @@ FWD_CASES = {
     # h = 16 (sums of ~256) it does not, whatever the order of the additions.
     "edge_max_d": lambda: W.custom(T=24, k=1, E=2, d=1 << 20, h=64, seed=15),
     "edge_max_h": lambda: W.custom(T=24, k=2, E=1, d=32, h=1 << 20, seed=16),
+    # the narrowest rows: d = h = 8 (one 16-byte row pitch, a K block mostly zero fill) and
+    # d = h = 1 (zero-padded to 8 inside the composite calls)
+    "edge_min_width": lambda: W.custom(T=40, k=2, E=3, d=8, h=8, seed=18, empty_experts=(2,)),
+    "edge_width_1": lambda: W.custom(T=30, k=2, E=3, d=1, h=1, seed=19),
     # one expert with 20000 rows: a wgrad contraction of 313 K blocks, accumulated in segments
     "edge_long_expert": lambda: W.custom(T=20000, k=1, E=2, d=64, h=64, seed=17, empty_experts=(1,)),
     "balanced": lambda: W.make("balanced"),
@@ -49,8 +53,8 @@ FWD_CASES = {
 }
 
 BWD_CASES = ["toy", "edge_small", "edge_wide", "edge_one_expert", "edge_sparse", "edge_max_experts",
-             "edge_odd_width", "edge_odd_width2", "edge_max_d", "edge_max_h", "edge_long_expert", "finegrained",
-             "skew"]
+             "edge_odd_width", "edge_odd_width2", "edge_max_d", "edge_max_h", "edge_min_width", "edge_width_1",
+             "edge_long_expert", "finegrained", "skew"]
 
 
 def _dy(wl, M):
