@@ -331,15 +331,15 @@ GEMM_SOURCES = ("common.cuh", "grouped_gemm.cu", "internal.h", "moe_gg.cu")
 
 
 def _code_only(text):
-    """C++ source without its comments and blank lines: what the compiler sees."""
+    """C++ source without its comments, blank lines and layout whitespace: what the compiler sees."""
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     text = re.sub(r"//[^\n]*", "", text)
-    return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+    return "\n".join(" ".join(line.split()) for line in text.splitlines() if line.strip())
 
 
 def kernel_source_hash():
     """Hash of the grouped GEMM's code (device code, launch arguments and tensor maps; comments
-    left out): DRAM traffic taken by the profiler is valid only for it. The routing and
+    and layout whitespace left out): DRAM traffic taken by the profiler is valid only for it. The routing and
     row-movement kernels (route.cu, permute.cu) do not enter it."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "ragged_grouped_gemm_device_gb300", "csrc")

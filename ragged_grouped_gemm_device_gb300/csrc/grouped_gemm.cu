@@ -533,7 +533,7 @@ __global__ void __launch_bounds__(THREADS, 1)
               // swizzle only permutes 16-byte pieces inside a 128-byte row, so those rows are the
               // contiguous bytes [valid * 128, 8192) of each box.
               const int pieces = (BK - valid) * 8;
-  #pragma unroll
+#pragma unroll
               for (int atom = 0; atom < SB / ATOM_BYTES; ++atom) {
                 uint4* base = reinterpret_cast<uint4*>(sp + atom * ATOM_BYTES + valid * 128);
                 for (int c = lane; c < pieces; c += 32) base[c] = make_uint4(0u, 0u, 0u, 0u);
@@ -555,7 +555,7 @@ __global__ void __launch_bounds__(THREADS, 1)
               tmem_cp_32x128b_x4(sft + 4, smem_desc_rows16(sfs + 512));
               tmem_cp_32x128b_x4(sft + 8, smem_desc_rows16(sfs + 1024));
               constexpr uint32_t idesc_mx = idesc_mxf8_e4m3(BM, BN);
-  #pragma unroll
+#pragma unroll
               for (int ks = 0; ks < MX_BK / MX_UK; ++ks) {
                 const uint64_t ad = smem_desc_sw128(sa + ks * MX_UK, 16, 1024);
                 const uint64_t bd = smem_desc_sw128(sb + ks * MX_UK, 16, 1024);
@@ -570,9 +570,9 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (lane == 0) {
             const uint32_t sa = stage0 + s * SB;
             const uint32_t sb = sa + APARTS * A_BYTES;
-  #pragma unroll
+#pragma unroll
             for (int part = 0; part < APARTS; ++part) {
-  #pragma unroll
+#pragma unroll
               for (int ks = 0; ks < BK / UK; ++ks) {
                 const uint32_t ap = sa + part * A_BYTES;
                 const uint64_t ad = ModeTraits<MODE>::a_mn
