@@ -39,6 +39,9 @@ def parse_args():
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default="large")
+    p.add_argument("--config", type=int, choices=range(5), default=None,
+                   help="a named workload by index (0 toy, 1 balanced, 2 finegrained, 3 skew, 4 large); "
+                        "overrides --workload")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-variants", action="store_true")
     p.add_argument("--sweep", choices=["capacity", "histogram", "configs", "precision", "oracle", "accumulation"],
@@ -49,7 +52,10 @@ def parse_args():
                         "and without the low half of the activation operand), oracle (the CPU "
                         "baseline on every workload, all cores and one), accumulation (the error of "
                         "long contractions against fp32 sums rounded to nearest and toward zero)")
-    return p.parse_args()
+    args = p.parse_args()
+    if args.config is not None:
+        args.workload = ("toy", "balanced", "finegrained", "skew", "large")[args.config]
+    return args
 
 
 def load_peaks():
