@@ -10,9 +10,9 @@
 // same experts (the down and the up/gate projection's): the second one's tiles follow the
 // first's in the same tile sequence, so one persistent launch covers both.
 //
-// Roles (352 threads, warp-specialised):
+// Roles (384 threads, warp-specialised):
 //   warp 0      TMA producer of the A operand: 128B-swizzled tiles into a 4-stage
-//               shared-memory ring (3 stages of A high, A low and B in the hi/lo wgrad).
+//               shared-memory ring (the wgrad's stages hold A high, A low and half of B).
 //   warp 10     TMA producer of the B operand into the same stages.
 //   warp 1      tensor-memory allocator and MMA issuer: tcgen05.mma 128x256x16 (bf16 in, fp32
 //               accumulate) into one of two 256-column TMEM accumulators, so the epilogue of a
@@ -24,12 +24,20 @@
 //               segment still multiplies the neighbouring rows (rows of a product are
 //               independent) but never stores them. For a segmented contraction they first
 //               add each later segment into the tile's accumulator (fp32, tcgen05.st).
-// The wgrad mode contracts over the M_e rows of an expert (Table 15): its operands are
-// MN-major and the rows of the last K block that belong to the next expert are zeroed in
-// shared memory before the MMA reads them. Its A operand comes as a bf16 high/low pair (the
-// activation and its rounding remainder); both halves are multiplied with the same B tile
-// into one fp32 accumulator, which keeps about 16 significant bits of the activations in the
-// weight gradient.
+//   warp 11     wgrad: zeroes the rows of the next expert in each expert's last K block.
+// The wgrad modes contract over the M_e rows of an expert (Table 15) with MN-major operands.
+// They run as pairs of CTAs (clusters of two, tcgen05 cta_group::2) on 256 x 256 gradient
+// tiles: each CTA stages its 128 gradient rows of A and 128 of the tile's 256 B rows, the even
+// CTA issues M = 256 MMAs that read both CTAs' stages and write each CTA's 128 accumulator rows
+// into its own tensor memory, and each CTA stores its rows. Per SM that moves 48 KB of
+// operands per 64-deep K block instead of 64 KB for the same MMA work. The odd CTA's copies
+// complete on the even CTA's barriers; the even CTA's MMAs release both CTAs' stages. An
+// expert's last K block runs only the 16-row K steps that hold its rows, and the rows of the
+// next expert inside the last of them are zeroed in both CTAs' stages by warp 11 before the MMA
+// issuer sees the stage as full. The A operand comes as a bf16 high/low pair (the activation
+// and its rounding remainder); both halves are multiplied with the same B tile into one fp32
+// accumulator, which keeps about 16 significant bits of the activations in the weight
+// gradient.
 #include <algorithm>
 #include <cstdio>
 #include <mutex>
@@ -45,13 +53,15 @@ constexpr int BN = 256;          // UMMA N: accumulator columns
 constexpr int BK = 64;           // one 128-byte swizzle atom of bf16 along K
 constexpr int UK = 16;           // K of one tcgen05.mma kind::f16
 constexpr int STAGES = 4;                     // ring depth of the row-grouped modes
+constexpr int MAX_STAGES = 6;                 // deepest ring of any mode (bf16-only wgrad)
 constexpr int A_BYTES = BM * BK * 2;          // 16 KB
 constexpr int B_BYTES = BN * BK * 2;          // 32 KB
 constexpr int RING_BYTES = STAGES * (A_BYTES + B_BYTES);  // 192 KB, shared by every mode
 constexpr int ATOM_BYTES = 64 * BK * 2;       // one MN-major 64x64 box: 8 KB
 constexpr int EPI_WARPS = 8;                 // epilogue warps: 2 per TMEM lane quadrant
 constexpr int PRODUCER_B_WARP = 2 + EPI_WARPS;  // second TMA producer (B operand)
-constexpr int THREADS = 32 * (PRODUCER_B_WARP + 1);
+constexpr int ZERO_WARP = PRODUCER_B_WARP + 1;   // wgrad: zeroes the rows of the next expert
+constexpr int THREADS = 32 * (ZERO_WARP + 1);
 constexpr int TMEM_COLS = 512;                // two 256-column accumulators
 constexpr int MAX_E = 1024;
 constexpr int RASTER_M = 16;                  // row tiles per raster group (see decode_tile)
@@ -79,8 +89,9 @@ constexpr int MX_BK = 128;                    // K elements per MXFP8 stage (128
 constexpr int MX_UK = 32;                     // K of one block-scaled MMA
 
 struct Ctl {
-  uint64_t full[STAGES];
-  uint64_t empty[STAGES];
+  uint64_t full[MAX_STAGES];
+  uint64_t empty[MAX_STAGES];
+  uint64_t tail_full[MAX_STAGES];  // wgrad: the stage of an expert's last K block has landed
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t done;
@@ -115,10 +126,23 @@ struct ModeTraits {
   // one in the MXFP8 modes, whose scale slots take the other half of the 512 columns
   static constexpr int nacc = mx ? 1 : 2;
   static constexpr int bk = mx ? MX_BK : BK;  // K elements per stage
-  // MODE_WGRAD stages hold A high, A low and B: 64 KB, three of them; the others 48 KB, four
+  // The wgrad modes run as pairs of CTAs (clusters of two) on 256-row gradient tiles: each CTA
+  // stages its 128 rows of A and half (128) of the tile's 256 B rows, and the even CTA of the
+  // pair issues M = 256 MMAs (cta_group::2) that read both CTAs' shared memory and write each
+  // CTA's 128 accumulator rows into its own tensor memory. Per SM that is 48 KB of operands
+  // (hi/lo) per 64-deep K block instead of 64 KB for the same MMA work.
+  static constexpr bool pair = wgrad;
+  static constexpr int cg = pair ? 2 : 1;              // CTA group of every tcgen05 instruction
+  static constexpr int tile_m = pair ? 2 * BM : BM;    // wgrad: gradient rows per tile
+  static constexpr int b_rows = pair ? BN / 2 : BN;    // B rows staged by this CTA
+  // MODE_WGRAD stages hold A high, A low and this CTA's half of B: 48 KB, four of them; the
+  // bf16-only wgrad 32 KB, six; the row-grouped modes 48 KB, four
   static constexpr int a_parts = (MODE == MODE_WGRAD) ? 2 : 1;
-  static constexpr int stage_bytes = a_parts * A_BYTES + B_BYTES;
+  static constexpr int stage_bytes = a_parts * A_BYTES + b_rows * BK * 2;
   static constexpr int stages = RING_BYTES / stage_bytes;
+  static_assert(stages <= MAX_STAGES, "ring deeper than the control block's barriers");
+  static_assert(tile_m % BM == 0 && out_cols_per_tile % 16 == 0 && bk % UK == 0, "tile shape");
+  static_assert(!wgrad || pair, "the wgrad modes run as CTA pairs");
   // A and B parts of each stage loaded by two producer threads (see the producer role)
   static constexpr bool split_producer = true;
 };
@@ -165,7 +189,7 @@ __device__ __forceinline__ Tile decode_tile(const Sched& s, int t) {
     ti.e = tt / per;
     const int r = tt - ti.e * per;
     const int mi = r / nt;
-    ti.m0 = mi * BM;
+    ti.m0 = mi * ModeTraits<MODE>::tile_m;
     ti.n0 = (r - mi * nt) * BN;
     ti.row0 = s.offs[ti.e];
     ti.kvalid = s.offs[ti.e + 1] - ti.row0;
@@ -268,6 +292,28 @@ __device__ __forceinline__ void st_global_v4(void* p, uint32_t a, uint32_t b, ui
   *reinterpret_cast<uint4*>(p) = make_uint4(a, b, c, d);
 }
 
+// Contraction rows [r0, r1) of every 64x64 box of a wgrad stage (SB bytes at sp) belong to the
+// next expert: zero them, in this CTA's stage and in the odd CTA's copy of it (same offsets). The
+// swizzle only permutes 16-byte pieces inside a 128-byte row, so those rows are the contiguous
+// bytes [r0 * 128, r1 * 128) of each box. One warp; the zeros are made visible to the tensor
+// cores' reads of both CTAs' shared memory.
+template <int SB>
+__device__ __forceinline__ void zero_stage_rows(uint8_t* sp, int r0, int r1, int lane) {
+  const int pieces = (r1 - r0) * 8;
+  const uint32_t peer = cluster_addr(smem_u32(sp), 1u);
+#pragma unroll
+  for (int atom = 0; atom < SB / ATOM_BYTES; ++atom) {
+    const int off = atom * ATOM_BYTES + r0 * 128;
+    uint4* base = reinterpret_cast<uint4*>(sp + off);
+    for (int c = lane; c < pieces; c += 32) {
+      base[c] = make_uint4(0u, 0u, 0u, 0u);
+      st_cluster_zero16(peer + off + c * 16);
+    }
+  }
+  fence_proxy_async_smem();
+  fence_proxy_async_cluster();
+}
+
 template <int MODE>
 __global__ void __launch_bounds__(THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs args) {
@@ -285,12 +331,17 @@ __global__ void __launch_bounds__(THREADS, 1)
   constexpr int EPI = ModeTraits<MODE>::epi;
   constexpr int NACC = ModeTraits<MODE>::nacc;
   constexpr bool MX = ModeTraits<MODE>::mx;
+  constexpr bool PAIR = ModeTraits<MODE>::pair;
+  constexpr int CG = ModeTraits<MODE>::cg;
+  constexpr uint32_t B_STAGE = ModeTraits<MODE>::b_rows * BK * 2;  // B bytes this CTA stages
   const int E = args.E;
   int* pre = offs + (E + 1);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
+  // CTA pairs: rank 0 issues the MMAs of the pair; both CTAs load, stage and store their halves
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
 
   // ---- problem list: row segments of the experts (the preparation step, in-kernel)
   const bool single = args.single_expert >= 0;
@@ -316,10 +367,11 @@ __global__ void __launch_bounds__(THREADS, 1)
   sc.pre = pre;
   sc.E = E;
   if constexpr (ModeTraits<MODE>::wgrad) {
-    sc.mt = (args.Mdim + BM - 1) / BM;
+    constexpr int TM = ModeTraits<MODE>::tile_m;
+    sc.mt = (args.Mdim + TM - 1) / TM;
     sc.nt = (args.N + BN - 1) / BN;
     const bool two = args.nprob == 2;
-    sc.mt2 = two ? (args.Mdim2 + BM - 1) / BM : 0;
+    sc.mt2 = two ? (args.Mdim2 + TM - 1) / TM : 0;
     sc.nt2 = two ? (args.N2 + BN - 1) / BN : 0;
     sc.kblocks = 0;
     sc.total0 = E * sc.mt * sc.nt;
@@ -349,13 +401,17 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   // ---- barriers and tensor memory
   if (tid == 0) {
+    // full: this CTA's producers (with pairs the even CTA's expect the odd CTA's bytes too, and
+    // the odd CTA's are unused); tempty: every epilogue thread, or with pairs (on the even CTA
+    // only) one arrival per epilogue warp of both CTAs
     for (int s = 0; s < NST; ++s) {
       mbar_init(smem_u32(&ctl->full[s]), ModeTraits<MODE>::split_producer ? 2 : 1);
       mbar_init(smem_u32(&ctl->empty[s]), 1);
+      mbar_init(smem_u32(&ctl->tail_full[s]), ModeTraits<MODE>::split_producer ? 2 : 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&ctl->tfull[b]), 1);
-      mbar_init(smem_u32(&ctl->tempty[b]), 32 * EPI_WARPS);
+      mbar_init(smem_u32(&ctl->tempty[b]), PAIR ? 2 * EPI_WARPS : 32 * EPI_WARPS);
     }
     mbar_init(smem_u32(&ctl->done), 1);
     ctl->abort_flag = 0;
@@ -370,15 +426,18 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(&ctl->tmem_base), TMEM_COLS);
-    tmem_relinquish();
+    tmem_alloc<CG>(smem_u32(&ctl->tmem_base), TMEM_COLS);
+    tmem_relinquish<CG>();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // the peer's barriers must be initialised before any arrival or commit can reach them
+  if constexpr (PAIR) cluster_sync_all();
   if constexpr (!ModeTraits<MODE>::wgrad) sc.total = pre[E] * sc.nt;
-  const int t_first = static_cast<int>(blockIdx.x);
-  const int t_step = static_cast<int>(gridDim.x);
+  // CTA pairs take tiles in turn by cluster, single CTAs by block
+  const int t_first = PAIR ? static_cast<int>(cluster_id_x()) : static_cast<int>(blockIdx.x);
+  const int t_step = PAIR ? static_cast<int>(nclusters_x()) : static_cast<int>(gridDim.x);
   const uint32_t tmem_base = ctl->tmem_base;
   volatile int* abort_flag = &ctl->abort_flag;
   const long long tmo = args.timeout_ns;
@@ -390,7 +449,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   // warp the B part. Each arrives on the stage's full barrier (count 2) with the bytes it will
   // deliver, so the phase completes when both have arrived and every byte has landed, in
   // whatever order. One instruction stream per part halves the serial issue latency per stage
-  // (the MN-major B part alone is four boxes).
+  // (the MN-major B part alone is four boxes). With CTA pairs the even CTA's producers expect
+  // the bytes of both CTAs' parts and the odd CTA's copies complete on the even CTA's barrier
+  // (the odd CTA only loads after its own empty barrier, released by the even CTA's MMAs of
+  // the stage's previous use, so its bytes always count towards the current phase).
   constexpr bool SPLIT = ModeTraits<MODE>::split_producer;
   const int prole = (warp == 0) ? 0 : (SPLIT && warp == PRODUCER_B_WARP) ? 1 : -1;
   if (prole >= 0) {
@@ -403,8 +465,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         const Tile ti = decode_tile<MODE>(sc, t);
         const int eg = ti.e + expert_base;
         constexpr uint32_t A_SF = MX ? 512u : 0u, B_SF = MX ? 1024u : 0u;
-        const uint32_t bytes = (do_a ? static_cast<uint32_t>(APARTS * A_BYTES) + A_SF : 0u) +
-                               (do_b ? static_cast<uint32_t>(B_BYTES) + B_SF : 0u);
+        const uint32_t bytes = ((do_a ? static_cast<uint32_t>(APARTS * A_BYTES) + A_SF : 0u) +
+                                (do_b ? B_STAGE + B_SF : 0u)) * (PAIR ? 2u : 1u);
         for (int kb = 0; kb < ti.kblocks; ++kb, ++it) {
           const int s = it % NST;
           const uint32_t ph = (it / NST) & 1u;
@@ -412,8 +474,14 @@ __global__ void __launch_bounds__(THREADS, 1)
             ok = false;
             break;
           }
-          const uint32_t fb = smem_u32(&ctl->full[s]);
-          mbar_arrive_expect_tx(fb, bytes);
+          // wgrad: the last K block of an expert whose rows end inside a 16-row K step completes
+          // on the stage's tail_full barrier instead; the zeroing warp completes full after it
+          // has zeroed the next expert's rows
+          bool ztail = false;
+          if constexpr (ModeTraits<MODE>::wgrad) ztail = kb == ti.kblocks - 1 && (ti.kvalid % UK) != 0;
+          const uint32_t fl = smem_u32(ztail ? &ctl->tail_full[s] : &ctl->full[s]);
+          const uint32_t fb = (PAIR && rank != 0) ? cluster_addr(fl, 0u) : fl;
+          if (!(PAIR && rank != 0)) mbar_arrive_expect_tx(fb, bytes);
           const uint32_t sa = stage0 + s * SB;
           const uint32_t sb = sa + APARTS * A_BYTES;
           const int k0 = kb * BK;
@@ -469,24 +537,31 @@ __global__ void __launch_bounds__(THREADS, 1)
           } else if constexpr (MODE == MODE_DGRAD_SWIGLU) {
             if (do_b) tma_load_3d(sb, &maps.b, k0, ti.n0, eg, fb);  // 256 rows of W_down in one box
           } else {
-            // MN-major 64 x 64 boxes: two of A (and two of its low half), four of B, from the
-            // operands of this tile's gradient
+            // MN-major 64 x 64 boxes from the operands of this tile's gradient: this CTA's 128
+            // rows of the 256-row tile (two boxes of A and two of its low half) and its 128 of
+            // the tile's 256 B rows (two boxes). Rows past the gradient read as zeros.
             const int rk = ti.row0 + k0;  // first contraction row of this K block
+            auto load = [&](uint32_t dst, const CUtensorMap* map, int c0) {
+              if (rank != 0) tma_load_2d_peer(dst, map, c0, rk, fb);
+              else tma_load_2d(dst, map, c0, rk, fb);
+            };
             if (do_a) {
               const CUtensorMap* ma = ti.prob ? &maps.a2 : &maps.a;
+              const int am = ti.m0 + static_cast<int>(rank) * BM;
 #pragma unroll
-              for (int i = 0; i < BM / 64; ++i) tma_load_2d(sa + i * ATOM_BYTES, ma, ti.m0 + 64 * i, rk, fb);
+              for (int i = 0; i < BM / 64; ++i) load(sa + i * ATOM_BYTES, ma, am + 64 * i);
               if constexpr (APARTS == 2) {
                 const CUtensorMap* ml = ti.prob ? &maps.a_lo2 : &maps.a_lo;
 #pragma unroll
-                for (int i = 0; i < BM / 64; ++i)
-                  tma_load_2d(sa + A_BYTES + i * ATOM_BYTES, ml, ti.m0 + 64 * i, rk, fb);
+                for (int i = 0; i < BM / 64; ++i) load(sa + A_BYTES + i * ATOM_BYTES, ml, am + 64 * i);
               }
             }
             if (do_b) {
               const CUtensorMap* mb = ti.prob ? &maps.b2 : &maps.b;
+              constexpr int BR = ModeTraits<MODE>::b_rows;
+              const int bn = ti.n0 + static_cast<int>(rank) * BR;
 #pragma unroll
-              for (int i = 0; i < BN / 64; ++i) tma_load_2d(sb + i * ATOM_BYTES, mb, ti.n0 + 64 * i, rk, fb);
+              for (int i = 0; i < BR / 64; ++i) load(sb + i * ATOM_BYTES, mb, bn + 64 * i);
             }
           }
         }
@@ -494,14 +569,29 @@ __global__ void __launch_bounds__(THREADS, 1)
       // drain: the copies this thread issued into each stage must land before the CTA can exit.
       // After an abort a stage may lack the other producer's part and never complete; the first
       // wait that runs out (drain_ns, seconds) has outlasted every copy issued here, so stop.
-      const uint32_t first = it > NST ? it - NST : 0u;
-      for (uint32_t j = first; j < it; ++j)
-        if (!mbar_wait(smem_u32(&ctl->full[j % NST]), (j / NST) & 1u, abort_flag, status, args.drain_ns, false))
-          break;
+      // The odd CTA of a pair cannot wait on the even CTA's barriers: its copies have landed
+      // once the even CTA's MMAs consumed them (the pair leaves together, after the even CTA's
+      // last MMA); after an abort it gives them a bounded 200 us instead.
+      if (PAIR && rank != 0) {
+        if (!ok) {
+          const uint64_t t0 = globaltimer_ns();
+          while (globaltimer_ns() - t0 < 200000ull) __nanosleep(1000);
+        }
+      } else {
+        const uint32_t first = it > NST ? it - NST : 0u;
+        for (uint32_t j = first; j < it; ++j)
+          if (!mbar_wait(smem_u32(&ctl->full[j % NST]), (j / NST) & 1u, abort_flag, status, args.drain_ns, false))
+            break;
+      }
     }
-  } else if (warp == 1) {
+  } else if (warp == 1 && rank == 0) {
     // =========================================================== MMA issuer
-    constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, ModeTraits<MODE>::a_mn, ModeTraits<MODE>::b_mn);
+    // (with CTA pairs, on the even CTA only: M = 256 over both CTAs' stages)
+    constexpr uint32_t idesc =
+        idesc_bf16_f32(PAIR ? 2 * BM : BM, BN, ModeTraits<MODE>::a_mn, ModeTraits<MODE>::b_mn);
+    // barriers of the odd CTA that this CTA's commits also arrive on (pairs)
+    [[maybe_unused]] const uint32_t peer_empty0 = PAIR ? cluster_addr(smem_u32(&ctl->empty[0]), 1u) : 0u;
+    [[maybe_unused]] const uint32_t peer_tfull0 = PAIR ? cluster_addr(smem_u32(&ctl->tfull[0]), 1u) : 0u;
     uint32_t it = 0, turn = 0;
     uint32_t use0 = 0, use1 = 0;  // completed uses of accumulator buffers 0 and 1 (registers)
     bool ok = true;
@@ -513,8 +603,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int seg_len = nseg == 1 ? ti.kblocks : SEG_KB;
       for (int sg = 0; sg < nseg && ok; ++sg) {
         const uint32_t buf = sg == 0 ? turn : (turn ^ 1u);
-        ok = warp_all(mbar_wait(smem_u32(&ctl->tempty[buf]), ((buf ? use1 : use0) & 1u) ^ 1u, abort_flag, status,
-                                tmo));
+        ok = warp_all(mbar_wait(smem_u32(&ctl->tempty[buf]), ((buf ? use1 : use0) & 1u) ^ 1u, abort_flag,
+                                      status, tmo));
         if (!ok) break;
         tc_fence_after();
         const uint32_t dtm = tmem_base + buf * BN;
@@ -525,22 +615,13 @@ __global__ void __launch_bounds__(THREADS, 1)
           ok = warp_all(mbar_wait(smem_u32(&ctl->full[s]), ph, abort_flag, status, tmo));
           if (!ok) break;
           tc_fence_after();
-          uint8_t* sp = stages + s * SB;
+          // wgrad: the last K block of an expert runs only the 16-row K steps that hold its
+          // rows (kq of them); the rows of the next expert inside the last of those have been
+          // zeroed by the zeroing warp before it completed the stage's full barrier
+          [[maybe_unused]] int kq = BK / UK;
           if constexpr (ModeTraits<MODE>::wgrad) {
             const int valid = ti.kvalid - kb * BK;
-            if (valid < BK) {
-              // rows [valid, 64) of every 64x64 box belong to the next expert: zero them. The
-              // swizzle only permutes 16-byte pieces inside a 128-byte row, so those rows are the
-              // contiguous bytes [valid * 128, 8192) of each box.
-              const int pieces = (BK - valid) * 8;
-#pragma unroll
-              for (int atom = 0; atom < SB / ATOM_BYTES; ++atom) {
-                uint4* base = reinterpret_cast<uint4*>(sp + atom * ATOM_BYTES + valid * 128);
-                for (int c = lane; c < pieces; c += 32) base[c] = make_uint4(0u, 0u, 0u, 0u);
-              }
-              fence_proxy_async_smem();
-            }
-            __syncwarp();
+            if (valid < BK) kq = (valid + UK - 1) / UK;
           }
           if constexpr (MX) {
             if (lane == 0) {
@@ -574,6 +655,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int part = 0; part < APARTS; ++part) {
 #pragma unroll
               for (int ks = 0; ks < BK / UK; ++ks) {
+                if (ks >= kq) break;
                 const uint32_t ap = sa + part * A_BYTES;
                 const uint64_t ad = ModeTraits<MODE>::a_mn
                                         ? smem_desc_sw128(ap + ks * (UK * 128), ATOM_BYTES, 1024)
@@ -581,16 +663,21 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const uint64_t bd = ModeTraits<MODE>::b_mn
                                         ? smem_desc_sw128(sb + ks * (UK * 128), ATOM_BYTES, 1024)
                                         : smem_desc_sw128(sb + ks * (UK * 2), 16, 1024);
-                mma_bf16_ss(dtm, ad, bd, idesc, ((kb - kb0) | ks | part) != 0 ? 1u : 0u);
+                mma_bf16_ss<CG>(dtm, ad, bd, idesc, ((kb - kb0) | ks | part) != 0 ? 1u : 0u);
               }
             }
-            // release the stage to the producers once these MMAs have read it
-            mma_commit(smem_u32(&ctl->empty[s]));
+            // release the stage to the producers (of both CTAs of a pair) once these MMAs have
+            // read it
+            mma_commit<CG>(smem_u32(&ctl->empty[s]));
+            if constexpr (PAIR) mma_commit<CG>(peer_empty0 + s * static_cast<uint32_t>(sizeof(uint64_t)));
           }
           __syncwarp();
         }
         if (!ok) break;
-        if (lane == 0) mma_commit(smem_u32(&ctl->tfull[buf]));
+        if (lane == 0) {
+          mma_commit<CG>(smem_u32(&ctl->tfull[buf]));
+          if constexpr (PAIR) mma_commit<CG>(peer_tfull0 + buf * static_cast<uint32_t>(sizeof(uint64_t)));
+        }
         __syncwarp();
         if (buf) ++use1; else ++use0;
       }
@@ -598,9 +685,29 @@ __global__ void __launch_bounds__(THREADS, 1)
       if constexpr (NACC == 2) turn ^= 1u;
     }
     // every MMA this thread issued must finish before tensor memory is released
-    if (lane == 0) mma_commit(smem_u32(&ctl->done));
+    if (lane == 0) mma_commit<CG>(smem_u32(&ctl->done));
     __syncwarp();
     mbar_wait(smem_u32(&ctl->done), 0u, abort_flag, status, args.drain_ns, false);
+  } else if (ModeTraits<MODE>::wgrad && warp == ZERO_WARP && rank == 0) {
+    // =========================================================== tail zeroing (wgrad, even CTA)
+    // For each expert whose rows end inside a 16-row K step: once its last K block has landed in
+    // both CTAs (tail_full), zero the next expert's rows of that K step in both CTAs' copies of
+    // the stage, then complete the stage's full barrier for the MMA issuer. tail_full's phases
+    // advance only at these blocks, and a stage's next one cannot land before the MMAs have
+    // consumed this one, so each wait is for the barrier's current phase.
+    uint32_t it = 0, tpar = 0;
+    for (int t = t_first; t < sc.total; t += t_step) {
+      const Tile ti = decode_tile<MODE>(sc, t);
+      it += static_cast<uint32_t>(ti.kblocks);
+      if (ti.kblocks == 0 || (ti.kvalid % UK) == 0) continue;
+      const int sl = static_cast<int>((it - 1u) % NST);
+      if (!warp_all(mbar_wait(smem_u32(&ctl->tail_full[sl]), (tpar >> sl) & 1u, abort_flag, status, tmo))) break;
+      tpar ^= 1u << sl;
+      const int valid = ti.kvalid - (ti.kblocks - 1) * BK;
+      zero_stage_rows<SB>(stages + sl * SB, valid, ((valid + UK - 1) / UK) * UK, lane);
+      __syncwarp();
+      if (lane == 0) mbar_arrive_count(smem_u32(&ctl->full[sl]), ModeTraits<MODE>::split_producer ? 2u : 1u);
+    }
   } else if (warp >= 2 && warp < 2 + EPI_WARPS) {
     // =========================================================== epilogue (warps 2..9)
     const int q = warp & 3;           // TMEM lane quadrant this warp may access
@@ -609,6 +716,18 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint32_t turn = 0;
     uint32_t use0 = 0, use1 = 0;      // completed uses of accumulator buffers 0 and 1
     uint32_t box_ctr = 0;             // dgrad: staging boxes this warp has stored
+    // hand accumulator buffer b back to the MMA issuer: with CTA pairs one arrival per warp on
+    // the even CTA's barrier (the odd CTA's accumulator rows are written by the even CTA's MMAs)
+    [[maybe_unused]] const uint32_t tempty0 = PAIR ? cluster_addr(smem_u32(&ctl->tempty[0]), 0u) : 0u;
+    auto release_acc = [&](uint32_t b) {
+      tc_fence_before();
+      if constexpr (PAIR) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive_remote(tempty0 + b * static_cast<uint32_t>(sizeof(uint64_t)));
+      } else {
+        mbar_arrive(smem_u32(&ctl->tempty[b]));
+      }
+    };
     for (int t = t_first; t < sc.total; t += t_step) {
       const Tile ti = decode_tile<MODE>(sc, t);
       // wgrad: the gradient this tile belongs to
@@ -616,8 +735,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       [[maybe_unused]] const int gM = ti.prob ? args.Mdim2 : args.Mdim;
       if constexpr (ModeTraits<MODE>::wgrad) {
         if (ti.kblocks == 0) {
-          // empty expert: its gradient is zero
-          const int mrow = ti.m0 + r_in;
+          // empty expert: its gradient is zero (this CTA's 128 rows of the tile)
+          const int mrow = ti.m0 + static_cast<int>(rank) * BM + r_in;
           if (mrow < gM) {
             float* dst = reinterpret_cast<float*>(ti.prob ? args.out_b : args.out) +
                          (static_cast<long long>(ti.e + expert_base) * gM + mrow) * (ti.prob ? args.ldo_b : args.ldo);
@@ -650,7 +769,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       }
       const uint32_t buf = turn;
-      if (!warp_all(mbar_wait(smem_u32(&ctl->tfull[buf]), (buf ? use1 : use0) & 1u, abort_flag, status, tmo))) break;
+      if (!warp_all(mbar_wait(smem_u32(&ctl->tfull[buf]), (buf ? use1 : use0) & 1u, abort_flag, status, tmo)))
+        break;
       tc_fence_after();
       const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * BN;
       const int nseg = num_segments<NACC>(ti.kblocks);
@@ -682,8 +802,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             tmem_st16(tb + col, vr);
           }
           tmem_st_wait();
-          tc_fence_before();
-          mbar_arrive(smem_u32(&ctl->tempty[pb]));
+          release_acc(pb);
           if (pb) ++use1; else ++use0;
         }
         if (!seg_ok) break;
@@ -1007,7 +1126,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         uint8_t* sbuf = staging + (warp - 2) * STAGE_OUT_BYTES;
         const uint32_t sbuf_addr = smem_u32(sbuf);
         const int sw = (lane >> 1) & 3;
-        const bool rows_in = ti.m0 + q * 32 < gM;  // warp-uniform
+        const int m_cta = ti.m0 + static_cast<int>(rank) * BM;  // this CTA's rows of the tile
+        const bool rows_in = m_cta + q * 32 < gM;  // warp-uniform
         const CUtensorMap* mo = ti.prob ? &maps.out2 : &maps.out;
 #pragma unroll 1
         for (int c = half * (BN / 32); c < (half + 1) * (BN / 32); ++c) {
@@ -1025,13 +1145,12 @@ __global__ void __launch_bounds__(THREADS, 1)
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            tma_store_3d(mo, sbuf_addr, ti.n0 + c * 16, ti.m0 + q * 32, ti.e + expert_base);
+            tma_store_3d(mo, sbuf_addr, ti.n0 + c * 16, m_cta + q * 32, ti.e + expert_base);
             bulk_commit_group();
           }
         }
       }
-      tc_fence_before();
-      mbar_arrive(smem_u32(&ctl->tempty[buf]));
+      release_acc(buf);
       if (buf) ++use1; else ++use0;
       if constexpr (NACC == 2) turn ^= 1u;
     }
@@ -1042,9 +1161,12 @@ __global__ void __launch_bounds__(THREADS, 1)
     bulk_wait_group0();
   tc_fence_before();
   __syncthreads();
+  // with CTA pairs the even CTA's MMAs write this CTA's tensor memory and read its shared memory:
+  // neither CTA releases (or exits) before both are done
+  if constexpr (PAIR) cluster_sync_all();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, TMEM_COLS);
+    tmem_dealloc<CG>(tmem_base, TMEM_COLS);
   }
 }
 
@@ -1076,8 +1198,34 @@ moe_status_t launch_mode(const GemmMaps& maps, const GemmArgs& args, long long m
       reinterpret_cast<const void*>(grouped_gemm_kernel<MODE>), static_cast<int>(smem_bytes_for(MAX_E)));
   if (attr_err != cudaSuccess) return cuda_fail(attr_err);
   const long long sms = device_sm_count();
-  const int grid = static_cast<int>(std::max(1LL, std::min(sms, max_tiles)));
-  grouped_gemm_kernel<MODE><<<grid, THREADS, smem, stream>>>(maps, args);
+  if constexpr (ModeTraits<MODE>::pair) {
+    // clusters of two CTAs (one per SM), as many as can be resident at once; max_tiles counts
+    // the 256-row pair tiles
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(std::max(2LL, sms & ~1LL)));
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, grouped_gemm_kernel<MODE>, &cfg) != cudaSuccess || clusters < 1) {
+      cudaGetLastError();
+      clusters = static_cast<int>(std::max(1LL, sms / 2));
+    }
+    const long long pairs = std::max(1LL, std::min<long long>(clusters, max_tiles));
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs));
+    const cudaError_t lerr = cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<MODE>, maps, args);
+    if (lerr != cudaSuccess) return cuda_fail(lerr);
+  } else {
+    const int grid = static_cast<int>(std::max(1LL, std::min(sms, max_tiles)));
+    grouped_gemm_kernel<MODE><<<grid, THREADS, smem, stream>>>(maps, args);
+  }
   const cudaError_t err = cudaGetLastError();
   return err == cudaSuccess ? MOE_OK : cuda_fail(err);
 }

@@ -231,8 +231,9 @@ moe_status_t wgrad_maps(const WgradProblem& w, long long rows, int E, CUtensorMa
   return MOE_OK;
 }
 
+// tiles of one problem: 256 gradient rows (a CTA pair) x 256 columns
 long long wgrad_tiles(const WgradProblem& w, int E) {
-  return static_cast<long long>(E) * ((w.p_cols + 127) / 128) * ((w.q_cols + 255) / 256);
+  return static_cast<long long>(E) * ((w.p_cols + 255) / 256) * ((w.q_cols + 255) / 256);
 }
 
 // a11 / a13: one or two wgrad problems over the same experts in one persistent launch (the
