@@ -56,27 +56,15 @@ __device__ __forceinline__ void mbar_arrive_count(uint32_t bar, uint32_t count) 
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
 
-// CLUSTER: acquire at cluster scope, for a barrier that threads of the peer CTA arrive on
-template <bool CLUSTER = false>
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
-  if constexpr (CLUSTER) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-  } else {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-  }
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
   return ok != 0;
 }
 
@@ -84,16 +72,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // false) when the CTA's abort flag is raised, or after timeout_ns, in which case it raises the
 // flag and records MOE_DEV_TIMEOUT. `honour_abort` = false is used by teardown waits that must
 // drain in-flight copies even after an abort.
-template <bool CLUSTER = false>
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                           int32_t* status, long long timeout_ns,
                                           bool honour_abort = true) {
-  if (mbar_try_wait<CLUSTER>(bar, parity)) return true;
+  if (mbar_try_wait(bar, parity)) return true;
   // try_wait itself suspends the thread for a while when the phase is not complete, so the
   // clock and the abort flag are checked after every unsuccessful try
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
-    if (mbar_try_wait<CLUSTER>(bar, parity)) return true;
+    if (mbar_try_wait(bar, parity)) return true;
     if (honour_abort && *abort_flag) return false;
     if (static_cast<long long>(globaltimer_ns() - t0) > timeout_ns) {
       *abort_flag = 1;
