@@ -215,6 +215,20 @@ def custom(T: int, k: int, E: int, d: int, h: int, seed: int = 0, invalid_frac: 
     return wl
 
 
+def exact_counts(counts, d: int, h: int, seed: int = 0, name: str = "exact_counts") -> Workload:
+    """top_k = 1 and expert e receives exactly counts[e] tokens, in a seeded random token order:
+    segment lengths chosen around the tile and K-step boundaries of the kernels."""
+    counts = np.asarray(counts, np.int64)
+    rng = _rng(seed, _TAG_IDS, 7, counts.size, int(counts.sum()))
+    ids = np.repeat(np.arange(counts.size, dtype=np.int32), counts)
+    ids = ids[rng.permutation(ids.size)]
+    T = int(ids.size)
+    wl = Workload(name, T=T, k=1, E=int(counts.size), d=d, h=h, seed=seed)
+    wl.ids = ids.reshape(T, 1).astype(np.int32)
+    wl.weights = _rng(seed, _TAG_W, T, 1).uniform(0.0, 1.0, size=(T, 1)).astype(np.float32)
+    return wl
+
+
 NAMES = ("toy", "balanced", "finegrained", "skew", "large")
 
 

@@ -102,6 +102,34 @@ def test_grouped_backward(lib, name):
     assert np.isnan(G.host(run.dxp)[M:]).all()
 
 
+# Segment lengths around the CTA-pair wgrad's boundaries: an expert's last K block holds 1..64
+# rows and its rows end exactly on a 16-row K step (16, 48, 64, 128, 256) or inside one (1, 15,
+# 17, 63, 65, ...); one expert is empty. The gradient heights (h and 2h: 72/144, 160/320,
+# 256/512 rows) leave the odd CTA of the last 256-row pair tile none of the gradient's rows, part
+# of them or all of them, and the widths d (200, 384, 136) end inside a 256-column tile.
+EXACT_COUNTS = [1, 15, 16, 17, 48, 63, 64, 65, 100, 128, 0, 200, 255, 256, 257, 513]
+
+
+@pytest.mark.parametrize("d,h", [(200, 72), (384, 160), (136, 256)])
+def test_wgrad_pair_expert_boundaries(lib, d, h):
+    wl = W.exact_counts(EXACT_COUNTS, d=d, h=h, seed=21)
+    run = G.DevicePipeline(wl).route().permute().forward()
+    r, xp, y, u, a = G.oracle_run(wl)
+    M = r["M"]
+    assert list(r["counts"]) == EXACT_COUNTS
+    dy, dyh = _dy(wl, M)
+    run.backward(dy)
+    torch.cuda.synchronize()
+    assert run.status.item() == 0
+    dxp, dw_ug, dw_down, du = O.expert_backward(dyh, xp, u, r["offsets"], wl.w_ug, wl.w_down)
+    got_ug, got_dn = G.host(run.dw_ug), G.host(run.dw_down)
+    nz = r["counts"] > 0
+    G.assert_close(got_ug[nz], dw_ug[nz], f"dW_ug[{d}x{h}]")
+    G.assert_close(got_dn[nz], dw_down[nz], f"dW_down[{d}x{h}]")
+    assert not got_ug[~nz].any() and not got_dn[~nz].any(), "empty experts must get zero gradients"
+    G.assert_close(G.host(run.dxp)[:M], dxp[:M], f"dxp[{d}x{h}]")
+
+
 @pytest.mark.slow
 def test_large_forward_backward_sampled_experts(lib):
     """The large workload at full size; the oracle checks every row and gradient of a sample of

@@ -33,3 +33,16 @@ def test_balanced_counts_and_permutations():
     assert perms[0].tolist() == list(range(16))
     assert all(sorted(p.tolist()) == list(range(16)) for p in perms)
     assert len({tuple(p.tolist()) for p in perms}) == 4
+
+
+def test_exact_counts_workload():
+    counts = [1, 15, 0, 513, 64]
+    wl = W.exact_counts(counts, d=64, h=32, seed=5)
+    assert (wl.T, wl.k, wl.E) == (sum(counts), 1, len(counts))
+    r = O.route_offsets(wl.ids, wl.E)
+    assert list(r["counts"]) == counts and r["M"] == sum(counts)
+    again = W.exact_counts(counts, d=64, h=32, seed=5)
+    assert np.array_equal(again.ids, wl.ids) and np.array_equal(again.weights, wl.weights)
+    # the token order is shuffled, not grouped by expert
+    assert not np.array_equal(wl.ids[:, 0], np.sort(wl.ids[:, 0]))
+    assert ((wl.weights >= 0) & (wl.weights < 1)).all()
